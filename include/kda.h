@@ -1,0 +1,145 @@
+/*
+ * kda.h -- C ABI of libkda: Kimi Delta Attention (KDA) forward on one GPU.
+ *
+ * KDA is the gated delta rule with a per-channel decay described in
+ * "はじめての自然言語処理 -- Kimi K3" (ogis-ri.co.jp), section 3.1 "KDA":
+ *
+ *     S_t = (I - beta_t k_t k_t^T) Diag(exp g_t) S_{t-1} + beta_t k_t v_t^T,
+ *     o_t = S_t^T q_t,
+ *
+ * with S_t a d_k x d_v state per (sequence, head), q_t, k_t, g_t d_k-vectors,
+ * v_t a d_v-vector, beta_t a scalar (the shapes list and the four-step
+ * delta-rule paragraph; the one-line form is the report's equation (1)).
+ * kda_chunk_fwd evaluates it chunkwise ("chunk をまたぐところだけ逐次" and the
+ * chunk-decay paragraphs of the same section); kda_recurrent_step is the
+ * per-token sequential update used for decode (the serving paragraph of
+ * "Kimi K3 architecture", orkas.ai: the state update is sequential).
+ *
+ * Conventions for every call:
+ *   - Pointers are DEVICE pointers unless stated; tensors are dense, row-major,
+ *     contiguous, and must be 16-byte aligned (cu_seqlens / state_indices:
+ *     4-byte aligned).  The caller allocates and owns all memory; the library
+ *     allocates nothing and keeps no state between calls.
+ *   - Calls are asynchronous on `stream` (0 = legacy default stream) and do not
+ *     synchronise the host.  Argument errors are detected on the host, before
+ *     anything is launched; on error nothing is written.  Launch failures map
+ *     to KDA_ERR_CUDA.  Faults of a launched kernel surface at the caller's next
+ *     synchronisation, as for any CUDA call.
+ *   - q, k, v, g, beta and out share `dims->dtype` (fp32 or bf16); recurrent
+ *     states are always fp32.  Supported head sizes: dk, dv in {64, 128}.
+ *   - No scale is applied to q (o = S^T q exactly); callers fold any 1/sqrt(dk)
+ *     into q.  q and k are used as given (their L2 normalisation is the
+ *     caller's).  g is the log decay; the kernels rely on the lower bound
+ *     g >= -5 of the "lower-bound" paragraph (so that a 16-token tile's
+ *     cumulative log decay stays >= -80 and e^80 fits bf16/fp32): g in [-5, 0]
+ *     is a precondition, not checked; outside it results are unspecified.
+ */
+#ifndef KDA_H
+#define KDA_H
+
+#include <stddef.h>
+#include <stdint.h>
+#include <cuda_runtime_api.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+    KDA_OK = 0,
+    KDA_ERR_NULL = 1,        /* a required pointer is NULL                       */
+    KDA_ERR_SHAPE = 2,       /* inconsistent or non-positive dimensions           */
+    KDA_ERR_UNSUPPORTED = 3, /* valid but not implemented (head size, dtype, impl) */
+    KDA_ERR_ALIGN = 4,       /* a pointer is not aligned as required              */
+    KDA_ERR_WORKSPACE = 5,   /* reserved: workspace too small                     */
+    KDA_ERR_CUDA = 6,        /* a CUDA runtime call or launch failed              */
+    KDA_ERR_TIMEOUT = 7      /* reserved: a bounded device wait gave up           */
+} kda_status_t;
+
+typedef enum { KDA_F32 = 0, KDA_BF16 = 1 } kda_dtype_t;
+
+/* Which chunk-forward kernel to run.  AUTO picks the tensor-core kernel where
+ * it applies (bf16, dk = dv = 128) and the SIMT fp32 kernel otherwise. */
+typedef enum { KDA_IMPL_AUTO = 0, KDA_IMPL_SIMT = 1, KDA_IMPL_TC = 2 } kda_impl_t;
+
+/* Problem dimensions.
+ *   dense : batch = B, seqlen = T, num_seqs = B, tensors [B, T, H, d].
+ *   packed: batch = 1, seqlen = total tokens, num_seqs = N, tensors
+ *           [1, total, H, d], cu_seqlens int32[N+1] on the device with
+ *           cu[0] = 0 <= cu[1] <= ... <= cu[N] = seqlen (each sequence is
+ *           chunked from its own start; empty sequences are allowed).
+ *   decode: batch = rows N, seqlen = 1, num_seqs = slots in the state pool. */
+typedef struct {
+    int32_t batch;
+    int32_t seqlen;
+    int32_t num_seqs;
+    int32_t heads;
+    int32_t dk;
+    int32_t dv;
+    kda_dtype_t dtype;
+} kda_dims_t;
+
+/* kda_chunk_fwd -- chunkwise-parallel KDA prefill, and prefix-cache resume.
+ *
+ * Operation: for every sequence n and head h, starting from
+ * initial_state[n,h] (zeros when NULL), run the recurrence above over the
+ * sequence's tokens, writing o_t to `out` and the state after the last token
+ * to final_state[n,h] (skipped when NULL).  Resume from a cached state at a
+ * sequence boundary is the same call with initial_state = the saved state
+ * ("prefix を再利用する", orkas.ai serving paragraph; prefill-cache support,
+ * poyo.ai "KDAとプレフィックスキャッシュ").
+ *   q, k, g   : [batch, seqlen, H, dk]  dtype
+ *   v, out    : [batch, seqlen, H, dv]  dtype (out is written)
+ *   beta      : [batch, seqlen, H]      dtype
+ *   initial_state, final_state : fp32 [num_seqs, H, dk, dv]; they may be the
+ *               same pointer (in-place resume); partial overlap is not allowed.
+ *   cu_seqlens: int32 [num_seqs + 1] device, or NULL for dense batches.
+ *               Offsets are clamped to [0, seqlen] on the device.
+ * Returns KDA_OK or an error listed above; seqlen = 0 is valid (only the
+ * final state is written: a copy of the initial state, or zeros). */
+kda_status_t kda_chunk_fwd(const void *q, const void *k, const void *v,
+                           const void *g, const void *beta,
+                           const float *initial_state, const int32_t *cu_seqlens,
+                           void *out, float *final_state,
+                           const kda_dims_t *dims, cudaStream_t stream);
+
+/* As kda_chunk_fwd, with an explicit kernel choice (tests and benchmarks).
+ * Returns KDA_ERR_UNSUPPORTED when the chosen kernel cannot run the shape. */
+kda_status_t kda_chunk_fwd_with(kda_impl_t impl,
+                                const void *q, const void *k, const void *v,
+                                const void *g, const void *beta,
+                                const float *initial_state, const int32_t *cu_seqlens,
+                                void *out, float *final_state,
+                                const kda_dims_t *dims, cudaStream_t stream);
+
+/* The kernel kda_chunk_fwd would run for `dims` (KDA_IMPL_SIMT or
+ * KDA_IMPL_TC), or -1 when the dims are invalid. */
+int kda_chunk_fwd_selected_impl(const kda_dims_t *dims);
+
+/* kda_recurrent_step -- one decode token per row, state updated in place.
+ *
+ * Operation per row n and head h, on the state S = state[slot][h] with
+ * slot = state_indices ? state_indices[n] : n, in the order of the four-step
+ * delta-rule paragraph (forget, read with the current key, delta, write):
+ *   vhat = (Diag(exp g) S)^T k,  e = v - vhat,
+ *   S <- Diag(exp g) S + beta k e^T,  o = S^T q.
+ *   q, k, g : [N, H, dk] dtype;  v, out : [N, H, dv] dtype;  beta : [N, H]
+ *   state   : fp32 [num_seqs, H, dk, dv], read and written in place.
+ *   state_indices: int32 [N] device or NULL (identity; then num_seqs >= N).
+ *               Rows whose slot is outside [0, num_seqs) are skipped: neither
+ *               their state nor their output is written.  Two rows must not
+ *               name the same slot.
+ * dims: batch = N rows, seqlen = 1, num_seqs = pool slots. */
+kda_status_t kda_recurrent_step(const void *q, const void *k, const void *v,
+                                const void *g, const void *beta, float *state,
+                                const int32_t *state_indices, void *out,
+                                const kda_dims_t *dims, cudaStream_t stream);
+
+/* A static, human-readable name for a status code (never NULL). */
+const char *kda_status_string(kda_status_t status);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* KDA_H */

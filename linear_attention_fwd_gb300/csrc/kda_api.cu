@@ -1,0 +1,120 @@
+// libkda C ABI: argument validation and kernel dispatch.  No allocation, no
+// host synchronisation, no global mutable state besides per-function
+// attribute caches inside the launchers.
+#include <cstdint>
+#include <cuda_runtime.h>
+
+#include "kda_internal.h"
+
+namespace {
+
+bool aligned(const void *p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+bool head_size_ok(int d) { return d == 64 || d == 128; }
+
+kda_status_t check_chunk(kda_impl_t impl, const void *q, const void *k, const void *v,
+                         const void *g, const void *beta, const float *s0, const int32_t *cu,
+                         const void *out, const float *sT, const kda_dims_t *d) {
+    if (d == nullptr) return KDA_ERR_NULL;
+    if (d->dtype != KDA_F32 && d->dtype != KDA_BF16) return KDA_ERR_UNSUPPORTED;
+    if (!head_size_ok(d->dk) || !head_size_ok(d->dv)) return KDA_ERR_UNSUPPORTED;
+    if (d->heads <= 0 || d->batch <= 0 || d->seqlen < 0 || d->num_seqs <= 0) return KDA_ERR_SHAPE;
+    if (cu == nullptr) {
+        if (d->num_seqs != d->batch) return KDA_ERR_SHAPE;
+    } else if (d->batch != 1) {
+        return KDA_ERR_SHAPE;
+    }
+    const int64_t tokens = (int64_t)d->batch * d->seqlen;
+    if (tokens > 0 && (!q || !k || !v || !g || !beta || !out)) return KDA_ERR_NULL;
+    const uintptr_t es = d->dtype == KDA_F32 ? 4 : 2;
+    const void *ptrs[] = {q, k, v, g, out, s0, sT};
+    for (const void *p : ptrs)
+        if (p && !aligned(p, 16)) return KDA_ERR_ALIGN;
+    if (beta && !aligned(beta, es)) return KDA_ERR_ALIGN;
+    if (cu && !aligned(cu, 4)) return KDA_ERR_ALIGN;
+    if (s0 && sT && s0 != sT) {
+        const char *a = reinterpret_cast<const char *>(s0), *b = reinterpret_cast<const char *>(sT);
+        const int64_t bytes = (int64_t)d->num_seqs * d->heads * d->dk * d->dv * 4;
+        if (a < b + bytes && b < a + bytes) return KDA_ERR_SHAPE;  // partial overlap
+    }
+    if (impl == KDA_IMPL_TC && !kda::chunk_tc_supported(d->dk, d->dv, d->dtype))
+        return KDA_ERR_UNSUPPORTED;
+    if (impl != KDA_IMPL_AUTO && impl != KDA_IMPL_SIMT && impl != KDA_IMPL_TC)
+        return KDA_ERR_UNSUPPORTED;
+    return KDA_OK;
+}
+
+}  // namespace
+
+extern "C" const char *kda_status_string(kda_status_t s) {
+    switch (s) {
+        case KDA_OK: return "ok";
+        case KDA_ERR_NULL: return "a required pointer is NULL";
+        case KDA_ERR_SHAPE: return "inconsistent or non-positive dimensions";
+        case KDA_ERR_UNSUPPORTED: return "unsupported head size, dtype or kernel choice";
+        case KDA_ERR_ALIGN: return "pointer not aligned as required";
+        case KDA_ERR_WORKSPACE: return "workspace too small";
+        case KDA_ERR_CUDA: return "CUDA launch or runtime error";
+        case KDA_ERR_TIMEOUT: return "a bounded device wait gave up";
+    }
+    return "unknown status";
+}
+
+extern "C" int kda_chunk_fwd_selected_impl(const kda_dims_t *d) {
+    if (d == nullptr || !head_size_ok(d->dk) || !head_size_ok(d->dv)) return -1;
+    if (d->dtype != KDA_F32 && d->dtype != KDA_BF16) return -1;
+    return kda::chunk_tc_supported(d->dk, d->dv, d->dtype) ? KDA_IMPL_TC : KDA_IMPL_SIMT;
+}
+
+extern "C" kda_status_t kda_chunk_fwd_with(kda_impl_t impl, const void *q, const void *k,
+                                           const void *v, const void *g, const void *beta,
+                                           const float *initial_state, const int32_t *cu_seqlens,
+                                           void *out, float *final_state, const kda_dims_t *d,
+                                           cudaStream_t stream) {
+    kda_status_t st = check_chunk(impl, q, k, v, g, beta, initial_state, cu_seqlens, out,
+                                  final_state, d);
+    if (st != KDA_OK) return st;
+    kda::ChunkArgs a{q, k, v, g, beta, initial_state, cu_seqlens, out, final_state,
+                     (int64_t)d->seqlen, d->num_seqs, d->heads};
+    cudaError_t e;
+    if ((int64_t)d->batch * d->seqlen == 0) {
+        if (final_state == nullptr || final_state == initial_state) return KDA_OK;
+        e = kda::launch_state_copy(a, d->dk, d->dv, stream);
+    } else {
+        if (impl == KDA_IMPL_AUTO)
+            impl = kda::chunk_tc_supported(d->dk, d->dv, d->dtype) ? KDA_IMPL_TC : KDA_IMPL_SIMT;
+        e = impl == KDA_IMPL_TC ? kda::launch_chunk_tc(a, d->dk, d->dv, d->dtype, stream)
+                                : kda::launch_chunk_simt(a, d->dk, d->dv, d->dtype, stream);
+    }
+    return e == cudaSuccess ? KDA_OK : KDA_ERR_CUDA;
+}
+
+extern "C" kda_status_t kda_chunk_fwd(const void *q, const void *k, const void *v, const void *g,
+                                      const void *beta, const float *initial_state,
+                                      const int32_t *cu_seqlens, void *out, float *final_state,
+                                      const kda_dims_t *dims, cudaStream_t stream) {
+    return kda_chunk_fwd_with(KDA_IMPL_AUTO, q, k, v, g, beta, initial_state, cu_seqlens, out,
+                              final_state, dims, stream);
+}
+
+extern "C" kda_status_t kda_recurrent_step(const void *q, const void *k, const void *v,
+                                           const void *g, const void *beta, float *state,
+                                           const int32_t *state_indices, void *out,
+                                           const kda_dims_t *d, cudaStream_t stream) {
+    if (d == nullptr) return KDA_ERR_NULL;
+    if (d->dtype != KDA_F32 && d->dtype != KDA_BF16) return KDA_ERR_UNSUPPORTED;
+    if (!head_size_ok(d->dk) || !head_size_ok(d->dv)) return KDA_ERR_UNSUPPORTED;
+    if (d->seqlen != 1 || d->batch < 0 || d->heads <= 0 || d->num_seqs <= 0) return KDA_ERR_SHAPE;
+    if (state_indices == nullptr && d->num_seqs < d->batch) return KDA_ERR_SHAPE;
+    if (d->batch == 0) return KDA_OK;
+    if (!q || !k || !v || !g || !beta || !state || !out) return KDA_ERR_NULL;
+    const uintptr_t es = d->dtype == KDA_F32 ? 4 : 2;
+    const void *ptrs[] = {q, k, v, g, out, state};
+    for (const void *p : ptrs)
+        if (!aligned(p, 16)) return KDA_ERR_ALIGN;
+    if (!aligned(beta, es)) return KDA_ERR_ALIGN;
+    if (state_indices && !aligned(state_indices, 4)) return KDA_ERR_ALIGN;
+    kda::DecodeArgs a{q, k, v, g, beta, state, state_indices, out, d->batch, d->num_seqs, d->heads};
+    cudaError_t e = kda::launch_decode(a, d->dk, d->dv, d->dtype, stream);
+    return e == cudaSuccess ? KDA_OK : KDA_ERR_CUDA;
+}

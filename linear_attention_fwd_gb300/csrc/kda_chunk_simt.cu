@@ -1,0 +1,309 @@
+// KDA chunkwise forward, SIMT fp32 kernel.
+//
+// The fp32-mode path (fp32 inputs need fp32 arithmetic throughout, which the
+// bf16 tensor-core path cannot give) and the general fallback for head sizes
+// the tensor-core kernel does not take.  It evaluates the same chunk algebra
+// as the tensor-core kernel.
+//
+// Chunk form ("はじめての自然言語処理 -- Kimi K3" section 3.1, chunkwise paragraphs
+// and "chunk 内の減衰と、その数値範囲"): per chunk of C = 64 tokens, with
+// gamma_r = sum_{s<=r} g_s and S the state entering the chunk,
+//   A_rs = beta_r sum_c k_rc k_sc e^{gamma_rc - gamma_sc}   (s <  r)
+//   M_rs =        sum_c q_rc k_sc e^{gamma_rc - gamma_sc}   (s <= r, the Tril mask)
+//   (I + A) U = diag(beta) (V - Kbar S)          (delta-rule correction, WY form)
+//   O = Qbar S + M U                              (inter-chunk + intra-chunk terms)
+//   S <- Diag(e^{gamma_last}) S + Kp^T U
+// where Qbar = Q e^{gamma}, Kbar = K e^{gamma}, Kp = K e^{gamma_last - gamma}.
+// The decay between positions is folded into the operands (q times Gamma, k
+// divided by Gamma: the report's equation (4)), split at 16-token sub-tiles:
+// relative to b_I = gamma just before sub-tile I starts, x = e^{gamma - b_I} is
+// in [e^-80, 1] and 1/x in [1, e^80] because g >= -5 (the lower-bound
+// paragraph), so the diagonal sub-tiles are ordinary dot products with no
+// per-position-pair exponentials.
+//
+// One CTA of 256 threads per (sequence, head, 64-column slice of d_v).
+#include <cuda_runtime.h>
+#include <cuda_bf16.h>
+
+#include "kda_internal.h"
+
+namespace kda {
+namespace {
+
+constexpr int kThreads = 256;
+constexpr int kDvs = 64;               // d_v columns per CTA
+constexpr int kNb = kChunk / kSub;     // sub-tiles per chunk (4)
+constexpr int kLdu = kDvs + 8;         // row stride of the V/Y/U tile (conflict-free solve)
+
+template <int DK>
+struct SimtSmem {
+    static constexpr int LDQ = DK;       // Q~ / Qbar tile
+    static constexpr int LDK = DK;       // K~ / Kbar tile
+    static constexpr int LDH = DK + 1;   // gamma, then K^ / Kp tile (odd: column reads)
+    static constexpr int kQ = 0;
+    static constexpr int kK = kQ + kChunk * LDQ;
+    static constexpr int kH = kK + kChunk * LDK;
+    static constexpr int kU = kH + kChunk * LDH;
+    static constexpr int kS = kU + kChunk * kLdu;
+    static constexpr int kA = kS + DK * kDvs;
+    static constexpr int kM = kA + kChunk * kChunk;
+    static constexpr int kB = kM + kChunk * kChunk;
+    static constexpr int kRef = kB + kChunk;        // b_I            [4][DK]
+    static constexpr int kEB = kRef + kNb * DK;     // e^{b_I}        [4][DK]
+    static constexpr int kEL = kEB + kNb * DK;      // e^{gl - b_I}   [4][DK]
+    static constexpr int kW = kEL + kNb * DK;       // e^{b_I - b_J}  [6][DK]
+    static constexpr int kDec = kW + 6 * DK;        // e^{gl}         [DK]
+    static constexpr int kFloats = kDec + DK;
+    static constexpr size_t kBytes = sizeof(float) * kFloats;
+};
+
+__device__ __forceinline__ int pair_index(int I, int J) { return I * (I - 1) / 2 + J; }
+
+template <typename Tin, int DK, int DV>
+__global__ void __launch_bounds__(kThreads, 1)
+kda_chunk_simt_kernel(ChunkArgs a) {
+    using L = SimtSmem<DK>;
+    constexpr int C = kChunk;
+    constexpr int NSL = DV / kDvs;
+    extern __shared__ float sm[];
+    float *Qs = sm + L::kQ, *Ks = sm + L::kK, *Hs = sm + L::kH, *Us = sm + L::kU;
+    float *Ss = sm + L::kS, *As = sm + L::kA, *Ms = sm + L::kM, *Bs = sm + L::kB;
+    float *Ref = sm + L::kRef, *EB = sm + L::kEB, *EL = sm + L::kEL, *Wv = sm + L::kW;
+    float *Dec = sm + L::kDec;
+
+    const int t = threadIdx.x;
+    const int slice = blockIdx.x % NSL;
+    const int uh = blockIdx.x / NSL;
+    const int h = uh % a.heads, n = uh / a.heads;
+    const int H = a.heads;
+    int64_t bos, eos;
+    seq_range(a, n, bos, eos);
+    const int64_t len = eos - bos;
+    const int col0 = slice * kDvs;
+
+    const Tin *q = static_cast<const Tin *>(a.q);
+    const Tin *k = static_cast<const Tin *>(a.k);
+    const Tin *v = static_cast<const Tin *>(a.v);
+    const Tin *g = static_cast<const Tin *>(a.g);
+    const Tin *beta = static_cast<const Tin *>(a.beta);
+    Tin *out = static_cast<Tin *>(a.out);
+
+    // state slice [DK][64]
+    const int64_t soff = ((int64_t)n * H + h) * DK * DV + col0;
+    for (int x = t; x < DK * kDvs; x += kThreads) {
+        const int c = x / kDvs, j = x % kDvs;
+        Ss[x] = a.s0 ? a.s0[soff + (int64_t)c * DV + j] : 0.f;
+    }
+
+    const int j = t & (kDvs - 1);   // column owned in the GEMM-like phases
+    const int rq = t >> 6;          // row phase (0..3)
+
+    for (int64_t c0 = 0; c0 < len; c0 += C) {
+        const int nr = (int)(len - c0 < C ? len - c0 : C);
+        __syncthreads();   // previous chunk fully consumed
+        // ---- load the chunk (rows past the sequence end are zero: k = 0, beta = 0, g = 0)
+        for (int x = t; x < C * DK; x += kThreads) {
+            const int r = x / DK, c = x % DK;
+            float qv = 0.f, kv = 0.f, gv = 0.f;
+            if (r < nr) {
+                const int64_t off = ((bos + c0 + r) * H + h) * DK + c;
+                qv = to_f(q[off]); kv = to_f(k[off]); gv = to_f(g[off]);
+            }
+            Qs[r * L::LDQ + c] = qv; Ks[r * L::LDK + c] = kv; Hs[r * L::LDH + c] = gv;
+        }
+        for (int x = t; x < C * kDvs; x += kThreads) {
+            const int r = x / kDvs, c = x % kDvs;
+            Us[r * kLdu + c] = r < nr ? to_f(v[((bos + c0 + r) * H + h) * DV + col0 + c]) : 0.f;
+        }
+        if (t < C) Bs[t] = t < nr ? to_f(beta[(bos + c0 + t) * H + h]) : 0.f;
+        __syncthreads();
+
+        // ---- cumulative log decay per channel and the per-sub-tile reference vectors
+        if (t < DK) {
+            const int c = t;
+            float run = 0.f, ref[kNb];
+            ref[0] = 0.f;
+            for (int r = 0; r < C; ++r) {
+                if (r > 0 && (r % kSub) == 0) ref[r / kSub] = run;
+                run += Hs[r * L::LDH + c];
+                Hs[r * L::LDH + c] = run;
+            }
+            const float gl = run;
+            for (int I = 0; I < kNb; ++I) {
+                Ref[I * DK + c] = ref[I];
+                EB[I * DK + c] = expf(ref[I]);
+                EL[I * DK + c] = expf(gl - ref[I]);
+                for (int J = 0; J < I; ++J) Wv[pair_index(I, J) * DK + c] = expf(ref[I] - ref[J]);
+            }
+            Dec[c] = expf(gl);
+        }
+        __syncthreads();
+        // x = e^{gamma - b_I} in [e^-80, 1];  Q~ = Q x,  K~ = K x,  K^ = K / x
+        for (int x = t; x < C * DK; x += kThreads) {
+            const int r = x / DK, c = x % DK;
+            const float d = Hs[r * L::LDH + c] - Ref[(r / kSub) * DK + c];
+            const float kv = Ks[r * L::LDK + c];
+            Qs[r * L::LDQ + c] *= expf(d);
+            Ks[r * L::LDK + c] = kv * expf(d);
+            Hs[r * L::LDH + c] = kv * expf(-d);
+        }
+        __syncthreads();
+
+        // ---- A and M: dense dot products per 16x16 sub-tile pair (I >= J)
+        {
+            const int s = t & (C - 1);
+            const int Js = s / kSub;
+            float accA[16], accM[16];
+#pragma unroll
+            for (int m = 0; m < 16; ++m) { accA[m] = 0.f; accM[m] = 0.f; }
+            for (int c = 0; c < DK; ++c) {
+                const float kh = Hs[s * L::LDH + c];
+                float khI[kNb];
+#pragma unroll
+                for (int I = 0; I < kNb; ++I)
+                    khI[I] = I > Js ? kh * Wv[pair_index(I, Js) * DK + c] : kh;
+#pragma unroll
+                for (int m = 0; m < 16; ++m) {
+                    const int r = rq + 4 * m;
+                    accA[m] += Ks[r * L::LDK + c] * khI[m >> 2];
+                    accM[m] += Qs[r * L::LDQ + c] * khI[m >> 2];
+                }
+            }
+#pragma unroll
+            for (int m = 0; m < 16; ++m) {
+                const int r = rq + 4 * m;
+                As[r * C + s] = s < r ? Bs[r] * accA[m] : 0.f;
+                Ms[r * C + s] = s <= r ? accM[m] : 0.f;
+            }
+        }
+        __syncthreads();
+        // Qbar = Q~ e^{b_I}, Kbar = K~ e^{b_I}, Kp = K^ e^{gl - b_I}
+        for (int x = t; x < C * DK; x += kThreads) {
+            const int r = x / DK, c = x % DK, I = r / kSub;
+            Qs[r * L::LDQ + c] *= EB[I * DK + c];
+            Ks[r * L::LDK + c] *= EB[I * DK + c];
+            Hs[r * L::LDH + c] *= EL[I * DK + c];
+        }
+        __syncthreads();
+
+        // ---- Y = diag(beta) (V - Kbar S), in place over V
+        {
+            float acc[16];
+#pragma unroll
+            for (int m = 0; m < 16; ++m) acc[m] = 0.f;
+            for (int c = 0; c < DK; ++c) {
+                const float sv = Ss[c * kDvs + j];
+#pragma unroll
+                for (int m = 0; m < 16; ++m) acc[m] += Ks[(rq + 4 * m) * L::LDK + c] * sv;
+            }
+#pragma unroll
+            for (int m = 0; m < 16; ++m) {
+                const int r = rq + 4 * m;
+                Us[r * kLdu + j] = Bs[r] * (Us[r * kLdu + j] - acc[m]);
+            }
+        }
+        __syncthreads();
+        // ---- (I + A) U = Y by forward substitution (row r uses rows s < r)
+        {
+            const int jj = t >> 2, part = t & 3;
+            for (int r = 1; r < C; ++r) {
+                float acc = 0.f;
+                for (int s = part; s < r; s += 4) acc += As[r * C + s] * Us[s * kLdu + jj];
+                acc += __shfl_xor_sync(0xffffffffu, acc, 1);
+                acc += __shfl_xor_sync(0xffffffffu, acc, 2);
+                if (part == 0) Us[r * kLdu + jj] -= acc;
+                __syncthreads();
+            }
+        }
+        // ---- O = Qbar S + M U
+        {
+            float acc[16];
+#pragma unroll
+            for (int m = 0; m < 16; ++m) acc[m] = 0.f;
+            for (int c = 0; c < DK; ++c) {
+                const float sv = Ss[c * kDvs + j];
+#pragma unroll
+                for (int m = 0; m < 16; ++m) acc[m] += Qs[(rq + 4 * m) * L::LDQ + c] * sv;
+            }
+            for (int s = 0; s < C; ++s) {
+                const float u = Us[s * kLdu + j];
+#pragma unroll
+                for (int m = 0; m < 16; ++m) acc[m] += Ms[(rq + 4 * m) * C + s] * u;
+            }
+#pragma unroll
+            for (int m = 0; m < 16; ++m) {
+                const int r = rq + 4 * m;
+                if (r < nr) out[((bos + c0 + r) * H + h) * DV + col0 + j] = from_f<Tin>(acc[m]);
+            }
+        }
+        __syncthreads();
+        // ---- S <- Diag(e^{gl}) S + Kp^T U
+        {
+            constexpr int MR = DK / 4;
+            float acc[MR];
+#pragma unroll
+            for (int m = 0; m < MR; ++m) acc[m] = 0.f;
+            for (int r = 0; r < C; ++r) {
+                const float u = Us[r * kLdu + j];
+#pragma unroll
+                for (int m = 0; m < MR; ++m) acc[m] += Hs[r * L::LDH + rq + 4 * m] * u;
+            }
+#pragma unroll
+            for (int m = 0; m < MR; ++m) {
+                const int c = rq + 4 * m;
+                Ss[c * kDvs + j] = Dec[c] * Ss[c * kDvs + j] + acc[m];
+            }
+        }
+    }
+    __syncthreads();
+    if (a.sT) {
+        for (int x = t; x < DK * kDvs; x += kThreads) {
+            const int c = x / kDvs, jj = x % kDvs;
+            a.sT[soff + (int64_t)c * DV + jj] = Ss[x];
+        }
+    }
+}
+
+__global__ void kda_state_copy_kernel(const float *src, float *dst, int64_t n) {
+    for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < n;
+         i += (int64_t)gridDim.x * blockDim.x)
+        dst[i] = src ? src[i] : 0.f;
+}
+
+template <typename Tin, int DK, int DV>
+cudaError_t launch_simt_t(const ChunkArgs &a, cudaStream_t st) {
+    constexpr size_t smem = SimtSmem<DK>::kBytes;
+    static_assert(smem <= 227 * 1024, "shared memory budget");
+    cudaError_t e = cudaFuncSetAttribute(kda_chunk_simt_kernel<Tin, DK, DV>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess) return e;
+    const int64_t units = (int64_t)a.num_seqs * a.heads * (DV / kDvs);
+    if (units > 0x7fffffffLL) return cudaErrorInvalidValue;
+    kda_chunk_simt_kernel<Tin, DK, DV><<<(unsigned)units, kThreads, smem, st>>>(a);
+    return cudaGetLastError();
+}
+
+template <typename Tin>
+cudaError_t launch_simt_d(const ChunkArgs &a, int dk, int dv, cudaStream_t st) {
+    if (dk == 128 && dv == 128) return launch_simt_t<Tin, 128, 128>(a, st);
+    if (dk == 128 && dv == 64) return launch_simt_t<Tin, 128, 64>(a, st);
+    if (dk == 64 && dv == 128) return launch_simt_t<Tin, 64, 128>(a, st);
+    if (dk == 64 && dv == 64) return launch_simt_t<Tin, 64, 64>(a, st);
+    return cudaErrorInvalidValue;
+}
+
+}  // namespace
+
+cudaError_t launch_chunk_simt(const ChunkArgs &a, int dk, int dv, kda_dtype_t dt, cudaStream_t st) {
+    return dt == KDA_F32 ? launch_simt_d<float>(a, dk, dv, st)
+                         : launch_simt_d<__nv_bfloat16>(a, dk, dv, st);
+}
+
+cudaError_t launch_state_copy(const ChunkArgs &a, int dk, int dv, cudaStream_t st) {
+    const int64_t n = (int64_t)a.num_seqs * a.heads * dk * dv;
+    const int64_t blocks = (n + 255) / 256;
+    kda_state_copy_kernel<<<(unsigned)(blocks < 4096 ? blocks : 4096), 256, 0, st>>>(a.s0, a.sT, n);
+    return cudaGetLastError();
+}
+
+}  // namespace kda

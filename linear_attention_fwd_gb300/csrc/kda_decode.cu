@@ -1,0 +1,131 @@
+// KDA recurrent decode step: one token per (row, head), fp32 state in place.
+//
+// Per state column j (columns of S are independent, since v_j only touches
+// column j), in the order of the four-step delta rule of "はじめての自然言語処理
+// -- Kimi K3" section 3.1 (forget, read with the current key, delta, write):
+//   vhat_j = sum_i alpha_i k_i S_ij,   p_j = sum_i alpha_i q_i S_ij,
+//   e_j = v_j - vhat_j,   S_ij <- alpha_i S_ij + beta k_i e_j,
+//   o_j = sum_i q_i S'_ij = p_j + beta (k.q) e_j.
+// The state is streamed through registers exactly once (one HBM read and one
+// HBM write of d_k*d_v*4 bytes per (row, head)); that traffic is the roofline.
+#include <cuda_runtime.h>
+#include <cuda_bf16.h>
+
+#include "kda_internal.h"
+
+namespace kda {
+namespace {
+
+constexpr int kDecodeThreads = 256;
+
+template <typename Tin, int DK, int DV>
+__global__ void __launch_bounds__(kDecodeThreads)
+kda_recurrent_step_kernel(DecodeArgs a) {
+    constexpr int CG = DV / 4;                 // float4 column groups
+    constexpr int RG = kDecodeThreads / CG;    // row groups
+    constexpr int RPT = DK / RG;               // rows per thread
+    static_assert(RPT >= 1 && RG * RPT == DK, "tile split");
+
+    const int unit = blockIdx.x;
+    const int n = unit / a.heads, h = unit - n * a.heads;
+    const int slot = a.idx ? __ldg(a.idx + n) : n;
+    if (slot < 0 || slot >= a.slots) return;   // uniform across the block
+
+    __shared__ float sq[DK], sk[DK], sa[DK], sv[DV], se[DV];
+    __shared__ float red_v[RG][DV], red_p[RG][DV];
+    __shared__ float s_qk;
+
+    const int t = threadIdx.x;
+    const int cg = t % CG, rg = t / CG;
+    const int64_t row = (int64_t)n * a.heads + h;
+    float *S = a.state + ((int64_t)slot * a.heads + h) * (DK * DV);
+
+    // Issue the state loads first: they are the only traffic that matters.
+    float4 s[RPT];
+#pragma unroll
+    for (int m = 0; m < RPT; ++m)
+        s[m] = __ldcs(reinterpret_cast<const float4 *>(S + (rg * RPT + m) * DV) + cg);
+
+    const Tin *q = static_cast<const Tin *>(a.q) + row * DK;
+    const Tin *k = static_cast<const Tin *>(a.k) + row * DK;
+    const Tin *g = static_cast<const Tin *>(a.g) + row * DK;
+    const Tin *v = static_cast<const Tin *>(a.v) + row * DV;
+    for (int i = t; i < DK; i += kDecodeThreads) {
+        sq[i] = to_f(q[i]);
+        sk[i] = to_f(k[i]);
+        sa[i] = expf(to_f(g[i]));
+    }
+    for (int j = t; j < DV; j += kDecodeThreads) sv[j] = to_f(v[j]);
+    const float beta = to_f(static_cast<const Tin *>(a.beta)[row]);
+    __syncthreads();
+
+    if (t < 32) {  // k . q
+        float d = 0.f;
+        for (int i = t; i < DK; i += 32) d += sk[i] * sq[i];
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) d += __shfl_xor_sync(0xffffffffu, d, o);
+        if (t == 0) s_qk = d;
+    }
+
+    float4 pv = make_float4(0.f, 0.f, 0.f, 0.f), pp = pv;
+#pragma unroll
+    for (int m = 0; m < RPT; ++m) {
+        const int i = rg * RPT + m;
+        const float ak = sa[i] * sk[i], aq = sa[i] * sq[i];
+        pv.x += ak * s[m].x; pv.y += ak * s[m].y; pv.z += ak * s[m].z; pv.w += ak * s[m].w;
+        pp.x += aq * s[m].x; pp.y += aq * s[m].y; pp.z += aq * s[m].z; pp.w += aq * s[m].w;
+    }
+    *reinterpret_cast<float4 *>(&red_v[rg][4 * cg]) = pv;
+    *reinterpret_cast<float4 *>(&red_p[rg][4 * cg]) = pp;
+    __syncthreads();
+
+    Tin *out = static_cast<Tin *>(a.out) + row * DV;
+    for (int j = t; j < DV; j += kDecodeThreads) {
+        float vh = 0.f, p = 0.f;
+#pragma unroll
+        for (int r = 0; r < RG; ++r) { vh += red_v[r][j]; p += red_p[r][j]; }
+        const float e = sv[j] - vh;
+        se[j] = e;
+        out[j] = from_f<Tin>(p + beta * s_qk * e);
+    }
+    __syncthreads();
+
+    const float4 e4 = *reinterpret_cast<const float4 *>(&se[4 * cg]);
+#pragma unroll
+    for (int m = 0; m < RPT; ++m) {
+        const int i = rg * RPT + m;
+        const float al = sa[i], bk = beta * sk[i];
+        float4 o;
+        o.x = al * s[m].x + bk * e4.x;
+        o.y = al * s[m].y + bk * e4.y;
+        o.z = al * s[m].z + bk * e4.z;
+        o.w = al * s[m].w + bk * e4.w;
+        __stcs(reinterpret_cast<float4 *>(S + i * DV) + cg, o);
+    }
+}
+
+template <typename Tin, int DK, int DV>
+cudaError_t launch_decode_t(const DecodeArgs &a, cudaStream_t st) {
+    const int64_t units = (int64_t)a.rows * a.heads;
+    if (units > 0x7fffffffLL) return cudaErrorInvalidValue;
+    kda_recurrent_step_kernel<Tin, DK, DV><<<(unsigned)units, kDecodeThreads, 0, st>>>(a);
+    return cudaGetLastError();
+}
+
+template <typename Tin>
+cudaError_t launch_decode_d(const DecodeArgs &a, int dk, int dv, cudaStream_t st) {
+    if (dk == 128 && dv == 128) return launch_decode_t<Tin, 128, 128>(a, st);
+    if (dk == 128 && dv == 64) return launch_decode_t<Tin, 128, 64>(a, st);
+    if (dk == 64 && dv == 128) return launch_decode_t<Tin, 64, 128>(a, st);
+    if (dk == 64 && dv == 64) return launch_decode_t<Tin, 64, 64>(a, st);
+    return cudaErrorInvalidValue;
+}
+
+}  // namespace
+
+cudaError_t launch_decode(const DecodeArgs &a, int dk, int dv, kda_dtype_t dt, cudaStream_t st) {
+    return dt == KDA_F32 ? launch_decode_d<float>(a, dk, dv, st)
+                         : launch_decode_d<__nv_bfloat16>(a, dk, dv, st);
+}
+
+}  // namespace kda

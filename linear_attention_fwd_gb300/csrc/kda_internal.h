@@ -1,0 +1,68 @@
+// Internal declarations shared by libkda's translation units.
+#pragma once
+
+#include <cstdint>
+#include <cuda_runtime.h>
+#include <cuda_bf16.h>
+
+#include "../../include/kda.h"
+
+namespace kda {
+
+// Chunk length and sub-tile length of the chunkwise form.  A 16-token sub-tile
+// keeps every decay factor the kernels form inside [e^-80, e^80] under g >= -5.
+constexpr int kChunk = 64;
+constexpr int kSub = 16;
+
+struct ChunkArgs {
+    const void *q, *k, *v, *g, *beta;
+    const float *s0;          // [N, H, dk, dv] or nullptr
+    const int32_t *cu;        // [N + 1] or nullptr (dense)
+    void *out;
+    float *sT;                // [N, H, dk, dv] or nullptr
+    int64_t seqlen;           // tokens per dense row, or total packed tokens
+    int32_t num_seqs;         // N
+    int32_t heads;            // H
+};
+
+struct DecodeArgs {
+    const void *q, *k, *v, *g, *beta;
+    float *state;
+    const int32_t *idx;       // [N] or nullptr
+    void *out;
+    int32_t rows;             // N
+    int32_t slots;            // pool size
+    int32_t heads;
+};
+
+// Token range [bos, eos) of sequence n, read on the device and clamped so that
+// a malformed offsets array can never index outside the packed tensors.
+__device__ __forceinline__ void seq_range(const ChunkArgs &a, int n, int64_t &bos, int64_t &eos) {
+    if (a.cu == nullptr) {
+        bos = (int64_t)n * a.seqlen;
+        eos = bos + a.seqlen;
+    } else {
+        int64_t b = __ldg(a.cu + n), e = __ldg(a.cu + n + 1);
+        b = b < 0 ? 0 : (b > a.seqlen ? a.seqlen : b);
+        e = e < b ? b : (e > a.seqlen ? a.seqlen : e);
+        bos = b;
+        eos = e;
+    }
+}
+
+template <typename T> __device__ __forceinline__ float to_f(T x);
+template <> __device__ __forceinline__ float to_f<float>(float x) { return x; }
+template <> __device__ __forceinline__ float to_f<__nv_bfloat16>(__nv_bfloat16 x) { return __bfloat162float(x); }
+
+template <typename T> __device__ __forceinline__ T from_f(float x);
+template <> __device__ __forceinline__ float from_f<float>(float x) { return x; }
+template <> __device__ __forceinline__ __nv_bfloat16 from_f<__nv_bfloat16>(float x) { return __float2bfloat16_rn(x); }
+
+// Launchers (host).  Each returns cudaSuccess or the launch error.
+cudaError_t launch_chunk_simt(const ChunkArgs &a, int dk, int dv, kda_dtype_t dt, cudaStream_t s);
+cudaError_t launch_chunk_tc(const ChunkArgs &a, int dk, int dv, kda_dtype_t dt, cudaStream_t s);
+bool chunk_tc_supported(int dk, int dv, kda_dtype_t dt);
+cudaError_t launch_decode(const DecodeArgs &a, int dk, int dv, kda_dtype_t dt, cudaStream_t s);
+cudaError_t launch_state_copy(const ChunkArgs &a, int dk, int dv, cudaStream_t s);
+
+}  // namespace kda

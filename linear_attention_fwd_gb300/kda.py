@@ -1,0 +1,171 @@
+"""ctypes binding of libkda (include/kda.h): argument marshalling only.
+
+Every computation runs in libkda's CUDA kernels; this module only checks
+tensor metadata, fills ``kda_dims_t`` and passes device pointers and the
+current CUDA stream.  There is no fallback: if ``libkda.so`` has not been built
+the first call raises.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+import torch
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "libkda.so")
+
+KDA_OK, KDA_ERR_NULL, KDA_ERR_SHAPE, KDA_ERR_UNSUPPORTED = 0, 1, 2, 3
+KDA_ERR_ALIGN, KDA_ERR_WORKSPACE, KDA_ERR_CUDA, KDA_ERR_TIMEOUT = 4, 5, 6, 7
+KDA_F32, KDA_BF16 = 0, 1
+IMPLS = {"auto": 0, "simt": 1, "tc": 2}
+IMPL_NAMES = {v: k for k, v in IMPLS.items()}
+
+# every symbol include/kda.h declares
+EXPORTED = ("kda_chunk_fwd", "kda_chunk_fwd_with", "kda_chunk_fwd_selected_impl",
+            "kda_recurrent_step", "kda_status_string")
+
+
+class KdaDims(ctypes.Structure):
+    _fields_ = [("batch", ctypes.c_int32), ("seqlen", ctypes.c_int32),
+                ("num_seqs", ctypes.c_int32), ("heads", ctypes.c_int32),
+                ("dk", ctypes.c_int32), ("dv", ctypes.c_int32), ("dtype", ctypes.c_int32)]
+
+
+class KdaError(RuntimeError):
+    def __init__(self, status: int, where: str):
+        self.status = status
+        super().__init__(f"{where}: {kda_status_string(status)} (status {status})")
+
+
+_lib = None
+
+
+def lib() -> ctypes.CDLL:
+    """Load libkda.so (built in-tree by ``linear_attention_fwd_gb300.build``)."""
+    global _lib
+    if _lib is None:
+        if not os.path.exists(LIB_PATH):
+            raise RuntimeError(f"{LIB_PATH} is missing: build it with "
+                               "`python -c 'import __graft_entry__ as g; g.build()'`")
+        L = ctypes.CDLL(LIB_PATH)
+        vp, dp = ctypes.c_void_p, ctypes.POINTER(KdaDims)
+        L.kda_chunk_fwd.restype = ctypes.c_int
+        L.kda_chunk_fwd.argtypes = [vp] * 9 + [dp, vp]
+        L.kda_chunk_fwd_with.restype = ctypes.c_int
+        L.kda_chunk_fwd_with.argtypes = [ctypes.c_int] + [vp] * 9 + [dp, vp]
+        L.kda_chunk_fwd_selected_impl.restype = ctypes.c_int
+        L.kda_chunk_fwd_selected_impl.argtypes = [dp]
+        L.kda_recurrent_step.restype = ctypes.c_int
+        L.kda_recurrent_step.argtypes = [vp] * 8 + [dp, vp]
+        L.kda_status_string.restype = ctypes.c_char_p
+        L.kda_status_string.argtypes = [ctypes.c_int]
+        _lib = L
+    return _lib
+
+
+def kda_status_string(status: int) -> str:
+    return lib().kda_status_string(int(status)).decode()
+
+
+def _dtype_code(t: torch.dtype) -> int:
+    if t == torch.float32:
+        return KDA_F32
+    if t == torch.bfloat16:
+        return KDA_BF16
+    raise TypeError(f"unsupported dtype {t} (fp32 or bf16)")
+
+
+def _ptr(t):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _stream_handle(stream) -> ctypes.c_void_p:
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return ctypes.c_void_p(stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream))
+
+
+def _check_dev(name, t, device, dtype=None):
+    if t is None:
+        return
+    if not t.is_cuda or t.device != device:
+        raise ValueError(f"{name} must be on {device}")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    if dtype is not None and t.dtype != dtype:
+        raise TypeError(f"{name} must be {dtype}, got {t.dtype}")
+
+
+def chunk_dims(q, v, cu_seqlens=None) -> KdaDims:
+    B, T, H, dk = q.shape
+    dv = v.shape[-1]
+    n = B if cu_seqlens is None else cu_seqlens.numel() - 1
+    return KdaDims(B, T, n, H, dk, dv, _dtype_code(q.dtype))
+
+
+def kda_chunk_fwd(q, k, v, g, beta, initial_state=None, cu_seqlens=None, *, out=None,
+                  final_state=None, output_final_state: bool = True, impl: str = "auto",
+                  stream=None):
+    """Chunkwise KDA forward (prefill / prefix-cache resume) through libkda.
+
+    q, k, g: [B, T, H, dk]; v: [B, T, H, dv]; beta: [B, T, H] (all fp32 or all
+    bf16, CUDA, contiguous).  initial_state: fp32 [N, H, dk, dv] or None.
+    cu_seqlens: int32 [N+1] (packed sequences, B == 1) or None.
+    Returns (out [B, T, H, dv], final_state [N, H, dk, dv] fp32 or None).
+    """
+    dev = q.device
+    for name, t in (("q", q), ("k", k), ("v", v), ("g", g), ("beta", beta)):
+        _check_dev(name, t, dev, q.dtype)
+    _check_dev("initial_state", initial_state, dev, torch.float32)
+    _check_dev("cu_seqlens", cu_seqlens, dev, torch.int32)
+    B, T, H, dk = q.shape
+    dv = v.shape[-1]
+    if k.shape != q.shape or g.shape != q.shape or v.shape[:3] != q.shape[:3] \
+            or beta.shape != q.shape[:3]:
+        raise ValueError("inconsistent q/k/v/g/beta shapes")
+    dims = chunk_dims(q, v, cu_seqlens)
+    if out is None:
+        out = torch.empty((B, T, H, dv), dtype=q.dtype, device=dev)
+    _check_dev("out", out, dev, q.dtype)
+    if final_state is None and output_final_state:
+        final_state = torch.empty((dims.num_seqs, H, dk, dv), dtype=torch.float32, device=dev)
+    _check_dev("final_state", final_state, dev, torch.float32)
+    st = lib().kda_chunk_fwd_with(IMPLS[impl], _ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta),
+                                  _ptr(initial_state), _ptr(cu_seqlens), _ptr(out),
+                                  _ptr(final_state), ctypes.byref(dims), _stream_handle(stream))
+    if st != KDA_OK:
+        raise KdaError(st, "kda_chunk_fwd")
+    return out, final_state
+
+
+def kda_chunk_fwd_selected_impl(q, v, cu_seqlens=None) -> str:
+    code = lib().kda_chunk_fwd_selected_impl(ctypes.byref(chunk_dims(q, v, cu_seqlens)))
+    return IMPL_NAMES.get(code, "invalid")
+
+
+def kda_recurrent_step(q, k, v, g, beta, state, state_indices=None, *, out=None, stream=None):
+    """One decode token per row through libkda; ``state`` is updated in place.
+
+    q, k, g: [N, H, dk]; v: [N, H, dv]; beta: [N, H]; state: fp32 [P, H, dk, dv];
+    state_indices: int32 [N] or None.  Returns out [N, H, dv].
+    """
+    dev = q.device
+    for name, t in (("q", q), ("k", k), ("v", v), ("g", g), ("beta", beta)):
+        _check_dev(name, t, dev, q.dtype)
+    _check_dev("state", state, dev, torch.float32)
+    _check_dev("state_indices", state_indices, dev, torch.int32)
+    N, H, dk = q.shape
+    dv = v.shape[-1]
+    if state.shape[1:] != (H, dk, dv):
+        raise ValueError("state must be [P, H, dk, dv]")
+    dims = KdaDims(N, 1, state.shape[0], H, dk, dv, _dtype_code(q.dtype))
+    if out is None:
+        out = torch.empty((N, H, dv), dtype=q.dtype, device=dev)
+    _check_dev("out", out, dev, q.dtype)
+    st = lib().kda_recurrent_step(_ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta), _ptr(state),
+                                  _ptr(state_indices), _ptr(out), ctypes.byref(dims),
+                                  _stream_handle(stream))
+    if st != KDA_OK:
+        raise KdaError(st, "kda_recurrent_step")
+    return out

@@ -1,0 +1,124 @@
+"""libkda loads without a GPU, exports every symbol include/kda.h declares, and
+rejects bad arguments on the host before anything is launched.
+
+None of these calls reaches a kernel: each one fails validation first, so they
+run on a machine without a GPU (the pointers are never dereferenced).
+"""
+import ctypes
+import os
+import re
+
+import pytest
+
+from linear_attention_fwd_gb300 import build as kbuild
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "kda.h")
+
+
+@pytest.fixture(scope="module")
+def K():
+    kbuild.build()
+    from linear_attention_fwd_gb300 import kda
+    kda.lib()
+    return kda
+
+
+def declared_functions():
+    src = open(HEADER).read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    return sorted(set(re.findall(r"\b(kda_[a-z_]+)\s*\(", src)))
+
+
+def test_every_declared_symbol_is_exported(K):
+    names = declared_functions()
+    assert set(names) == set(K.EXPORTED), names
+    for n in names:
+        assert hasattr(K.lib(), n), n
+
+
+def test_status_strings(K):
+    for code in range(8):
+        s = K.kda_status_string(code)
+        assert s and s != "unknown status"
+    assert K.kda_status_string(99) == "unknown status"
+
+
+FAKE = 1 << 20          # 16-byte aligned, never dereferenced (validation fails first)
+
+
+def dims(**kw):
+    from linear_attention_fwd_gb300.kda import KdaDims
+    d = dict(batch=2, seqlen=100, num_seqs=2, heads=4, dk=128, dv=128, dtype=1)
+    d.update(kw)
+    return KdaDims(**d)
+
+
+def call_chunk(K, d, impl=0, q=FAKE, k=FAKE, v=FAKE, g=FAKE, beta=FAKE, s0=None, cu=None,
+               out=FAKE, sT=None):
+    vp = ctypes.c_void_p
+    args = [vp(x) if x is not None else None for x in (q, k, v, g, beta, s0, cu, out, sT)]
+    dp = ctypes.byref(d) if d is not None else None
+    return K.lib().kda_chunk_fwd_with(impl, *args, dp, None)
+
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(dk=96), 3), (dict(dv=32), 3), (dict(dtype=7), 3),
+    (dict(heads=0), 2), (dict(batch=0), 2), (dict(seqlen=-1), 2), (dict(num_seqs=3), 2),
+])
+def test_chunk_rejects_bad_dims(K, kw, code):
+    assert call_chunk(K, dims(**kw)) == code
+
+
+def test_chunk_rejects_null_and_misaligned(K):
+    assert call_chunk(K, None) == K.KDA_ERR_NULL
+    assert call_chunk(K, dims(), q=None) == K.KDA_ERR_NULL
+    assert call_chunk(K, dims(), out=None) == K.KDA_ERR_NULL
+    assert call_chunk(K, dims(), v=FAKE + 8) == K.KDA_ERR_ALIGN
+    assert call_chunk(K, dims(), s0=FAKE + 4) == K.KDA_ERR_ALIGN
+    assert call_chunk(K, dims(), beta=FAKE + 1) == K.KDA_ERR_ALIGN
+    # packed sequences need batch == 1
+    assert call_chunk(K, dims(batch=2, num_seqs=5), cu=FAKE) == K.KDA_ERR_SHAPE
+    # partially overlapping initial / final states
+    assert call_chunk(K, dims(), s0=FAKE, sT=FAKE + 4096) == K.KDA_ERR_SHAPE
+    # unknown kernel choice
+    assert call_chunk(K, dims(), impl=9) == K.KDA_ERR_UNSUPPORTED
+
+
+def test_tc_kernel_refuses_shapes_it_does_not_cover(K):
+    assert call_chunk(K, dims(dtype=0), impl=2) == K.KDA_ERR_UNSUPPORTED
+    assert call_chunk(K, dims(dk=64, dv=64), impl=2) == K.KDA_ERR_UNSUPPORTED
+
+
+def test_selected_impl(K):
+    sel = K.lib().kda_chunk_fwd_selected_impl
+    assert sel(ctypes.byref(dims(dtype=0))) == 1           # fp32 -> SIMT kernel
+    assert sel(ctypes.byref(dims(dk=64, dv=64))) == 1
+    assert sel(ctypes.byref(dims(dk=96))) == -1
+    assert sel(ctypes.byref(dims())) in (1, 2)
+
+
+def call_step(K, d, q=FAKE, state=FAKE, idx=None, beta=FAKE, out=FAKE):
+    vp = ctypes.c_void_p
+    a = [vp(x) if x is not None else None for x in (q, FAKE, FAKE, FAKE, beta, state, idx, out)]
+    return K.lib().kda_recurrent_step(*a, ctypes.byref(d) if d is not None else None, None)
+
+
+def test_recurrent_step_validation(K):
+    d1 = lambda **kw: dims(**{**dict(batch=8, seqlen=1, num_seqs=8), **kw})
+    assert call_step(K, None) == K.KDA_ERR_NULL
+    assert call_step(K, d1(seqlen=2)) == K.KDA_ERR_SHAPE
+    assert call_step(K, d1(num_seqs=4)) == K.KDA_ERR_SHAPE     # pool smaller than rows
+    assert call_step(K, d1(dk=48)) == K.KDA_ERR_UNSUPPORTED
+    assert call_step(K, d1(), state=None) == K.KDA_ERR_NULL
+    assert call_step(K, d1(), q=FAKE + 2) == K.KDA_ERR_ALIGN
+    assert call_step(K, d1(), idx=FAKE + 2) == K.KDA_ERR_ALIGN
+    assert call_step(K, d1(batch=0)) == K.KDA_OK                # no rows: nothing to do
+
+
+def test_binding_fails_loudly_without_library(monkeypatch, tmp_path):
+    from linear_attention_fwd_gb300 import kda
+    monkeypatch.setattr(kda, "_lib", None)
+    monkeypatch.setattr(kda, "LIB_PATH", str(tmp_path / "missing.so"))
+    with pytest.raises(RuntimeError, match="missing"):
+        kda.lib()
