@@ -15,7 +15,7 @@ import torch
 import oracle
 from linear_attention_fwd_gb300 import inputs
 from tests.helpers import rel_max_err
-from tests.parity import compare_prefill, f64
+from tests.parity import bf16_floor, check_prefill, compare_prefill, f64, out_bar
 
 pytestmark = pytest.mark.gpu
 
@@ -35,7 +35,7 @@ def _prefill(K, name, heads):
     assert torch.isfinite(out).all() and torch.isfinite(sT).all()
     res = compare_prefill(inp, out, sT, heads=heads)
     print(name, res)
-    assert res["out"] <= 2e-2 and res["state"] <= 2e-2, res
+    check_prefill(res, torch.bfloat16)
 
 
 def test_prefill_b4_h32_t8192(K):
@@ -69,5 +69,6 @@ def test_decode_n256_h64_1000_steps(K):
         sl = lambda t: t[:, n, h][None, :, None]
         ro, rs = oracle.forward(sl(inp["q"]), sl(inp["k"]), sl(inp["v"]), sl(inp["g"]),
                                 inp["beta"][:, n, h][None, :, None], s0[n, h][None, None])
-        assert rel_max_err(f64(outs[:, n, h]), ro[0, :, 0]) <= 2e-2
+        assert rel_max_err(f64(outs[:, n, h]), ro[0, :, 0]) <= out_bar(torch.bfloat16,
+                                                                       bf16_floor(ro[0, :, 0]))
         assert rel_max_err(f64(state[n, h]), rs[0, 0]) <= 2e-2

@@ -12,7 +12,7 @@ import torch
 import oracle
 from linear_attention_fwd_gb300 import inputs
 from tests.helpers import rel_max_err
-from tests.parity import TOL, compare_prefill, f64
+from tests.parity import TOL, bf16_floor, check_prefill, compare_prefill, f64, out_bar
 
 pytestmark = pytest.mark.gpu
 
@@ -42,10 +42,7 @@ def run(K, inp, impl="auto", with_state=True):
 
 
 def check(res, dtype):
-    tol = TOL[dtype]
-    assert res["out"] <= tol, res
-    if "state" in res:
-        assert res["state"] <= tol, res
+    check_prefill(res, dtype)
 
 
 # --------------------------------------------------------------------------- small, exhaustive
@@ -93,7 +90,10 @@ def test_decay_bound_extreme(K):
         for impl in impls_for(K, dtype, d):
             inp = inputs.make_prefill(batch=1, seqlen=512, heads=2, dk=d, dv=d, dtype=dtype,
                                       device="cuda", seed=9, g_mode="near_bound", init_state=True)
-            assert torch.all(inp["g"] == -5.0)
+            if dtype == torch.bfloat16:      # -5 + 0.01 U(0,1) rounds to exactly -5 in bf16
+                assert torch.all(inp["g"] == -5.0)
+            else:
+                assert inp["g"].min() >= -5.0 and inp["g"].max() <= -4.99
             out, sT = run(K, inp, impl)
             res = compare_prefill(inp, out, sT)
             check(res, dtype)
@@ -115,9 +115,11 @@ def test_inplace_resume_and_split_invariance(K):
                             state, None, final_state=state)
     o2, _ = K.kda_chunk_fwd(second["q"], second["k"], second["v"], second["g"], second["beta"],
                             state, None, final_state=state)
-    ref_o = f64(full_out)
-    assert rel_max_err(f64(torch.cat([o1, o2], 1)), ref_o) <= 2e-2
-    assert rel_max_err(f64(state), f64(full_S)) <= 2e-2
+    # the carried fp32 state matches the one-shot run to fp32 round-off
+    assert rel_max_err(f64(state), f64(full_S)) <= 1e-5
+    # outputs differ from the one-shot run by at most one bf16 ulp
+    torch.testing.assert_close(torch.cat([o1, o2], 1).float(), full_out.float(),
+                               rtol=2.0 ** -7, atol=1e-6)
     # and both halves agree with the oracle run over the whole sequence
     check(compare_prefill(inp, torch.cat([o1, o2], 1), state), dtype)
 
@@ -164,7 +166,8 @@ def test_recurrent_step_multi_step(K, dtype, d):
         a = {kk: ins[kk][s].contiguous() for kk in ins}
         o = K.kda_recurrent_step(a["q"], a["k"], a["v"], a["g"], a["beta"], st, idx)
         ro = oracle.decode_step(a["q"], a["k"], a["v"], a["g"], a["beta"], pool, idx.cpu())
-        assert rel_max_err(f64(o), ro) <= TOL[dtype]
+        floor = bf16_floor(ro) if dtype == torch.bfloat16 else 0.0
+        assert rel_max_err(f64(o), ro) <= out_bar(dtype, floor)
     assert rel_max_err(f64(st), pool) <= TOL[dtype]
     torch.testing.assert_close(st[[1, 3, 6]], inputs.make_decode_state(
         num_slots=P, heads=H, dk=d, dv=d, device="cuda", seed=11)[[1, 3, 6]], rtol=0, atol=0)
