@@ -1,14 +1,745 @@
 // KDA chunkwise forward on the sm_103a tensor cores (tcgen05 + TMEM + TMA).
+//
+// bf16 inputs/outputs, d_k = d_v = 128, chunk C = 64, fp32 recurrent state.
+// One CTA (8 warps) per (sequence, head); the fp32 state lives in tensor
+// memory for the whole sequence (transposed: TMEM lane j = value channel,
+// column i = key channel), so the only HBM traffic is the q/k/v/g/beta tiles,
+// the output, and the initial / final states.
+//
+// Chunk algebra ("はじめての自然言語処理 -- Kimi K3" section 3.1: chunkwise form,
+// Tril intra-chunk term, decay folded into q times Gamma and k over Gamma as in
+// the report's equation (4), 16-token tiles made dense by the g >= -5 bound):
+//   per 16-token sub-tile I with reference b_I = gamma before its start,
+//     x = e^{gamma - b_I} in [e^-80, 1],  Q~ = Q x,  K~ = K x,  K^ = K / x;
+//   A_rs = beta_r (K~ K^^T)_rs * (e^{b_I - b_J} per channel, J < I),  s <  r
+//   M_rs =        (Q~ K^^T)_rs * (same), s < r;   M_rr = q_r . k_r (exact)
+//   T' = (I + A)^-1 diag(beta),  W = T' Kbar,  U~ = T' V,
+//   U = U~ - W S,  O = Qbar S + M U,  S <- Diag(e^{gamma_last}) S + Kp^T U.
+//
+// Operand precision: the sub-tile-scaled operands of A and M span
+// [e^-80, e^80] and are bf16 (the range the decay bound was chosen for); every
+// other tensor-core operand (S, U, W, T, Qbar, Kp, beta V, M) is O(1) and is
+// rounded to fp16 for 3 more mantissa bits; accumulation is fp32 throughout.
+//
+// Per chunk:
+//   TMA       Q, K, V, G tiles (64 x 128 bf16, 128-byte swizzle) -> smem
+//   SIMT      sub-tile cumulative decay, x and 1/x, scaled operands
+//   mma.sync  A and M as 16x16 sub-tile products (the per-pair decay factor is
+//             applied to the B fragments in registers)
+//   SIMT      blocked forward-substitution inverse T = (I + A)^-1
+//   mma.sync  W = T' Kbar;   tcgen05: U~^T = V^T T'^T into TMEM
+//   tcgen05   U^T = U~^T - S^T W^T,  O^T = S^T Qbar^T;  then  O^T += U^T M^T,
+//             S^T <- S^T Diag(dec) + U^T Kp  (accumulated in TMEM)
+#include <cuda.h>
+#include <cudaTypedefs.h>
+#include <cuda_bf16.h>
 #include <cuda_runtime.h>
 
 #include "kda_internal.h"
+#include "tc_ptx.cuh"
 
 namespace kda {
 
-bool chunk_tc_supported(int, int, kda_dtype_t) { return false; }
+__device__ unsigned int g_kda_tc_timeouts = 0;
 
-cudaError_t launch_chunk_tc(const ChunkArgs &, int, int, kda_dtype_t, cudaStream_t) {
-    return cudaErrorNotSupported;
+namespace {
+
+using namespace ptx;
+
+constexpr int C = 64;         // chunk
+constexpr int D = 128;        // d_k = d_v
+constexpr int NT = 256;       // threads
+constexpr float LOG2E = 1.4426950408889634f;
+
+// 2^x on the special-function unit (flushes results below 2^-126 to zero,
+// which only removes contributions under 1e-38 of an O(1) result).
+__device__ __forceinline__ float ex2(float x) {
+    float y;
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
+
+// shared memory map, byte offsets from a 1024-aligned base
+constexpr uint32_t OFF_Q = 0;          // Q -> Q~ -> Qbar        [64 r][128 i]  swizzled
+constexpr uint32_t OFF_K = 16384;      // K -> K~ -> beta Kbar   [64 r][128 i]
+constexpr uint32_t OFF_V = 32768;      // V                      [64 r][128 j]
+constexpr uint32_t OFF_G = 49152;      // G -> K^hi (bf16) -> V^T (fp16) [128 j][64 s]
+constexpr uint32_t OFF_SST = 65536;    // S^T fp16 [128 j][128 i]; Q~hi, K~ bf16 during the prologue
+constexpr uint32_t OFF_UST = 98304;    // U^T fp16 [128 j][64 r]; Q~lo bf16 during the prologue
+constexpr uint32_t OFF_WT = 114688;    // -W fp16 [64 r][128 i]; K^lo bf16 in the prologue; U^T lo
+constexpr uint32_t OFF_KPT = 131072;   // Kp^T fp16              [128 i][64 r]
+constexpr uint32_t OFF_MT = 147456;    // M fp16                 [64 r][64 s]
+constexpr uint32_t OFF_TT = 155648;    // T fp16                 [64 r][64 s]
+constexpr uint32_t OFF_AF = 163840;    // A (fp32) -> O staging (bf16 [64 r][128 j])
+constexpr int LDA = 72;
+constexpr uint32_t OFF_TD = OFF_AF + 64 * LDA * 4;      // T dense fp32 [64][LDT]
+constexpr int LDT = 68;
+constexpr uint32_t OFF_XS = OFF_TD + 64 * LDT * 4;      // inverse scratch [3][16][16] fp32
+constexpr uint32_t OFF_TOT = OFF_XS + 3 * 256 * 4;      // sub-tile log2-decay totals [4][128]
+constexpr uint32_t OFF_EB = OFF_TOT + 4 * 128 * 4;      // e^{b_I}          [4][128]
+constexpr uint32_t OFF_EL = OFF_EB + 4 * 128 * 4;       // e^{gl - b_I}     [4][128]
+constexpr uint32_t OFF_W6 = OFF_EL + 4 * 128 * 4;       // e^{b_I - b_J}    [6][128] bf16
+constexpr uint32_t OFF_DEC = OFF_W6 + 6 * 128 * 2;      // e^{gl}           [128]
+constexpr uint32_t OFF_BETA = OFF_DEC + 128 * 4;        // beta             [64]
+constexpr uint32_t OFF_MRR = OFF_BETA + 64 * 4;         // q_r . k_r        [64]
+constexpr uint32_t OFF_MLO = (OFF_MRR + 64 * 4 + 1023) / 1024 * 1024;   // M - fp16(M), fp16 [64 r][64 s]
+constexpr uint32_t OFF_BAR = OFF_MLO + 8192;            // 2 mbarriers, TMEM address
+constexpr uint32_t SMEM_USED = OFF_BAR + 64;
+constexpr uint32_t SMEM_BYTES = SMEM_USED + 1024;       // + alignment slack
+static_assert(SMEM_BYTES <= 227 * 1024, "shared memory budget");
+static_assert(OFF_AF % 16 == 0 && OFF_TD % 16 == 0 && OFF_MLO % 1024 == 0 && OFF_BAR % 8 == 0, "alignment");
+
+// tensor memory columns (fp32, 128 lanes)
+constexpr uint32_t TM_S = 0;     // S^T            128 columns
+constexpr uint32_t TM_U = 128;   // U~^T -> U^T     64 columns
+constexpr uint32_t TM_O = 192;   // O^T             64 columns
+constexpr uint32_t TM_COLS = 256;
+
+constexpr uint32_t IDESC_N64 = idesc_f16_f32(128, 64);
+constexpr uint32_t IDESC_N128 = idesc_f16_f32(128, 128);
+
+// Byte offset of element (row, col) in a 128-byte-swizzled K-major tile of
+// `rows` rows whose columns are split into 64-element halves.
+__device__ __forceinline__ uint32_t sw(int row, int col, int rows) {
+    return (uint32_t)((col >> 6) * rows * 128 + row * 128 + ((((col & 63) >> 3) ^ (row & 7)) << 4) +
+                      ((col & 7) << 1));
+}
+
+__device__ __forceinline__ int pair_index(int I, int J) { return I * (I - 1) / 2 + J; }
+
+// Longest packed sequences first (the hardware dispatches low block indices
+// first); dense batches and large sequence counts keep their natural order.
+__device__ __forceinline__ void select_unit(const ChunkArgs &a, int b, int &n, int &h) {
+    __shared__ int s_pick;
+    const int H = a.heads;
+    h = b % H;
+    const int r = b / H;
+    n = r;
+    if (a.cu == nullptr || a.num_seqs > NT) return;
+    if (threadIdx.x == 0) s_pick = r;
+    __syncthreads();
+    const int t = threadIdx.x;
+    if (t < a.num_seqs) {
+        int64_t b0, e0;
+        seq_range(a, t, b0, e0);
+        const int64_t lt = e0 - b0;
+        int rank = 0;
+        for (int s = 0; s < a.num_seqs; ++s) {
+            int64_t bs, es;
+            seq_range(a, s, bs, es);
+            const int64_t ls = es - bs;
+            rank += (ls > lt) || (ls == lt && s < t);
+        }
+        if (rank == r) s_pick = t;
+    }
+    __syncthreads();
+    n = s_pick;
+}
+
+__device__ __forceinline__ void tma_tile(const CUtensorMap *map, uint32_t dst, uint32_t bar, int h,
+                                         int64_t tok) {
+    tma_load_3d(dst, map, bar, 0, h, (int)tok);
+    tma_load_3d(dst + 8192, map, bar, 64, h, (int)tok);
+}
+
+__global__ void __launch_bounds__(NT, 1)
+kda_chunk_tc_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant__ CUtensorMap tmk,
+                    const __grid_constant__ CUtensorMap tmv, const __grid_constant__ CUtensorMap tmg,
+                    const ChunkArgs a, const uint32_t wait_limit) {
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t *sm = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    const uint32_t sb = smem_u32(sm);
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int H = a.heads;
+
+    int n, h;
+    select_unit(a, blockIdx.x, n, h);
+    int64_t bos, eos;
+    seq_range(a, n, bos, eos);
+    const int64_t len = eos - bos;
+    const int nchunks = (int)((len + C - 1) / C);
+
+    const uint32_t bar_tma = sb + OFF_BAR, bar_mma = sb + OFF_BAR + 8;
+    volatile uint32_t *tmem_holder = reinterpret_cast<volatile uint32_t *>(sm + OFF_BAR + 16);
+    float *AF = reinterpret_cast<float *>(sm + OFF_AF);
+    float *TOT = reinterpret_cast<float *>(sm + OFF_TOT);
+    float *EB = reinterpret_cast<float *>(sm + OFF_EB);
+    float *EL = reinterpret_cast<float *>(sm + OFF_EL);
+    __nv_bfloat16 *W6 = reinterpret_cast<__nv_bfloat16 *>(sm + OFF_W6);
+    float *DEC = reinterpret_cast<float *>(sm + OFF_DEC);
+    float *BETA = reinterpret_cast<float *>(sm + OFF_BETA);
+    const __nv_bfloat16 *beta = static_cast<const __nv_bfloat16 *>(a.beta);
+    __nv_bfloat16 *out = static_cast<__nv_bfloat16 *>(a.out);
+
+    if (tid == 0) {
+        mbar_init(bar_tma, 1);
+        mbar_init(bar_mma, 1);
+        fence_mbar_init();
+        prefetch_tmap(&tmq);
+        prefetch_tmap(&tmk);
+        prefetch_tmap(&tmv);
+        prefetch_tmap(&tmg);
+    }
+    if (warp == 0) {
+        tmem_alloc(sb + OFF_BAR + 16, TM_COLS);
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *tmem_holder;
+    const uint32_t trow = tmem + ((uint32_t)((warp & 3) * 32) << 16);   // this warp's TMEM lanes
+
+    // ---- initial state -> TMEM (S^T: lane j, column i); warp w owns lanes 32(w%4).., columns 64(w/4)..
+    const int64_t sbase = ((int64_t)n * H + h) * D * D;
+    const int jl = 32 * (warp & 3) + lane;   // this thread's TMEM lane (value channel j)
+    const int half = warp >> 2;              // which half of the columns this warp handles
+    {
+#pragma unroll 1
+        for (int g2 = 0; g2 < 2; ++g2) {
+            const int i0 = 64 * half + 32 * g2;
+            float v[32];
+#pragma unroll
+            for (int c = 0; c < 32; ++c)
+                v[c] = a.s0 ? a.s0[sbase + (int64_t)(i0 + c) * D + jl] : 0.f;
+            tmem_st32(trow + TM_S + i0, v);
+        }
+    }
+    if (tid == 0 && nchunks > 0) {
+        mbar_arrive_expect_tx(bar_tma, 4 * 16384);
+        tma_tile(&tmq, sb + OFF_Q, bar_tma, h, bos);
+        tma_tile(&tmk, sb + OFF_K, bar_tma, h, bos);
+        tma_tile(&tmv, sb + OFF_V, bar_tma, h, bos);
+        tma_tile(&tmg, sb + OFF_G, bar_tma, h, bos);
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+
+    // the blocks of M above the diagonal blocks stay zero for the whole sequence
+    for (int x = tid; x < 64 * 32; x += NT) {
+        const int r = x >> 5, s2 = 2 * (x & 31);
+        if ((s2 >> 4) > (r >> 4)) {
+            *reinterpret_cast<uint32_t *>(sm + OFF_MT + sw(r, s2, 64)) = 0u;
+            *reinterpret_cast<uint32_t *>(sm + OFF_MLO + sw(r, s2, 64)) = 0u;
+        }
+    }
+    float *TD = reinterpret_cast<float *>(sm + OFF_TD);
+    float *MRR = reinterpret_cast<float *>(sm + OFF_MRR);
+    uint32_t tma_phase = 0, mma_phase = 0;
+    bool ok = true;
+    const int cp = tid & 63, blk = tid >> 6;   // elementwise ownership: channel pair, sub-tile
+    const int t4 = lane & 3, g = lane >> 2;    // mma.sync fragment coordinates
+
+#pragma unroll 1
+    for (int ci = 0; ci < nchunks; ++ci) {
+        const int64_t t0 = bos + (int64_t)ci * C;
+        const int nr = (int)(len - (int64_t)ci * C < C ? len - (int64_t)ci * C : C);
+        const bool more = ci + 1 < nchunks;
+
+        if (tid < C) BETA[tid] = tid < nr ? __bfloat162float(beta[(t0 + tid) * H + h]) : 0.f;
+        {
+            const bool got = mbar_wait(bar_tma, tma_phase, wait_limit);
+            tma_phase ^= 1;
+            if (__syncthreads_or(!got)) { ok = false; break; }
+        }
+
+        // ---- (1) q_r . k_r exactly (bf16 x bf16 products are exact in fp32): the raw
+        // diagonal 16x16 blocks of Q K^T on mma.sync, warps 0-3; all warps: sub-tile
+        // log2-decay totals (the local cumulative sums restart at every sub-tile).
+        if (warp < 4) {
+            const int I = warp;
+            float acc[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
+#pragma unroll
+            for (int kk = 0; kk < 8; ++kk) {
+                uint32_t a0, a1, a2, a3, b0, b1, b2, b3;
+                ldsm_x4(sb + OFF_Q + sw(16 * I + (lane & 15), 16 * kk + ((lane >> 4) << 3), 64), a0, a1, a2, a3);
+                ldsm_x4(sb + OFF_K + sw(16 * I + (lane & 7) + ((lane >> 4) << 3), 16 * kk + (((lane >> 3) & 1) << 3), 64),
+                        b0, b1, b2, b3);
+                mma_16816(acc[0], a0, a1, a2, a3, b0, b1);
+                mma_16816(acc[1], a0, a1, a2, a3, b2, b3);
+            }
+            // element (row g + 8hh, col 8nt + 2t4 + e) is diagonal when nt == hh and 2t4 + e == g
+#pragma unroll
+            for (int hh = 0; hh < 2; ++hh)
+#pragma unroll
+                for (int e = 0; e < 2; ++e)
+                    if (2 * t4 + e == g) MRR[16 * I + g + 8 * hh] = acc[hh][2 * hh + e];
+        }
+        {
+            const int c = 2 * cp;
+            float l0 = 0.f, l1 = 0.f;
+#pragma unroll
+            for (int rr = 0; rr < 16; ++rr) {
+                const int r = 16 * blk + rr;
+                const float2 g2 = unpack_bf16(*reinterpret_cast<uint32_t *>(sm + OFF_G + sw(r, c, 64)));
+                if (r < nr) { l0 = fmaf(g2.x, LOG2E, l0); l1 = fmaf(g2.y, LOG2E, l1); }
+            }
+            TOT[blk * 128 + c] = l0;
+            TOT[blk * 128 + c + 1] = l1;
+        }
+        __syncthreads();
+        if (tid < 128) {   // per-channel decay vectors of this chunk (log2 units)
+            const int c = tid;
+            const float b1 = TOT[c], b2 = b1 + TOT[128 + c], b3 = b2 + TOT[256 + c];
+            const float gl = b3 + TOT[384 + c];
+            const float bI[4] = {0.f, b1, b2, b3};
+#pragma unroll
+            for (int I = 0; I < 4; ++I) {
+                EB[I * 128 + c] = ex2(bI[I]);
+                EL[I * 128 + c] = ex2(gl - bI[I]);
+#pragma unroll
+                for (int J = 0; J < I; ++J) W6[pair_index(I, J) * 128 + c] = __float2bfloat16_rn(ex2(bI[I] - bI[J]));
+            }
+            DEC[c] = ex2(gl);
+        }
+        __syncthreads();
+
+        // ---- (2) operands, each rounded from the exact inputs:
+        //   bf16 (range e^+-80): Q~ = Q x as hi + lo (S^T and U^T buffers, idle here),
+        //   K~ = K x, K^ = K / x as hi + lo (over G, and the W buffer);
+        //   fp16: Qbar = Q x e^{b_I} (over Q), Kbar (over K), Kp = K / x e^{gl - b_I} (transposed).
+        {
+            const int c = 2 * cp;
+            const float eb0 = EB[blk * 128 + c], eb1 = EB[blk * 128 + c + 1];
+            const float el0 = EL[blk * 128 + c], el1 = EL[blk * 128 + c + 1];
+            float l0 = 0.f, l1 = 0.f;
+            uint32_t p0[8], p1[8];
+#pragma unroll
+            for (int rr = 0; rr < 16; rr += 2) {
+                float kp[2][2];
+#pragma unroll
+                for (int e = 0; e < 2; ++e) {
+                    const int r = 16 * blk + rr + e;
+                    const uint32_t off = sw(r, c, 64);
+                    float2 q2 = unpack_bf16(*reinterpret_cast<uint32_t *>(sm + OFF_Q + off));
+                    float2 k2 = unpack_bf16(*reinterpret_cast<uint32_t *>(sm + OFF_K + off));
+                    const float2 g2 = unpack_bf16(*reinterpret_cast<uint32_t *>(sm + OFF_G + off));
+                    if (r < nr) { l0 = fmaf(g2.x, LOG2E, l0); l1 = fmaf(g2.y, LOG2E, l1); }
+                    else { q2 = make_float2(0.f, 0.f); k2 = q2; }
+                    const float x0 = ex2(l0), x1 = ex2(l1);
+                    const float y0 = ex2(-l0), y1 = ex2(-l1);
+                    const float qt0 = q2.x * x0, qt1 = q2.y * x1;
+                    const float kh0 = k2.x * y0, kh1 = k2.y * y1;
+                    const uint32_t qh = pack_bf16(qt0, qt1), khh = pack_bf16(kh0, kh1);
+                    const float2 qhf = unpack_bf16(qh), khf = unpack_bf16(khh);
+                    *reinterpret_cast<uint32_t *>(sm + OFF_SST + off) = qh;
+                    *reinterpret_cast<uint32_t *>(sm + OFF_UST + off) = pack_bf16(qt0 - qhf.x, qt1 - qhf.y);
+                    *reinterpret_cast<uint32_t *>(sm + OFF_SST + 16384 + off) = pack_bf16(k2.x * x0, k2.y * x1);
+                    *reinterpret_cast<uint32_t *>(sm + OFF_G + off) = khh;
+                    *reinterpret_cast<uint32_t *>(sm + OFF_WT + off) = pack_bf16(kh0 - khf.x, kh1 - khf.y);
+                    *reinterpret_cast<uint32_t *>(sm + OFF_Q + off) = pack_f16(qt0 * eb0, qt1 * eb1);
+                    *reinterpret_cast<uint32_t *>(sm + OFF_K + off) = pack_f16(k2.x * x0 * eb0, k2.y * x1 * eb1);
+                    kp[e][0] = kh0 * el0;
+                    kp[e][1] = kh1 * el1;
+                }
+                p0[rr / 2] = pack_f16(kp[0][0], kp[1][0]);
+                p1[rr / 2] = pack_f16(kp[0][1], kp[1][1]);
+            }
+            *reinterpret_cast<uint4 *>(sm + OFF_KPT + sw(c, 16 * blk, 128)) = make_uint4(p0[0], p0[1], p0[2], p0[3]);
+            *reinterpret_cast<uint4 *>(sm + OFF_KPT + sw(c, 16 * blk + 8, 128)) = make_uint4(p0[4], p0[5], p0[6], p0[7]);
+            *reinterpret_cast<uint4 *>(sm + OFF_KPT + sw(c + 1, 16 * blk, 128)) = make_uint4(p1[0], p1[1], p1[2], p1[3]);
+            *reinterpret_cast<uint4 *>(sm + OFF_KPT + sw(c + 1, 16 * blk + 8, 128)) = make_uint4(p1[4], p1[5], p1[6], p1[7]);
+        }
+        __syncthreads();
+
+        // ---- (3) A = beta K~ K^T and M = Q~ K^T on the 10 sub-tile pairs (I >= J), spread over
+        // the warps; M is the 3-term product (Q~hi + Q~lo)(K^hi + K^lo)^T less the lo.lo term,
+        // and its diagonal is the exact q_r . k_r.
+#pragma unroll 1
+        for (int pi = warp; pi < 10; pi += 8) {
+            const int I = pi < 4 ? 3 : (pi < 7 ? 2 : (pi < 9 ? 1 : 0));
+            const int J = pi < 4 ? pi : (pi < 7 ? pi - 4 : (pi < 9 ? pi - 7 : 0));
+            float accA[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
+            float accM[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
+            const __nv_bfloat16 *w = W6 + (J < I ? pair_index(I, J) : 0) * 128 + 2 * t4;
+#pragma unroll 2
+            for (int kk = 0; kk < 8; ++kk) {
+                const uint32_t ao = sw(16 * I + (lane & 15), 16 * kk + ((lane >> 4) << 3), 64);
+                const uint32_t bo = sw(16 * J + (lane & 7) + ((lane >> 4) << 3), 16 * kk + (((lane >> 3) & 1) << 3), 64);
+                uint32_t ka[4], qh[4], ql[4], bh[4], bl[4];
+                ldsm_x4(sb + OFF_SST + 16384 + ao, ka[0], ka[1], ka[2], ka[3]);
+                ldsm_x4(sb + OFF_SST + ao, qh[0], qh[1], qh[2], qh[3]);
+                ldsm_x4(sb + OFF_UST + ao, ql[0], ql[1], ql[2], ql[3]);
+                ldsm_x4(sb + OFF_G + bo, bh[0], bh[1], bh[2], bh[3]);
+                ldsm_x4(sb + OFF_WT + bo, bl[0], bl[1], bl[2], bl[3]);
+                if (J < I) {
+                    const uint32_t wlo = *reinterpret_cast<const uint32_t *>(w + 16 * kk);
+                    const uint32_t whi = *reinterpret_cast<const uint32_t *>(w + 16 * kk + 8);
+                    bh[0] = mul_bf16x2(bh[0], wlo); bh[1] = mul_bf16x2(bh[1], whi);
+                    bh[2] = mul_bf16x2(bh[2], wlo); bh[3] = mul_bf16x2(bh[3], whi);
+                    bl[0] = mul_bf16x2(bl[0], wlo); bl[1] = mul_bf16x2(bl[1], whi);
+                    bl[2] = mul_bf16x2(bl[2], wlo); bl[3] = mul_bf16x2(bl[3], whi);
+                }
+#pragma unroll
+                for (int nt = 0; nt < 2; ++nt) {
+                    mma_16816(accA[nt], ka[0], ka[1], ka[2], ka[3], bh[2 * nt], bh[2 * nt + 1]);
+                    mma_16816(accM[nt], qh[0], qh[1], qh[2], qh[3], bh[2 * nt], bh[2 * nt + 1]);
+                    mma_16816(accM[nt], ql[0], ql[1], ql[2], ql[3], bh[2 * nt], bh[2 * nt + 1]);
+                    mma_16816(accM[nt], qh[0], qh[1], qh[2], qh[3], bl[2 * nt], bl[2 * nt + 1]);
+                }
+            }
+#pragma unroll
+            for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+                for (int hh = 0; hh < 2; ++hh) {
+                    const int r = 16 * I + g + 8 * hh;
+                    const int s0 = 16 * J + 8 * nt + 2 * t4;
+                    const float br = BETA[r];
+                    AF[r * LDA + s0] = s0 < r ? br * accA[nt][2 * hh] : 0.f;
+                    AF[r * LDA + s0 + 1] = s0 + 1 < r ? br * accA[nt][2 * hh + 1] : 0.f;
+                    const float m0 = s0 < r ? accM[nt][2 * hh] : (s0 == r ? MRR[r] : 0.f);
+                    const float m1 = s0 + 1 < r ? accM[nt][2 * hh + 1] : (s0 + 1 == r ? MRR[r] : 0.f);
+                    const uint32_t mh = pack_f16(m0, m1);
+                    const float2 mhf = unpack_f16(mh);
+                    *reinterpret_cast<uint32_t *>(sm + OFF_MT + sw(r, s0, 64)) = mh;
+                    *reinterpret_cast<uint32_t *>(sm + OFF_MLO + sw(r, s0, 64)) = pack_f16(m0 - mhf.x, m1 - mhf.y);
+                }
+        }
+        __syncthreads();
+
+        // ---- (4) V^T into the G buffer (bf16 values are exact in fp16); diagonal 16x16 blocks of T = (I + A)^-1 by
+        // forward substitution (threads 0-63, one column each); zero the upper blocks of T.
+        {
+            const int j = 2 * cp;
+            uint32_t p0[8], p1[8];
+#pragma unroll
+            for (int rr = 0; rr < 16; rr += 2) {
+                const int r = 16 * blk + rr;
+                const float2 v0 = unpack_bf16(*reinterpret_cast<uint32_t *>(sm + OFF_V + sw(r, j, 64)));
+                const float2 v1 = unpack_bf16(*reinterpret_cast<uint32_t *>(sm + OFF_V + sw(r + 1, j, 64)));
+                p0[rr / 2] = pack_f16(v0.x, v1.x);
+                p1[rr / 2] = pack_f16(v0.y, v1.y);
+            }
+            *reinterpret_cast<uint4 *>(sm + OFF_G + sw(j, 16 * blk, 128)) = make_uint4(p0[0], p0[1], p0[2], p0[3]);
+            *reinterpret_cast<uint4 *>(sm + OFF_G + sw(j, 16 * blk + 8, 128)) = make_uint4(p0[4], p0[5], p0[6], p0[7]);
+            *reinterpret_cast<uint4 *>(sm + OFF_G + sw(j + 1, 16 * blk, 128)) = make_uint4(p1[0], p1[1], p1[2], p1[3]);
+            *reinterpret_cast<uint4 *>(sm + OFF_G + sw(j + 1, 16 * blk + 8, 128)) = make_uint4(p1[4], p1[5], p1[6], p1[7]);
+        }
+        float tcol[16];
+        if (tid < 64) {
+            const int I = tid >> 4, jj = tid & 15;
+            const float *Ab = AF + (16 * I) * LDA + 16 * I;
+#pragma unroll
+            for (int r = 0; r < 16; ++r) {
+                float acc = 0.f;
+#pragma unroll
+                for (int s2 = 0; s2 < r; ++s2) acc = fmaf(Ab[r * LDA + s2], tcol[s2], acc);
+                tcol[r] = r == jj ? 1.f : (r < jj ? 0.f : -acc);
+            }
+#pragma unroll
+            for (int r = 0; r < 16; ++r) TD[(16 * I + r) * LDT + 16 * I + jj] = tcol[r];
+        } else {
+            // upper blocks (I < J) of T are zero: 6 blocks x 256 entries over 192 threads
+            for (int x = tid - 64; x < 6 * 256; x += NT - 64) {
+                const int bidx = x >> 8, e = x & 255;
+                const int I = bidx < 3 ? 0 : (bidx < 5 ? 1 : 2);
+                const int J = bidx < 3 ? bidx + 1 : (bidx < 5 ? bidx - 1 : 3);
+                TD[(16 * I + (e >> 4)) * LDT + 16 * J + (e & 15)] = 0.f;
+            }
+        }
+        __syncthreads();
+        // ---- (5) off-diagonal blocks by distance d = I - J: T_IJ = -T_II sum_{K=J}^{I-1} A_IK T_KJ
+        {
+            const int rr = tid >> 4, jj = tid & 15;
+            float *X = reinterpret_cast<float *>(sm + OFF_XS);
+#pragma unroll 1
+            for (int d = 1; d < 4; ++d) {
+                const int nb = 4 - d;
+                for (int b = 0; b < nb; ++b) {
+                    const int J = b, I = b + d;
+                    const float *arow = AF + (16 * I + rr) * LDA;
+                    float x = 0.f;
+                    for (int k = 16 * J; k < 16 * I; k += 4) {
+                        const float4 a4 = *reinterpret_cast<const float4 *>(arow + k);
+                        x = fmaf(a4.x, TD[(k + 0) * LDT + 16 * J + jj], x);
+                        x = fmaf(a4.y, TD[(k + 1) * LDT + 16 * J + jj], x);
+                        x = fmaf(a4.z, TD[(k + 2) * LDT + 16 * J + jj], x);
+                        x = fmaf(a4.w, TD[(k + 3) * LDT + 16 * J + jj], x);
+                    }
+                    X[b * 256 + rr * 16 + jj] = x;
+                }
+                __syncthreads();
+                for (int b = 0; b < nb; ++b) {
+                    const int J = b, I = b + d;
+                    const float *trow_ = TD + (16 * I + rr) * LDT + 16 * I;
+                    float t = 0.f;
+#pragma unroll
+                    for (int s2 = 0; s2 < 16; s2 += 4) {
+                        const float4 t4v = *reinterpret_cast<const float4 *>(trow_ + s2);
+                        t = fmaf(t4v.x, X[b * 256 + (s2 + 0) * 16 + jj], t);
+                        t = fmaf(t4v.y, X[b * 256 + (s2 + 1) * 16 + jj], t);
+                        t = fmaf(t4v.z, X[b * 256 + (s2 + 2) * 16 + jj], t);
+                        t = fmaf(t4v.w, X[b * 256 + (s2 + 3) * 16 + jj], t);
+                    }
+                    TD[(16 * I + rr) * LDT + 16 * J + jj] = -t;
+                }
+                __syncthreads();
+            }
+        }
+        // ---- (6) T' = T diag(beta) -> fp16 tile [64 r][64 s]
+        {
+            const int r = tid >> 2, q = tid & 3;
+            const float *src = TD + r * LDT + 16 * q;
+            const float *bq = BETA + 16 * q;
+            uint32_t pk[8];
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+                const float4 t4v = *reinterpret_cast<const float4 *>(src + 4 * e);
+                const float4 b4 = *reinterpret_cast<const float4 *>(bq + 4 * e);
+                pk[2 * e] = pack_f16(t4v.x * b4.x, t4v.y * b4.y);
+                pk[2 * e + 1] = pack_f16(t4v.z * b4.z, t4v.w * b4.w);
+            }
+            *reinterpret_cast<uint4 *>(sm + OFF_TT + sw(r, 16 * q, 64)) = make_uint4(pk[0], pk[1], pk[2], pk[3]);
+            *reinterpret_cast<uint4 *>(sm + OFF_TT + sw(r, 16 * q + 8, 64)) = make_uint4(pk[4], pk[5], pk[6], pk[7]);
+        }
+        fence_async_smem();
+        tc_fence_before();
+        __syncthreads();
+
+        // ---- (7) U~^T = V^T T'^T on tcgen05 (TMEM), W = T' Kbar on mma.sync
+        if (tid == 0) {
+            tc_fence_after();
+#pragma unroll
+            for (int ks = 0; ks < 4; ++ks)
+                mma_f16_ss(tmem + TM_U, sdesc_sw128(sb + OFF_G + ks * 32), sdesc_sw128(sb + OFF_TT + ks * 32),
+                           IDESC_N64, ks > 0);
+        }
+        {
+            const int I = warp & 3, ch = warp >> 2;
+            float acc[8][4];
+#pragma unroll
+            for (int x = 0; x < 8; ++x)
+#pragma unroll
+                for (int e = 0; e < 4; ++e) acc[x][e] = 0.f;
+#pragma unroll
+            for (int kk = 0; kk < 4; ++kk) {
+                uint32_t a0, a1, a2, a3;
+                ldsm_x4(sb + OFF_TT + sw(16 * I + (lane & 15), 16 * kk + ((lane >> 4) << 3), 64), a0, a1, a2, a3);
+#pragma unroll
+                for (int p = 0; p < 4; ++p) {
+                    const int i0 = 64 * ch + 16 * p;
+                    uint32_t b0, b1, b2, b3;
+                    ldsm_x4_t(sb + OFF_K + sw(16 * kk + (lane & 7) + (((lane >> 3) & 1) << 3),
+                                              i0 + ((lane >> 4) << 3), 64),
+                              b0, b1, b2, b3);
+                    mma_16816_f16(acc[2 * p], a0, a1, a2, a3, b0, b1);
+                    mma_16816_f16(acc[2 * p + 1], a0, a1, a2, a3, b2, b3);
+                }
+            }
+#pragma unroll
+            for (int x = 0; x < 8; ++x)
+#pragma unroll
+                for (int hh = 0; hh < 2; ++hh) {
+                    const int r = 16 * I + g + 8 * hh;
+                    const int i = 64 * ch + 8 * x + 2 * t4;
+                    *reinterpret_cast<uint32_t *>(sm + OFF_WT + sw(r, i, 64)) =
+                        pack_f16(-acc[x][2 * hh], -acc[x][2 * hh + 1]);
+                }
+        }
+        fence_async_smem();
+        __syncthreads();
+        if (tid == 0 && more) {   // K and V buffers are free: prefetch the next chunk's tiles
+            fence_async_smem();
+            mbar_arrive_expect_tx(bar_tma, 4 * 16384);
+            tma_tile(&tmk, sb + OFF_K, bar_tma, h, t0 + C);
+            tma_tile(&tmv, sb + OFF_V, bar_tma, h, t0 + C);
+        }
+
+        // ---- state path.  (a) S^T -> fp16 operand; S^T <- S^T Diag(dec) in place
+        {
+#pragma unroll 1
+            for (int g2 = 0; g2 < 2; ++g2) {
+                const int i0 = 64 * half + 32 * g2;
+                float v[32];
+                tmem_ld32(trow + TM_S + i0, v);
+#pragma unroll
+                for (int q8 = 0; q8 < 4; ++q8)
+                    *reinterpret_cast<uint4 *>(sm + OFF_SST + sw(jl, i0 + 8 * q8, 128)) =
+                        make_uint4(pack_f16(v[8 * q8], v[8 * q8 + 1]), pack_f16(v[8 * q8 + 2], v[8 * q8 + 3]),
+                                   pack_f16(v[8 * q8 + 4], v[8 * q8 + 5]), pack_f16(v[8 * q8 + 6], v[8 * q8 + 7]));
+#pragma unroll
+                for (int c = 0; c < 32; c += 4) {
+                    const float4 d4 = *reinterpret_cast<const float4 *>(DEC + i0 + c);
+                    v[c] *= d4.x; v[c + 1] *= d4.y; v[c + 2] *= d4.z; v[c + 3] *= d4.w;
+                }
+                tmem_st32(trow + TM_S + i0, v);
+            }
+        }
+        fence_async_smem();
+        tc_fence_before();
+        __syncthreads();
+        // (b) U^T = U~^T + S^T (-W)^T ;  O^T = S^T Qbar^T
+        if (tid == 0) {
+            tc_fence_after();
+#pragma unroll
+            for (int k = 0; k < 8; ++k)
+                mma_f16_ss(tmem + TM_U, sdesc_sw128(sb + OFF_SST + (k >> 2) * 16384 + (k & 3) * 32),
+                           sdesc_sw128(sb + OFF_WT + (k >> 2) * 8192 + (k & 3) * 32), IDESC_N64, 1);
+#pragma unroll
+            for (int k = 0; k < 8; ++k)
+                mma_f16_ss(tmem + TM_O, sdesc_sw128(sb + OFF_SST + (k >> 2) * 16384 + (k & 3) * 32),
+                           sdesc_sw128(sb + OFF_Q + (k >> 2) * 8192 + (k & 3) * 32), IDESC_N64, k > 0);
+            mma_commit(bar_mma);
+        }
+        {
+            const bool got = mbar_wait(bar_mma, mma_phase, wait_limit);
+            mma_phase ^= 1;
+            if (__syncthreads_or(!got)) { ok = false; break; }
+        }
+        tc_fence_after();
+        if (tid == 0 && more) {   // Q and G buffers are free now
+            tma_tile(&tmq, sb + OFF_Q, bar_tma, h, t0 + C);
+            tma_tile(&tmg, sb + OFF_G, bar_tma, h, t0 + C);
+        }
+        // (c) U^T -> fp16 hi (U^T buffer) + lo (W buffer, free once (b) completed); warp half h:
+        // columns 32h..32h+31
+        {
+            float v[32];
+            tmem_ld32(trow + TM_U + 32 * half, v);
+#pragma unroll
+            for (int q8 = 0; q8 < 4; ++q8) {
+                uint32_t hi[4], lo[4];
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                    const float a0 = v[8 * q8 + 2 * e], a1 = v[8 * q8 + 2 * e + 1];
+                    hi[e] = pack_f16(a0, a1);
+                    const float2 hf = unpack_f16(hi[e]);
+                    lo[e] = pack_f16(a0 - hf.x, a1 - hf.y);
+                }
+                const uint32_t off = sw(jl, 32 * half + 8 * q8, 128);
+                *reinterpret_cast<uint4 *>(sm + OFF_UST + off) = make_uint4(hi[0], hi[1], hi[2], hi[3]);
+                *reinterpret_cast<uint4 *>(sm + OFF_WT + off) = make_uint4(lo[0], lo[1], lo[2], lo[3]);
+            }
+        }
+        fence_async_smem();
+        tc_fence_before();
+        __syncthreads();
+        // (d) O^T += U^T M^T (hi.hi + lo.hi + hi.lo) ;  S^T += U^T Kp
+        if (tid == 0) {
+            tc_fence_after();
+#pragma unroll
+            for (int ks = 0; ks < 4; ++ks) {
+                mma_f16_ss(tmem + TM_O, sdesc_sw128(sb + OFF_UST + ks * 32), sdesc_sw128(sb + OFF_MT + ks * 32),
+                           IDESC_N64, 1);
+                mma_f16_ss(tmem + TM_O, sdesc_sw128(sb + OFF_WT + ks * 32), sdesc_sw128(sb + OFF_MT + ks * 32),
+                           IDESC_N64, 1);
+                mma_f16_ss(tmem + TM_O, sdesc_sw128(sb + OFF_UST + ks * 32), sdesc_sw128(sb + OFF_MLO + ks * 32),
+                           IDESC_N64, 1);
+            }
+#pragma unroll
+            for (int ks = 0; ks < 4; ++ks)
+                mma_f16_ss(tmem + TM_S, sdesc_sw128(sb + OFF_UST + ks * 32), sdesc_sw128(sb + OFF_KPT + ks * 32),
+                           IDESC_N128, 1);
+            mma_commit(bar_mma);
+        }
+        {
+            const bool got = mbar_wait(bar_mma, mma_phase, wait_limit);
+            mma_phase ^= 1;
+            if (__syncthreads_or(!got)) { ok = false; break; }
+        }
+        tc_fence_after();
+        // (e) O^T -> bf16 staging tile [64 r][128 j] (over A) -> 16-byte coalesced stores
+        {
+            __nv_bfloat16 *os = reinterpret_cast<__nv_bfloat16 *>(sm + OFF_AF);
+            float v[32];
+            tmem_ld32(trow + TM_O + 32 * half, v);
+#pragma unroll
+            for (int c = 0; c < 32; ++c) os[(32 * half + c) * D + jl] = __float2bfloat16_rn(v[c]);
+        }
+        tc_fence_before();
+        __syncthreads();
+        {
+            const uint4 *os = reinterpret_cast<const uint4 *>(sm + OFF_AF);
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+                const int idx = tid + NT * e;          // 64 rows x 16 uint4
+                const int r = idx >> 4, c16 = idx & 15;
+                if (r < nr)
+                    reinterpret_cast<uint4 *>(out + ((t0 + r) * H + h) * D)[c16] = os[idx];
+            }
+        }
+        __syncthreads();
+    }
+
+    if (!ok) {
+        // A bounded wait expired: let copies and MMAs in flight land (bounded
+        // again), flag the failure and mark this unit's outputs invalid.
+        if (tid == 0) {
+            mbar_wait(bar_mma, mma_phase, wait_limit);
+            mbar_wait(bar_tma, tma_phase, wait_limit);
+            atomicAdd(&g_kda_tc_timeouts, 1u);
+        }
+        __syncthreads();
+    }
+    tc_fence_after();
+    if (a.sT) {
+#pragma unroll 1
+        for (int g2 = 0; g2 < 2; ++g2) {
+            const int i0 = 64 * half + 32 * g2;
+            float v[32];
+            tmem_ld32(trow + TM_S + i0, v);
+#pragma unroll
+            for (int c = 0; c < 32; ++c)
+                a.sT[sbase + (int64_t)(i0 + c) * D + jl] = ok ? v[c] : __int_as_float(0x7fc00000);
+        }
+    }
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 0) {
+        tc_fence_after();
+        tmem_dealloc(tmem, TM_COLS);
+    }
+}
+
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+    if (fn == nullptr) {
+        void *p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+    }
+    return fn;
+}
+
+// [tokens][H][128] bf16 as a 3-D tensor (128, H, tokens); 64 x 1 x 64 boxes,
+// 128-byte swizzle (the layout the MMA operand descriptors expect).
+bool make_map(CUtensorMap *m, const void *ptr, int64_t tokens, int H) {
+    auto enc = encode_fn();
+    if (enc == nullptr) return false;
+    cuuint64_t dims[3] = {(cuuint64_t)D, (cuuint64_t)H, (cuuint64_t)tokens};
+    cuuint64_t strides[2] = {(cuuint64_t)D * 2, (cuuint64_t)H * D * 2};
+    cuuint32_t box[3] = {64, 1, 64};
+    cuuint32_t es[3] = {1, 1, 1};
+    return enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void *>(ptr), dims, strides, box, es,
+               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+}  // namespace
+
+bool chunk_tc_supported(int dk, int dv, kda_dtype_t dt) {
+    return dt == KDA_BF16 && dk == D && dv == D;
+}
+
+cudaError_t launch_chunk_tc(const ChunkArgs &a, int dk, int dv, kda_dtype_t dt, cudaStream_t st) {
+    if (!chunk_tc_supported(dk, dv, dt)) return cudaErrorNotSupported;
+    const int64_t tokens = a.cu ? a.seqlen : (int64_t)a.num_seqs * a.seqlen;
+    if (tokens >= (int64_t(1) << 31)) return cudaErrorInvalidValue;
+    CUtensorMap mq, mk, mv, mg;
+    if (!make_map(&mq, a.q, tokens, a.heads) || !make_map(&mk, a.k, tokens, a.heads) ||
+        !make_map(&mv, a.v, tokens, a.heads) || !make_map(&mg, a.g, tokens, a.heads))
+        return cudaErrorInvalidValue;
+    cudaError_t e = cudaFuncSetAttribute(kda_chunk_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         (int)SMEM_BYTES);
+    if (e != cudaSuccess) return e;
+    const int64_t units = (int64_t)a.num_seqs * a.heads;
+    if (units > 0x7fffffffLL) return cudaErrorInvalidValue;
+    kda_chunk_tc_kernel<<<(unsigned)units, NT, SMEM_BYTES, st>>>(mq, mk, mv, mg, a, 1u << 22);
+    return cudaGetLastError();
 }
 
 }  // namespace kda

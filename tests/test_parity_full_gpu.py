@@ -15,7 +15,7 @@ import torch
 import oracle
 from linear_attention_fwd_gb300 import inputs
 from tests.helpers import rel_max_err
-from tests.parity import bf16_floor, check_prefill, compare_prefill, f64, out_bar
+from tests.parity import check_prefill, compare_prefill, excess_err, f64
 
 pytestmark = pytest.mark.gpu
 
@@ -69,6 +69,5 @@ def test_decode_n256_h64_1000_steps(K):
         sl = lambda t: t[:, n, h][None, :, None]
         ro, rs = oracle.forward(sl(inp["q"]), sl(inp["k"]), sl(inp["v"]), sl(inp["g"]),
                                 inp["beta"][:, n, h][None, :, None], s0[n, h][None, None])
-        assert rel_max_err(f64(outs[:, n, h]), ro[0, :, 0]) <= out_bar(torch.bfloat16,
-                                                                       bf16_floor(ro[0, :, 0]))
+        assert excess_err(f64(outs[:, n, h]), ro[0, :, 0], torch.bfloat16) <= 2e-2
         assert rel_max_err(f64(state[n, h]), rs[0, 0]) <= 2e-2
