@@ -48,7 +48,7 @@ using namespace ptx;
 
 constexpr int C = 64;         // chunk
 constexpr int D = 128;        // d_k = d_v
-constexpr int NT = 256;       // threads
+constexpr int NT = 512;       // threads (16 warps)
 constexpr float LOG2E = 1.4426950408889634f;
 
 // 2^x on the special-function unit (flushes results below 2^-126 to zero,
@@ -75,15 +75,14 @@ constexpr int LDA = 72;
 constexpr uint32_t OFF_TD = OFF_AF + 64 * LDA * 4;      // T dense fp32 [64][LDT]
 constexpr int LDT = 68;
 constexpr uint32_t OFF_XS = OFF_TD + 64 * LDT * 4;      // inverse scratch [3][16][16] fp32
-constexpr uint32_t OFF_TOT = OFF_XS + 3 * 256 * 4;      // sub-tile log2-decay totals [4][128]
-constexpr uint32_t OFF_EB = OFF_TOT + 4 * 128 * 4;      // e^{b_I}          [4][128]
+constexpr uint32_t OFF_EB = OFF_XS + 3 * 256 * 4;       // e^{b_I}          [4][128]
 constexpr uint32_t OFF_EL = OFF_EB + 4 * 128 * 4;       // e^{gl - b_I}     [4][128]
 constexpr uint32_t OFF_W6 = OFF_EL + 4 * 128 * 4;       // e^{b_I - b_J}    [6][128] bf16
 constexpr uint32_t OFF_DEC = OFF_W6 + 6 * 128 * 2;      // e^{gl}           [128]
 constexpr uint32_t OFF_BETA = OFF_DEC + 128 * 4;        // beta             [64]
 constexpr uint32_t OFF_MRR = OFF_BETA + 64 * 4;         // q_r . k_r        [64]
 constexpr uint32_t OFF_MLO = (OFF_MRR + 64 * 4 + 1023) / 1024 * 1024;   // M - fp16(M), fp16 [64 r][64 s]
-constexpr uint32_t OFF_BAR = OFF_MLO + 8192;            // 2 mbarriers, TMEM address
+constexpr uint32_t OFF_BAR = OFF_MLO + 8192;            // 4 mbarriers, TMEM address
 constexpr uint32_t SMEM_USED = OFF_BAR + 64;
 constexpr uint32_t SMEM_BYTES = SMEM_USED + 1024;       // + alignment slack
 static_assert(SMEM_BYTES <= 227 * 1024, "shared memory budget");
@@ -159,21 +158,27 @@ kda_chunk_tc_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_consta
     const int64_t len = eos - bos;
     const int nchunks = (int)((len + C - 1) / C);
 
-    const uint32_t bar_tma = sb + OFF_BAR, bar_mma = sb + OFF_BAR + 8;
-    volatile uint32_t *tmem_holder = reinterpret_cast<volatile uint32_t *>(sm + OFF_BAR + 16);
+    // mbarriers: TMA tiles landed; U^T ready; O^T ready; state update done
+    const uint32_t bar_tma = sb + OFF_BAR, bar_u = sb + OFF_BAR + 8;
+    const uint32_t bar_o = sb + OFF_BAR + 16, bar_s = sb + OFF_BAR + 24;
+    volatile uint32_t *tmem_holder = reinterpret_cast<volatile uint32_t *>(sm + OFF_BAR + 32);
     float *AF = reinterpret_cast<float *>(sm + OFF_AF);
-    float *TOT = reinterpret_cast<float *>(sm + OFF_TOT);
+    float *TD = reinterpret_cast<float *>(sm + OFF_TD);
+    float *PART = TD;   // sub-tile half sums [8][128], before T is formed
     float *EB = reinterpret_cast<float *>(sm + OFF_EB);
     float *EL = reinterpret_cast<float *>(sm + OFF_EL);
     __nv_bfloat16 *W6 = reinterpret_cast<__nv_bfloat16 *>(sm + OFF_W6);
     float *DEC = reinterpret_cast<float *>(sm + OFF_DEC);
     float *BETA = reinterpret_cast<float *>(sm + OFF_BETA);
+    float *MRR = reinterpret_cast<float *>(sm + OFF_MRR);
     const __nv_bfloat16 *beta = static_cast<const __nv_bfloat16 *>(a.beta);
     __nv_bfloat16 *out = static_cast<__nv_bfloat16 *>(a.out);
 
     if (tid == 0) {
         mbar_init(bar_tma, 1);
-        mbar_init(bar_mma, 1);
+        mbar_init(bar_u, 1);
+        mbar_init(bar_o, 1);
+        mbar_init(bar_s, 1);
         fence_mbar_init();
         prefetch_tmap(&tmq);
         prefetch_tmap(&tmk);
@@ -181,7 +186,7 @@ kda_chunk_tc_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_consta
         prefetch_tmap(&tmg);
     }
     if (warp == 0) {
-        tmem_alloc(sb + OFF_BAR + 16, TM_COLS);
+        tmem_alloc(sb + OFF_BAR + 32, TM_COLS);
         tmem_relinquish();
     }
     tc_fence_before();
@@ -189,21 +194,17 @@ kda_chunk_tc_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_consta
     tc_fence_after();
     const uint32_t tmem = *tmem_holder;
     const uint32_t trow = tmem + ((uint32_t)((warp & 3) * 32) << 16);   // this warp's TMEM lanes
-
-    // ---- initial state -> TMEM (S^T: lane j, column i); warp w owns lanes 32(w%4).., columns 64(w/4)..
-    const int64_t sbase = ((int64_t)n * H + h) * D * D;
     const int jl = 32 * (warp & 3) + lane;   // this thread's TMEM lane (value channel j)
-    const int half = warp >> 2;              // which half of the columns this warp handles
+    const int quarter = warp >> 2;           // which 32-column group this warp handles (0..3)
+
+    // ---- initial state -> TMEM (S^T: lane j, column i)
+    const int64_t sbase = ((int64_t)n * H + h) * D * D;
     {
-#pragma unroll 1
-        for (int g2 = 0; g2 < 2; ++g2) {
-            const int i0 = 64 * half + 32 * g2;
-            float v[32];
+        float v[32];
 #pragma unroll
-            for (int c = 0; c < 32; ++c)
-                v[c] = a.s0 ? a.s0[sbase + (int64_t)(i0 + c) * D + jl] : 0.f;
-            tmem_st32(trow + TM_S + i0, v);
-        }
+        for (int c = 0; c < 32; ++c)
+            v[c] = a.s0 ? a.s0[sbase + (int64_t)(32 * quarter + c) * D + jl] : 0.f;
+        tmem_st32(trow + TM_S + 32 * quarter, v);
     }
     if (tid == 0 && nchunks > 0) {
         mbar_arrive_expect_tx(bar_tma, 4 * 16384);
@@ -212,10 +213,6 @@ kda_chunk_tc_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_consta
         tma_tile(&tmv, sb + OFF_V, bar_tma, h, bos);
         tma_tile(&tmg, sb + OFF_G, bar_tma, h, bos);
     }
-    tc_fence_before();
-    __syncthreads();
-    tc_fence_after();
-
     // the blocks of M above the diagonal blocks stay zero for the whole sequence
     for (int x = tid; x < 64 * 32; x += NT) {
         const int r = x >> 5, s2 = 2 * (x & 31);
@@ -224,11 +221,14 @@ kda_chunk_tc_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_consta
             *reinterpret_cast<uint32_t *>(sm + OFF_MLO + sw(r, s2, 64)) = 0u;
         }
     }
-    float *TD = reinterpret_cast<float *>(sm + OFF_TD);
-    float *MRR = reinterpret_cast<float *>(sm + OFF_MRR);
-    uint32_t tma_phase = 0, mma_phase = 0;
-    bool ok = true;
-    const int cp = tid & 63, blk = tid >> 6;   // elementwise ownership: channel pair, sub-tile
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+
+    uint32_t ph_tma = 0, ph_u = 0, ph_o = 0, ph_s = 0;
+    bool ok = true, s_pending = false;
+    const int cp = tid & 63, sub = tid >> 6;   // elementwise ownership: channel pair, 8-row group
+    const int blk = sub >> 1, hb = sub & 1;    // sub-tile and which half of it
     const int t4 = lane & 3, g = lane >> 2;    // mma.sync fragment coordinates
 
 #pragma unroll 1
@@ -239,14 +239,14 @@ kda_chunk_tc_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_consta
 
         if (tid < C) BETA[tid] = tid < nr ? __bfloat162float(beta[(t0 + tid) * H + h]) : 0.f;
         {
-            const bool got = mbar_wait(bar_tma, tma_phase, wait_limit);
-            tma_phase ^= 1;
+            const bool got = mbar_wait(bar_tma, ph_tma, wait_limit);
+            ph_tma ^= 1;
             if (__syncthreads_or(!got)) { ok = false; break; }
         }
 
         // ---- (1) q_r . k_r exactly (bf16 x bf16 products are exact in fp32): the raw
-        // diagonal 16x16 blocks of Q K^T on mma.sync, warps 0-3; all warps: sub-tile
-        // log2-decay totals (the local cumulative sums restart at every sub-tile).
+        // diagonal 16x16 blocks of Q K^T on mma.sync, warps 0-3; all threads: log2-decay
+        // sums over their 8-row half of a sub-tile (cumulative sums restart at each sub-tile).
         if (warp < 4) {
             const int I = warp;
             float acc[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
@@ -270,19 +270,22 @@ kda_chunk_tc_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_consta
             const int c = 2 * cp;
             float l0 = 0.f, l1 = 0.f;
 #pragma unroll
-            for (int rr = 0; rr < 16; ++rr) {
-                const int r = 16 * blk + rr;
+            for (int rr = 0; rr < 8; ++rr) {
+                const int r = 16 * blk + 8 * hb + rr;
                 const float2 g2 = unpack_bf16(*reinterpret_cast<uint32_t *>(sm + OFF_G + sw(r, c, 64)));
                 if (r < nr) { l0 = fmaf(g2.x, LOG2E, l0); l1 = fmaf(g2.y, LOG2E, l1); }
             }
-            TOT[blk * 128 + c] = l0;
-            TOT[blk * 128 + c + 1] = l1;
+            PART[sub * 128 + c] = l0;
+            PART[sub * 128 + c + 1] = l1;
         }
         __syncthreads();
         if (tid < 128) {   // per-channel decay vectors of this chunk (log2 units)
             const int c = tid;
-            const float b1 = TOT[c], b2 = b1 + TOT[128 + c], b3 = b2 + TOT[256 + c];
-            const float gl = b3 + TOT[384 + c];
+            float t[4];
+#pragma unroll
+            for (int I = 0; I < 4; ++I) t[I] = PART[(2 * I) * 128 + c] + PART[(2 * I + 1) * 128 + c];
+            const float b1 = t[0], b2 = b1 + t[1], b3 = b2 + t[2];
+            const float gl = b3 + t[3];
             const float bI[4] = {0.f, b1, b2, b3};
 #pragma unroll
             for (int I = 0; I < 4; ++I) {
@@ -293,7 +296,16 @@ kda_chunk_tc_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_consta
             }
             DEC[c] = ex2(gl);
         }
-        __syncthreads();
+        // the previous chunk's state update still reads the U^T buffer: wait for it
+        if (s_pending) {
+            const bool got = mbar_wait(bar_s, ph_s, wait_limit);
+            ph_s ^= 1;
+            s_pending = false;
+            if (__syncthreads_or(!got)) { ok = false; break; }
+        } else {
+            __syncthreads();
+        }
+        tc_fence_after();
 
         // ---- (2) operands, each rounded from the exact inputs:
         //   bf16 (range e^+-80): Q~ = Q x as hi + lo (S^T and U^T buffers, idle here),
@@ -303,14 +315,15 @@ kda_chunk_tc_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_consta
             const int c = 2 * cp;
             const float eb0 = EB[blk * 128 + c], eb1 = EB[blk * 128 + c + 1];
             const float el0 = EL[blk * 128 + c], el1 = EL[blk * 128 + c + 1];
-            float l0 = 0.f, l1 = 0.f;
-            uint32_t p0[8], p1[8];
+            float l0 = hb ? PART[(2 * blk) * 128 + c] : 0.f;
+            float l1 = hb ? PART[(2 * blk) * 128 + c + 1] : 0.f;
+            uint32_t p0[4], p1[4];
 #pragma unroll
-            for (int rr = 0; rr < 16; rr += 2) {
+            for (int rr = 0; rr < 8; rr += 2) {
                 float kp[2][2];
 #pragma unroll
                 for (int e = 0; e < 2; ++e) {
-                    const int r = 16 * blk + rr + e;
+                    const int r = 16 * blk + 8 * hb + rr + e;
                     const uint32_t off = sw(r, c, 64);
                     float2 q2 = unpack_bf16(*reinterpret_cast<uint32_t *>(sm + OFF_Q + off));
                     float2 k2 = unpack_bf16(*reinterpret_cast<uint32_t *>(sm + OFF_K + off));
@@ -336,24 +349,29 @@ kda_chunk_tc_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_consta
                 p0[rr / 2] = pack_f16(kp[0][0], kp[1][0]);
                 p1[rr / 2] = pack_f16(kp[0][1], kp[1][1]);
             }
-            *reinterpret_cast<uint4 *>(sm + OFF_KPT + sw(c, 16 * blk, 128)) = make_uint4(p0[0], p0[1], p0[2], p0[3]);
-            *reinterpret_cast<uint4 *>(sm + OFF_KPT + sw(c, 16 * blk + 8, 128)) = make_uint4(p0[4], p0[5], p0[6], p0[7]);
-            *reinterpret_cast<uint4 *>(sm + OFF_KPT + sw(c + 1, 16 * blk, 128)) = make_uint4(p1[0], p1[1], p1[2], p1[3]);
-            *reinterpret_cast<uint4 *>(sm + OFF_KPT + sw(c + 1, 16 * blk + 8, 128)) = make_uint4(p1[4], p1[5], p1[6], p1[7]);
+            const int rc = 16 * blk + 8 * hb;
+            *reinterpret_cast<uint4 *>(sm + OFF_KPT + sw(c, rc, 128)) = make_uint4(p0[0], p0[1], p0[2], p0[3]);
+            *reinterpret_cast<uint4 *>(sm + OFF_KPT + sw(c + 1, rc, 128)) = make_uint4(p1[0], p1[1], p1[2], p1[3]);
         }
         __syncthreads();
 
-        // ---- (3) A = beta K~ K^T and M = Q~ K^T on the 10 sub-tile pairs (I >= J), spread over
-        // the warps; M is the 3-term product (Q~hi + Q~lo)(K^hi + K^lo)^T less the lo.lo term,
-        // and its diagonal is the exact q_r . k_r.
-#pragma unroll 1
-        for (int pi = warp; pi < 10; pi += 8) {
+        // ---- (3) A = beta K~ K^T and M = Q~ K^T on the 10 sub-tile pairs (I >= J), one pair per
+        // warp with independent accumulator chains; M is the 3-term product
+        // (Q~hi + Q~lo)(K^hi + K^lo)^T less the lo.lo term, with the exact q_r . k_r on its diagonal.
+        if (warp < 10) {
+            const int pi = warp;
             const int I = pi < 4 ? 3 : (pi < 7 ? 2 : (pi < 9 ? 1 : 0));
             const int J = pi < 4 ? pi : (pi < 7 ? pi - 4 : (pi < 9 ? pi - 7 : 0));
-            float accA[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
-            float accM[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
+            float accA[2][4], accM[3][2][4];
+#pragma unroll
+            for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                    accA[nt][e] = 0.f;
+                    accM[0][nt][e] = 0.f; accM[1][nt][e] = 0.f; accM[2][nt][e] = 0.f;
+                }
             const __nv_bfloat16 *w = W6 + (J < I ? pair_index(I, J) : 0) * 128 + 2 * t4;
-#pragma unroll 2
+#pragma unroll 4
             for (int kk = 0; kk < 8; ++kk) {
                 const uint32_t ao = sw(16 * I + (lane & 15), 16 * kk + ((lane >> 4) << 3), 64);
                 const uint32_t bo = sw(16 * J + (lane & 7) + ((lane >> 4) << 3), 16 * kk + (((lane >> 3) & 1) << 3), 64);
@@ -366,17 +384,18 @@ kda_chunk_tc_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_consta
                 if (J < I) {
                     const uint32_t wlo = *reinterpret_cast<const uint32_t *>(w + 16 * kk);
                     const uint32_t whi = *reinterpret_cast<const uint32_t *>(w + 16 * kk + 8);
-                    bh[0] = mul_bf16x2(bh[0], wlo); bh[1] = mul_bf16x2(bh[1], whi);
-                    bh[2] = mul_bf16x2(bh[2], wlo); bh[3] = mul_bf16x2(bh[3], whi);
-                    bl[0] = mul_bf16x2(bl[0], wlo); bl[1] = mul_bf16x2(bl[1], whi);
-                    bl[2] = mul_bf16x2(bl[2], wlo); bl[3] = mul_bf16x2(bl[3], whi);
+#pragma unroll
+                    for (int e = 0; e < 4; e += 2) {
+                        bh[e] = mul_bf16x2(bh[e], wlo); bh[e + 1] = mul_bf16x2(bh[e + 1], whi);
+                        bl[e] = mul_bf16x2(bl[e], wlo); bl[e + 1] = mul_bf16x2(bl[e + 1], whi);
+                    }
                 }
 #pragma unroll
                 for (int nt = 0; nt < 2; ++nt) {
                     mma_16816(accA[nt], ka[0], ka[1], ka[2], ka[3], bh[2 * nt], bh[2 * nt + 1]);
-                    mma_16816(accM[nt], qh[0], qh[1], qh[2], qh[3], bh[2 * nt], bh[2 * nt + 1]);
-                    mma_16816(accM[nt], ql[0], ql[1], ql[2], ql[3], bh[2 * nt], bh[2 * nt + 1]);
-                    mma_16816(accM[nt], qh[0], qh[1], qh[2], qh[3], bl[2 * nt], bl[2 * nt + 1]);
+                    mma_16816(accM[0][nt], qh[0], qh[1], qh[2], qh[3], bh[2 * nt], bh[2 * nt + 1]);
+                    mma_16816(accM[1][nt], ql[0], ql[1], ql[2], ql[3], bh[2 * nt], bh[2 * nt + 1]);
+                    mma_16816(accM[2][nt], qh[0], qh[1], qh[2], qh[3], bl[2 * nt], bl[2 * nt + 1]);
                 }
             }
 #pragma unroll
@@ -388,8 +407,10 @@ kda_chunk_tc_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_consta
                     const float br = BETA[r];
                     AF[r * LDA + s0] = s0 < r ? br * accA[nt][2 * hh] : 0.f;
                     AF[r * LDA + s0 + 1] = s0 + 1 < r ? br * accA[nt][2 * hh + 1] : 0.f;
-                    const float m0 = s0 < r ? accM[nt][2 * hh] : (s0 == r ? MRR[r] : 0.f);
-                    const float m1 = s0 + 1 < r ? accM[nt][2 * hh + 1] : (s0 + 1 == r ? MRR[r] : 0.f);
+                    const float mv0 = accM[0][nt][2 * hh] + (accM[1][nt][2 * hh] + accM[2][nt][2 * hh]);
+                    const float mv1 = accM[0][nt][2 * hh + 1] + (accM[1][nt][2 * hh + 1] + accM[2][nt][2 * hh + 1]);
+                    const float m0 = s0 < r ? mv0 : (s0 == r ? MRR[r] : 0.f);
+                    const float m1 = s0 + 1 < r ? mv1 : (s0 + 1 == r ? MRR[r] : 0.f);
                     const uint32_t mh = pack_f16(m0, m1);
                     const float2 mhf = unpack_f16(mh);
                     *reinterpret_cast<uint32_t *>(sm + OFF_MT + sw(r, s0, 64)) = mh;
@@ -398,26 +419,26 @@ kda_chunk_tc_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_consta
         }
         __syncthreads();
 
-        // ---- (4) V^T into the G buffer (bf16 values are exact in fp16); diagonal 16x16 blocks of T = (I + A)^-1 by
-        // forward substitution (threads 0-63, one column each); zero the upper blocks of T.
+        // ---- (4) V^T into the G buffer (bf16 values are exact in fp16); diagonal 16x16 blocks
+        // of T = (I + A)^-1 by forward substitution (threads 0-63, one column each); the
+        // other threads zero the upper blocks of T.
         {
             const int j = 2 * cp;
-            uint32_t p0[8], p1[8];
+            uint32_t p0[4], p1[4];
 #pragma unroll
-            for (int rr = 0; rr < 16; rr += 2) {
-                const int r = 16 * blk + rr;
+            for (int rr = 0; rr < 8; rr += 2) {
+                const int r = 16 * blk + 8 * hb + rr;
                 const float2 v0 = unpack_bf16(*reinterpret_cast<uint32_t *>(sm + OFF_V + sw(r, j, 64)));
                 const float2 v1 = unpack_bf16(*reinterpret_cast<uint32_t *>(sm + OFF_V + sw(r + 1, j, 64)));
                 p0[rr / 2] = pack_f16(v0.x, v1.x);
                 p1[rr / 2] = pack_f16(v0.y, v1.y);
             }
-            *reinterpret_cast<uint4 *>(sm + OFF_G + sw(j, 16 * blk, 128)) = make_uint4(p0[0], p0[1], p0[2], p0[3]);
-            *reinterpret_cast<uint4 *>(sm + OFF_G + sw(j, 16 * blk + 8, 128)) = make_uint4(p0[4], p0[5], p0[6], p0[7]);
-            *reinterpret_cast<uint4 *>(sm + OFF_G + sw(j + 1, 16 * blk, 128)) = make_uint4(p1[0], p1[1], p1[2], p1[3]);
-            *reinterpret_cast<uint4 *>(sm + OFF_G + sw(j + 1, 16 * blk + 8, 128)) = make_uint4(p1[4], p1[5], p1[6], p1[7]);
+            const int rc = 16 * blk + 8 * hb;
+            *reinterpret_cast<uint4 *>(sm + OFF_G + sw(j, rc, 128)) = make_uint4(p0[0], p0[1], p0[2], p0[3]);
+            *reinterpret_cast<uint4 *>(sm + OFF_G + sw(j + 1, rc, 128)) = make_uint4(p1[0], p1[1], p1[2], p1[3]);
         }
-        float tcol[16];
         if (tid < 64) {
+            float tcol[16];
             const int I = tid >> 4, jj = tid & 15;
             const float *Ab = AF + (16 * I) * LDA + 16 * I;
 #pragma unroll
@@ -430,7 +451,6 @@ kda_chunk_tc_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_consta
 #pragma unroll
             for (int r = 0; r < 16; ++r) TD[(16 * I + r) * LDT + 16 * I + jj] = tcol[r];
         } else {
-            // upper blocks (I < J) of T are zero: 6 blocks x 256 entries over 192 threads
             for (int x = tid - 64; x < 6 * 256; x += NT - 64) {
                 const int bidx = x >> 8, e = x & 255;
                 const int I = bidx < 3 ? 0 : (bidx < 5 ? 1 : 2);
@@ -439,59 +459,61 @@ kda_chunk_tc_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_consta
             }
         }
         __syncthreads();
-        // ---- (5) off-diagonal blocks by distance d = I - J: T_IJ = -T_II sum_{K=J}^{I-1} A_IK T_KJ
+        // ---- (5) off-diagonal blocks by distance d = I - J: T_IJ = -T_II sum_{K=J}^{I-1} A_IK T_KJ;
+        // the (4 - d) blocks of a distance are spread over all threads, 256 entries each.
         {
-            const int rr = tid >> 4, jj = tid & 15;
             float *X = reinterpret_cast<float *>(sm + OFF_XS);
-#pragma unroll 1
+#pragma unroll
             for (int d = 1; d < 4; ++d) {
-                const int nb = 4 - d;
-                for (int b = 0; b < nb; ++b) {
+                const int items = (4 - d) * 256;
+#pragma unroll
+                for (int it = tid; it < items; it += NT) {
+                    const int b = it >> 8, rr = (it >> 4) & 15, jj = it & 15;
                     const int J = b, I = b + d;
-                    const float *arow = AF + (16 * I + rr) * LDA;
-                    float x = 0.f;
-                    for (int k = 16 * J; k < 16 * I; k += 4) {
+                    const float *arow = AF + (16 * I + rr) * LDA + 16 * J;
+                    const float *tcol_ = TD + (16 * J) * LDT + 16 * J + jj;
+                    float x[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+                    for (int k = 0; k < 16 * d; k += 4) {
                         const float4 a4 = *reinterpret_cast<const float4 *>(arow + k);
-                        x = fmaf(a4.x, TD[(k + 0) * LDT + 16 * J + jj], x);
-                        x = fmaf(a4.y, TD[(k + 1) * LDT + 16 * J + jj], x);
-                        x = fmaf(a4.z, TD[(k + 2) * LDT + 16 * J + jj], x);
-                        x = fmaf(a4.w, TD[(k + 3) * LDT + 16 * J + jj], x);
+                        x[0] = fmaf(a4.x, tcol_[(k + 0) * LDT], x[0]);
+                        x[1] = fmaf(a4.y, tcol_[(k + 1) * LDT], x[1]);
+                        x[2] = fmaf(a4.z, tcol_[(k + 2) * LDT], x[2]);
+                        x[3] = fmaf(a4.w, tcol_[(k + 3) * LDT], x[3]);
                     }
-                    X[b * 256 + rr * 16 + jj] = x;
+                    X[it] = (x[0] + x[1]) + (x[2] + x[3]);
                 }
                 __syncthreads();
-                for (int b = 0; b < nb; ++b) {
+#pragma unroll
+                for (int it = tid; it < items; it += NT) {
+                    const int b = it >> 8, rr = (it >> 4) & 15, jj = it & 15;
                     const int J = b, I = b + d;
                     const float *trow_ = TD + (16 * I + rr) * LDT + 16 * I;
-                    float t = 0.f;
+                    const float *xb = X + b * 256 + jj;
+                    float t[2] = {0.f, 0.f};
 #pragma unroll
                     for (int s2 = 0; s2 < 16; s2 += 4) {
                         const float4 t4v = *reinterpret_cast<const float4 *>(trow_ + s2);
-                        t = fmaf(t4v.x, X[b * 256 + (s2 + 0) * 16 + jj], t);
-                        t = fmaf(t4v.y, X[b * 256 + (s2 + 1) * 16 + jj], t);
-                        t = fmaf(t4v.z, X[b * 256 + (s2 + 2) * 16 + jj], t);
-                        t = fmaf(t4v.w, X[b * 256 + (s2 + 3) * 16 + jj], t);
+                        t[0] = fmaf(t4v.x, xb[(s2 + 0) * 16], t[0]);
+                        t[1] = fmaf(t4v.y, xb[(s2 + 1) * 16], t[1]);
+                        t[0] = fmaf(t4v.z, xb[(s2 + 2) * 16], t[0]);
+                        t[1] = fmaf(t4v.w, xb[(s2 + 3) * 16], t[1]);
                     }
-                    TD[(16 * I + rr) * LDT + 16 * J + jj] = -t;
+                    TD[(16 * I + rr) * LDT + 16 * J + jj] = -(t[0] + t[1]);
                 }
                 __syncthreads();
             }
         }
         // ---- (6) T' = T diag(beta) -> fp16 tile [64 r][64 s]
         {
-            const int r = tid >> 2, q = tid & 3;
-            const float *src = TD + r * LDT + 16 * q;
-            const float *bq = BETA + 16 * q;
-            uint32_t pk[8];
-#pragma unroll
-            for (int e = 0; e < 4; ++e) {
-                const float4 t4v = *reinterpret_cast<const float4 *>(src + 4 * e);
-                const float4 b4 = *reinterpret_cast<const float4 *>(bq + 4 * e);
-                pk[2 * e] = pack_f16(t4v.x * b4.x, t4v.y * b4.y);
-                pk[2 * e + 1] = pack_f16(t4v.z * b4.z, t4v.w * b4.w);
-            }
-            *reinterpret_cast<uint4 *>(sm + OFF_TT + sw(r, 16 * q, 64)) = make_uint4(pk[0], pk[1], pk[2], pk[3]);
-            *reinterpret_cast<uint4 *>(sm + OFF_TT + sw(r, 16 * q + 8, 64)) = make_uint4(pk[4], pk[5], pk[6], pk[7]);
+            const int r = tid >> 3, q8 = tid & 7;
+            const float *src = TD + r * LDT + 8 * q8;
+            const float *bq = BETA + 8 * q8;
+            const float4 ta = *reinterpret_cast<const float4 *>(src), tb = *reinterpret_cast<const float4 *>(src + 4);
+            const float4 ba = *reinterpret_cast<const float4 *>(bq), bb = *reinterpret_cast<const float4 *>(bq + 4);
+            *reinterpret_cast<uint4 *>(sm + OFF_TT + sw(r, 8 * q8, 64)) =
+                make_uint4(pack_f16(ta.x * ba.x, ta.y * ba.y), pack_f16(ta.z * ba.z, ta.w * ba.w),
+                           pack_f16(tb.x * bb.x, tb.y * bb.y), pack_f16(tb.z * bb.z, tb.w * bb.w));
         }
         fence_async_smem();
         tc_fence_before();
@@ -506,10 +528,10 @@ kda_chunk_tc_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_consta
                            IDESC_N64, ks > 0);
         }
         {
-            const int I = warp & 3, ch = warp >> 2;
-            float acc[8][4];
+            const int I = warp & 3, cq = warp >> 2;
+            float acc[4][4];
 #pragma unroll
-            for (int x = 0; x < 8; ++x)
+            for (int x = 0; x < 4; ++x)
 #pragma unroll
                 for (int e = 0; e < 4; ++e) acc[x][e] = 0.f;
 #pragma unroll
@@ -517,8 +539,8 @@ kda_chunk_tc_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_consta
                 uint32_t a0, a1, a2, a3;
                 ldsm_x4(sb + OFF_TT + sw(16 * I + (lane & 15), 16 * kk + ((lane >> 4) << 3), 64), a0, a1, a2, a3);
 #pragma unroll
-                for (int p = 0; p < 4; ++p) {
-                    const int i0 = 64 * ch + 16 * p;
+                for (int p = 0; p < 2; ++p) {
+                    const int i0 = 32 * cq + 16 * p;
                     uint32_t b0, b1, b2, b3;
                     ldsm_x4_t(sb + OFF_K + sw(16 * kk + (lane & 7) + (((lane >> 3) & 1) << 3),
                                               i0 + ((lane >> 4) << 3), 64),
@@ -528,11 +550,11 @@ kda_chunk_tc_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_consta
                 }
             }
 #pragma unroll
-            for (int x = 0; x < 8; ++x)
+            for (int x = 0; x < 4; ++x)
 #pragma unroll
                 for (int hh = 0; hh < 2; ++hh) {
                     const int r = 16 * I + g + 8 * hh;
-                    const int i = 64 * ch + 8 * x + 2 * t4;
+                    const int i = 32 * cq + 8 * x + 2 * t4;
                     *reinterpret_cast<uint32_t *>(sm + OFF_WT + sw(r, i, 64)) =
                         pack_f16(-acc[x][2 * hh], -acc[x][2 * hh + 1]);
                 }
@@ -548,55 +570,49 @@ kda_chunk_tc_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_consta
 
         // ---- state path.  (a) S^T -> fp16 operand; S^T <- S^T Diag(dec) in place
         {
-#pragma unroll 1
-            for (int g2 = 0; g2 < 2; ++g2) {
-                const int i0 = 64 * half + 32 * g2;
-                float v[32];
-                tmem_ld32(trow + TM_S + i0, v);
+            const int i0 = 32 * quarter;
+            float v[32];
+            tmem_ld32(trow + TM_S + i0, v);
 #pragma unroll
-                for (int q8 = 0; q8 < 4; ++q8)
-                    *reinterpret_cast<uint4 *>(sm + OFF_SST + sw(jl, i0 + 8 * q8, 128)) =
-                        make_uint4(pack_f16(v[8 * q8], v[8 * q8 + 1]), pack_f16(v[8 * q8 + 2], v[8 * q8 + 3]),
-                                   pack_f16(v[8 * q8 + 4], v[8 * q8 + 5]), pack_f16(v[8 * q8 + 6], v[8 * q8 + 7]));
+            for (int q8 = 0; q8 < 4; ++q8)
+                *reinterpret_cast<uint4 *>(sm + OFF_SST + sw(jl, i0 + 8 * q8, 128)) =
+                    make_uint4(pack_f16(v[8 * q8], v[8 * q8 + 1]), pack_f16(v[8 * q8 + 2], v[8 * q8 + 3]),
+                               pack_f16(v[8 * q8 + 4], v[8 * q8 + 5]), pack_f16(v[8 * q8 + 6], v[8 * q8 + 7]));
 #pragma unroll
-                for (int c = 0; c < 32; c += 4) {
-                    const float4 d4 = *reinterpret_cast<const float4 *>(DEC + i0 + c);
-                    v[c] *= d4.x; v[c + 1] *= d4.y; v[c + 2] *= d4.z; v[c + 3] *= d4.w;
-                }
-                tmem_st32(trow + TM_S + i0, v);
+            for (int c = 0; c < 32; c += 4) {
+                const float4 d4 = *reinterpret_cast<const float4 *>(DEC + i0 + c);
+                v[c] *= d4.x; v[c + 1] *= d4.y; v[c + 2] *= d4.z; v[c + 3] *= d4.w;
             }
+            tmem_st32(trow + TM_S + i0, v);
         }
         fence_async_smem();
         tc_fence_before();
         __syncthreads();
-        // (b) U^T = U~^T + S^T (-W)^T ;  O^T = S^T Qbar^T
+        // (b) U^T = U~^T + S^T (-W)^T  [commit: U] ;  O^T = S^T Qbar^T  [committed with (d)]
         if (tid == 0) {
             tc_fence_after();
 #pragma unroll
             for (int k = 0; k < 8; ++k)
                 mma_f16_ss(tmem + TM_U, sdesc_sw128(sb + OFF_SST + (k >> 2) * 16384 + (k & 3) * 32),
                            sdesc_sw128(sb + OFF_WT + (k >> 2) * 8192 + (k & 3) * 32), IDESC_N64, 1);
+            mma_commit(bar_u);
 #pragma unroll
             for (int k = 0; k < 8; ++k)
                 mma_f16_ss(tmem + TM_O, sdesc_sw128(sb + OFF_SST + (k >> 2) * 16384 + (k & 3) * 32),
                            sdesc_sw128(sb + OFF_Q + (k >> 2) * 8192 + (k & 3) * 32), IDESC_N64, k > 0);
-            mma_commit(bar_mma);
         }
         {
-            const bool got = mbar_wait(bar_mma, mma_phase, wait_limit);
-            mma_phase ^= 1;
+            const bool got = mbar_wait(bar_u, ph_u, wait_limit);
+            ph_u ^= 1;
             if (__syncthreads_or(!got)) { ok = false; break; }
         }
         tc_fence_after();
-        if (tid == 0 && more) {   // Q and G buffers are free now
-            tma_tile(&tmq, sb + OFF_Q, bar_tma, h, t0 + C);
+        if (tid == 0 && more)   // G (V^T) was read by the U~ products, complete now
             tma_tile(&tmg, sb + OFF_G, bar_tma, h, t0 + C);
-        }
-        // (c) U^T -> fp16 hi (U^T buffer) + lo (W buffer, free once (b) completed); warp half h:
-        // columns 32h..32h+31
-        {
+        // (c) U^T -> fp16 hi (U^T buffer) + lo (W buffer, its -W has been consumed)
+        if (warp < 8) {
             float v[32];
-            tmem_ld32(trow + TM_U + 32 * half, v);
+            tmem_ld32(trow + TM_U + 32 * quarter, v);
 #pragma unroll
             for (int q8 = 0; q8 < 4; ++q8) {
                 uint32_t hi[4], lo[4];
@@ -607,7 +623,7 @@ kda_chunk_tc_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_consta
                     const float2 hf = unpack_f16(hi[e]);
                     lo[e] = pack_f16(a0 - hf.x, a1 - hf.y);
                 }
-                const uint32_t off = sw(jl, 32 * half + 8 * q8, 128);
+                const uint32_t off = sw(jl, 32 * quarter + 8 * q8, 128);
                 *reinterpret_cast<uint4 *>(sm + OFF_UST + off) = make_uint4(hi[0], hi[1], hi[2], hi[3]);
                 *reinterpret_cast<uint4 *>(sm + OFF_WT + off) = make_uint4(lo[0], lo[1], lo[2], lo[3]);
             }
@@ -615,7 +631,7 @@ kda_chunk_tc_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_consta
         fence_async_smem();
         tc_fence_before();
         __syncthreads();
-        // (d) O^T += U^T M^T (hi.hi + lo.hi + hi.lo) ;  S^T += U^T Kp
+        // (d) O^T += U^T M^T (hi.hi + lo.hi + hi.lo) [commit: O] ;  S^T += U^T Kp [commit: S]
         if (tid == 0) {
             tc_fence_after();
 #pragma unroll
@@ -627,32 +643,36 @@ kda_chunk_tc_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_consta
                 mma_f16_ss(tmem + TM_O, sdesc_sw128(sb + OFF_UST + ks * 32), sdesc_sw128(sb + OFF_MLO + ks * 32),
                            IDESC_N64, 1);
             }
+            mma_commit(bar_o);
 #pragma unroll
             for (int ks = 0; ks < 4; ++ks)
                 mma_f16_ss(tmem + TM_S, sdesc_sw128(sb + OFF_UST + ks * 32), sdesc_sw128(sb + OFF_KPT + ks * 32),
                            IDESC_N128, 1);
-            mma_commit(bar_mma);
+            mma_commit(bar_s);
         }
+        s_pending = true;
         {
-            const bool got = mbar_wait(bar_mma, mma_phase, wait_limit);
-            mma_phase ^= 1;
+            const bool got = mbar_wait(bar_o, ph_o, wait_limit);
+            ph_o ^= 1;
             if (__syncthreads_or(!got)) { ok = false; break; }
         }
         tc_fence_after();
+        if (tid == 0 && more)   // Qbar was read by the inter-chunk O products, complete now
+            tma_tile(&tmq, sb + OFF_Q, bar_tma, h, t0 + C);
         // (e) O^T -> bf16 staging tile [64 r][128 j] (over A) -> 16-byte coalesced stores
-        {
+        if (warp < 8) {
             __nv_bfloat16 *os = reinterpret_cast<__nv_bfloat16 *>(sm + OFF_AF);
             float v[32];
-            tmem_ld32(trow + TM_O + 32 * half, v);
+            tmem_ld32(trow + TM_O + 32 * quarter, v);
 #pragma unroll
-            for (int c = 0; c < 32; ++c) os[(32 * half + c) * D + jl] = __float2bfloat16_rn(v[c]);
+            for (int c = 0; c < 32; ++c) os[(32 * quarter + c) * D + jl] = __float2bfloat16_rn(v[c]);
         }
         tc_fence_before();
         __syncthreads();
         {
             const uint4 *os = reinterpret_cast<const uint4 *>(sm + OFF_AF);
 #pragma unroll
-            for (int e = 0; e < 4; ++e) {
+            for (int e = 0; e < 1024 / NT; ++e) {
                 const int idx = tid + NT * e;          // 64 rows x 16 uint4
                 const int r = idx >> 4, c16 = idx & 15;
                 if (r < nr)
@@ -662,27 +682,28 @@ kda_chunk_tc_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_consta
         __syncthreads();
     }
 
+    if (ok && s_pending) {   // the last state update
+        const bool got = mbar_wait(bar_s, ph_s, wait_limit);
+        ph_s ^= 1;
+        if (__syncthreads_or(!got)) ok = false;
+    }
     if (!ok) {
         // A bounded wait expired: let copies and MMAs in flight land (bounded
-        // again), flag the failure and mark this unit's outputs invalid.
+        // again), flag the failure and mark this unit's final state invalid.
         if (tid == 0) {
-            mbar_wait(bar_mma, mma_phase, wait_limit);
-            mbar_wait(bar_tma, tma_phase, wait_limit);
+            mbar_wait(bar_s, ph_s, wait_limit);
+            mbar_wait(bar_tma, ph_tma, wait_limit);
             atomicAdd(&g_kda_tc_timeouts, 1u);
         }
         __syncthreads();
     }
     tc_fence_after();
     if (a.sT) {
-#pragma unroll 1
-        for (int g2 = 0; g2 < 2; ++g2) {
-            const int i0 = 64 * half + 32 * g2;
-            float v[32];
-            tmem_ld32(trow + TM_S + i0, v);
+        float v[32];
+        tmem_ld32(trow + TM_S + 32 * quarter, v);
 #pragma unroll
-            for (int c = 0; c < 32; ++c)
-                a.sT[sbase + (int64_t)(i0 + c) * D + jl] = ok ? v[c] : __int_as_float(0x7fc00000);
-        }
+        for (int c = 0; c < 32; ++c)
+            a.sT[sbase + (int64_t)(32 * quarter + c) * D + jl] = ok ? v[c] : __int_as_float(0x7fc00000);
     }
     tc_fence_before();
     __syncthreads();
