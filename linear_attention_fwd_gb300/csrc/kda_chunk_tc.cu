@@ -13,7 +13,7 @@
 //     x = e^{gamma - b_I} in [e^-80, 1],  Q~ = Q x,  K~ = K x,  K^ = K / x;
 //   A_rs = beta_r (K~ K^^T)_rs * (e^{b_I - b_J} per channel, J < I),  s <  r
 //   M_rs =        (Q~ K^^T)_rs * (same), s < r;   M_rr = q_r . k_r (exact)
-//   T' = (I + A)^-1 diag(beta),  W = T' Kbar,  U~ = T' V,
+//   [W | U~] = (I + A)^-1 diag(beta) [Kbar | V]  (blocked forward solve),
 //   U = U~ - W S,  O = Qbar S + M U,  S <- Diag(e^{gamma_last}) S + Kp^T U.
 //
 // Operand precision: the sub-tile-scaled operands of A and M span
@@ -26,8 +26,8 @@
 //   SIMT      sub-tile cumulative decay, x and 1/x, scaled operands
 //   mma.sync  A and M as 16x16 sub-tile products (the per-pair decay factor is
 //             applied to the B fragments in registers)
-//   SIMT      blocked forward-substitution inverse T = (I + A)^-1
-//   mma.sync  W = T' Kbar;   tcgen05: U~^T = V^T T'^T into TMEM
+//   SIMT      16x16 diagonal inverses (I + A_II)^-1 by forward substitution
+//   mma.sync  W, U~ by a column-parallel blocked forward solve (warp-level syncs only)
 //   tcgen05   U^T = U~^T - S^T W^T,  O^T = S^T Qbar^T;  then  O^T += U^T M^T,
 //             S^T <- S^T Diag(dec) + U^T Kp  (accumulated in TMEM)
 #include <cuda.h>
@@ -62,17 +62,17 @@ __device__ __forceinline__ float ex2(float x) {
 // shared memory map, byte offsets from a 1024-aligned base
 constexpr uint32_t OFF_Q = 0;          // Q -> Q~ -> Qbar        [64 r][128 i]  swizzled
 constexpr uint32_t OFF_K = 16384;      // K -> K~ -> beta Kbar   [64 r][128 i]
-constexpr uint32_t OFF_V = 32768;      // V                      [64 r][128 j]
-constexpr uint32_t OFF_G = 49152;      // G -> K^hi (bf16) -> V^T (fp16) [128 j][64 s]
+constexpr uint32_t OFF_V = 32768;      // V (bf16)               [64 r][128 j]
+constexpr uint32_t OFF_G = 49152;      // G -> K^hi (bf16) -> U~^T hi (fp16) [128 j][64 r]
 constexpr uint32_t OFF_SST = 65536;    // S^T fp16 [128 j][128 i]; Q~hi, K~ bf16 during the prologue
 constexpr uint32_t OFF_UST = 98304;    // U^T fp16 [128 j][64 r]; Q~lo bf16 during the prologue
 constexpr uint32_t OFF_WT = 114688;    // -W fp16 [64 r][128 i]; K^lo bf16 in the prologue; U^T lo
 constexpr uint32_t OFF_KPT = 131072;   // Kp^T fp16              [128 i][64 r]
 constexpr uint32_t OFF_MT = 147456;    // M fp16                 [64 r][64 s]
-constexpr uint32_t OFF_TT = 155648;    // T fp16                 [64 r][64 s]
-constexpr uint32_t OFF_AF = 163840;    // A (fp32) -> O staging (bf16 [64 r][128 j])
+constexpr uint32_t OFF_TT = 155648;    // AT fp16: A_IJ (I > J), (I + A_II)^-1 on the diagonal
+constexpr uint32_t OFF_AF = 163840;    // A diag blocks (fp32) -> solve scratch -> O staging
 constexpr int LDA = 72;
-constexpr uint32_t OFF_TD = OFF_AF + 64 * LDA * 4;      // T dense fp32 [64][LDT]
+constexpr uint32_t OFF_TD = OFF_AF + 64 * LDA * 4;      // sub-tile sums; U~^T lo fp16 [128 j][64 r]
 constexpr int LDT = 68;
 constexpr uint32_t OFF_XS = OFF_TD + 64 * LDT * 4;      // inverse scratch [3][16][16] fp32
 constexpr uint32_t OFF_EB = OFF_XS + 3 * 256 * 4;       // e^{b_I}          [4][128]
@@ -90,7 +90,7 @@ static_assert(OFF_AF % 16 == 0 && OFF_TD % 16 == 0 && OFF_MLO % 1024 == 0 && OFF
 
 // tensor memory columns (fp32, 128 lanes)
 constexpr uint32_t TM_S = 0;     // S^T            128 columns
-constexpr uint32_t TM_U = 128;   // U~^T -> U^T     64 columns
+constexpr uint32_t TM_U = 128;   // S^T (-W)^T      64 columns
 constexpr uint32_t TM_O = 192;   // O^T             64 columns
 constexpr uint32_t TM_COLS = 256;
 
@@ -160,8 +160,8 @@ kda_chunk_tc_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_consta
 
     // mbarriers: TMA tiles landed; U^T ready; O^T ready; state update done
     const uint32_t bar_tma = sb + OFF_BAR, bar_u = sb + OFF_BAR + 8;
-    const uint32_t bar_o = sb + OFF_BAR + 16, bar_s = sb + OFF_BAR + 24;
-    volatile uint32_t *tmem_holder = reinterpret_cast<volatile uint32_t *>(sm + OFF_BAR + 32);
+    const uint32_t bar_o = sb + OFF_BAR + 16, bar_s = sb + OFF_BAR + 24, bar_q = sb + OFF_BAR + 32;
+    volatile uint32_t *tmem_holder = reinterpret_cast<volatile uint32_t *>(sm + OFF_BAR + 40);
     float *AF = reinterpret_cast<float *>(sm + OFF_AF);
     float *TD = reinterpret_cast<float *>(sm + OFF_TD);
     float *PART = TD;   // sub-tile half sums [8][128], before T is formed
@@ -179,6 +179,7 @@ kda_chunk_tc_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_consta
         mbar_init(bar_u, 1);
         mbar_init(bar_o, 1);
         mbar_init(bar_s, 1);
+        mbar_init(bar_q, 1);
         fence_mbar_init();
         prefetch_tmap(&tmq);
         prefetch_tmap(&tmk);
@@ -186,7 +187,7 @@ kda_chunk_tc_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_consta
         prefetch_tmap(&tmg);
     }
     if (warp == 0) {
-        tmem_alloc(sb + OFF_BAR + 32, TM_COLS);
+        tmem_alloc(sb + OFF_BAR + 40, TM_COLS);
         tmem_relinquish();
     }
     tc_fence_before();
@@ -225,7 +226,30 @@ kda_chunk_tc_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_consta
     __syncthreads();
     tc_fence_after();
 
-    uint32_t ph_tma = 0, ph_u = 0, ph_o = 0, ph_s = 0;
+    uint32_t ph_tma = 0, ph_u = 0, ph_o = 0, ph_s = 0, ph_q = 0;
+    bool out_pending = false;
+    int64_t t0_out = 0;
+    int nr_out = 0;
+    // O^T (TMEM) -> bf16 staging tile [64 r][128 j] over the A buffer; warp w: lanes 32(w%4)..,
+    // rows 16(w/4)..16(w/4)+15
+    auto stage_output = [&]() {
+        __nv_bfloat16 *os = reinterpret_cast<__nv_bfloat16 *>(sm + OFF_AF);
+        float v[16];
+        tmem_ld16(trow + TM_O + 16 * quarter, v);
+#pragma unroll
+        for (int c = 0; c < 16; ++c) os[(16 * quarter + c) * D + jl] = __float2bfloat16_rn(v[c]);
+    };
+    // staging tile -> out, 16-byte coalesced stores of the rows inside the sequence
+    auto store_output = [&]() {
+        const uint4 *os = reinterpret_cast<const uint4 *>(sm + OFF_AF);
+#pragma unroll
+        for (int e = 0; e < 1024 / NT; ++e) {
+            const int idx = tid + NT * e;          // 64 rows x 16 uint4
+            const int r = idx >> 4, c16 = idx & 15;
+            if (r < nr_out)
+                reinterpret_cast<uint4 *>(out + ((t0_out + r) * H + h) * D)[c16] = os[idx];
+        }
+    };
     bool ok = true, s_pending = false;
     const int cp = tid & 63, sub = tid >> 6;   // elementwise ownership: channel pair, 8-row group
     const int blk = sub >> 1, hb = sub & 1;    // sub-tile and which half of it
@@ -238,11 +262,14 @@ kda_chunk_tc_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_consta
         const bool more = ci + 1 < nchunks;
 
         if (tid < C) BETA[tid] = tid < nr ? __bfloat162float(beta[(t0 + tid) * H + h]) : 0.f;
+        if (out_pending) stage_output();   // the previous chunk's O^T
+        tc_fence_before();
         {
             const bool got = mbar_wait(bar_tma, ph_tma, wait_limit);
             ph_tma ^= 1;
             if (__syncthreads_or(!got)) { ok = false; break; }
         }
+        if (out_pending) { store_output(); out_pending = false; }
 
         // ---- (1) q_r . k_r exactly (bf16 x bf16 products are exact in fp32): the raw
         // diagonal 16x16 blocks of Q K^T on mma.sync, warps 0-3; all threads: log2-decay
@@ -355,47 +382,92 @@ kda_chunk_tc_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_consta
         }
         __syncthreads();
 
-        // ---- (3) A = beta K~ K^T and M = Q~ K^T on the 10 sub-tile pairs (I >= J), one pair per
-        // warp with independent accumulator chains; M is the 3-term product
-        // (Q~hi + Q~lo)(K^hi + K^lo)^T less the lo.lo term, with the exact q_r . k_r on its diagonal.
-        if (warp < 10) {
-            const int pi = warp;
-            const int I = pi < 4 ? 3 : (pi < 7 ? 2 : (pi < 9 ? 1 : 0));
-            const int J = pi < 4 ? pi : (pi < 7 ? pi - 4 : (pi < 9 ? pi - 7 : 0));
-            float accA[2][4], accM[3][2][4];
-#pragma unroll
-            for (int nt = 0; nt < 2; ++nt)
-#pragma unroll
-                for (int e = 0; e < 4; ++e) {
-                    accA[nt][e] = 0.f;
-                    accM[0][nt][e] = 0.f; accM[1][nt][e] = 0.f; accM[2][nt][e] = 0.f;
-                }
-            const __nv_bfloat16 *w = W6 + (J < I ? pair_index(I, J) : 0) * 128 + 2 * t4;
+        // ---- (3) A = beta K~ K^T and M = Q~ K^T on the 10 sub-tile pairs (I >= J).  Warps 0-7:
+        // the 4 diagonal pairs, one 16x8 column half each, M as the 3-term product
+        // (Q~hi + Q~lo)(K^hi + K^lo)^T less lo.lo with the exact q_r . k_r on its diagonal; the two
+        // warps of a diagonal pair then invert (I + A_II) by forward substitution.  Warps 8-13:
+        // the 6 off-diagonal pairs, single bf16 products with the per-channel factor e^{b_I - b_J}
+        // applied to the right operand.  Off-diagonal A blocks go to the fp16 tile AT, whose
+        // diagonal blocks receive T_II = (I + A_II)^-1.
+        if (warp < 8) {
+            const int I = warp >> 1, nt = warp & 1;
+            float accA[4] = {0.f, 0.f, 0.f, 0.f};
+            float accM[3][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
 #pragma unroll 4
             for (int kk = 0; kk < 8; ++kk) {
                 const uint32_t ao = sw(16 * I + (lane & 15), 16 * kk + ((lane >> 4) << 3), 64);
-                const uint32_t bo = sw(16 * J + (lane & 7) + ((lane >> 4) << 3), 16 * kk + (((lane >> 3) & 1) << 3), 64);
+                const uint32_t bo = sw(16 * I + (lane & 7) + ((lane >> 4) << 3), 16 * kk + (((lane >> 3) & 1) << 3), 64);
                 uint32_t ka[4], qh[4], ql[4], bh[4], bl[4];
                 ldsm_x4(sb + OFF_SST + 16384 + ao, ka[0], ka[1], ka[2], ka[3]);
                 ldsm_x4(sb + OFF_SST + ao, qh[0], qh[1], qh[2], qh[3]);
                 ldsm_x4(sb + OFF_UST + ao, ql[0], ql[1], ql[2], ql[3]);
                 ldsm_x4(sb + OFF_G + bo, bh[0], bh[1], bh[2], bh[3]);
                 ldsm_x4(sb + OFF_WT + bo, bl[0], bl[1], bl[2], bl[3]);
-                if (J < I) {
-                    const uint32_t wlo = *reinterpret_cast<const uint32_t *>(w + 16 * kk);
-                    const uint32_t whi = *reinterpret_cast<const uint32_t *>(w + 16 * kk + 8);
+                mma_16816(accA, ka[0], ka[1], ka[2], ka[3], bh[2 * nt], bh[2 * nt + 1]);
+                mma_16816(accM[0], qh[0], qh[1], qh[2], qh[3], bh[2 * nt], bh[2 * nt + 1]);
+                mma_16816(accM[1], ql[0], ql[1], ql[2], ql[3], bh[2 * nt], bh[2 * nt + 1]);
+                mma_16816(accM[2], qh[0], qh[1], qh[2], qh[3], bl[2 * nt], bl[2 * nt + 1]);
+            }
 #pragma unroll
-                    for (int e = 0; e < 4; e += 2) {
-                        bh[e] = mul_bf16x2(bh[e], wlo); bh[e + 1] = mul_bf16x2(bh[e + 1], whi);
-                        bl[e] = mul_bf16x2(bl[e], wlo); bl[e + 1] = mul_bf16x2(bl[e + 1], whi);
-                    }
+            for (int hh = 0; hh < 2; ++hh) {
+                const int r = 16 * I + g + 8 * hh;
+                const int s0 = 16 * I + 8 * nt + 2 * t4;
+                const float br = BETA[r];
+                AF[r * LDA + s0] = s0 < r ? br * accA[2 * hh] : 0.f;
+                AF[r * LDA + s0 + 1] = s0 + 1 < r ? br * accA[2 * hh + 1] : 0.f;
+                const float mv0 = accM[0][2 * hh] + (accM[1][2 * hh] + accM[2][2 * hh]);
+                const float mv1 = accM[0][2 * hh + 1] + (accM[1][2 * hh + 1] + accM[2][2 * hh + 1]);
+                const float m0 = s0 < r ? mv0 : (s0 == r ? MRR[r] : 0.f);
+                const float m1 = s0 + 1 < r ? mv1 : (s0 + 1 == r ? MRR[r] : 0.f);
+                const uint32_t mh = pack_f16(m0, m1);
+                const float2 mhf = unpack_f16(mh);
+                *reinterpret_cast<uint32_t *>(sm + OFF_MT + sw(r, s0, 64)) = mh;
+                *reinterpret_cast<uint32_t *>(sm + OFF_MLO + sw(r, s0, 64)) = pack_f16(m0 - mhf.x, m1 - mhf.y);
+            }
+            named_bar(1 + I, 64);   // both column halves of A_II are in place
+            if (nt == 0 && lane < 16) {
+                // column jj of T_II: t_jj = 1, t_r = -sum_{s<r} A_rs t_s (rows above jj are 0)
+                const int jj = lane;
+                const float *Ab = AF + (16 * I) * LDA + 16 * I;
+                float tcol[16];
+#pragma unroll
+                for (int r = 0; r < 16; ++r) {
+                    float acc = 0.f;
+#pragma unroll
+                    for (int s2 = 0; s2 < r; ++s2) acc = fmaf(Ab[r * LDA + s2], tcol[s2], acc);
+                    tcol[r] = r == jj ? 1.f : (r < jj ? 0.f : -acc);
                 }
+                __half *at = reinterpret_cast<__half *>(sm + OFF_TT);
+#pragma unroll
+                for (int r = 0; r < 16; ++r)
+                    at[sw(16 * I + r, 16 * I + jj, 64) >> 1] = __float2half_rn(tcol[r]);
+            }
+        } else if (warp < 14) {
+            const int po = warp - 8;   // (1,0) (2,0) (2,1) (3,0) (3,1) (3,2)
+            const int I = po < 1 ? 1 : (po < 3 ? 2 : 3);
+            const int J = po < 1 ? 0 : (po < 3 ? po - 1 : po - 3);
+            float accA[2][4], accM[2][4];
+#pragma unroll
+            for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+                for (int e = 0; e < 4; ++e) { accA[nt][e] = 0.f; accM[nt][e] = 0.f; }
+            const __nv_bfloat16 *w = W6 + pair_index(I, J) * 128 + 2 * t4;
+#pragma unroll 4
+            for (int kk = 0; kk < 8; ++kk) {
+                const uint32_t ao = sw(16 * I + (lane & 15), 16 * kk + ((lane >> 4) << 3), 64);
+                const uint32_t bo = sw(16 * J + (lane & 7) + ((lane >> 4) << 3), 16 * kk + (((lane >> 3) & 1) << 3), 64);
+                uint32_t ka[4], qh[4], bh[4];
+                ldsm_x4(sb + OFF_SST + 16384 + ao, ka[0], ka[1], ka[2], ka[3]);
+                ldsm_x4(sb + OFF_SST + ao, qh[0], qh[1], qh[2], qh[3]);
+                ldsm_x4(sb + OFF_G + bo, bh[0], bh[1], bh[2], bh[3]);
+                const uint32_t wlo = *reinterpret_cast<const uint32_t *>(w + 16 * kk);
+                const uint32_t whi = *reinterpret_cast<const uint32_t *>(w + 16 * kk + 8);
+                bh[0] = mul_bf16x2(bh[0], wlo); bh[1] = mul_bf16x2(bh[1], whi);
+                bh[2] = mul_bf16x2(bh[2], wlo); bh[3] = mul_bf16x2(bh[3], whi);
 #pragma unroll
                 for (int nt = 0; nt < 2; ++nt) {
                     mma_16816(accA[nt], ka[0], ka[1], ka[2], ka[3], bh[2 * nt], bh[2 * nt + 1]);
-                    mma_16816(accM[0][nt], qh[0], qh[1], qh[2], qh[3], bh[2 * nt], bh[2 * nt + 1]);
-                    mma_16816(accM[1][nt], ql[0], ql[1], ql[2], ql[3], bh[2 * nt], bh[2 * nt + 1]);
-                    mma_16816(accM[2][nt], qh[0], qh[1], qh[2], qh[3], bl[2 * nt], bl[2 * nt + 1]);
+                    mma_16816(accM[nt], qh[0], qh[1], qh[2], qh[3], bh[2 * nt], bh[2 * nt + 1]);
                 }
             }
 #pragma unroll
@@ -405,12 +477,9 @@ kda_chunk_tc_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_consta
                     const int r = 16 * I + g + 8 * hh;
                     const int s0 = 16 * J + 8 * nt + 2 * t4;
                     const float br = BETA[r];
-                    AF[r * LDA + s0] = s0 < r ? br * accA[nt][2 * hh] : 0.f;
-                    AF[r * LDA + s0 + 1] = s0 + 1 < r ? br * accA[nt][2 * hh + 1] : 0.f;
-                    const float mv0 = accM[0][nt][2 * hh] + (accM[1][nt][2 * hh] + accM[2][nt][2 * hh]);
-                    const float mv1 = accM[0][nt][2 * hh + 1] + (accM[1][nt][2 * hh + 1] + accM[2][nt][2 * hh + 1]);
-                    const float m0 = s0 < r ? mv0 : (s0 == r ? MRR[r] : 0.f);
-                    const float m1 = s0 + 1 < r ? mv1 : (s0 + 1 == r ? MRR[r] : 0.f);
+                    *reinterpret_cast<uint32_t *>(sm + OFF_TT + sw(r, s0, 64)) =
+                        pack_f16(br * accA[nt][2 * hh], br * accA[nt][2 * hh + 1]);
+                    const float m0 = accM[nt][2 * hh], m1 = accM[nt][2 * hh + 1];
                     const uint32_t mh = pack_f16(m0, m1);
                     const float2 mhf = unpack_f16(mh);
                     *reinterpret_cast<uint32_t *>(sm + OFF_MT + sw(r, s0, 64)) = mh;
@@ -419,149 +488,78 @@ kda_chunk_tc_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_consta
         }
         __syncthreads();
 
-        // ---- (4) V^T into the G buffer (bf16 values are exact in fp16); diagonal 16x16 blocks
-        // of T = (I + A)^-1 by forward substitution (threads 0-63, one column each); the
-        // other threads zero the upper blocks of T.
+        // ---- (4) W = T diag(beta) Kbar and U~ = T diag(beta) V, T = (I + A)^-1, as the blocked
+        // forward solve (I + A) X = diag(beta) [Kbar | V]: stage I forms
+        // Y_I = beta_I B_I - sum_{J<I} A_IJ X_J and X_I = T_II Y_I.  Each warp owns 16 of the 256
+        // right-hand-side columns through all four stages, so only warp-level syncs are needed.
+        // Outputs: -W (fp16, W buffer); U~^T as fp16 hi (over G) + lo (sums buffer).
         {
-            const int j = 2 * cp;
-            uint32_t p0[4], p1[4];
+            const bool vhalf = warp >= 8;
+            const int c0 = 16 * (warp & 7);
+            const uint32_t rhs_off = vhalf ? OFF_V : OFF_K;          // B = Kbar (fp16) or V (bf16)
+            uint8_t *ysc = sm + OFF_AF + warp * 768;                  // Y_I, 16 x 16 fp16, 48-byte rows
 #pragma unroll
-            for (int rr = 0; rr < 8; rr += 2) {
-                const int r = 16 * blk + 8 * hb + rr;
-                const float2 v0 = unpack_bf16(*reinterpret_cast<uint32_t *>(sm + OFF_V + sw(r, j, 64)));
-                const float2 v1 = unpack_bf16(*reinterpret_cast<uint32_t *>(sm + OFF_V + sw(r + 1, j, 64)));
-                p0[rr / 2] = pack_f16(v0.x, v1.x);
-                p1[rr / 2] = pack_f16(v0.y, v1.y);
-            }
-            const int rc = 16 * blk + 8 * hb;
-            *reinterpret_cast<uint4 *>(sm + OFF_G + sw(j, rc, 128)) = make_uint4(p0[0], p0[1], p0[2], p0[3]);
-            *reinterpret_cast<uint4 *>(sm + OFF_G + sw(j + 1, rc, 128)) = make_uint4(p1[0], p1[1], p1[2], p1[3]);
-        }
-        if (tid < 64) {
-            float tcol[16];
-            const int I = tid >> 4, jj = tid & 15;
-            const float *Ab = AF + (16 * I) * LDA + 16 * I;
+            for (int I = 0; I < 4; ++I) {
+                float acc[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
 #pragma unroll
-            for (int r = 0; r < 16; ++r) {
-                float acc = 0.f;
+                for (int J = 0; J < I; ++J) {
+                    uint32_t a[4], b[4];
+                    ldsm_x4(sb + OFF_TT + sw(16 * I + (lane & 15), 16 * J + ((lane >> 4) << 3), 64), a[0], a[1], a[2], a[3]);
+                    if (vhalf) { a[0] = neg_f16x2(a[0]); a[1] = neg_f16x2(a[1]); a[2] = neg_f16x2(a[2]); a[3] = neg_f16x2(a[3]); }
+                    if (vhalf)   // U~hi^T [j][r]: rows are the n index, plain ldmatrix
+                        ldsm_x4(sb + OFF_G + sw(c0 + (lane & 7) + ((lane >> 4) << 3), 16 * J + (((lane >> 3) & 1) << 3), 128),
+                                b[0], b[1], b[2], b[3]);
+                    else         // -W [r][i]: rows are the k index, transposing ldmatrix
+                        ldsm_x4_t(sb + OFF_WT + sw(16 * J + (lane & 7) + (((lane >> 3) & 1) << 3), c0 + ((lane >> 4) << 3), 64),
+                                  b[0], b[1], b[2], b[3]);
+                    mma_16816_f16(acc[0], a[0], a[1], a[2], a[3], b[0], b[1]);
+                    mma_16816_f16(acc[1], a[0], a[1], a[2], a[3], b[2], b[3]);
+                }
 #pragma unroll
-                for (int s2 = 0; s2 < r; ++s2) acc = fmaf(Ab[r * LDA + s2], tcol[s2], acc);
-                tcol[r] = r == jj ? 1.f : (r < jj ? 0.f : -acc);
-            }
+                for (int nt = 0; nt < 2; ++nt)
 #pragma unroll
-            for (int r = 0; r < 16; ++r) TD[(16 * I + r) * LDT + 16 * I + jj] = tcol[r];
-        } else {
-            for (int x = tid - 64; x < 6 * 256; x += NT - 64) {
-                const int bidx = x >> 8, e = x & 255;
-                const int I = bidx < 3 ? 0 : (bidx < 5 ? 1 : 2);
-                const int J = bidx < 3 ? bidx + 1 : (bidx < 5 ? bidx - 1 : 3);
-                TD[(16 * I + (e >> 4)) * LDT + 16 * J + (e & 15)] = 0.f;
-            }
-        }
-        __syncthreads();
-        // ---- (5) off-diagonal blocks by distance d = I - J: T_IJ = -T_II sum_{K=J}^{I-1} A_IK T_KJ;
-        // the (4 - d) blocks of a distance are spread over all threads, 256 entries each.
-        {
-            float *X = reinterpret_cast<float *>(sm + OFF_XS);
-#pragma unroll
-            for (int d = 1; d < 4; ++d) {
-                const int items = (4 - d) * 256;
-#pragma unroll
-                for (int it = tid; it < items; it += NT) {
-                    const int b = it >> 8, rr = (it >> 4) & 15, jj = it & 15;
-                    const int J = b, I = b + d;
-                    const float *arow = AF + (16 * I + rr) * LDA + 16 * J;
-                    const float *tcol_ = TD + (16 * J) * LDT + 16 * J + jj;
-                    float x[4] = {0.f, 0.f, 0.f, 0.f};
-#pragma unroll
-                    for (int k = 0; k < 16 * d; k += 4) {
-                        const float4 a4 = *reinterpret_cast<const float4 *>(arow + k);
-                        x[0] = fmaf(a4.x, tcol_[(k + 0) * LDT], x[0]);
-                        x[1] = fmaf(a4.y, tcol_[(k + 1) * LDT], x[1]);
-                        x[2] = fmaf(a4.z, tcol_[(k + 2) * LDT], x[2]);
-                        x[3] = fmaf(a4.w, tcol_[(k + 3) * LDT], x[3]);
+                    for (int hh = 0; hh < 2; ++hh) {
+                        const int r = 16 * I + g + 8 * hh;
+                        const int c = c0 + 8 * nt + 2 * t4;
+                        const uint32_t raw = *reinterpret_cast<const uint32_t *>(sm + rhs_off + sw(r, c, 64));
+                        const float2 bv = vhalf ? unpack_bf16(raw) : unpack_f16(raw);
+                        const float br = BETA[r];
+                        const float y0 = fmaf(br, bv.x, acc[nt][2 * hh]), y1 = fmaf(br, bv.y, acc[nt][2 * hh + 1]);
+                        *reinterpret_cast<uint32_t *>(ysc + (g + 8 * hh) * 48 + (8 * nt + 2 * t4) * 2) = pack_f16(y0, y1);
                     }
-                    X[it] = (x[0] + x[1]) + (x[2] + x[3]);
-                }
-                __syncthreads();
+                __syncwarp();
+                uint32_t a[4], b[4];
+                ldsm_x4(sb + OFF_TT + sw(16 * I + (lane & 15), 16 * I + ((lane >> 4) << 3), 64), a[0], a[1], a[2], a[3]);
+                ldsm_x4_t(smem_u32(ysc) + ((lane & 7) + (((lane >> 3) & 1) << 3)) * 48 + ((lane >> 4) << 3) * 2,
+                          b[0], b[1], b[2], b[3]);
+                float x[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
+                mma_16816_f16(x[0], a[0], a[1], a[2], a[3], b[0], b[1]);
+                mma_16816_f16(x[1], a[0], a[1], a[2], a[3], b[2], b[3]);
 #pragma unroll
-                for (int it = tid; it < items; it += NT) {
-                    const int b = it >> 8, rr = (it >> 4) & 15, jj = it & 15;
-                    const int J = b, I = b + d;
-                    const float *trow_ = TD + (16 * I + rr) * LDT + 16 * I;
-                    const float *xb = X + b * 256 + jj;
-                    float t[2] = {0.f, 0.f};
+                for (int nt = 0; nt < 2; ++nt)
 #pragma unroll
-                    for (int s2 = 0; s2 < 16; s2 += 4) {
-                        const float4 t4v = *reinterpret_cast<const float4 *>(trow_ + s2);
-                        t[0] = fmaf(t4v.x, xb[(s2 + 0) * 16], t[0]);
-                        t[1] = fmaf(t4v.y, xb[(s2 + 1) * 16], t[1]);
-                        t[0] = fmaf(t4v.z, xb[(s2 + 2) * 16], t[0]);
-                        t[1] = fmaf(t4v.w, xb[(s2 + 3) * 16], t[1]);
+                    for (int hh = 0; hh < 2; ++hh) {
+                        const int r = 16 * I + g + 8 * hh;
+                        const int c = c0 + 8 * nt + 2 * t4;
+                        const float x0 = x[nt][2 * hh], x1 = x[nt][2 * hh + 1];
+                        if (vhalf) {   // U~ transposed, [j][r]: hi over G, lo over the sums buffer
+                            const __half h0 = __float2half_rn(x0), h1 = __float2half_rn(x1);
+                            __half *uh = reinterpret_cast<__half *>(sm + OFF_G);
+                            __half *ul = reinterpret_cast<__half *>(sm + OFF_TD);
+                            uh[sw(c, r, 128) >> 1] = h0;
+                            uh[sw(c + 1, r, 128) >> 1] = h1;
+                            ul[sw(c, r, 128) >> 1] = __float2half_rn(x0 - __half2float(h0));
+                            ul[sw(c + 1, r, 128) >> 1] = __float2half_rn(x1 - __half2float(h1));
+                        } else {
+                            *reinterpret_cast<uint32_t *>(sm + OFF_WT + sw(r, c, 64)) = pack_f16(-x0, -x1);
+                        }
                     }
-                    TD[(16 * I + rr) * LDT + 16 * J + jj] = -(t[0] + t[1]);
-                }
-                __syncthreads();
+                __syncwarp();
             }
-        }
-        // ---- (6) T' = T diag(beta) -> fp16 tile [64 r][64 s]
-        {
-            const int r = tid >> 3, q8 = tid & 7;
-            const float *src = TD + r * LDT + 8 * q8;
-            const float *bq = BETA + 8 * q8;
-            const float4 ta = *reinterpret_cast<const float4 *>(src), tb = *reinterpret_cast<const float4 *>(src + 4);
-            const float4 ba = *reinterpret_cast<const float4 *>(bq), bb = *reinterpret_cast<const float4 *>(bq + 4);
-            *reinterpret_cast<uint4 *>(sm + OFF_TT + sw(r, 8 * q8, 64)) =
-                make_uint4(pack_f16(ta.x * ba.x, ta.y * ba.y), pack_f16(ta.z * ba.z, ta.w * ba.w),
-                           pack_f16(tb.x * bb.x, tb.y * bb.y), pack_f16(tb.z * bb.z, tb.w * bb.w));
-        }
-        fence_async_smem();
-        tc_fence_before();
-        __syncthreads();
-
-        // ---- (7) U~^T = V^T T'^T on tcgen05 (TMEM), W = T' Kbar on mma.sync
-        if (tid == 0) {
-            tc_fence_after();
-#pragma unroll
-            for (int ks = 0; ks < 4; ++ks)
-                mma_f16_ss(tmem + TM_U, sdesc_sw128(sb + OFF_G + ks * 32), sdesc_sw128(sb + OFF_TT + ks * 32),
-                           IDESC_N64, ks > 0);
-        }
-        {
-            const int I = warp & 3, cq = warp >> 2;
-            float acc[4][4];
-#pragma unroll
-            for (int x = 0; x < 4; ++x)
-#pragma unroll
-                for (int e = 0; e < 4; ++e) acc[x][e] = 0.f;
-#pragma unroll
-            for (int kk = 0; kk < 4; ++kk) {
-                uint32_t a0, a1, a2, a3;
-                ldsm_x4(sb + OFF_TT + sw(16 * I + (lane & 15), 16 * kk + ((lane >> 4) << 3), 64), a0, a1, a2, a3);
-#pragma unroll
-                for (int p = 0; p < 2; ++p) {
-                    const int i0 = 32 * cq + 16 * p;
-                    uint32_t b0, b1, b2, b3;
-                    ldsm_x4_t(sb + OFF_K + sw(16 * kk + (lane & 7) + (((lane >> 3) & 1) << 3),
-                                              i0 + ((lane >> 4) << 3), 64),
-                              b0, b1, b2, b3);
-                    mma_16816_f16(acc[2 * p], a0, a1, a2, a3, b0, b1);
-                    mma_16816_f16(acc[2 * p + 1], a0, a1, a2, a3, b2, b3);
-                }
-            }
-#pragma unroll
-            for (int x = 0; x < 4; ++x)
-#pragma unroll
-                for (int hh = 0; hh < 2; ++hh) {
-                    const int r = 16 * I + g + 8 * hh;
-                    const int i = 32 * cq + 8 * x + 2 * t4;
-                    *reinterpret_cast<uint32_t *>(sm + OFF_WT + sw(r, i, 64)) =
-                        pack_f16(-acc[x][2 * hh], -acc[x][2 * hh + 1]);
-                }
         }
         fence_async_smem();
         __syncthreads();
-        if (tid == 0 && more) {   // K and V buffers are free: prefetch the next chunk's tiles
+        if (tid == 0 && more) {   // Kbar and V are consumed: prefetch the next chunk's K and V
             fence_async_smem();
             mbar_arrive_expect_tx(bar_tma, 4 * 16384);
             tma_tile(&tmk, sb + OFF_K, bar_tma, h, t0 + C);
@@ -588,18 +586,19 @@ kda_chunk_tc_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_consta
         fence_async_smem();
         tc_fence_before();
         __syncthreads();
-        // (b) U^T = U~^T + S^T (-W)^T  [commit: U] ;  O^T = S^T Qbar^T  [committed with (d)]
+        // (b) U^T = S^T (-W)^T  [commit: U] ;  O^T = S^T Qbar^T  [commit: Q]
         if (tid == 0) {
             tc_fence_after();
 #pragma unroll
             for (int k = 0; k < 8; ++k)
                 mma_f16_ss(tmem + TM_U, sdesc_sw128(sb + OFF_SST + (k >> 2) * 16384 + (k & 3) * 32),
-                           sdesc_sw128(sb + OFF_WT + (k >> 2) * 8192 + (k & 3) * 32), IDESC_N64, 1);
+                           sdesc_sw128(sb + OFF_WT + (k >> 2) * 8192 + (k & 3) * 32), IDESC_N64, k > 0);
             mma_commit(bar_u);
 #pragma unroll
             for (int k = 0; k < 8; ++k)
                 mma_f16_ss(tmem + TM_O, sdesc_sw128(sb + OFF_SST + (k >> 2) * 16384 + (k & 3) * 32),
                            sdesc_sw128(sb + OFF_Q + (k >> 2) * 8192 + (k & 3) * 32), IDESC_N64, k > 0);
+            mma_commit(bar_q);
         }
         {
             const bool got = mbar_wait(bar_u, ph_u, wait_limit);
@@ -607,30 +606,50 @@ kda_chunk_tc_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_consta
             if (__syncthreads_or(!got)) { ok = false; break; }
         }
         tc_fence_after();
-        if (tid == 0 && more)   // G (V^T) was read by the U~ products, complete now
-            tma_tile(&tmg, sb + OFF_G, bar_tma, h, t0 + C);
-        // (c) U^T -> fp16 hi (U^T buffer) + lo (W buffer, its -W has been consumed)
-        if (warp < 8) {
-            float v[32];
-            tmem_ld32(trow + TM_U + 32 * quarter, v);
+        // (c) U = U~ + S^T(-W)^T -> fp16 hi (U^T buffer) + lo (W buffer, its -W has been consumed);
+        // warp w: lanes 32(w%4).., columns 16(w/4)..16(w/4)+15
+        {
+            const int r0 = 16 * quarter;
+            float v[16];
+            tmem_ld16(trow + TM_U + r0, v);
+            uint32_t uh[8], ul[8];   // U~^T row jl, columns r0..r0+15, hi and lo
+            {
+                const uint4 h0 = *reinterpret_cast<const uint4 *>(sm + OFF_G + sw(jl, r0, 128));
+                const uint4 h1 = *reinterpret_cast<const uint4 *>(sm + OFF_G + sw(jl, r0 + 8, 128));
+                const uint4 l0 = *reinterpret_cast<const uint4 *>(sm + OFF_TD + sw(jl, r0, 128));
+                const uint4 l1 = *reinterpret_cast<const uint4 *>(sm + OFF_TD + sw(jl, r0 + 8, 128));
+                uh[0] = h0.x; uh[1] = h0.y; uh[2] = h0.z; uh[3] = h0.w; uh[4] = h1.x; uh[5] = h1.y; uh[6] = h1.z; uh[7] = h1.w;
+                ul[0] = l0.x; ul[1] = l0.y; ul[2] = l0.z; ul[3] = l0.w; ul[4] = l1.x; ul[5] = l1.y; ul[6] = l1.z; ul[7] = l1.w;
+            }
+            uint32_t hi[8], lo[8];
 #pragma unroll
-            for (int q8 = 0; q8 < 4; ++q8) {
-                uint32_t hi[4], lo[4];
+            for (int e = 0; e < 8; ++e) {
+                const float2 fh = unpack_f16(uh[e]), fl = unpack_f16(ul[e]);
+                const float a0 = v[2 * e] + (fh.x + fl.x);
+                const float a1 = v[2 * e + 1] + (fh.y + fl.y);
+                hi[e] = pack_f16(a0, a1);
+                const float2 hf = unpack_f16(hi[e]);
+                lo[e] = pack_f16(a0 - hf.x, a1 - hf.y);
+            }
 #pragma unroll
-                for (int e = 0; e < 4; ++e) {
-                    const float a0 = v[8 * q8 + 2 * e], a1 = v[8 * q8 + 2 * e + 1];
-                    hi[e] = pack_f16(a0, a1);
-                    const float2 hf = unpack_f16(hi[e]);
-                    lo[e] = pack_f16(a0 - hf.x, a1 - hf.y);
-                }
-                const uint32_t off = sw(jl, 32 * quarter + 8 * q8, 128);
-                *reinterpret_cast<uint4 *>(sm + OFF_UST + off) = make_uint4(hi[0], hi[1], hi[2], hi[3]);
-                *reinterpret_cast<uint4 *>(sm + OFF_WT + off) = make_uint4(lo[0], lo[1], lo[2], lo[3]);
+            for (int q8 = 0; q8 < 2; ++q8) {
+                const uint32_t off = sw(jl, r0 + 8 * q8, 128);
+                *reinterpret_cast<uint4 *>(sm + OFF_UST + off) = make_uint4(hi[4 * q8], hi[4 * q8 + 1], hi[4 * q8 + 2], hi[4 * q8 + 3]);
+                *reinterpret_cast<uint4 *>(sm + OFF_WT + off) = make_uint4(lo[4 * q8], lo[4 * q8 + 1], lo[4 * q8 + 2], lo[4 * q8 + 3]);
             }
         }
         fence_async_smem();
         tc_fence_before();
         __syncthreads();
+        bool gq = true;
+        if (tid == 0) {   // Qbar (read by the O^T = S^T Qbar^T group) and U~hi (over G) are consumed
+            gq = mbar_wait(bar_q, ph_q, wait_limit);
+            if (gq && more) {
+                tma_tile(&tmq, sb + OFF_Q, bar_tma, h, t0 + C);
+                tma_tile(&tmg, sb + OFF_G, bar_tma, h, t0 + C);
+            }
+        }
+        ph_q ^= 1;
         // (d) O^T += U^T M^T (hi.hi + lo.hi + hi.lo) [commit: O] ;  S^T += U^T Kp [commit: S]
         if (tid == 0) {
             tc_fence_after();
@@ -654,34 +673,22 @@ kda_chunk_tc_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_consta
         {
             const bool got = mbar_wait(bar_o, ph_o, wait_limit);
             ph_o ^= 1;
-            if (__syncthreads_or(!got)) { ok = false; break; }
+            if (__syncthreads_or(!got || !gq)) { ok = false; break; }
         }
         tc_fence_after();
-        if (tid == 0 && more)   // Qbar was read by the inter-chunk O products, complete now
-            tma_tile(&tmq, sb + OFF_Q, bar_tma, h, t0 + C);
-        // (e) O^T -> bf16 staging tile [64 r][128 j] (over A) -> 16-byte coalesced stores
-        if (warp < 8) {
-            __nv_bfloat16 *os = reinterpret_cast<__nv_bfloat16 *>(sm + OFF_AF);
-            float v[32];
-            tmem_ld32(trow + TM_O + 32 * quarter, v);
-#pragma unroll
-            for (int c = 0; c < 32; ++c) os[(32 * quarter + c) * D + jl] = __float2bfloat16_rn(v[c]);
-        }
-        tc_fence_before();
-        __syncthreads();
-        {
-            const uint4 *os = reinterpret_cast<const uint4 *>(sm + OFF_AF);
-#pragma unroll
-            for (int e = 0; e < 1024 / NT; ++e) {
-                const int idx = tid + NT * e;          // 64 rows x 16 uint4
-                const int r = idx >> 4, c16 = idx & 15;
-                if (r < nr)
-                    reinterpret_cast<uint4 *>(out + ((t0 + r) * H + h) * D)[c16] = os[idx];
-            }
-        }
-        __syncthreads();
+        // (e) the output of this chunk is staged and stored during the next chunk's first phases
+        out_pending = true;
+        t0_out = t0;
+        nr_out = nr;
     }
 
+    if (ok && out_pending) {   // the last chunk's output
+        stage_output();
+        tc_fence_before();
+        __syncthreads();
+        store_output();
+        __syncthreads();
+    }
     if (ok && s_pending) {   // the last state update
         const bool got = mbar_wait(bar_s, ph_s, wait_limit);
         ph_s ^= 1;
