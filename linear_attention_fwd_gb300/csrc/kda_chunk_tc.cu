@@ -1,7 +1,7 @@
 // KDA chunkwise forward on the sm_103a tensor cores (tcgen05 + TMEM + TMA).
 //
 // bf16 inputs/outputs, d_k = d_v = 128, chunk C = 64, fp32 recurrent state.
-// One CTA (8 warps) per (sequence, head); the fp32 state lives in tensor
+// One CTA (16 warps) per (sequence, head); the fp32 state lives in tensor
 // memory for the whole sequence (transposed: TMEM lane j = value channel,
 // column i = key channel), so the only HBM traffic is the q/k/v/g/beta tiles,
 // the output, and the initial / final states.
@@ -13,23 +13,24 @@
 //     x = e^{gamma - b_I} in [e^-80, 1],  Q~ = Q x,  K~ = K x,  K^ = K / x;
 //   A_rs = beta_r (K~ K^^T)_rs * (e^{b_I - b_J} per channel, J < I),  s <  r
 //   M_rs =        (Q~ K^^T)_rs * (same), s < r;   M_rr = q_r . k_r (exact)
-//   [W | U~] = (I + A)^-1 diag(beta) [Kbar | V]  (blocked forward solve),
-//   U = U~ - W S,  O = Qbar S + M U,  S <- Diag(e^{gamma_last}) S + Kp^T U.
+//   T = (I + A)^-1 (16x16 diagonal inverses, then the off-diagonal blocks level by level)
+//   U = T diag(beta) (V - Kbar S),  O = Qbar S + M U,  S <- Diag(e^{gamma_last}) S + Kp^T U.
 //
 // Operand precision: the sub-tile-scaled operands of A and M span
 // [e^-80, e^80] and are bf16 (the range the decay bound was chosen for); every
-// other tensor-core operand (S, U, W, T, Qbar, Kp, beta V, M) is O(1) and is
-// rounded to fp16 for 3 more mantissa bits; accumulation is fp32 throughout.
+// other tensor-core operand (S, V - Kbar S, T, U, Qbar, Kbar, Kp, M) is O(1) and
+// is rounded to fp16 for 3 more mantissa bits; accumulation is fp32 throughout.
 //
-// Per chunk:
+// Per chunk (the fp16 copies of S, beta (V - Kbar S) and U are tensor-memory
+// operands, so the state path never goes through shared memory):
 //   TMA       Q, K, V, G tiles (64 x 128 bf16, 128-byte swizzle) -> smem
-//   SIMT      sub-tile cumulative decay, x and 1/x, scaled operands
+//   SIMT      sub-tile cumulative decay, x and 1/x, scaled operands; S -> fp16
+//   tcgen05   P^T = S^T Kbar^T,  O^T = S^T Qbar^T           (overlapping the next two steps)
 //   mma.sync  A and M as 16x16 sub-tile products (the per-pair decay factor is
-//             applied to the B fragments in registers)
-//   SIMT      16x16 diagonal inverses (I + A_II)^-1 by forward substitution
-//   mma.sync  W, U~ by a column-parallel blocked forward solve (warp-level syncs only)
-//   tcgen05   U^T = U~^T - S^T W^T,  O^T = S^T Qbar^T;  then  O^T += U^T M^T,
-//             S^T <- S^T Diag(dec) + U^T Kp  (accumulated in TMEM)
+//             applied to the B fragments in registers); diagonal inverses by
+//             forward substitution; off-diagonal blocks of T
+//   SIMT      Z^T = (V^T - P^T) diag(beta) -> fp16
+//   tcgen05   U^T = Z^T T^T;  then  S^T <- S^T Diag(dec) + U^T Kp,  O^T += U^T M^T
 #include <cuda.h>
 #include <cudaTypedefs.h>
 #include <cuda_bf16.h>
@@ -60,39 +61,46 @@ __device__ __forceinline__ float ex2(float x) {
 }
 
 // shared memory map, byte offsets from a 1024-aligned base
-constexpr uint32_t OFF_Q = 0;          // Q -> Q~ -> Qbar        [64 r][128 i]  swizzled
-constexpr uint32_t OFF_K = 16384;      // K -> K~ -> beta Kbar   [64 r][128 i]
-constexpr uint32_t OFF_V = 32768;      // V (bf16)               [64 r][128 j]
-constexpr uint32_t OFF_G = 49152;      // G -> K^hi (bf16) -> U~^T hi (fp16) [128 j][64 r]
-constexpr uint32_t OFF_SST = 65536;    // S^T fp16 [128 j][128 i]; Q~hi, K~ bf16 during the prologue
-constexpr uint32_t OFF_UST = 98304;    // U^T fp16 [128 j][64 r]; Q~lo bf16 during the prologue
-constexpr uint32_t OFF_WT = 114688;    // -W fp16 [64 r][128 i]; K^lo bf16 in the prologue; U^T lo
-constexpr uint32_t OFF_KPT = 131072;   // Kp^T fp16              [128 i][64 r]
-constexpr uint32_t OFF_MT = 147456;    // M fp16                 [64 r][64 s]
-constexpr uint32_t OFF_TT = 155648;    // AT fp16: A_IJ (I > J), (I + A_II)^-1 on the diagonal
-constexpr uint32_t OFF_AF = 163840;    // A diag blocks (fp32) -> solve scratch -> O staging
+constexpr uint32_t OFF_Q = 0;          // Q -> Qbar (fp16)         [64 r][128 i]  swizzled
+constexpr uint32_t OFF_K = 16384;      // K -> Kbar (fp16)         [64 r][128 i]
+constexpr uint32_t OFF_V = 32768;      // V (bf16)                 [64 r][128 j]
+constexpr uint32_t OFF_G = 49152;      // G -> K^hi (bf16)         [64 r][128 i]
+constexpr uint32_t OFF_SST = 65536;    // Q~hi, K~ (bf16)          2 x [64 r][128 i]
+constexpr uint32_t OFF_UST = 98304;    // Q~lo (bf16)              [64 r][128 i]
+constexpr uint32_t OFF_WT = 114688;    // K^lo (bf16)              [64 r][128 i]
+constexpr uint32_t OFF_KPT = 131072;   // Kp^T fp16                [128 i][64 r]
+constexpr uint32_t OFF_MT = 147456;    // M fp16                   [64 r][64 s]
+constexpr uint32_t OFF_TT = 155648;    // A_IJ (I > J) fp16        [64 r][64 s]
+constexpr uint32_t OFF_AF = 163840;    // A diagonal blocks (fp32) -> output staging
 constexpr int LDA = 72;
-constexpr uint32_t OFF_TD = OFF_AF + 64 * LDA * 4;      // sub-tile sums; U~^T lo fp16 [128 j][64 r]
-constexpr int LDT = 68;
-constexpr uint32_t OFF_XS = OFF_TD + 64 * LDT * 4;      // inverse scratch [3][16][16] fp32
-constexpr uint32_t OFF_EB = OFF_XS + 3 * 256 * 4;       // e^{b_I}          [4][128]
+constexpr uint32_t OFF_PART = OFF_AF + 64 * LDA * 4;    // sub-tile half sums [8][128] fp32
+constexpr uint32_t OFF_T = (OFF_PART + 8 * 128 * 4 + 1023) / 1024 * 1024;   // T fp16 [64 r][64 s]
+constexpr uint32_t OFF_EB = OFF_T + 8192;               // e^{b_I}          [4][128]
 constexpr uint32_t OFF_EL = OFF_EB + 4 * 128 * 4;       // e^{gl - b_I}     [4][128]
 constexpr uint32_t OFF_W6 = OFF_EL + 4 * 128 * 4;       // e^{b_I - b_J}    [6][128] bf16
 constexpr uint32_t OFF_DEC = OFF_W6 + 6 * 128 * 2;      // e^{gl}           [128]
 constexpr uint32_t OFF_BETA = OFF_DEC + 128 * 4;        // beta             [64]
 constexpr uint32_t OFF_MRR = OFF_BETA + 64 * 4;         // q_r . k_r        [64]
 constexpr uint32_t OFF_MLO = (OFF_MRR + 64 * 4 + 1023) / 1024 * 1024;   // M - fp16(M), fp16 [64 r][64 s]
-constexpr uint32_t OFF_BAR = OFF_MLO + 8192;            // 4 mbarriers, TMEM address
+constexpr uint32_t OFF_BAR = OFF_MLO + 8192;            // 6 mbarriers, TMEM address
 constexpr uint32_t SMEM_USED = OFF_BAR + 64;
 constexpr uint32_t SMEM_BYTES = SMEM_USED + 1024;       // + alignment slack
 static_assert(SMEM_BYTES <= 227 * 1024, "shared memory budget");
-static_assert(OFF_AF % 16 == 0 && OFF_TD % 16 == 0 && OFF_MLO % 1024 == 0 && OFF_BAR % 8 == 0, "alignment");
+static_assert(OFF_AF % 16 == 0 && OFF_PART % 16 == 0 && OFF_T % 1024 == 0 && OFF_MLO % 1024 == 0 &&
+                  OFF_BAR % 8 == 0,
+              "alignment");
+static_assert(64 * 128 * 2 <= 64 * LDA * 4, "output staging fits over the A blocks");
 
-// tensor memory columns (fp32, 128 lanes)
-constexpr uint32_t TM_S = 0;     // S^T            128 columns
-constexpr uint32_t TM_U = 128;   // S^T (-W)^T      64 columns
-constexpr uint32_t TM_O = 192;   // O^T             64 columns
-constexpr uint32_t TM_COLS = 256;
+// tensor memory columns (128 lanes = value channel j)
+constexpr uint32_t TM_S = 0;      // S^T fp32                        128 columns
+constexpr uint32_t TM_P = 128;    // P^T = S^T Kbar^T fp32            64
+constexpr uint32_t TM_O = 192;    // O^T fp32                         64
+constexpr uint32_t TM_U = 256;    // U^T fp32                         64
+constexpr uint32_t TM_S16 = 320;  // S^T as fp16 pairs (MMA operand)  64
+constexpr uint32_t TM_Z = 384;    // Z^T fp16 pairs                   32
+constexpr uint32_t TM_UH = 416;   // U^T fp16 pairs, hi               32
+constexpr uint32_t TM_UL = 448;   // U^T - hi, fp16 pairs             32
+constexpr uint32_t TM_COLS = 512;
 
 constexpr uint32_t IDESC_N64 = idesc_f16_f32(128, 64);
 constexpr uint32_t IDESC_N128 = idesc_f16_f32(128, 128);
@@ -158,13 +166,13 @@ kda_chunk_tc_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_consta
     const int64_t len = eos - bos;
     const int nchunks = (int)((len + C - 1) / C);
 
-    // mbarriers: TMA tiles landed; U^T ready; O^T ready; state update done
-    const uint32_t bar_tma = sb + OFF_BAR, bar_u = sb + OFF_BAR + 8;
-    const uint32_t bar_o = sb + OFF_BAR + 16, bar_s = sb + OFF_BAR + 24, bar_q = sb + OFF_BAR + 32;
-    volatile uint32_t *tmem_holder = reinterpret_cast<volatile uint32_t *>(sm + OFF_BAR + 40);
+    // mbarriers: TMA tiles landed; P^T done; O^T = S^T Qbar^T done; U^T done; state update done;
+    // O^T += U^T M^T done
+    const uint32_t bar_tma = sb + OFF_BAR, bar_p = sb + OFF_BAR + 8, bar_q = sb + OFF_BAR + 16;
+    const uint32_t bar_u = sb + OFF_BAR + 24, bar_s = sb + OFF_BAR + 32, bar_o = sb + OFF_BAR + 40;
+    volatile uint32_t *tmem_holder = reinterpret_cast<volatile uint32_t *>(sm + OFF_BAR + 48);
     float *AF = reinterpret_cast<float *>(sm + OFF_AF);
-    float *TD = reinterpret_cast<float *>(sm + OFF_TD);
-    float *PART = TD;   // sub-tile half sums [8][128], before T is formed
+    float *PART = reinterpret_cast<float *>(sm + OFF_PART);
     float *EB = reinterpret_cast<float *>(sm + OFF_EB);
     float *EL = reinterpret_cast<float *>(sm + OFF_EL);
     __nv_bfloat16 *W6 = reinterpret_cast<__nv_bfloat16 *>(sm + OFF_W6);
@@ -176,10 +184,11 @@ kda_chunk_tc_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_consta
 
     if (tid == 0) {
         mbar_init(bar_tma, 1);
-        mbar_init(bar_u, 1);
-        mbar_init(bar_o, 1);
-        mbar_init(bar_s, 1);
+        mbar_init(bar_p, 1);
         mbar_init(bar_q, 1);
+        mbar_init(bar_u, 1);
+        mbar_init(bar_s, 1);
+        mbar_init(bar_o, 1);
         fence_mbar_init();
         prefetch_tmap(&tmq);
         prefetch_tmap(&tmk);
@@ -187,7 +196,7 @@ kda_chunk_tc_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_consta
         prefetch_tmap(&tmg);
     }
     if (warp == 0) {
-        tmem_alloc(sb + OFF_BAR + 40, TM_COLS);
+        tmem_alloc(sb + OFF_BAR + 48, TM_COLS);
         tmem_relinquish();
     }
     tc_fence_before();
@@ -196,7 +205,7 @@ kda_chunk_tc_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_consta
     const uint32_t tmem = *tmem_holder;
     const uint32_t trow = tmem + ((uint32_t)((warp & 3) * 32) << 16);   // this warp's TMEM lanes
     const int jl = 32 * (warp & 3) + lane;   // this thread's TMEM lane (value channel j)
-    const int quarter = warp >> 2;           // which 32-column group this warp handles (0..3)
+    const int quarter = warp >> 2;           // which column group this warp handles (0..3)
 
     // ---- initial state -> TMEM (S^T: lane j, column i)
     const int64_t sbase = ((int64_t)n * H + h) * D * D;
@@ -214,20 +223,21 @@ kda_chunk_tc_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_consta
         tma_tile(&tmv, sb + OFF_V, bar_tma, h, bos);
         tma_tile(&tmg, sb + OFF_G, bar_tma, h, bos);
     }
-    // the blocks of M above the diagonal blocks stay zero for the whole sequence
+    // the blocks of M and T above the diagonal blocks stay zero for the whole sequence
     for (int x = tid; x < 64 * 32; x += NT) {
         const int r = x >> 5, s2 = 2 * (x & 31);
         if ((s2 >> 4) > (r >> 4)) {
             *reinterpret_cast<uint32_t *>(sm + OFF_MT + sw(r, s2, 64)) = 0u;
             *reinterpret_cast<uint32_t *>(sm + OFF_MLO + sw(r, s2, 64)) = 0u;
+            *reinterpret_cast<uint32_t *>(sm + OFF_T + sw(r, s2, 64)) = 0u;
         }
     }
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
 
-    uint32_t ph_tma = 0, ph_u = 0, ph_o = 0, ph_s = 0, ph_q = 0;
-    bool out_pending = false;
+    uint32_t ph_tma = 0, ph_p = 0, ph_q = 0, ph_u = 0, ph_s = 0, ph_o = 0;
+    bool out_pending = false;   // the previous chunk's state update and O^T group are in flight
     int64_t t0_out = 0;
     int nr_out = 0;
     // O^T (TMEM) -> bf16 staging tile [64 r][128 j] over the A buffer; warp w: lanes 32(w%4)..,
@@ -250,7 +260,34 @@ kda_chunk_tc_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_consta
                 reinterpret_cast<uint4 *>(out + ((t0_out + r) * H + h) * D)[c16] = os[idx];
         }
     };
-    bool ok = true, s_pending = false;
+    // T_IJ = -(sum_{K=J+1..I} T_IK A_KJ) T_JJ for one 16x16 block below the diagonal (one warp)
+    auto t_block = [&](int I, int J) {
+        float acc[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
+        for (int K = J + 1; K <= I; ++K) {
+            uint32_t a4[4], b4[4];
+            ldsm_x4(sb + OFF_T + sw(16 * I + (lane & 15), 16 * K + ((lane >> 4) << 3), 64), a4[0], a4[1], a4[2], a4[3]);
+            ldsm_x4_t(sb + OFF_TT + sw(16 * K + (lane & 7) + (((lane >> 3) & 1) << 3), 16 * J + ((lane >> 4) << 3), 64),
+                      b4[0], b4[1], b4[2], b4[3]);
+            mma_16816_f16(acc[0], a4[0], a4[1], a4[2], a4[3], b4[0], b4[1]);
+            mma_16816_f16(acc[1], a4[0], a4[1], a4[2], a4[3], b4[2], b4[3]);
+        }
+        // the accumulator fragments of Y are the A fragments of Y T_JJ
+        const uint32_t y0 = neg_f16x2(pack_f16(acc[0][0], acc[0][1])), y1 = neg_f16x2(pack_f16(acc[0][2], acc[0][3]));
+        const uint32_t y2 = neg_f16x2(pack_f16(acc[1][0], acc[1][1])), y3 = neg_f16x2(pack_f16(acc[1][2], acc[1][3]));
+        uint32_t b4[4];
+        ldsm_x4_t(sb + OFF_T + sw(16 * J + (lane & 7) + (((lane >> 3) & 1) << 3), 16 * J + ((lane >> 4) << 3), 64),
+                  b4[0], b4[1], b4[2], b4[3]);
+        float x[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
+        mma_16816_f16(x[0], y0, y1, y2, y3, b4[0], b4[1]);
+        mma_16816_f16(x[1], y0, y1, y2, y3, b4[2], b4[3]);
+#pragma unroll
+        for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+            for (int hh = 0; hh < 2; ++hh)
+                *reinterpret_cast<uint32_t *>(sm + OFF_T + sw(16 * I + (lane >> 2) + 8 * hh, 16 * J + 8 * nt + 2 * (lane & 3), 64)) =
+                    pack_f16(x[nt][2 * hh], x[nt][2 * hh + 1]);
+    };
+    bool ok = true;
     const int cp = tid & 63, sub = tid >> 6;   // elementwise ownership: channel pair, 8-row group
     const int blk = sub >> 1, hb = sub & 1;    // sub-tile and which half of it
     const int t4 = lane & 3, g = lane >> 2;    // mma.sync fragment coordinates
@@ -262,14 +299,11 @@ kda_chunk_tc_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_consta
         const bool more = ci + 1 < nchunks;
 
         if (tid < C) BETA[tid] = tid < nr ? __bfloat162float(beta[(t0 + tid) * H + h]) : 0.f;
-        if (out_pending) stage_output();   // the previous chunk's O^T
-        tc_fence_before();
         {
             const bool got = mbar_wait(bar_tma, ph_tma, wait_limit);
             ph_tma ^= 1;
             if (__syncthreads_or(!got)) { ok = false; break; }
         }
-        if (out_pending) { store_output(); out_pending = false; }
 
         // ---- (1) q_r . k_r exactly (bf16 x bf16 products are exact in fp32): the raw
         // diagonal 16x16 blocks of Q K^T on mma.sync, warps 0-3; all threads: log2-decay
@@ -323,16 +357,40 @@ kda_chunk_tc_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_consta
             }
             DEC[c] = ex2(gl);
         }
-        // the previous chunk's state update still reads the U^T buffer: wait for it
-        if (s_pending) {
-            const bool got = mbar_wait(bar_s, ph_s, wait_limit);
+        // the previous chunk's state update and O^T group: then its output is staged
+        if (out_pending) {
+            const bool gs = mbar_wait(bar_s, ph_s, wait_limit);
+            const bool go = mbar_wait(bar_o, ph_o, wait_limit);
             ph_s ^= 1;
-            s_pending = false;
-            if (__syncthreads_or(!got)) { ok = false; break; }
+            ph_o ^= 1;
+            if (__syncthreads_or(!(gs && go))) { ok = false; break; }
+            tc_fence_after();
+            stage_output();
         } else {
             __syncthreads();
+            tc_fence_after();
         }
-        tc_fence_after();
+        // ---- (a) S^T -> fp16 pairs (the MMA operand), then S^T <- S^T Diag(dec) in place
+        {
+            const int i0 = 32 * quarter;
+            float v[32];
+            tmem_ld32(trow + TM_S + i0, v);
+            uint32_t hv[16];
+#pragma unroll
+            for (int c = 0; c < 16; ++c) hv[c] = pack_f16(v[2 * c], v[2 * c + 1]);
+            tmem_st16u(trow + TM_S16 + i0 / 2, hv);
+#pragma unroll
+            for (int c = 0; c < 32; c += 4) {
+                const float4 d4 = *reinterpret_cast<const float4 *>(DEC + i0 + c);
+                v[c] *= d4.x; v[c + 1] *= d4.y; v[c + 2] *= d4.z; v[c + 3] *= d4.w;
+            }
+            tmem_st32(trow + TM_S + i0, v);
+        }
+        if (out_pending) {
+            __syncthreads();   // the staging tile is complete
+            store_output();
+            out_pending = false;
+        }
 
         // ---- (2) operands, each rounded from the exact inputs:
         //   bf16 (range e^+-80): Q~ = Q x as hi + lo (S^T and U^T buffers, idle here),
@@ -380,15 +438,32 @@ kda_chunk_tc_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_consta
             *reinterpret_cast<uint4 *>(sm + OFF_KPT + sw(c, rc, 128)) = make_uint4(p0[0], p0[1], p0[2], p0[3]);
             *reinterpret_cast<uint4 *>(sm + OFF_KPT + sw(c + 1, rc, 128)) = make_uint4(p1[0], p1[1], p1[2], p1[3]);
         }
+
+        fence_async_smem();
+        tc_fence_before();
         __syncthreads();
+        // P^T = S^T Kbar^T [commit: P] ;  O^T = S^T Qbar^T [commit: Q] -- both run during (3)
+        if (tid == 0) {
+            tc_fence_after();
+#pragma unroll
+            for (int k = 0; k < 8; ++k)
+                mma_f16_ts(tmem + TM_P, tmem + TM_S16 + 8 * k,
+                           sdesc_sw128(sb + OFF_K + (k >> 2) * 8192 + (k & 3) * 32), IDESC_N64, k > 0);
+            mma_commit(bar_p);
+#pragma unroll
+            for (int k = 0; k < 8; ++k)
+                mma_f16_ts(tmem + TM_O, tmem + TM_S16 + 8 * k,
+                           sdesc_sw128(sb + OFF_Q + (k >> 2) * 8192 + (k & 3) * 32), IDESC_N64, k > 0);
+            mma_commit(bar_q);
+        }
 
         // ---- (3) A = beta K~ K^T and M = Q~ K^T on the 10 sub-tile pairs (I >= J).  Warps 0-7:
         // the 4 diagonal pairs, one 16x8 column half each, M as the 3-term product
         // (Q~hi + Q~lo)(K^hi + K^lo)^T less lo.lo with the exact q_r . k_r on its diagonal; the two
         // warps of a diagonal pair then invert (I + A_II) by forward substitution.  Warps 8-13:
         // the 6 off-diagonal pairs, single bf16 products with the per-channel factor e^{b_I - b_J}
-        // applied to the right operand.  Off-diagonal A blocks go to the fp16 tile AT, whose
-        // diagonal blocks receive T_II = (I + A_II)^-1.
+        // applied to the right operand.  Off-diagonal A blocks go to the fp16 tile AT; T_II = (I + A_II)^-1 goes to the
+        // diagonal blocks of the fp16 tile T.
         if (warp < 8) {
             const int I = warp >> 1, nt = warp & 1;
             float accA[4] = {0.f, 0.f, 0.f, 0.f};
@@ -437,7 +512,7 @@ kda_chunk_tc_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_consta
                     for (int s2 = 0; s2 < r; ++s2) acc = fmaf(Ab[r * LDA + s2], tcol[s2], acc);
                     tcol[r] = r == jj ? 1.f : (r < jj ? 0.f : -acc);
                 }
-                __half *at = reinterpret_cast<__half *>(sm + OFF_TT);
+                __half *at = reinterpret_cast<__half *>(sm + OFF_T);
 #pragma unroll
                 for (int r = 0; r < 16; ++r)
                     at[sw(16 * I + r, 16 * I + jj, 64) >> 1] = __float2half_rn(tcol[r]);
@@ -488,117 +563,57 @@ kda_chunk_tc_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_consta
         }
         __syncthreads();
 
-        // ---- (4) W = T diag(beta) Kbar and U~ = T diag(beta) V, T = (I + A)^-1, as the blocked
-        // forward solve (I + A) X = diag(beta) [Kbar | V]: stage I forms
-        // Y_I = beta_I B_I - sum_{J<I} A_IJ X_J and X_I = T_II Y_I.  Each warp owns 16 of the 256
-        // right-hand-side columns through all four stages, so only warp-level syncs are needed.
-        // Outputs: -W (fp16, W buffer); U~^T as fp16 hi (over G) + lo (sums buffer).
-        {
-            const bool vhalf = warp >= 8;
-            const int c0 = 16 * (warp & 7);
-            const uint32_t rhs_off = vhalf ? OFF_V : OFF_K;          // B = Kbar (fp16) or V (bf16)
-            uint8_t *ysc = sm + OFF_AF + warp * 768;                  // Y_I, 16 x 16 fp16, 48-byte rows
-#pragma unroll
-            for (int I = 0; I < 4; ++I) {
-                float acc[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
-#pragma unroll
-                for (int J = 0; J < I; ++J) {
-                    uint32_t a[4], b[4];
-                    ldsm_x4(sb + OFF_TT + sw(16 * I + (lane & 15), 16 * J + ((lane >> 4) << 3), 64), a[0], a[1], a[2], a[3]);
-                    if (vhalf) { a[0] = neg_f16x2(a[0]); a[1] = neg_f16x2(a[1]); a[2] = neg_f16x2(a[2]); a[3] = neg_f16x2(a[3]); }
-                    if (vhalf)   // U~hi^T [j][r]: rows are the n index, plain ldmatrix
-                        ldsm_x4(sb + OFF_G + sw(c0 + (lane & 7) + ((lane >> 4) << 3), 16 * J + (((lane >> 3) & 1) << 3), 128),
-                                b[0], b[1], b[2], b[3]);
-                    else         // -W [r][i]: rows are the k index, transposing ldmatrix
-                        ldsm_x4_t(sb + OFF_WT + sw(16 * J + (lane & 7) + (((lane >> 3) & 1) << 3), c0 + ((lane >> 4) << 3), 64),
-                                  b[0], b[1], b[2], b[3]);
-                    mma_16816_f16(acc[0], a[0], a[1], a[2], a[3], b[0], b[1]);
-                    mma_16816_f16(acc[1], a[0], a[1], a[2], a[3], b[2], b[3]);
-                }
-#pragma unroll
-                for (int nt = 0; nt < 2; ++nt)
-#pragma unroll
-                    for (int hh = 0; hh < 2; ++hh) {
-                        const int r = 16 * I + g + 8 * hh;
-                        const int c = c0 + 8 * nt + 2 * t4;
-                        const uint32_t raw = *reinterpret_cast<const uint32_t *>(sm + rhs_off + sw(r, c, 64));
-                        const float2 bv = vhalf ? unpack_bf16(raw) : unpack_f16(raw);
-                        const float br = BETA[r];
-                        const float y0 = fmaf(br, bv.x, acc[nt][2 * hh]), y1 = fmaf(br, bv.y, acc[nt][2 * hh + 1]);
-                        *reinterpret_cast<uint32_t *>(ysc + (g + 8 * hh) * 48 + (8 * nt + 2 * t4) * 2) = pack_f16(y0, y1);
-                    }
-                __syncwarp();
-                uint32_t a[4], b[4];
-                ldsm_x4(sb + OFF_TT + sw(16 * I + (lane & 15), 16 * I + ((lane >> 4) << 3), 64), a[0], a[1], a[2], a[3]);
-                ldsm_x4_t(smem_u32(ysc) + ((lane & 7) + (((lane >> 3) & 1) << 3)) * 48 + ((lane >> 4) << 3) * 2,
-                          b[0], b[1], b[2], b[3]);
-                float x[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
-                mma_16816_f16(x[0], a[0], a[1], a[2], a[3], b[0], b[1]);
-                mma_16816_f16(x[1], a[0], a[1], a[2], a[3], b[2], b[3]);
-#pragma unroll
-                for (int nt = 0; nt < 2; ++nt)
-#pragma unroll
-                    for (int hh = 0; hh < 2; ++hh) {
-                        const int r = 16 * I + g + 8 * hh;
-                        const int c = c0 + 8 * nt + 2 * t4;
-                        const float x0 = x[nt][2 * hh], x1 = x[nt][2 * hh + 1];
-                        if (vhalf) {   // U~ transposed, [j][r]: hi over G, lo over the sums buffer
-                            const __half h0 = __float2half_rn(x0), h1 = __float2half_rn(x1);
-                            __half *uh = reinterpret_cast<__half *>(sm + OFF_G);
-                            __half *ul = reinterpret_cast<__half *>(sm + OFF_TD);
-                            uh[sw(c, r, 128) >> 1] = h0;
-                            uh[sw(c + 1, r, 128) >> 1] = h1;
-                            ul[sw(c, r, 128) >> 1] = __float2half_rn(x0 - __half2float(h0));
-                            ul[sw(c + 1, r, 128) >> 1] = __float2half_rn(x1 - __half2float(h1));
-                        } else {
-                            *reinterpret_cast<uint32_t *>(sm + OFF_WT + sw(r, c, 64)) = pack_f16(-x0, -x1);
-                        }
-                    }
-                __syncwarp();
-            }
-        }
-        fence_async_smem();
-        __syncthreads();
-        if (tid == 0 && more) {   // Kbar and V are consumed: prefetch the next chunk's K and V
-            fence_async_smem();
+        // the next chunk's tiles: G (K^hi is consumed) now; Q and K once the two groups above
+        // have read Qbar and Kbar; V after (4)
+        bool got4 = true;
+        if (warp == 3 && lane == 0 && more) {
             mbar_arrive_expect_tx(bar_tma, 4 * 16384);
-            tma_tile(&tmk, sb + OFF_K, bar_tma, h, t0 + C);
-            tma_tile(&tmv, sb + OFF_V, bar_tma, h, t0 + C);
+            tma_tile(&tmg, sb + OFF_G, bar_tma, h, t0 + C);
+            got4 = mbar_wait(bar_p, ph_p, wait_limit) && mbar_wait(bar_q, ph_q, wait_limit);
+            if (got4) {
+                tma_tile(&tmq, sb + OFF_Q, bar_tma, h, t0 + C);
+                tma_tile(&tmk, sb + OFF_K, bar_tma, h, t0 + C);
+            }
         }
 
-        // ---- state path.  (a) S^T -> fp16 operand; S^T <- S^T Diag(dec) in place
-        {
-            const int i0 = 32 * quarter;
-            float v[32];
-            tmem_ld32(trow + TM_S + i0, v);
+        // ---- (4) warps 0-2: the off-diagonal blocks of T, level by level (T_IK with K > J is
+        // ready before T_IJ);  warps 4-11: Z^T = (V^T - P^T) diag(beta) -> fp16 pairs (TMEM)
+        if (warp < 3) {
+            t_block(warp + 1, warp);                 // (1,0) (2,1) (3,2)
+            named_bar(1, 96);
+            if (warp < 2) t_block(warp + 2, warp);   // (2,0) (3,1)
+            named_bar(1, 96);
+            if (warp == 0) t_block(3, 0);
+        } else if (warp >= 4 && warp < 12) {
+            got4 = mbar_wait(bar_p, ph_p, wait_limit);
+            tc_fence_after();
+            const int s0 = 32 * ((warp - 4) >> 2);
+            float pv[32];
+            tmem_ld32(trow + TM_P + s0, pv);
+            const __nv_bfloat16 *vt = reinterpret_cast<const __nv_bfloat16 *>(sm + OFF_V);
+            uint32_t zv[16];
 #pragma unroll
-            for (int q8 = 0; q8 < 4; ++q8)
-                *reinterpret_cast<uint4 *>(sm + OFF_SST + sw(jl, i0 + 8 * q8, 128)) =
-                    make_uint4(pack_f16(v[8 * q8], v[8 * q8 + 1]), pack_f16(v[8 * q8 + 2], v[8 * q8 + 3]),
-                               pack_f16(v[8 * q8 + 4], v[8 * q8 + 5]), pack_f16(v[8 * q8 + 6], v[8 * q8 + 7]));
-#pragma unroll
-            for (int c = 0; c < 32; c += 4) {
-                const float4 d4 = *reinterpret_cast<const float4 *>(DEC + i0 + c);
-                v[c] *= d4.x; v[c + 1] *= d4.y; v[c + 2] *= d4.z; v[c + 3] *= d4.w;
+            for (int c = 0; c < 16; ++c) {
+                const int s = s0 + 2 * c;
+                const float v0 = __bfloat162float(vt[sw(s, jl, 64) >> 1]);
+                const float v1 = __bfloat162float(vt[sw(s + 1, jl, 64) >> 1]);
+                zv[c] = pack_f16((v0 - pv[2 * c]) * BETA[s], (v1 - pv[2 * c + 1]) * BETA[s + 1]);
             }
-            tmem_st32(trow + TM_S + i0, v);
+            tmem_st16u(trow + TM_Z + s0 / 2, zv);
         }
+        ph_p ^= 1;
+        ph_q ^= 1;
         fence_async_smem();
         tc_fence_before();
-        __syncthreads();
-        // (b) U^T = S^T (-W)^T  [commit: U] ;  O^T = S^T Qbar^T  [commit: Q]
+        if (__syncthreads_or(!got4)) { ok = false; break; }
+        // U^T = Z^T T^T [commit: U];  V is consumed: the next chunk's V
         if (tid == 0) {
             tc_fence_after();
 #pragma unroll
-            for (int k = 0; k < 8; ++k)
-                mma_f16_ss(tmem + TM_U, sdesc_sw128(sb + OFF_SST + (k >> 2) * 16384 + (k & 3) * 32),
-                           sdesc_sw128(sb + OFF_WT + (k >> 2) * 8192 + (k & 3) * 32), IDESC_N64, k > 0);
+            for (int k = 0; k < 4; ++k)
+                mma_f16_ts(tmem + TM_U, tmem + TM_Z + 8 * k, sdesc_sw128(sb + OFF_T + k * 32), IDESC_N64, k > 0);
             mma_commit(bar_u);
-#pragma unroll
-            for (int k = 0; k < 8; ++k)
-                mma_f16_ss(tmem + TM_O, sdesc_sw128(sb + OFF_SST + (k >> 2) * 16384 + (k & 3) * 32),
-                           sdesc_sw128(sb + OFF_Q + (k >> 2) * 8192 + (k & 3) * 32), IDESC_N64, k > 0);
-            mma_commit(bar_q);
+            if (more) tma_tile(&tmv, sb + OFF_V, bar_tma, h, t0 + C);
         }
         {
             const bool got = mbar_wait(bar_u, ph_u, wait_limit);
@@ -606,99 +621,62 @@ kda_chunk_tc_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_consta
             if (__syncthreads_or(!got)) { ok = false; break; }
         }
         tc_fence_after();
-        // (c) U = U~ + S^T(-W)^T -> fp16 hi (U^T buffer) + lo (W buffer, its -W has been consumed);
-        // warp w: lanes 32(w%4).., columns 16(w/4)..16(w/4)+15
+        // ---- (5) U^T -> fp16 hi + lo pairs (TMEM); warp w: lanes 32(w%4).., columns 16(w/4)..
         {
             const int r0 = 16 * quarter;
-            float v[16];
-            tmem_ld16(trow + TM_U + r0, v);
-            uint32_t uh[8], ul[8];   // U~^T row jl, columns r0..r0+15, hi and lo
-            {
-                const uint4 h0 = *reinterpret_cast<const uint4 *>(sm + OFF_G + sw(jl, r0, 128));
-                const uint4 h1 = *reinterpret_cast<const uint4 *>(sm + OFF_G + sw(jl, r0 + 8, 128));
-                const uint4 l0 = *reinterpret_cast<const uint4 *>(sm + OFF_TD + sw(jl, r0, 128));
-                const uint4 l1 = *reinterpret_cast<const uint4 *>(sm + OFF_TD + sw(jl, r0 + 8, 128));
-                uh[0] = h0.x; uh[1] = h0.y; uh[2] = h0.z; uh[3] = h0.w; uh[4] = h1.x; uh[5] = h1.y; uh[6] = h1.z; uh[7] = h1.w;
-                ul[0] = l0.x; ul[1] = l0.y; ul[2] = l0.z; ul[3] = l0.w; ul[4] = l1.x; ul[5] = l1.y; ul[6] = l1.z; ul[7] = l1.w;
-            }
+            float uv[16];
+            tmem_ld16(trow + TM_U + r0, uv);
             uint32_t hi[8], lo[8];
 #pragma unroll
             for (int e = 0; e < 8; ++e) {
-                const float2 fh = unpack_f16(uh[e]), fl = unpack_f16(ul[e]);
-                const float a0 = v[2 * e] + (fh.x + fl.x);
-                const float a1 = v[2 * e + 1] + (fh.y + fl.y);
-                hi[e] = pack_f16(a0, a1);
+                hi[e] = pack_f16(uv[2 * e], uv[2 * e + 1]);
                 const float2 hf = unpack_f16(hi[e]);
-                lo[e] = pack_f16(a0 - hf.x, a1 - hf.y);
+                lo[e] = pack_f16(uv[2 * e] - hf.x, uv[2 * e + 1] - hf.y);
             }
-#pragma unroll
-            for (int q8 = 0; q8 < 2; ++q8) {
-                const uint32_t off = sw(jl, r0 + 8 * q8, 128);
-                *reinterpret_cast<uint4 *>(sm + OFF_UST + off) = make_uint4(hi[4 * q8], hi[4 * q8 + 1], hi[4 * q8 + 2], hi[4 * q8 + 3]);
-                *reinterpret_cast<uint4 *>(sm + OFF_WT + off) = make_uint4(lo[4 * q8], lo[4 * q8 + 1], lo[4 * q8 + 2], lo[4 * q8 + 3]);
-            }
+            tmem_st8u(trow + TM_UH + r0 / 2, hi);
+            tmem_st8u(trow + TM_UL + r0 / 2, lo);
         }
-        fence_async_smem();
         tc_fence_before();
         __syncthreads();
-        bool gq = true;
-        if (tid == 0) {   // Qbar (read by the O^T = S^T Qbar^T group) and U~hi (over G) are consumed
-            gq = mbar_wait(bar_q, ph_q, wait_limit);
-            if (gq && more) {
-                tma_tile(&tmq, sb + OFF_Q, bar_tma, h, t0 + C);
-                tma_tile(&tmg, sb + OFF_G, bar_tma, h, t0 + C);
-            }
-        }
-        ph_q ^= 1;
-        // (d) O^T += U^T M^T (hi.hi + lo.hi + hi.lo) [commit: O] ;  S^T += U^T Kp [commit: S]
+        // S^T += U^T Kp [commit: S] ;  O^T += U^T M^T (hi.hi + lo.hi + hi.lo) [commit: O]
         if (tid == 0) {
             tc_fence_after();
 #pragma unroll
+            for (int ks = 0; ks < 4; ++ks)
+                mma_f16_ts(tmem + TM_S, tmem + TM_UH + 8 * ks, sdesc_sw128(sb + OFF_KPT + ks * 32), IDESC_N128, 1);
+            mma_commit(bar_s);
+#pragma unroll
             for (int ks = 0; ks < 4; ++ks) {
-                mma_f16_ss(tmem + TM_O, sdesc_sw128(sb + OFF_UST + ks * 32), sdesc_sw128(sb + OFF_MT + ks * 32),
-                           IDESC_N64, 1);
-                mma_f16_ss(tmem + TM_O, sdesc_sw128(sb + OFF_WT + ks * 32), sdesc_sw128(sb + OFF_MT + ks * 32),
-                           IDESC_N64, 1);
-                mma_f16_ss(tmem + TM_O, sdesc_sw128(sb + OFF_UST + ks * 32), sdesc_sw128(sb + OFF_MLO + ks * 32),
-                           IDESC_N64, 1);
+                mma_f16_ts(tmem + TM_O, tmem + TM_UH + 8 * ks, sdesc_sw128(sb + OFF_MT + ks * 32), IDESC_N64, 1);
+                mma_f16_ts(tmem + TM_O, tmem + TM_UL + 8 * ks, sdesc_sw128(sb + OFF_MT + ks * 32), IDESC_N64, 1);
+                mma_f16_ts(tmem + TM_O, tmem + TM_UH + 8 * ks, sdesc_sw128(sb + OFF_MLO + ks * 32), IDESC_N64, 1);
             }
             mma_commit(bar_o);
-#pragma unroll
-            for (int ks = 0; ks < 4; ++ks)
-                mma_f16_ss(tmem + TM_S, sdesc_sw128(sb + OFF_UST + ks * 32), sdesc_sw128(sb + OFF_KPT + ks * 32),
-                           IDESC_N128, 1);
-            mma_commit(bar_s);
         }
-        s_pending = true;
-        {
-            const bool got = mbar_wait(bar_o, ph_o, wait_limit);
-            ph_o ^= 1;
-            if (__syncthreads_or(!got || !gq)) { ok = false; break; }
-        }
-        tc_fence_after();
-        // (e) the output of this chunk is staged and stored during the next chunk's first phases
         out_pending = true;
         t0_out = t0;
         nr_out = nr;
     }
 
-    if (ok && out_pending) {   // the last chunk's output
-        stage_output();
-        tc_fence_before();
-        __syncthreads();
-        store_output();
-        __syncthreads();
-    }
-    if (ok && s_pending) {   // the last state update
-        const bool got = mbar_wait(bar_s, ph_s, wait_limit);
+    if (ok && out_pending) {   // the last chunk's state update and output
+        const bool gs = mbar_wait(bar_s, ph_s, wait_limit);
+        const bool go = mbar_wait(bar_o, ph_o, wait_limit);
         ph_s ^= 1;
-        if (__syncthreads_or(!got)) ok = false;
+        ph_o ^= 1;
+        if (__syncthreads_or(!(gs && go))) {
+            ok = false;
+        } else {
+            tc_fence_after();
+            stage_output();
+            __syncthreads();
+            store_output();
+        }
     }
     if (!ok) {
         // A bounded wait expired: let copies and MMAs in flight land (bounded
         // again), flag the failure and mark this unit's final state invalid.
         if (tid == 0) {
-            mbar_wait(bar_s, ph_s, wait_limit);
+            mbar_wait(bar_o, ph_o, wait_limit);
             mbar_wait(bar_tma, ph_tma, wait_limit);
             atomicAdd(&g_kda_tc_timeouts, 1u);
         }
