@@ -61,8 +61,9 @@ __device__ __forceinline__ float ex2(float x) {
 }
 
 // shared memory map, byte offsets from a 1024-aligned base
-constexpr uint32_t OFF_Q = 0;          // Q -> Qbar (fp16)         [64 r][128 i]  swizzled
-constexpr uint32_t OFF_K = 16384;      // K -> Kbar (fp16)         [64 r][128 i]
+constexpr uint32_t OFF_Q = 0;          // Q -> Qbar (fp16)         [64 r][128 i]  swizzled, and
+constexpr uint32_t OFF_K = 8192;       // K -> Kbar (fp16): the two tiles interleave per 64-column
+                                       // half, so [Qbar; Kbar] is one 128-row MMA operand
 constexpr uint32_t OFF_V = 32768;      // V (bf16)                 [64 r][128 j]
 constexpr uint32_t OFF_G = 49152;      // G -> K^hi (bf16)         [64 r][128 i]
 constexpr uint32_t OFF_SST = 65536;    // Q~hi, K~ (bf16)          2 x [64 r][128 i]
@@ -93,9 +94,9 @@ static_assert(64 * 128 * 2 <= 64 * LDA * 4, "output staging fits over the A bloc
 
 // tensor memory columns (128 lanes = value channel j)
 constexpr uint32_t TM_S = 0;      // S^T fp32                        128 columns
-constexpr uint32_t TM_P = 128;    // P^T = S^T Kbar^T fp32            64
-constexpr uint32_t TM_O = 192;    // O^T fp32                         64
-constexpr uint32_t TM_U = 256;    // U^T fp32                         64
+constexpr uint32_t TM_O = 128;    // O^T fp32 (follows S^T: one N = 192 group updates both)   64
+constexpr uint32_t TM_P = 192;    // P^T = S^T Kbar^T fp32 (follows O^T)                     64
+constexpr uint32_t TM_U = 256;    // U^T fp32, then the low-order terms of O^T                 64
 constexpr uint32_t TM_S16 = 320;  // S^T as fp16 pairs (MMA operand)  64
 constexpr uint32_t TM_Z = 384;    // Z^T fp16 pairs                   32
 constexpr uint32_t TM_UH = 416;   // U^T fp16 pairs, hi               32
@@ -104,12 +105,19 @@ constexpr uint32_t TM_COLS = 512;
 
 constexpr uint32_t IDESC_N64 = idesc_f16_f32(128, 64);
 constexpr uint32_t IDESC_N128 = idesc_f16_f32(128, 128);
+constexpr uint32_t IDESC_N192 = idesc_f16_f32(128, 192);
+static_assert(OFF_MT == OFF_KPT + 16384 && TM_O == TM_S + 128 && TM_P == TM_O + 64, "adjacent operands");
 
 // Byte offset of element (row, col) in a 128-byte-swizzled K-major tile of
 // `rows` rows whose columns are split into 64-element halves.
 __device__ __forceinline__ uint32_t sw(int row, int col, int rows) {
     return (uint32_t)((col >> 6) * rows * 128 + row * 128 + ((((col & 63) >> 3) ^ (row & 7)) << 4) +
                       ((col & 7) << 1));
+}
+
+// The same for the interleaved Q / K tiles (64-column halves 16 KB apart).
+__device__ __forceinline__ uint32_t swqk(int row, int col) {
+    return (uint32_t)((col >> 6) * 16384 + row * 128 + ((((col & 63) >> 3) ^ (row & 7)) << 4) + ((col & 7) << 1));
 }
 
 __device__ __forceinline__ int pair_index(int I, int J) { return I * (I - 1) / 2 + J; }
@@ -144,9 +152,9 @@ __device__ __forceinline__ void select_unit(const ChunkArgs &a, int b, int &n, i
 }
 
 __device__ __forceinline__ void tma_tile(const CUtensorMap *map, uint32_t dst, uint32_t bar, int h,
-                                         int64_t tok) {
+                                         int64_t tok, uint32_t half_stride = 8192) {
     tma_load_3d(dst, map, bar, 0, h, (int)tok);
-    tma_load_3d(dst + 8192, map, bar, 64, h, (int)tok);
+    tma_load_3d(dst + half_stride, map, bar, 64, h, (int)tok);
 }
 
 __global__ void __launch_bounds__(NT, 1)
@@ -166,9 +174,9 @@ kda_chunk_tc_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_consta
     const int64_t len = eos - bos;
     const int nchunks = (int)((len + C - 1) / C);
 
-    // mbarriers: TMA tiles landed; P^T done; O^T = S^T Qbar^T done; U^T done; state update done;
-    // O^T += U^T M^T done
-    const uint32_t bar_tma = sb + OFF_BAR, bar_p = sb + OFF_BAR + 8, bar_q = sb + OFF_BAR + 16;
+    // mbarriers: TMA tiles landed; [O^T | P^T] done; U^T done; state (and O^T high-order) update
+    // done; O^T low-order terms done
+    const uint32_t bar_tma = sb + OFF_BAR, bar_p = sb + OFF_BAR + 8;
     const uint32_t bar_u = sb + OFF_BAR + 24, bar_s = sb + OFF_BAR + 32, bar_o = sb + OFF_BAR + 40;
     volatile uint32_t *tmem_holder = reinterpret_cast<volatile uint32_t *>(sm + OFF_BAR + 48);
     float *AF = reinterpret_cast<float *>(sm + OFF_AF);
@@ -185,7 +193,6 @@ kda_chunk_tc_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_consta
     if (tid == 0) {
         mbar_init(bar_tma, 1);
         mbar_init(bar_p, 1);
-        mbar_init(bar_q, 1);
         mbar_init(bar_u, 1);
         mbar_init(bar_s, 1);
         mbar_init(bar_o, 1);
@@ -206,6 +213,9 @@ kda_chunk_tc_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_consta
     const uint32_t trow = tmem + ((uint32_t)((warp & 3) * 32) << 16);   // this warp's TMEM lanes
     const int jl = 32 * (warp & 3) + lane;   // this thread's TMEM lane (value channel j)
     const int quarter = warp >> 2;           // which column group this warp handles (0..3)
+    // shared-memory operand descriptors are this base plus (byte offset >> 4): computed once,
+    // outside the single-thread issue branches, so that issuing an MMA costs no address math
+    const uint64_t dsm = sdesc_sw128(sb);
 
     // ---- initial state -> TMEM (S^T: lane j, column i)
     const int64_t sbase = ((int64_t)n * H + h) * D * D;
@@ -218,8 +228,8 @@ kda_chunk_tc_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_consta
     }
     if (tid == 0 && nchunks > 0) {
         mbar_arrive_expect_tx(bar_tma, 4 * 16384);
-        tma_tile(&tmq, sb + OFF_Q, bar_tma, h, bos);
-        tma_tile(&tmk, sb + OFF_K, bar_tma, h, bos);
+        tma_tile(&tmq, sb + OFF_Q, bar_tma, h, bos, 16384);
+        tma_tile(&tmk, sb + OFF_K, bar_tma, h, bos, 16384);
         tma_tile(&tmv, sb + OFF_V, bar_tma, h, bos);
         tma_tile(&tmg, sb + OFF_G, bar_tma, h, bos);
     }
@@ -236,18 +246,19 @@ kda_chunk_tc_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_consta
     __syncthreads();
     tc_fence_after();
 
-    uint32_t ph_tma = 0, ph_p = 0, ph_q = 0, ph_u = 0, ph_s = 0, ph_o = 0;
+    uint32_t ph_tma = 0, ph_p = 0, ph_u = 0, ph_s = 0, ph_o = 0;
     bool out_pending = false;   // the previous chunk's state update and O^T group are in flight
     int64_t t0_out = 0;
     int nr_out = 0;
-    // O^T (TMEM) -> bf16 staging tile [64 r][128 j] over the A buffer; warp w: lanes 32(w%4)..,
+    // O^T (TMEM: high-order part + low-order terms) -> bf16 staging tile [64 r][128 j] over the A buffer; warp w: lanes 32(w%4)..,
     // rows 16(w/4)..16(w/4)+15
     auto stage_output = [&]() {
         __nv_bfloat16 *os = reinterpret_cast<__nv_bfloat16 *>(sm + OFF_AF);
-        float v[16];
+        float v[16], w[16];
         tmem_ld16(trow + TM_O + 16 * quarter, v);
+        tmem_ld16(trow + TM_U + 16 * quarter, w);
 #pragma unroll
-        for (int c = 0; c < 16; ++c) os[(16 * quarter + c) * D + jl] = __float2bfloat16_rn(v[c]);
+        for (int c = 0; c < 16; ++c) os[(16 * quarter + c) * D + jl] = __float2bfloat16_rn(v[c] + w[c]);
     };
     // staging tile -> out, 16-byte coalesced stores of the rows inside the sequence
     auto store_output = [&]() {
@@ -292,13 +303,18 @@ kda_chunk_tc_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_consta
     const int blk = sub >> 1, hb = sub & 1;    // sub-tile and which half of it
     const int t4 = lane & 3, g = lane >> 2;    // mma.sync fragment coordinates
 
+    float bnext = (tid < C && tid < len) ? __bfloat162float(beta[(bos + tid) * H + h]) : 0.f;
 #pragma unroll 1
     for (int ci = 0; ci < nchunks; ++ci) {
         const int64_t t0 = bos + (int64_t)ci * C;
         const int nr = (int)(len - (int64_t)ci * C < C ? len - (int64_t)ci * C : C);
         const bool more = ci + 1 < nchunks;
 
-        if (tid < C) BETA[tid] = tid < nr ? __bfloat162float(beta[(t0 + tid) * H + h]) : 0.f;
+        if (tid < C) {   // this chunk's beta (loaded one chunk ahead); the next chunk's
+            BETA[tid] = bnext;
+            const int64_t nn = more ? len - (int64_t)(ci + 1) * C : 0;
+            bnext = tid < nn ? __bfloat162float(beta[(t0 + C + tid) * H + h]) : 0.f;
+        }
         {
             const bool got = mbar_wait(bar_tma, ph_tma, wait_limit);
             ph_tma ^= 1;
@@ -314,8 +330,8 @@ kda_chunk_tc_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_consta
 #pragma unroll
             for (int kk = 0; kk < 8; ++kk) {
                 uint32_t a0, a1, a2, a3, b0, b1, b2, b3;
-                ldsm_x4(sb + OFF_Q + sw(16 * I + (lane & 15), 16 * kk + ((lane >> 4) << 3), 64), a0, a1, a2, a3);
-                ldsm_x4(sb + OFF_K + sw(16 * I + (lane & 7) + ((lane >> 4) << 3), 16 * kk + (((lane >> 3) & 1) << 3), 64),
+                ldsm_x4(sb + OFF_Q + swqk(16 * I + (lane & 15), 16 * kk + ((lane >> 4) << 3)), a0, a1, a2, a3);
+                ldsm_x4(sb + OFF_K + swqk(16 * I + (lane & 7) + ((lane >> 4) << 3), 16 * kk + (((lane >> 3) & 1) << 3)),
                         b0, b1, b2, b3);
                 mma_16816(acc[0], a0, a1, a2, a3, b0, b1);
                 mma_16816(acc[1], a0, a1, a2, a3, b2, b3);
@@ -409,9 +425,9 @@ kda_chunk_tc_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_consta
 #pragma unroll
                 for (int e = 0; e < 2; ++e) {
                     const int r = 16 * blk + 8 * hb + rr + e;
-                    const uint32_t off = sw(r, c, 64);
-                    float2 q2 = unpack_bf16(*reinterpret_cast<uint32_t *>(sm + OFF_Q + off));
-                    float2 k2 = unpack_bf16(*reinterpret_cast<uint32_t *>(sm + OFF_K + off));
+                    const uint32_t off = sw(r, c, 64), oqk = swqk(r, c);
+                    float2 q2 = unpack_bf16(*reinterpret_cast<uint32_t *>(sm + OFF_Q + oqk));
+                    float2 k2 = unpack_bf16(*reinterpret_cast<uint32_t *>(sm + OFF_K + oqk));
                     const float2 g2 = unpack_bf16(*reinterpret_cast<uint32_t *>(sm + OFF_G + off));
                     if (r < nr) { l0 = fmaf(g2.x, LOG2E, l0); l1 = fmaf(g2.y, LOG2E, l1); }
                     else { q2 = make_float2(0.f, 0.f); k2 = q2; }
@@ -426,8 +442,8 @@ kda_chunk_tc_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_consta
                     *reinterpret_cast<uint32_t *>(sm + OFF_SST + 16384 + off) = pack_bf16(k2.x * x0, k2.y * x1);
                     *reinterpret_cast<uint32_t *>(sm + OFF_G + off) = khh;
                     *reinterpret_cast<uint32_t *>(sm + OFF_WT + off) = pack_bf16(kh0 - khf.x, kh1 - khf.y);
-                    *reinterpret_cast<uint32_t *>(sm + OFF_Q + off) = pack_f16(qt0 * eb0, qt1 * eb1);
-                    *reinterpret_cast<uint32_t *>(sm + OFF_K + off) = pack_f16(k2.x * x0 * eb0, k2.y * x1 * eb1);
+                    *reinterpret_cast<uint32_t *>(sm + OFF_Q + oqk) = pack_f16(qt0 * eb0, qt1 * eb1);
+                    *reinterpret_cast<uint32_t *>(sm + OFF_K + oqk) = pack_f16(k2.x * x0 * eb0, k2.y * x1 * eb1);
                     kp[e][0] = kh0 * el0;
                     kp[e][1] = kh1 * el1;
                 }
@@ -442,33 +458,34 @@ kda_chunk_tc_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_consta
         fence_async_smem();
         tc_fence_before();
         __syncthreads();
-        // P^T = S^T Kbar^T [commit: P] ;  O^T = S^T Qbar^T [commit: Q] -- both run during (3)
-        if (tid == 0) {
+        // [O^T | P^T] = S^T [Qbar; Kbar]^T [commit: P], issued by a warp that (3) leaves idle
+        if (warp == 15 && lane == 0) {
             tc_fence_after();
 #pragma unroll
             for (int k = 0; k < 8; ++k)
-                mma_f16_ts(tmem + TM_P, tmem + TM_S16 + 8 * k,
-                           sdesc_sw128(sb + OFF_K + (k >> 2) * 8192 + (k & 3) * 32), IDESC_N64, k > 0);
+                mma_f16_ts(tmem + TM_O, tmem + TM_S16 + 8 * k, dsm + ((OFF_Q + (k >> 2) * 16384 + (k & 3) * 32) >> 4),
+                           IDESC_N128, k > 0);
             mma_commit(bar_p);
-#pragma unroll
-            for (int k = 0; k < 8; ++k)
-                mma_f16_ts(tmem + TM_O, tmem + TM_S16 + 8 * k,
-                           sdesc_sw128(sb + OFF_Q + (k >> 2) * 8192 + (k & 3) * 32), IDESC_N64, k > 0);
-            mma_commit(bar_q);
         }
 
-        // ---- (3) A = beta K~ K^T and M = Q~ K^T on the 10 sub-tile pairs (I >= J).  Warps 0-7:
-        // the 4 diagonal pairs, one 16x8 column half each, M as the 3-term product
-        // (Q~hi + Q~lo)(K^hi + K^lo)^T less lo.lo with the exact q_r . k_r on its diagonal; the two
-        // warps of a diagonal pair then invert (I + A_II) by forward substitution.  Warps 8-13:
-        // the 6 off-diagonal pairs, single bf16 products with the per-channel factor e^{b_I - b_J}
-        // applied to the right operand.  Off-diagonal A blocks go to the fp16 tile AT; T_II = (I + A_II)^-1 goes to the
-        // diagonal blocks of the fp16 tile T.
-        if (warp < 8) {
-            const int I = warp >> 1, nt = warp & 1;
-            float accA[4] = {0.f, 0.f, 0.f, 0.f};
-            float accM[3][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
-#pragma unroll 4
+        // ---- (3) A = beta K~ K^T and M = Q~ K^T on the 10 sub-tile pairs (I >= J).  Warps 0-3:
+        // the diagonal pair (I, I), I = warp, both 8-column halves, M as the 3-term product
+        // (Q~hi + Q~lo)(K^hi + K^lo)^T less lo.lo with the exact q_r . k_r on its diagonal; the
+        // warp then inverts (I + A_II) by forward substitution (one SM sub-partition per block).
+        // Warps 4-9: the 6 off-diagonal pairs, single bf16 products with the per-channel factor
+        // e^{b_I - b_J} applied to the right operand.  Off-diagonal A blocks go to the fp16
+        // tile AT; T_II = (I + A_II)^-1 goes to the diagonal blocks of the fp16 tile T.
+        if (warp < 4) {
+            const int I = warp;
+            float accA[2][4], accM[3][2][4];
+#pragma unroll
+            for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                    accA[nt][e] = 0.f;
+                    accM[0][nt][e] = 0.f; accM[1][nt][e] = 0.f; accM[2][nt][e] = 0.f;
+                }
+#pragma unroll 2
             for (int kk = 0; kk < 8; ++kk) {
                 const uint32_t ao = sw(16 * I + (lane & 15), 16 * kk + ((lane >> 4) << 3), 64);
                 const uint32_t bo = sw(16 * I + (lane & 7) + ((lane >> 4) << 3), 16 * kk + (((lane >> 3) & 1) << 3), 64);
@@ -478,29 +495,34 @@ kda_chunk_tc_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_consta
                 ldsm_x4(sb + OFF_UST + ao, ql[0], ql[1], ql[2], ql[3]);
                 ldsm_x4(sb + OFF_G + bo, bh[0], bh[1], bh[2], bh[3]);
                 ldsm_x4(sb + OFF_WT + bo, bl[0], bl[1], bl[2], bl[3]);
-                mma_16816(accA, ka[0], ka[1], ka[2], ka[3], bh[2 * nt], bh[2 * nt + 1]);
-                mma_16816(accM[0], qh[0], qh[1], qh[2], qh[3], bh[2 * nt], bh[2 * nt + 1]);
-                mma_16816(accM[1], ql[0], ql[1], ql[2], ql[3], bh[2 * nt], bh[2 * nt + 1]);
-                mma_16816(accM[2], qh[0], qh[1], qh[2], qh[3], bl[2 * nt], bl[2 * nt + 1]);
+#pragma unroll
+                for (int nt = 0; nt < 2; ++nt) {
+                    mma_16816(accA[nt], ka[0], ka[1], ka[2], ka[3], bh[2 * nt], bh[2 * nt + 1]);
+                    mma_16816(accM[0][nt], qh[0], qh[1], qh[2], qh[3], bh[2 * nt], bh[2 * nt + 1]);
+                    mma_16816(accM[1][nt], ql[0], ql[1], ql[2], ql[3], bh[2 * nt], bh[2 * nt + 1]);
+                    mma_16816(accM[2][nt], qh[0], qh[1], qh[2], qh[3], bl[2 * nt], bl[2 * nt + 1]);
+                }
             }
 #pragma unroll
-            for (int hh = 0; hh < 2; ++hh) {
-                const int r = 16 * I + g + 8 * hh;
-                const int s0 = 16 * I + 8 * nt + 2 * t4;
-                const float br = BETA[r];
-                AF[r * LDA + s0] = s0 < r ? br * accA[2 * hh] : 0.f;
-                AF[r * LDA + s0 + 1] = s0 + 1 < r ? br * accA[2 * hh + 1] : 0.f;
-                const float mv0 = accM[0][2 * hh] + (accM[1][2 * hh] + accM[2][2 * hh]);
-                const float mv1 = accM[0][2 * hh + 1] + (accM[1][2 * hh + 1] + accM[2][2 * hh + 1]);
-                const float m0 = s0 < r ? mv0 : (s0 == r ? MRR[r] : 0.f);
-                const float m1 = s0 + 1 < r ? mv1 : (s0 + 1 == r ? MRR[r] : 0.f);
-                const uint32_t mh = pack_f16(m0, m1);
-                const float2 mhf = unpack_f16(mh);
-                *reinterpret_cast<uint32_t *>(sm + OFF_MT + sw(r, s0, 64)) = mh;
-                *reinterpret_cast<uint32_t *>(sm + OFF_MLO + sw(r, s0, 64)) = pack_f16(m0 - mhf.x, m1 - mhf.y);
-            }
-            named_bar(1 + I, 64);   // both column halves of A_II are in place
-            if (nt == 0 && lane < 16) {
+            for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+                for (int hh = 0; hh < 2; ++hh) {
+                    const int r = 16 * I + g + 8 * hh;
+                    const int s0 = 16 * I + 8 * nt + 2 * t4;
+                    const float br = BETA[r];
+                    AF[r * LDA + s0] = s0 < r ? br * accA[nt][2 * hh] : 0.f;
+                    AF[r * LDA + s0 + 1] = s0 + 1 < r ? br * accA[nt][2 * hh + 1] : 0.f;
+                    const float mv0 = accM[0][nt][2 * hh] + (accM[1][nt][2 * hh] + accM[2][nt][2 * hh]);
+                    const float mv1 = accM[0][nt][2 * hh + 1] + (accM[1][nt][2 * hh + 1] + accM[2][nt][2 * hh + 1]);
+                    const float m0 = s0 < r ? mv0 : (s0 == r ? MRR[r] : 0.f);
+                    const float m1 = s0 + 1 < r ? mv1 : (s0 + 1 == r ? MRR[r] : 0.f);
+                    const uint32_t mh = pack_f16(m0, m1);
+                    const float2 mhf = unpack_f16(mh);
+                    *reinterpret_cast<uint32_t *>(sm + OFF_MT + sw(r, s0, 64)) = mh;
+                    *reinterpret_cast<uint32_t *>(sm + OFF_MLO + sw(r, s0, 64)) = pack_f16(m0 - mhf.x, m1 - mhf.y);
+                }
+            __syncwarp();   // the whole of A_II is in place
+            if (lane < 16) {
                 // column jj of T_II: t_jj = 1, t_r = -sum_{s<r} A_rs t_s (rows above jj are 0)
                 const int jj = lane;
                 const float *Ab = AF + (16 * I) * LDA + 16 * I;
@@ -517,8 +539,8 @@ kda_chunk_tc_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_consta
                 for (int r = 0; r < 16; ++r)
                     at[sw(16 * I + r, 16 * I + jj, 64) >> 1] = __float2half_rn(tcol[r]);
             }
-        } else if (warp < 14) {
-            const int po = warp - 8;   // (1,0) (2,0) (2,1) (3,0) (3,1) (3,2)
+        } else if (warp < 10) {
+            const int po = warp - 4;   // (1,0) (2,0) (2,1) (3,0) (3,1) (3,2)
             const int I = po < 1 ? 1 : (po < 3 ? 2 : 3);
             const int J = po < 1 ? 0 : (po < 3 ? po - 1 : po - 3);
             float accA[2][4], accM[2][4];
@@ -569,10 +591,10 @@ kda_chunk_tc_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_consta
         if (warp == 3 && lane == 0 && more) {
             mbar_arrive_expect_tx(bar_tma, 4 * 16384);
             tma_tile(&tmg, sb + OFF_G, bar_tma, h, t0 + C);
-            got4 = mbar_wait(bar_p, ph_p, wait_limit) && mbar_wait(bar_q, ph_q, wait_limit);
+            got4 = mbar_wait(bar_p, ph_p, wait_limit);
             if (got4) {
-                tma_tile(&tmq, sb + OFF_Q, bar_tma, h, t0 + C);
-                tma_tile(&tmk, sb + OFF_K, bar_tma, h, t0 + C);
+                tma_tile(&tmq, sb + OFF_Q, bar_tma, h, t0 + C, 16384);
+                tma_tile(&tmk, sb + OFF_K, bar_tma, h, t0 + C, 16384);
             }
         }
 
@@ -602,7 +624,6 @@ kda_chunk_tc_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_consta
             tmem_st16u(trow + TM_Z + s0 / 2, zv);
         }
         ph_p ^= 1;
-        ph_q ^= 1;
         fence_async_smem();
         tc_fence_before();
         if (__syncthreads_or(!got4)) { ok = false; break; }
@@ -611,7 +632,7 @@ kda_chunk_tc_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_consta
             tc_fence_after();
 #pragma unroll
             for (int k = 0; k < 4; ++k)
-                mma_f16_ts(tmem + TM_U, tmem + TM_Z + 8 * k, sdesc_sw128(sb + OFF_T + k * 32), IDESC_N64, k > 0);
+                mma_f16_ts(tmem + TM_U, tmem + TM_Z + 8 * k, dsm + ((OFF_T + k * 32) >> 4), IDESC_N64, k > 0);
             mma_commit(bar_u);
             if (more) tma_tile(&tmv, sb + OFF_V, bar_tma, h, t0 + C);
         }
@@ -638,19 +659,22 @@ kda_chunk_tc_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_consta
         }
         tc_fence_before();
         __syncthreads();
-        // S^T += U^T Kp [commit: S] ;  O^T += U^T M^T (hi.hi + lo.hi + hi.lo) [commit: O]
+        // [S^T | O^T] += U^T_hi [Kp^T; M]^T [commit: S];  low-order terms of O^T,
+        // U^T_lo M^T + U^T_hi Mlo^T, into the U^T columns (consumed) [commit: O]
         if (tid == 0) {
             tc_fence_after();
 #pragma unroll
             for (int ks = 0; ks < 4; ++ks)
-                mma_f16_ts(tmem + TM_S, tmem + TM_UH + 8 * ks, sdesc_sw128(sb + OFF_KPT + ks * 32), IDESC_N128, 1);
+                mma_f16_ts(tmem + TM_S, tmem + TM_UH + 8 * ks, dsm + ((OFF_KPT + ks * 32) >> 4), IDESC_N192, 1);
             mma_commit(bar_s);
+        } else if (tid == 32) {
+            tc_fence_after();
 #pragma unroll
-            for (int ks = 0; ks < 4; ++ks) {
-                mma_f16_ts(tmem + TM_O, tmem + TM_UH + 8 * ks, sdesc_sw128(sb + OFF_MT + ks * 32), IDESC_N64, 1);
-                mma_f16_ts(tmem + TM_O, tmem + TM_UL + 8 * ks, sdesc_sw128(sb + OFF_MT + ks * 32), IDESC_N64, 1);
-                mma_f16_ts(tmem + TM_O, tmem + TM_UH + 8 * ks, sdesc_sw128(sb + OFF_MLO + ks * 32), IDESC_N64, 1);
-            }
+            for (int ks = 0; ks < 4; ++ks)
+                mma_f16_ts(tmem + TM_U, tmem + TM_UL + 8 * ks, dsm + ((OFF_MT + ks * 32) >> 4), IDESC_N64, ks > 0);
+#pragma unroll
+            for (int ks = 0; ks < 4; ++ks)
+                mma_f16_ts(tmem + TM_U, tmem + TM_UH + 8 * ks, dsm + ((OFF_MLO + ks * 32) >> 4), IDESC_N64, 1);
             mma_commit(bar_o);
         }
         out_pending = true;
