@@ -65,18 +65,19 @@ constexpr uint32_t OFF_Q = 0;          // Q -> Qbar (fp16)         [64 r][128 i]
 constexpr uint32_t OFF_K = 8192;       // K -> Kbar (fp16): the two tiles interleave per 64-column
                                        // half, so [Qbar; Kbar] is one 128-row MMA operand
 constexpr uint32_t OFF_V = 32768;      // V (bf16)                 [64 r][128 j]
-constexpr uint32_t OFF_G = 49152;      // G -> K^hi (bf16)         [64 r][128 i]
+constexpr uint32_t OFF_G = 49152;      // G (bf16)                 [64 r][128 i]
 constexpr uint32_t OFF_SST = 65536;    // Q~hi, K~ (bf16)          2 x [64 r][128 i]
 constexpr uint32_t OFF_UST = 98304;    // Q~lo (bf16)              [64 r][128 i]
 constexpr uint32_t OFF_WT = 114688;    // K^lo (bf16)              [64 r][128 i]
 constexpr uint32_t OFF_KPT = 131072;   // Kp^T fp16                [128 i][64 r]
 constexpr uint32_t OFF_MT = 147456;    // M fp16                   [64 r][64 s]
 constexpr uint32_t OFF_TT = 155648;    // A_IJ (I > J) fp16        [64 r][64 s]
-constexpr uint32_t OFF_AF = 163840;    // A diagonal blocks (fp32) -> output staging
-constexpr int LDA = 72;
-constexpr uint32_t OFF_PART = OFF_AF + 64 * LDA * 4;    // sub-tile half sums [8][128] fp32
-constexpr uint32_t OFF_T = (OFF_PART + 8 * 128 * 4 + 1023) / 1024 * 1024;   // T fp16 [64 r][64 s]
-constexpr uint32_t OFF_EB = OFF_T + 8192;               // e^{b_I}          [4][128]
+constexpr uint32_t OFF_T = 163840;     // T fp16 [64 r][64 s]; with AT, the output staging tile
+constexpr uint32_t OFF_STG = OFF_TT;   //   [64 r][128 j] bf16 at the start of a chunk
+constexpr uint32_t OFF_KH = 172032;    // K^hi (bf16)              [64 r][128 i]
+constexpr uint32_t OFF_PART = 188416;  // sub-tile half sums [8][128] fp32; A_II (fp32, [4][16][LDA])
+constexpr int LDA = 20;                //   once the decay vectors are consumed
+constexpr uint32_t OFF_EB = OFF_PART + 8 * 128 * 4;     // e^{b_I}          [4][128]
 constexpr uint32_t OFF_EL = OFF_EB + 4 * 128 * 4;       // e^{gl - b_I}     [4][128]
 constexpr uint32_t OFF_W6 = OFF_EL + 4 * 128 * 4;       // e^{b_I - b_J}    [6][128] bf16
 constexpr uint32_t OFF_DEC = OFF_W6 + 6 * 128 * 2;      // e^{gl}           [128]
@@ -87,10 +88,11 @@ constexpr uint32_t OFF_BAR = OFF_MLO + 8192;            // 6 mbarriers, TMEM add
 constexpr uint32_t SMEM_USED = OFF_BAR + 64;
 constexpr uint32_t SMEM_BYTES = SMEM_USED + 1024;       // + alignment slack
 static_assert(SMEM_BYTES <= 227 * 1024, "shared memory budget");
-static_assert(OFF_AF % 16 == 0 && OFF_PART % 16 == 0 && OFF_T % 1024 == 0 && OFF_MLO % 1024 == 0 &&
-                  OFF_BAR % 8 == 0,
+static_assert(OFF_KH % 1024 == 0 && OFF_PART % 16 == 0 && OFF_T % 1024 == 0 && OFF_MLO % 1024 == 0 &&
+                  OFF_BAR % 8 == 0 && OFF_KH == OFF_T + 8192 && OFF_PART == OFF_KH + 16384,
               "alignment");
-static_assert(64 * 128 * 2 <= 64 * LDA * 4, "output staging fits over the A blocks");
+static_assert(OFF_T == OFF_TT + 8192, "the output staging tile spans AT and T");
+static_assert(4 * 16 * LDA * 4 <= OFF_W6 - OFF_PART, "A_II fits over the sums and vectors");
 
 // tensor memory columns (128 lanes = value channel j)
 constexpr uint32_t TM_S = 0;      // S^T fp32                        128 columns
@@ -174,12 +176,12 @@ kda_chunk_tc_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_consta
     const int64_t len = eos - bos;
     const int nchunks = (int)((len + C - 1) / C);
 
-    // mbarriers: TMA tiles landed; [O^T | P^T] done; U^T done; state (and O^T high-order) update
-    // done; O^T low-order terms done
-    const uint32_t bar_tma = sb + OFF_BAR, bar_p = sb + OFF_BAR + 8;
+    // mbarriers: Q, K, G tiles landed; [O^T | P^T] done; V tile landed; U^T done; state (and
+    // O^T high-order) update done; O^T low-order terms done
+    const uint32_t bar_tma = sb + OFF_BAR, bar_p = sb + OFF_BAR + 8, bar_v = sb + OFF_BAR + 16;
     const uint32_t bar_u = sb + OFF_BAR + 24, bar_s = sb + OFF_BAR + 32, bar_o = sb + OFF_BAR + 40;
     volatile uint32_t *tmem_holder = reinterpret_cast<volatile uint32_t *>(sm + OFF_BAR + 48);
-    float *AF = reinterpret_cast<float *>(sm + OFF_AF);
+    float *AF = reinterpret_cast<float *>(sm + OFF_PART);   // A_II blocks, [4][16][LDA]
     float *PART = reinterpret_cast<float *>(sm + OFF_PART);
     float *EB = reinterpret_cast<float *>(sm + OFF_EB);
     float *EL = reinterpret_cast<float *>(sm + OFF_EL);
@@ -193,6 +195,7 @@ kda_chunk_tc_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_consta
     if (tid == 0) {
         mbar_init(bar_tma, 1);
         mbar_init(bar_p, 1);
+        mbar_init(bar_v, 1);
         mbar_init(bar_u, 1);
         mbar_init(bar_s, 1);
         mbar_init(bar_o, 1);
@@ -227,42 +230,44 @@ kda_chunk_tc_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_consta
         tmem_st32(trow + TM_S + 32 * quarter, v);
     }
     if (tid == 0 && nchunks > 0) {
-        mbar_arrive_expect_tx(bar_tma, 4 * 16384);
+        mbar_arrive_expect_tx(bar_tma, 3 * 16384);
         tma_tile(&tmq, sb + OFF_Q, bar_tma, h, bos, 16384);
         tma_tile(&tmk, sb + OFF_K, bar_tma, h, bos, 16384);
-        tma_tile(&tmv, sb + OFF_V, bar_tma, h, bos);
         tma_tile(&tmg, sb + OFF_G, bar_tma, h, bos);
+        mbar_arrive_expect_tx(bar_v, 16384);
+        tma_tile(&tmv, sb + OFF_V, bar_v, h, bos);
     }
-    // the blocks of M and T above the diagonal blocks stay zero for the whole sequence
+    // the blocks of M above the diagonal blocks stay zero for the whole sequence
     for (int x = tid; x < 64 * 32; x += NT) {
         const int r = x >> 5, s2 = 2 * (x & 31);
         if ((s2 >> 4) > (r >> 4)) {
             *reinterpret_cast<uint32_t *>(sm + OFF_MT + sw(r, s2, 64)) = 0u;
             *reinterpret_cast<uint32_t *>(sm + OFF_MLO + sw(r, s2, 64)) = 0u;
-            *reinterpret_cast<uint32_t *>(sm + OFF_T + sw(r, s2, 64)) = 0u;
         }
     }
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
 
-    uint32_t ph_tma = 0, ph_p = 0, ph_u = 0, ph_s = 0, ph_o = 0;
+    uint32_t ph_tma = 0, ph_p = 0, ph_v = 0, ph_u = 0, ph_s = 0, ph_o = 0;
     bool out_pending = false;   // the previous chunk's state update and O^T group are in flight
     int64_t t0_out = 0;
     int nr_out = 0;
-    // O^T (TMEM: high-order part + low-order terms) -> bf16 staging tile [64 r][128 j] over the A buffer; warp w: lanes 32(w%4)..,
-    // rows 16(w/4)..16(w/4)+15
+    // O^T (TMEM: high-order part + low-order terms) -> bf16 staging tile [64 r][128 j] over the
+    // AT and T tiles, by warps 8-15; warp w: lanes 32(w%4).., rows 32((w-8)/4)..+31
     auto stage_output = [&]() {
-        __nv_bfloat16 *os = reinterpret_cast<__nv_bfloat16 *>(sm + OFF_AF);
-        float v[16], w[16];
-        tmem_ld16(trow + TM_O + 16 * quarter, v);
-        tmem_ld16(trow + TM_U + 16 * quarter, w);
+        if (warp < 8) return;
+        __nv_bfloat16 *os = reinterpret_cast<__nv_bfloat16 *>(sm + OFF_STG);
+        const int r0 = 32 * ((warp - 8) >> 2);
+        float v[32], w[32];
+        tmem_ld32(trow + TM_O + r0, v);
+        tmem_ld32(trow + TM_U + r0, w);
 #pragma unroll
-        for (int c = 0; c < 16; ++c) os[(16 * quarter + c) * D + jl] = __float2bfloat16_rn(v[c] + w[c]);
+        for (int c = 0; c < 32; ++c) os[(r0 + c) * D + jl] = __float2bfloat16_rn(v[c] + w[c]);
     };
     // staging tile -> out, 16-byte coalesced stores of the rows inside the sequence
     auto store_output = [&]() {
-        const uint4 *os = reinterpret_cast<const uint4 *>(sm + OFF_AF);
+        const uint4 *os = reinterpret_cast<const uint4 *>(sm + OFF_STG);
 #pragma unroll
         for (int e = 0; e < 1024 / NT; ++e) {
             const int idx = tid + NT * e;          // 64 rows x 16 uint4
@@ -303,29 +308,27 @@ kda_chunk_tc_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_consta
     const int blk = sub >> 1, hb = sub & 1;    // sub-tile and which half of it
     const int t4 = lane & 3, g = lane >> 2;    // mma.sync fragment coordinates
 
-    float bnext = (tid < C && tid < len) ? __bfloat162float(beta[(bos + tid) * H + h]) : 0.f;
-#pragma unroll 1
-    for (int ci = 0; ci < nchunks; ++ci) {
-        const int64_t t0 = bos + (int64_t)ci * C;
-        const int nr = (int)(len - (int64_t)ci * C < C ? len - (int64_t)ci * C : C);
-        const bool more = ci + 1 < nchunks;
-
-        if (tid < C) {   // this chunk's beta (loaded one chunk ahead); the next chunk's
-            BETA[tid] = bnext;
-            const int64_t nn = more ? len - (int64_t)(ci + 1) * C : 0;
-            bnext = tid < nn ? __bfloat162float(beta[(t0 + C + tid) * H + h]) : 0.f;
-        }
-        {
-            const bool got = mbar_wait(bar_tma, ph_tma, wait_limit);
-            ph_tma ^= 1;
-            if (__syncthreads_or(!got)) { ok = false; break; }
-        }
-
-        // ---- (1) q_r . k_r exactly (bf16 x bf16 products are exact in fp32): the raw
-        // diagonal 16x16 blocks of Q K^T on mma.sync, warps 0-3; all threads: log2-decay
-        // sums over their 8-row half of a sub-tile (cumulative sums restart at each sub-tile).
-        if (warp < 4) {
-            const int I = warp;
+    // (1) of a chunk whose Q, K, G tiles have landed (nr rows inside the sequence): warps 0-7:
+    // log2-decay sums over the two 8-row halves of sub-tile warp/2 (cumulative sums restart at
+    // each sub-tile);  warps 8-11: q_r . k_r exactly (bf16 x bf16 products are exact in fp32)
+    // from the raw diagonal 16x16 blocks of Q K^T on mma.sync
+    auto prephase = [&](int nr) {
+        if (warp < 8) {
+            const int c = 2 * cp, q = tid >> 6;
+#pragma unroll
+            for (int half = 0; half < 2; ++half) {
+                float l0 = 0.f, l1 = 0.f;
+#pragma unroll
+                for (int rr = 0; rr < 8; ++rr) {
+                    const int r = 16 * q + 8 * half + rr;
+                    const float2 g2 = unpack_bf16(*reinterpret_cast<uint32_t *>(sm + OFF_G + sw(r, c, 64)));
+                    if (r < nr) { l0 = fmaf(g2.x, LOG2E, l0); l1 = fmaf(g2.y, LOG2E, l1); }
+                }
+                PART[(2 * q + half) * 128 + c] = l0;
+                PART[(2 * q + half) * 128 + c + 1] = l1;
+            }
+        } else if (warp < 12) {
+            const int I = warp - 8;
             float acc[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
 #pragma unroll
             for (int kk = 0; kk < 8; ++kk) {
@@ -343,67 +346,70 @@ kda_chunk_tc_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_consta
                 for (int e = 0; e < 2; ++e)
                     if (2 * t4 + e == g) MRR[16 * I + g + 8 * hh] = acc[hh][2 * hh + e];
         }
-        {
-            const int c = 2 * cp;
-            float l0 = 0.f, l1 = 0.f;
+    };
+    // per-channel decay vectors of that chunk (log2 units); thread: channel c, sub-tile I
+    auto vectors = [&]() {
+        const int c = tid & 127, I = tid >> 7;
+        float t[4];
 #pragma unroll
-            for (int rr = 0; rr < 8; ++rr) {
-                const int r = 16 * blk + 8 * hb + rr;
-                const float2 g2 = unpack_bf16(*reinterpret_cast<uint32_t *>(sm + OFF_G + sw(r, c, 64)));
-                if (r < nr) { l0 = fmaf(g2.x, LOG2E, l0); l1 = fmaf(g2.y, LOG2E, l1); }
-            }
-            PART[sub * 128 + c] = l0;
-            PART[sub * 128 + c + 1] = l1;
+        for (int J = 0; J < 4; ++J) t[J] = PART[(2 * J) * 128 + c] + PART[(2 * J + 1) * 128 + c];
+        const float bI[4] = {0.f, t[0], t[0] + t[1], t[0] + t[1] + t[2]};
+        const float gl = bI[3] + t[3];
+        EB[I * 128 + c] = ex2(bI[I]);
+        EL[I * 128 + c] = ex2(gl - bI[I]);
+#pragma unroll
+        for (int J = 0; J < 3; ++J)
+            if (J < I) W6[pair_index(I, J) * 128 + c] = __float2bfloat16_rn(ex2(bI[I] - bI[J]));
+        if (I == 0) DEC[c] = ex2(gl);
+    };
+    float bnext = (tid < C && tid < len) ? __bfloat162float(beta[(bos + tid) * H + h]) : 0.f;
+#pragma unroll 1
+    for (int ci = 0; ci < nchunks; ++ci) {
+        const int64_t t0 = bos + (int64_t)ci * C;
+        const int nr = (int)(len - (int64_t)ci * C < C ? len - (int64_t)ci * C : C);
+        const bool more = ci + 1 < nchunks;
+
+        if (tid < C) {   // this chunk's beta (loaded one chunk ahead); the next chunk's
+            BETA[tid] = bnext;
+            const int64_t nn = more ? len - (int64_t)(ci + 1) * C : 0;
+            bnext = tid < nn ? __bfloat162float(beta[(t0 + C + tid) * H + h]) : 0.f;
         }
-        __syncthreads();
-        if (tid < 128) {   // per-channel decay vectors of this chunk (log2 units)
-            const int c = tid;
-            float t[4];
-#pragma unroll
-            for (int I = 0; I < 4; ++I) t[I] = PART[(2 * I) * 128 + c] + PART[(2 * I + 1) * 128 + c];
-            const float b1 = t[0], b2 = b1 + t[1], b3 = b2 + t[2];
-            const float gl = b3 + t[3];
-            const float bI[4] = {0.f, b1, b2, b3};
-#pragma unroll
-            for (int I = 0; I < 4; ++I) {
-                EB[I * 128 + c] = ex2(bI[I]);
-                EL[I * 128 + c] = ex2(gl - bI[I]);
-#pragma unroll
-                for (int J = 0; J < I; ++J) W6[pair_index(I, J) * 128 + c] = __float2bfloat16_rn(ex2(bI[I] - bI[J]));
-            }
-            DEC[c] = ex2(gl);
-        }
-        // the previous chunk's state update and O^T group: then its output is staged
-        if (out_pending) {
-            const bool gs = mbar_wait(bar_s, ph_s, wait_limit);
-            const bool go = mbar_wait(bar_o, ph_o, wait_limit);
-            ph_s ^= 1;
-            ph_o ^= 1;
-            if (__syncthreads_or(!(gs && go))) { ok = false; break; }
-            tc_fence_after();
-            stage_output();
+        bool got = mbar_wait(bar_tma, ph_tma, wait_limit);   // checked at the next barrier
+        ph_tma ^= 1;
+        // ---- (1) warps 0-11: decay sums and q_r . k_r;  warps 12-15: once the previous state
+        // update has landed, S^T -> fp16 pairs (the MMA operand of this chunk)
+        if (warp < 12) {
+            prephase(nr);
         } else {
-            __syncthreads();
+            if (out_pending) got = mbar_wait(bar_s, ph_s, wait_limit) && got;
             tc_fence_after();
-        }
-        // ---- (a) S^T -> fp16 pairs (the MMA operand), then S^T <- S^T Diag(dec) in place
-        {
-            const int i0 = 32 * quarter;
-            float v[32];
-            tmem_ld32(trow + TM_S + i0, v);
-            uint32_t hv[16];
+#pragma unroll 1
+            for (int i0 = 0; i0 < 128; i0 += 32) {
+                float v[32];
+                tmem_ld32(trow + TM_S + i0, v);
+                uint32_t hv[16];
 #pragma unroll
-            for (int c = 0; c < 16; ++c) hv[c] = pack_f16(v[2 * c], v[2 * c + 1]);
-            tmem_st16u(trow + TM_S16 + i0 / 2, hv);
-#pragma unroll
-            for (int c = 0; c < 32; c += 4) {
-                const float4 d4 = *reinterpret_cast<const float4 *>(DEC + i0 + c);
-                v[c] *= d4.x; v[c + 1] *= d4.y; v[c + 2] *= d4.z; v[c + 3] *= d4.w;
+                for (int c = 0; c < 16; ++c) hv[c] = pack_f16(v[2 * c], v[2 * c + 1]);
+                tmem_st16u(trow + TM_S16 + i0 / 2, hv);
             }
-            tmem_st32(trow + TM_S + i0, v);
         }
+        if (out_pending) ph_s ^= 1;
+        tc_fence_before();
+        if (__syncthreads_or(!got)) { ok = false; break; }
+        tc_fence_after();
+        vectors();
+        // the previous chunk's output: staged once its low-order O^T terms have landed
         if (out_pending) {
-            __syncthreads();   // the staging tile is complete
+            if (warp >= 8) {
+                got = mbar_wait(bar_o, ph_o, wait_limit) && got;
+                tc_fence_after();
+                stage_output();
+            }
+            ph_o ^= 1;
+        }
+        tc_fence_before();
+        if (__syncthreads_or(!got)) { ok = false; break; }
+        if (out_pending) {
             store_output();
             out_pending = false;
         }
@@ -440,7 +446,7 @@ kda_chunk_tc_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_consta
                     *reinterpret_cast<uint32_t *>(sm + OFF_SST + off) = qh;
                     *reinterpret_cast<uint32_t *>(sm + OFF_UST + off) = pack_bf16(qt0 - qhf.x, qt1 - qhf.y);
                     *reinterpret_cast<uint32_t *>(sm + OFF_SST + 16384 + off) = pack_bf16(k2.x * x0, k2.y * x1);
-                    *reinterpret_cast<uint32_t *>(sm + OFF_G + off) = khh;
+                    *reinterpret_cast<uint32_t *>(sm + OFF_KH + off) = khh;
                     *reinterpret_cast<uint32_t *>(sm + OFF_WT + off) = pack_bf16(kh0 - khf.x, kh1 - khf.y);
                     *reinterpret_cast<uint32_t *>(sm + OFF_Q + oqk) = pack_f16(qt0 * eb0, qt1 * eb1);
                     *reinterpret_cast<uint32_t *>(sm + OFF_K + oqk) = pack_f16(k2.x * x0 * eb0, k2.y * x1 * eb1);
@@ -458,7 +464,10 @@ kda_chunk_tc_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_consta
         fence_async_smem();
         tc_fence_before();
         __syncthreads();
-        // [O^T | P^T] = S^T [Qbar; Kbar]^T [commit: P], issued by a warp that (3) leaves idle
+        // [O^T | P^T] = S^T [Qbar; Kbar]^T [commit: P], issued by a warp that (3) leaves idle;
+        // the same thread loads the next chunk's G (consumed) and, once the group has read Qbar
+        // and Kbar, its Q and K
+        bool gtma = true;
         if (warp == 15 && lane == 0) {
             tc_fence_after();
 #pragma unroll
@@ -466,6 +475,15 @@ kda_chunk_tc_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_consta
                 mma_f16_ts(tmem + TM_O, tmem + TM_S16 + 8 * k, dsm + ((OFF_Q + (k >> 2) * 16384 + (k & 3) * 32) >> 4),
                            IDESC_N128, k > 0);
             mma_commit(bar_p);
+            if (more) {
+                mbar_arrive_expect_tx(bar_tma, 3 * 16384);
+                tma_tile(&tmg, sb + OFF_G, bar_tma, h, t0 + C);
+                gtma = mbar_wait(bar_p, ph_p, wait_limit);
+                if (gtma) {
+                    tma_tile(&tmq, sb + OFF_Q, bar_tma, h, t0 + C, 16384);
+                    tma_tile(&tmk, sb + OFF_K, bar_tma, h, t0 + C, 16384);
+                }
+            }
         }
 
         // ---- (3) A = beta K~ K^T and M = Q~ K^T on the 10 sub-tile pairs (I >= J).  Warps 0-3:
@@ -493,7 +511,7 @@ kda_chunk_tc_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_consta
                 ldsm_x4(sb + OFF_SST + 16384 + ao, ka[0], ka[1], ka[2], ka[3]);
                 ldsm_x4(sb + OFF_SST + ao, qh[0], qh[1], qh[2], qh[3]);
                 ldsm_x4(sb + OFF_UST + ao, ql[0], ql[1], ql[2], ql[3]);
-                ldsm_x4(sb + OFF_G + bo, bh[0], bh[1], bh[2], bh[3]);
+                ldsm_x4(sb + OFF_KH + bo, bh[0], bh[1], bh[2], bh[3]);
                 ldsm_x4(sb + OFF_WT + bo, bl[0], bl[1], bl[2], bl[3]);
 #pragma unroll
                 for (int nt = 0; nt < 2; ++nt) {
@@ -510,8 +528,8 @@ kda_chunk_tc_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_consta
                     const int r = 16 * I + g + 8 * hh;
                     const int s0 = 16 * I + 8 * nt + 2 * t4;
                     const float br = BETA[r];
-                    AF[r * LDA + s0] = s0 < r ? br * accA[nt][2 * hh] : 0.f;
-                    AF[r * LDA + s0 + 1] = s0 + 1 < r ? br * accA[nt][2 * hh + 1] : 0.f;
+                    AF[r * LDA + (s0 & 15)] = s0 < r ? br * accA[nt][2 * hh] : 0.f;
+                    AF[r * LDA + (s0 & 15) + 1] = s0 + 1 < r ? br * accA[nt][2 * hh + 1] : 0.f;
                     const float mv0 = accM[0][nt][2 * hh] + (accM[1][nt][2 * hh] + accM[2][nt][2 * hh]);
                     const float mv1 = accM[0][nt][2 * hh + 1] + (accM[1][nt][2 * hh + 1] + accM[2][nt][2 * hh + 1]);
                     const float m0 = s0 < r ? mv0 : (s0 == r ? MRR[r] : 0.f);
@@ -525,7 +543,7 @@ kda_chunk_tc_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_consta
             if (lane < 16) {
                 // column jj of T_II: t_jj = 1, t_r = -sum_{s<r} A_rs t_s (rows above jj are 0)
                 const int jj = lane;
-                const float *Ab = AF + (16 * I) * LDA + 16 * I;
+                const float *Ab = AF + (16 * I) * LDA;
                 float tcol[16];
 #pragma unroll
                 for (int r = 0; r < 16; ++r) {
@@ -539,7 +557,14 @@ kda_chunk_tc_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_consta
                 for (int r = 0; r < 16; ++r)
                     at[sw(16 * I + r, 16 * I + jj, 64) >> 1] = __float2half_rn(tcol[r]);
             }
-        } else if (warp < 10) {
+        } else if (warp >= 10 && warp < 14) {   // the blocks of T above the diagonal (staging used them)
+            for (int x = tid - 320; x < 192; x += 128) {
+                const int b = x >> 5, rr = (x >> 1) & 15, hf = x & 1;   // (0,1) (0,2) (0,3) (1,2) (1,3) (2,3)
+                const int I = b < 3 ? 0 : (b < 5 ? 1 : 2);
+                const int J = b < 3 ? b + 1 : (b < 5 ? b - 1 : 3);
+                *reinterpret_cast<uint4 *>(sm + OFF_T + sw(16 * I + rr, 16 * J + 8 * hf, 64)) = make_uint4(0u, 0u, 0u, 0u);
+            }
+        } else if (warp >= 4 && warp < 10) {
             const int po = warp - 4;   // (1,0) (2,0) (2,1) (3,0) (3,1) (3,2)
             const int I = po < 1 ? 1 : (po < 3 ? 2 : 3);
             const int J = po < 1 ? 0 : (po < 3 ? po - 1 : po - 3);
@@ -556,7 +581,7 @@ kda_chunk_tc_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_consta
                 uint32_t ka[4], qh[4], bh[4];
                 ldsm_x4(sb + OFF_SST + 16384 + ao, ka[0], ka[1], ka[2], ka[3]);
                 ldsm_x4(sb + OFF_SST + ao, qh[0], qh[1], qh[2], qh[3]);
-                ldsm_x4(sb + OFF_G + bo, bh[0], bh[1], bh[2], bh[3]);
+                ldsm_x4(sb + OFF_KH + bo, bh[0], bh[1], bh[2], bh[3]);
                 const uint32_t wlo = *reinterpret_cast<const uint32_t *>(w + 16 * kk);
                 const uint32_t whi = *reinterpret_cast<const uint32_t *>(w + 16 * kk + 8);
                 bh[0] = mul_bf16x2(bh[0], wlo); bh[1] = mul_bf16x2(bh[1], whi);
@@ -585,19 +610,7 @@ kda_chunk_tc_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_consta
         }
         __syncthreads();
 
-        // the next chunk's tiles: G (K^hi is consumed) now; Q and K once the two groups above
-        // have read Qbar and Kbar; V after (4)
-        bool got4 = true;
-        if (warp == 3 && lane == 0 && more) {
-            mbar_arrive_expect_tx(bar_tma, 4 * 16384);
-            tma_tile(&tmg, sb + OFF_G, bar_tma, h, t0 + C);
-            got4 = mbar_wait(bar_p, ph_p, wait_limit);
-            if (got4) {
-                tma_tile(&tmq, sb + OFF_Q, bar_tma, h, t0 + C, 16384);
-                tma_tile(&tmk, sb + OFF_K, bar_tma, h, t0 + C, 16384);
-            }
-        }
-
+        bool got4 = gtma;
         // ---- (4) warps 0-2: the off-diagonal blocks of T, level by level (T_IK with K > J is
         // ready before T_IJ);  warps 4-11: Z^T = (V^T - P^T) diag(beta) -> fp16 pairs (TMEM)
         if (warp < 3) {
@@ -607,7 +620,7 @@ kda_chunk_tc_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_consta
             named_bar(1, 96);
             if (warp == 0) t_block(3, 0);
         } else if (warp >= 4 && warp < 12) {
-            got4 = mbar_wait(bar_p, ph_p, wait_limit);
+            got4 = mbar_wait(bar_p, ph_p, wait_limit) && mbar_wait(bar_v, ph_v, wait_limit);
             tc_fence_after();
             const int s0 = 32 * ((warp - 4) >> 2);
             float pv[32];
@@ -622,8 +635,21 @@ kda_chunk_tc_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_consta
                 zv[c] = pack_f16((v0 - pv[2 * c]) * BETA[s], (v1 - pv[2 * c + 1]) * BETA[s + 1]);
             }
             tmem_st16u(trow + TM_Z + s0 / 2, zv);
+        } else if (warp >= 12) {   // S^T <- S^T Diag(dec) in place (S^T was read as fp16 in (1))
+#pragma unroll 1
+            for (int i0 = 0; i0 < 128; i0 += 32) {
+                float v[32];
+                tmem_ld32(trow + TM_S + i0, v);
+#pragma unroll
+                for (int c = 0; c < 32; c += 4) {
+                    const float4 d4 = *reinterpret_cast<const float4 *>(DEC + i0 + c);
+                    v[c] *= d4.x; v[c + 1] *= d4.y; v[c + 2] *= d4.z; v[c + 3] *= d4.w;
+                }
+                tmem_st32(trow + TM_S + i0, v);
+            }
         }
         ph_p ^= 1;
+        ph_v ^= 1;
         fence_async_smem();
         tc_fence_before();
         if (__syncthreads_or(!got4)) { ok = false; break; }
@@ -634,7 +660,10 @@ kda_chunk_tc_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_consta
             for (int k = 0; k < 4; ++k)
                 mma_f16_ts(tmem + TM_U, tmem + TM_Z + 8 * k, dsm + ((OFF_T + k * 32) >> 4), IDESC_N64, k > 0);
             mma_commit(bar_u);
-            if (more) tma_tile(&tmv, sb + OFF_V, bar_tma, h, t0 + C);
+            if (more) {
+                mbar_arrive_expect_tx(bar_v, 16384);
+                tma_tile(&tmv, sb + OFF_V, bar_v, h, t0 + C);
+            }
         }
         {
             const bool got = mbar_wait(bar_u, ph_u, wait_limit);
@@ -702,6 +731,7 @@ kda_chunk_tc_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_consta
         if (tid == 0) {
             mbar_wait(bar_o, ph_o, wait_limit);
             mbar_wait(bar_tma, ph_tma, wait_limit);
+            mbar_wait(bar_v, ph_v, wait_limit);
             atomicAdd(&g_kda_tc_timeouts, 1u);
         }
         __syncthreads();
