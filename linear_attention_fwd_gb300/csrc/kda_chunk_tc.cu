@@ -18,8 +18,9 @@
 //
 // Operand precision: the sub-tile-scaled operands of A and M span
 // [e^-80, e^80] and are bf16 (the range the decay bound was chosen for); every
-// other tensor-core operand (S, V - Kbar S, T, U, Qbar, Kbar, Kp, M) is O(1) and
-// is rounded to fp16 for 3 more mantissa bits; accumulation is fp32 throughout.
+// other tensor-core operand (S, Z = diag(beta)(V - Kbar S), T, U, Qbar, Kbar, Kp, M)
+// is O(1) and is rounded to fp16 for 3 more mantissa bits, Z, U and M as hi + lo
+// pairs where one rounding would show in the outputs; accumulation is fp32 throughout.
 //
 // Per chunk (the fp16 copies of S, beta (V - Kbar S) and U are tensor-memory
 // operands, so the state path never goes through shared memory):
@@ -103,6 +104,7 @@ constexpr uint32_t TM_S16 = 320;  // S^T as fp16 pairs (MMA operand)  64
 constexpr uint32_t TM_Z = 384;    // Z^T fp16 pairs                   32
 constexpr uint32_t TM_UH = 416;   // U^T fp16 pairs, hi               32
 constexpr uint32_t TM_UL = 448;   // U^T - hi, fp16 pairs             32
+constexpr uint32_t TM_ZL = 480;   // Z^T - hi, fp16 pairs             32
 constexpr uint32_t TM_COLS = 512;
 
 constexpr uint32_t IDESC_N64 = idesc_f16_f32(128, 64);
@@ -415,9 +417,11 @@ kda_chunk_tc_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_consta
         }
 
         // ---- (2) operands, each rounded from the exact inputs:
-        //   bf16 (range e^+-80): Q~ = Q x as hi + lo (S^T and U^T buffers, idle here),
-        //   K~ = K x, K^ = K / x as hi + lo (over G, and the W buffer);
+        //   bf16 (range e^+-80): Q~ = Q x and K^ = K / x as hi + lo, K~ = K x;
         //   fp16: Qbar = Q x e^{b_I} (over Q), Kbar (over K), Kp = K / x e^{gl - b_I} (transposed).
+        // Rows past the end of the sequence hold finite data (the next sequence, or TMA zero
+        // fill) and need no masking: their beta is 0, their decay is not accumulated, and the
+        // entries of A and M they would feed lie above the diagonal or in rows never stored.
         {
             const int c = 2 * cp;
             const float eb0 = EB[blk * 128 + c], eb1 = EB[blk * 128 + c + 1];
@@ -432,24 +436,24 @@ kda_chunk_tc_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_consta
                 for (int e = 0; e < 2; ++e) {
                     const int r = 16 * blk + 8 * hb + rr + e;
                     const uint32_t off = sw(r, c, 64), oqk = swqk(r, c);
-                    float2 q2 = unpack_bf16(*reinterpret_cast<uint32_t *>(sm + OFF_Q + oqk));
-                    float2 k2 = unpack_bf16(*reinterpret_cast<uint32_t *>(sm + OFF_K + oqk));
+                    const float2 q2 = unpack_bf16(*reinterpret_cast<uint32_t *>(sm + OFF_Q + oqk));
+                    const float2 k2 = unpack_bf16(*reinterpret_cast<uint32_t *>(sm + OFF_K + oqk));
                     const float2 g2 = unpack_bf16(*reinterpret_cast<uint32_t *>(sm + OFF_G + off));
                     if (r < nr) { l0 = fmaf(g2.x, LOG2E, l0); l1 = fmaf(g2.y, LOG2E, l1); }
-                    else { q2 = make_float2(0.f, 0.f); k2 = q2; }
                     const float x0 = ex2(l0), x1 = ex2(l1);
                     const float y0 = ex2(-l0), y1 = ex2(-l1);
                     const float qt0 = q2.x * x0, qt1 = q2.y * x1;
+                    const float kt0 = k2.x * x0, kt1 = k2.y * x1;
                     const float kh0 = k2.x * y0, kh1 = k2.y * y1;
                     const uint32_t qh = pack_bf16(qt0, qt1), khh = pack_bf16(kh0, kh1);
                     const float2 qhf = unpack_bf16(qh), khf = unpack_bf16(khh);
                     *reinterpret_cast<uint32_t *>(sm + OFF_SST + off) = qh;
                     *reinterpret_cast<uint32_t *>(sm + OFF_UST + off) = pack_bf16(qt0 - qhf.x, qt1 - qhf.y);
-                    *reinterpret_cast<uint32_t *>(sm + OFF_SST + 16384 + off) = pack_bf16(k2.x * x0, k2.y * x1);
+                    *reinterpret_cast<uint32_t *>(sm + OFF_SST + 16384 + off) = pack_bf16(kt0, kt1);
                     *reinterpret_cast<uint32_t *>(sm + OFF_KH + off) = khh;
                     *reinterpret_cast<uint32_t *>(sm + OFF_WT + off) = pack_bf16(kh0 - khf.x, kh1 - khf.y);
                     *reinterpret_cast<uint32_t *>(sm + OFF_Q + oqk) = pack_f16(qt0 * eb0, qt1 * eb1);
-                    *reinterpret_cast<uint32_t *>(sm + OFF_K + oqk) = pack_f16(k2.x * x0 * eb0, k2.y * x1 * eb1);
+                    *reinterpret_cast<uint32_t *>(sm + OFF_K + oqk) = pack_f16(kt0 * eb0, kt1 * eb1);
                     kp[e][0] = kh0 * el0;
                     kp[e][1] = kh1 * el1;
                 }
@@ -486,10 +490,12 @@ kda_chunk_tc_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_consta
             }
         }
 
-        // ---- (3) A = beta K~ K^T and M = Q~ K^T on the 10 sub-tile pairs (I >= J).  Warps 0-3:
-        // the diagonal pair (I, I), I = warp, both 8-column halves, M as the 3-term product
-        // (Q~hi + Q~lo)(K^hi + K^lo)^T less lo.lo with the exact q_r . k_r on its diagonal; the
-        // warp then inverts (I + A_II) by forward substitution (one SM sub-partition per block).
+        // ---- (3) A = beta K~ K^T and M = Q~ K^T on the 10 sub-tile pairs (I >= J), bf16
+        // products with fp32 accumulation.  Warps 0-3: the diagonal pair (I, I), I = warp, both
+        // 8-column halves, M as the 3-term product (Q~hi + Q~lo)(K^hi + K^lo)^T less lo.lo with
+        // the exact q_r . k_r on its diagonal (the largest entries of M, where one bf16 rounding
+        // of each operand shows in the outputs); the warp then inverts (I + A_II) by forward
+        // substitution (one SM sub-partition per block).
         // Warps 4-9: the 6 off-diagonal pairs, single bf16 products with the per-channel factor
         // e^{b_I - b_J} applied to the right operand.  Off-diagonal A blocks go to the fp16
         // tile AT; T_II = (I + A_II)^-1 goes to the diagonal blocks of the fp16 tile T.
@@ -626,15 +632,19 @@ kda_chunk_tc_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_consta
             float pv[32];
             tmem_ld32(trow + TM_P + s0, pv);
             const __nv_bfloat16 *vt = reinterpret_cast<const __nv_bfloat16 *>(sm + OFF_V);
-            uint32_t zv[16];
+            uint32_t zv[16], zl[16];   // hi and lo: one fp16 rounding of U alone costs 2^-12
 #pragma unroll
             for (int c = 0; c < 16; ++c) {
                 const int s = s0 + 2 * c;
                 const float v0 = __bfloat162float(vt[sw(s, jl, 64) >> 1]);
                 const float v1 = __bfloat162float(vt[sw(s + 1, jl, 64) >> 1]);
-                zv[c] = pack_f16((v0 - pv[2 * c]) * BETA[s], (v1 - pv[2 * c + 1]) * BETA[s + 1]);
+                const float z0 = (v0 - pv[2 * c]) * BETA[s], z1 = (v1 - pv[2 * c + 1]) * BETA[s + 1];
+                zv[c] = pack_f16(z0, z1);
+                const float2 zh = unpack_f16(zv[c]);
+                zl[c] = pack_f16(z0 - zh.x, z1 - zh.y);
             }
             tmem_st16u(trow + TM_Z + s0 / 2, zv);
+            tmem_st16u(trow + TM_ZL + s0 / 2, zl);
         } else if (warp >= 12) {   // S^T <- S^T Diag(dec) in place (S^T was read as fp16 in (1))
 #pragma unroll 1
             for (int i0 = 0; i0 < 128; i0 += 32) {
@@ -653,12 +663,15 @@ kda_chunk_tc_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_consta
         fence_async_smem();
         tc_fence_before();
         if (__syncthreads_or(!got4)) { ok = false; break; }
-        // U^T = Z^T T^T [commit: U];  V is consumed: the next chunk's V
+        // U^T = (Z^T_hi + Z^T_lo) T^T [commit: U];  V is consumed: the next chunk's V
         if (tid == 0) {
             tc_fence_after();
 #pragma unroll
             for (int k = 0; k < 4; ++k)
                 mma_f16_ts(tmem + TM_U, tmem + TM_Z + 8 * k, dsm + ((OFF_T + k * 32) >> 4), IDESC_N64, k > 0);
+#pragma unroll
+            for (int k = 0; k < 4; ++k)
+                mma_f16_ts(tmem + TM_U, tmem + TM_ZL + 8 * k, dsm + ((OFF_T + k * 32) >> 4), IDESC_N64, 1);
             mma_commit(bar_u);
             if (more) {
                 mbar_arrive_expect_tx(bar_v, 16384);
@@ -798,7 +811,7 @@ cudaError_t launch_chunk_tc(const ChunkArgs &a, int dk, int dv, kda_dtype_t dt, 
     if (e != cudaSuccess) return e;
     const int64_t units = (int64_t)a.num_seqs * a.heads;
     if (units > 0x7fffffffLL) return cudaErrorInvalidValue;
-    kda_chunk_tc_kernel<<<(unsigned)units, NT, SMEM_BYTES, st>>>(mq, mk, mv, mg, a, 1u << 22);
+    kda_chunk_tc_kernel<<<(unsigned)units, NT, SMEM_BYTES, st>>>(mq, mk, mv, mg, a, 1u << 20);
     return cudaGetLastError();
 }
 

@@ -27,17 +27,18 @@ __device__ __forceinline__ void mbar_arrive_expect_tx(uint32_t bar, uint32_t byt
                  : "memory");
 }
 // Waits for the phase with parity `parity` to complete; gives up after
-// `limit` polls (each poll may suspend the thread for a short, hardware-defined
-// time).  Returns true when the phase completed.
+// `limit` polls.  Each poll suspends the thread until the phase completes or
+// about a microsecond has passed, so waiting warps take few issue slots from
+// working ones.  Returns true when the phase completed.
 __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, uint32_t limit) {
     for (uint32_t i = 0; i < limit; ++i) {
         uint32_t done;
         asm volatile(
             "{\n\t.reg .pred p;\n\t"
-            "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+            "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
             "selp.u32 %0, 1, 0, p;\n\t}"
             : "=r"(done)
-            : "r"(bar), "r"(parity)
+            : "r"(bar), "r"(parity), "r"(1000u)
             : "memory");
         if (done) return true;
     }
