@@ -85,7 +85,8 @@ constexpr uint32_t OFF_DEC = OFF_W6 + 6 * 128 * 2;      // e^{gl}           [128
 constexpr uint32_t OFF_BETA = OFF_DEC + 128 * 4;        // beta             [64]
 constexpr uint32_t OFF_MRR = OFF_BETA + 64 * 4;         // q_r . k_r        [64]
 constexpr uint32_t OFF_MLO = (OFF_MRR + 64 * 4 + 1023) / 1024 * 1024;   // M - fp16(M), fp16 [64 r][64 s]
-constexpr uint32_t OFF_BAR = OFF_MLO + 8192;            // 6 mbarriers, TMEM address
+constexpr uint32_t OFF_SCR = OFF_MLO + 8192;            // split-K partial sums [4][4][32] float4
+constexpr uint32_t OFF_BAR = OFF_SCR + 8192;            // 6 mbarriers, TMEM address
 constexpr uint32_t SMEM_USED = OFF_BAR + 64;
 constexpr uint32_t SMEM_BYTES = SMEM_USED + 1024;       // + alignment slack
 static_assert(SMEM_BYTES <= 227 * 1024, "shared memory budget");
@@ -198,7 +199,7 @@ kda_chunk_tc_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_consta
         mbar_init(bar_tma, 1);
         mbar_init(bar_p, 1);
         mbar_init(bar_v, 1);
-        mbar_init(bar_u, 1);
+        mbar_init(bar_u, 2);
         mbar_init(bar_s, 1);
         mbar_init(bar_o, 1);
         fence_mbar_init();
@@ -256,14 +257,13 @@ kda_chunk_tc_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_consta
     int64_t t0_out = 0;
     int nr_out = 0;
     // O^T (TMEM: high-order part + low-order terms) -> bf16 staging tile [64 r][128 j] over the
-    // AT and T tiles, by warps 8-15; warp w: lanes 32(w%4).., rows 32((w-8)/4)..+31
+    // AT and T tiles, by warps 0-7; warp w: lanes 32(w%4).., rows 32(w/4)..+31
     auto stage_output = [&]() {
-        if (warp < 8) return;
+        if (warp >= 8) return;
         __nv_bfloat16 *os = reinterpret_cast<__nv_bfloat16 *>(sm + OFF_STG);
-        const int r0 = 32 * ((warp - 8) >> 2);
+        const int r0 = 32 * (warp >> 2);
         float v[32], w[32];
-        tmem_ld32(trow + TM_O + r0, v);
-        tmem_ld32(trow + TM_U + r0, w);
+        tmem_ld32x2(trow + TM_O + r0, trow + TM_U + r0, v, w);
 #pragma unroll
         for (int c = 0; c < 32; ++c) os[(r0 + c) * D + jl] = __float2bfloat16_rn(v[c] + w[c]);
     };
@@ -382,17 +382,26 @@ kda_chunk_tc_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_consta
         // update has landed, S^T -> fp16 pairs (the MMA operand of this chunk)
         if (warp < 12) {
             prephase(nr);
+            if (out_pending && warp < 8) {   // the previous chunk's output, once its groups landed
+                got = mbar_wait(bar_s, ph_s, wait_limit) && mbar_wait(bar_o, ph_o, wait_limit) && got;
+                tc_fence_after();
+                stage_output();
+            }
         } else {
             if (out_pending) got = mbar_wait(bar_s, ph_s, wait_limit) && got;
             tc_fence_after();
 #pragma unroll 1
-            for (int i0 = 0; i0 < 128; i0 += 32) {
-                float v[32];
-                tmem_ld32(trow + TM_S + i0, v);
-                uint32_t hv[16];
+            for (int i0 = 0; i0 < 128; i0 += 64) {
+                float v[32], w[32];
+                tmem_ld32x2(trow + TM_S + i0, trow + TM_S + i0 + 32, v, w);
+                uint32_t hv[16], hw[16];
 #pragma unroll
-                for (int c = 0; c < 16; ++c) hv[c] = pack_f16(v[2 * c], v[2 * c + 1]);
+                for (int c = 0; c < 16; ++c) {
+                    hv[c] = pack_f16(v[2 * c], v[2 * c + 1]);
+                    hw[c] = pack_f16(w[2 * c], w[2 * c + 1]);
+                }
                 tmem_st16u(trow + TM_S16 + i0 / 2, hv);
+                tmem_st16u(trow + TM_S16 + i0 / 2 + 16, hw);
             }
         }
         if (out_pending) ph_s ^= 1;
@@ -400,17 +409,8 @@ kda_chunk_tc_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_consta
         if (__syncthreads_or(!got)) { ok = false; break; }
         tc_fence_after();
         vectors();
-        // the previous chunk's output: staged once its low-order O^T terms have landed
-        if (out_pending) {
-            if (warp >= 8) {
-                got = mbar_wait(bar_o, ph_o, wait_limit) && got;
-                tc_fence_after();
-                stage_output();
-            }
-            ph_o ^= 1;
-        }
-        tc_fence_before();
-        if (__syncthreads_or(!got)) { ok = false; break; }
+        if (out_pending) ph_o ^= 1;
+        __syncthreads();
         if (out_pending) {
             store_output();
             out_pending = false;
@@ -424,10 +424,10 @@ kda_chunk_tc_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_consta
         // entries of A and M they would feed lie above the diagonal or in rows never stored.
         {
             const int c = 2 * cp;
-            const float eb0 = EB[blk * 128 + c], eb1 = EB[blk * 128 + c + 1];
-            const float el0 = EL[blk * 128 + c], el1 = EL[blk * 128 + c + 1];
-            float l0 = hb ? PART[(2 * blk) * 128 + c] : 0.f;
-            float l1 = hb ? PART[(2 * blk) * 128 + c + 1] : 0.f;
+            const float2 eb = *reinterpret_cast<const float2 *>(EB + blk * 128 + c);
+            const float2 el = *reinterpret_cast<const float2 *>(EL + blk * 128 + c);
+            float2 l = hb ? *reinterpret_cast<const float2 *>(PART + (2 * blk) * 128 + c) : make_float2(0.f, 0.f);
+            const float2 minus1 = make_float2(-1.f, -1.f);
             uint32_t p0[4], p1[4];
 #pragma unroll
             for (int rr = 0; rr < 8; rr += 2) {
@@ -439,23 +439,24 @@ kda_chunk_tc_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_consta
                     const float2 q2 = unpack_bf16(*reinterpret_cast<uint32_t *>(sm + OFF_Q + oqk));
                     const float2 k2 = unpack_bf16(*reinterpret_cast<uint32_t *>(sm + OFF_K + oqk));
                     const float2 g2 = unpack_bf16(*reinterpret_cast<uint32_t *>(sm + OFF_G + off));
-                    if (r < nr) { l0 = fmaf(g2.x, LOG2E, l0); l1 = fmaf(g2.y, LOG2E, l1); }
-                    const float x0 = ex2(l0), x1 = ex2(l1);
-                    const float y0 = ex2(-l0), y1 = ex2(-l1);
-                    const float qt0 = q2.x * x0, qt1 = q2.y * x1;
-                    const float kt0 = k2.x * x0, kt1 = k2.y * x1;
-                    const float kh0 = k2.x * y0, kh1 = k2.y * y1;
-                    const uint32_t qh = pack_bf16(qt0, qt1), khh = pack_bf16(kh0, kh1);
-                    const float2 qhf = unpack_bf16(qh), khf = unpack_bf16(khh);
+                    const float w2 = r < nr ? LOG2E : 0.f;   // decay past the sequence end is not summed
+                    l = __ffma2_rn(g2, make_float2(w2, w2), l);
+                    const float2 x = make_float2(ex2(l.x), ex2(l.y));
+                    const float2 y = make_float2(ex2(-l.x), ex2(-l.y));
+                    const float2 qt = __fmul2_rn(q2, x), kt = __fmul2_rn(k2, x), kh = __fmul2_rn(k2, y);
+                    const uint32_t qh = pack_bf16(qt.x, qt.y), khh = pack_bf16(kh.x, kh.y);
+                    const float2 ql = __ffma2_rn(unpack_bf16(qh), minus1, qt);
+                    const float2 kl = __ffma2_rn(unpack_bf16(khh), minus1, kh);
                     *reinterpret_cast<uint32_t *>(sm + OFF_SST + off) = qh;
-                    *reinterpret_cast<uint32_t *>(sm + OFF_UST + off) = pack_bf16(qt0 - qhf.x, qt1 - qhf.y);
-                    *reinterpret_cast<uint32_t *>(sm + OFF_SST + 16384 + off) = pack_bf16(kt0, kt1);
+                    *reinterpret_cast<uint32_t *>(sm + OFF_UST + off) = pack_bf16(ql.x, ql.y);
+                    *reinterpret_cast<uint32_t *>(sm + OFF_SST + 16384 + off) = pack_bf16(kt.x, kt.y);
                     *reinterpret_cast<uint32_t *>(sm + OFF_KH + off) = khh;
-                    *reinterpret_cast<uint32_t *>(sm + OFF_WT + off) = pack_bf16(kh0 - khf.x, kh1 - khf.y);
-                    *reinterpret_cast<uint32_t *>(sm + OFF_Q + oqk) = pack_f16(qt0 * eb0, qt1 * eb1);
-                    *reinterpret_cast<uint32_t *>(sm + OFF_K + oqk) = pack_f16(kt0 * eb0, kt1 * eb1);
-                    kp[e][0] = kh0 * el0;
-                    kp[e][1] = kh1 * el1;
+                    *reinterpret_cast<uint32_t *>(sm + OFF_WT + off) = pack_bf16(kl.x, kl.y);
+                    const float2 qb = __fmul2_rn(qt, eb), kb = __fmul2_rn(kt, eb), kp2 = __fmul2_rn(kh, el);
+                    *reinterpret_cast<uint32_t *>(sm + OFF_Q + oqk) = pack_f16(qb.x, qb.y);
+                    *reinterpret_cast<uint32_t *>(sm + OFF_K + oqk) = pack_f16(kb.x, kb.y);
+                    kp[e][0] = kp2.x;
+                    kp[e][1] = kp2.y;
                 }
                 p0[rr / 2] = pack_f16(kp[0][0], kp[1][0]);
                 p1[rr / 2] = pack_f16(kp[0][1], kp[1][1]);
@@ -491,16 +492,17 @@ kda_chunk_tc_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_consta
         }
 
         // ---- (3) A = beta K~ K^T and M = Q~ K^T on the 10 sub-tile pairs (I >= J), bf16
-        // products with fp32 accumulation.  Warps 0-3: the diagonal pair (I, I), I = warp, both
+        // products with fp32 accumulation.  Warps 0-7: the diagonal pair (I, I), I = warp % 4, both
         // 8-column halves, M as the 3-term product (Q~hi + Q~lo)(K^hi + K^lo)^T less lo.lo with
         // the exact q_r . k_r on its diagonal (the largest entries of M, where one bf16 rounding
-        // of each operand shows in the outputs); the warp then inverts (I + A_II) by forward
+        // of each operand shows in the outputs); warps I and I + 4 split the 128 channels and
+        // warp I adds the other half's partial sums, then inverts (I + A_II) by forward
         // substitution (one SM sub-partition per block).
-        // Warps 4-9: the 6 off-diagonal pairs, single bf16 products with the per-channel factor
+        // Warps 8-13: the 6 off-diagonal pairs, single bf16 products with the per-channel factor
         // e^{b_I - b_J} applied to the right operand.  Off-diagonal A blocks go to the fp16
         // tile AT; T_II = (I + A_II)^-1 goes to the diagonal blocks of the fp16 tile T.
-        if (warp < 4) {
-            const int I = warp;
+        if (warp < 8) {
+            const int I = warp & 3, kh = warp >> 2;
             float accA[2][4], accM[3][2][4];
 #pragma unroll
             for (int nt = 0; nt < 2; ++nt)
@@ -510,7 +512,7 @@ kda_chunk_tc_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_consta
                     accM[0][nt][e] = 0.f; accM[1][nt][e] = 0.f; accM[2][nt][e] = 0.f;
                 }
 #pragma unroll 2
-            for (int kk = 0; kk < 8; ++kk) {
+            for (int kk = 4 * kh; kk < 4 * kh + 4; ++kk) {
                 const uint32_t ao = sw(16 * I + (lane & 15), 16 * kk + ((lane >> 4) << 3), 64);
                 const uint32_t bo = sw(16 * I + (lane & 7) + ((lane >> 4) << 3), 16 * kk + (((lane >> 3) & 1) << 3), 64);
                 uint32_t ka[4], qh[4], ql[4], bh[4], bl[4];
@@ -527,6 +529,26 @@ kda_chunk_tc_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_consta
                     mma_16816(accM[2][nt], qh[0], qh[1], qh[2], qh[3], bl[2 * nt], bl[2 * nt + 1]);
                 }
             }
+            float4 *scr = reinterpret_cast<float4 *>(sm + OFF_SCR) + I * 128 + lane;   // [I][4][32]
+#pragma unroll
+            for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+                for (int e = 0; e < 4; ++e) accM[0][nt][e] += accM[1][nt][e] + accM[2][nt][e];
+            if (kh == 1) {   // hand the partial sums of channels 64..127 to warp I
+#pragma unroll
+                for (int nt = 0; nt < 2; ++nt) {
+                    scr[(2 * nt) * 32] = make_float4(accA[nt][0], accA[nt][1], accA[nt][2], accA[nt][3]);
+                    scr[(2 * nt + 1) * 32] = make_float4(accM[0][nt][0], accM[0][nt][1], accM[0][nt][2], accM[0][nt][3]);
+                }
+                named_bar_arrive(1 + I, 64);
+            } else {
+            named_bar(1 + I, 64);
+#pragma unroll
+            for (int nt = 0; nt < 2; ++nt) {
+                const float4 pa = scr[(2 * nt) * 32], pm = scr[(2 * nt + 1) * 32];
+                accA[nt][0] += pa.x; accA[nt][1] += pa.y; accA[nt][2] += pa.z; accA[nt][3] += pa.w;
+                accM[0][nt][0] += pm.x; accM[0][nt][1] += pm.y; accM[0][nt][2] += pm.z; accM[0][nt][3] += pm.w;
+            }
 #pragma unroll
             for (int nt = 0; nt < 2; ++nt)
 #pragma unroll
@@ -536,10 +558,8 @@ kda_chunk_tc_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_consta
                     const float br = BETA[r];
                     AF[r * LDA + (s0 & 15)] = s0 < r ? br * accA[nt][2 * hh] : 0.f;
                     AF[r * LDA + (s0 & 15) + 1] = s0 + 1 < r ? br * accA[nt][2 * hh + 1] : 0.f;
-                    const float mv0 = accM[0][nt][2 * hh] + (accM[1][nt][2 * hh] + accM[2][nt][2 * hh]);
-                    const float mv1 = accM[0][nt][2 * hh + 1] + (accM[1][nt][2 * hh + 1] + accM[2][nt][2 * hh + 1]);
-                    const float m0 = s0 < r ? mv0 : (s0 == r ? MRR[r] : 0.f);
-                    const float m1 = s0 + 1 < r ? mv1 : (s0 + 1 == r ? MRR[r] : 0.f);
+                    const float m0 = s0 < r ? accM[0][nt][2 * hh] : (s0 == r ? MRR[r] : 0.f);
+                    const float m1 = s0 + 1 < r ? accM[0][nt][2 * hh + 1] : (s0 + 1 == r ? MRR[r] : 0.f);
                     const uint32_t mh = pack_f16(m0, m1);
                     const float2 mhf = unpack_f16(mh);
                     *reinterpret_cast<uint32_t *>(sm + OFF_MT + sw(r, s0, 64)) = mh;
@@ -553,9 +573,15 @@ kda_chunk_tc_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_consta
                 float tcol[16];
 #pragma unroll
                 for (int r = 0; r < 16; ++r) {
+                    float arow[16];
+#pragma unroll
+                    for (int q4 = 0; q4 < (r + 3) / 4; ++q4) {
+                        const float4 a4 = *reinterpret_cast<const float4 *>(Ab + r * LDA + 4 * q4);
+                        arow[4 * q4] = a4.x; arow[4 * q4 + 1] = a4.y; arow[4 * q4 + 2] = a4.z; arow[4 * q4 + 3] = a4.w;
+                    }
                     float acc = 0.f;
 #pragma unroll
-                    for (int s2 = 0; s2 < r; ++s2) acc = fmaf(Ab[r * LDA + s2], tcol[s2], acc);
+                    for (int s2 = 0; s2 < r; ++s2) acc = fmaf(arow[s2], tcol[s2], acc);
                     tcol[r] = r == jj ? 1.f : (r < jj ? 0.f : -acc);
                 }
                 __half *at = reinterpret_cast<__half *>(sm + OFF_T);
@@ -563,15 +589,16 @@ kda_chunk_tc_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_consta
                 for (int r = 0; r < 16; ++r)
                     at[sw(16 * I + r, 16 * I + jj, 64) >> 1] = __float2half_rn(tcol[r]);
             }
-        } else if (warp >= 10 && warp < 14) {   // the blocks of T above the diagonal (staging used them)
-            for (int x = tid - 320; x < 192; x += 128) {
+            }
+        } else if (warp == 14) {   // the blocks of T above the diagonal (staging used them)
+            for (int x = lane; x < 192; x += 32) {
                 const int b = x >> 5, rr = (x >> 1) & 15, hf = x & 1;   // (0,1) (0,2) (0,3) (1,2) (1,3) (2,3)
                 const int I = b < 3 ? 0 : (b < 5 ? 1 : 2);
                 const int J = b < 3 ? b + 1 : (b < 5 ? b - 1 : 3);
                 *reinterpret_cast<uint4 *>(sm + OFF_T + sw(16 * I + rr, 16 * J + 8 * hf, 64)) = make_uint4(0u, 0u, 0u, 0u);
             }
-        } else if (warp >= 4 && warp < 10) {
-            const int po = warp - 4;   // (1,0) (2,0) (2,1) (3,0) (3,1) (3,2)
+        } else if (warp >= 8 && warp < 14) {
+            const int po = warp - 8;   // (1,0) (2,0) (2,1) (3,0) (3,1) (3,2)
             const int I = po < 1 ? 1 : (po < 3 ? 2 : 3);
             const int J = po < 1 ? 0 : (po < 3 ? po - 1 : po - 3);
             float accA[2][4], accM[2][4];
@@ -636,26 +663,34 @@ kda_chunk_tc_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_consta
 #pragma unroll
             for (int c = 0; c < 16; ++c) {
                 const int s = s0 + 2 * c;
-                const float v0 = __bfloat162float(vt[sw(s, jl, 64) >> 1]);
-                const float v1 = __bfloat162float(vt[sw(s + 1, jl, 64) >> 1]);
-                const float z0 = (v0 - pv[2 * c]) * BETA[s], z1 = (v1 - pv[2 * c + 1]) * BETA[s + 1];
-                zv[c] = pack_f16(z0, z1);
-                const float2 zh = unpack_f16(zv[c]);
-                zl[c] = pack_f16(z0 - zh.x, z1 - zh.y);
+                const float2 v2 = make_float2(__bfloat162float(vt[sw(s, jl, 64) >> 1]),
+                                              __bfloat162float(vt[sw(s + 1, jl, 64) >> 1]));
+                const float2 z = __fmul2_rn(__fadd2_rn(v2, make_float2(-pv[2 * c], -pv[2 * c + 1])),
+                                            *reinterpret_cast<const float2 *>(BETA + s));
+                zv[c] = pack_f16(z.x, z.y);
+                const float2 zlo = __ffma2_rn(unpack_f16(zv[c]), make_float2(-1.f, -1.f), z);
+                zl[c] = pack_f16(zlo.x, zlo.y);
             }
             tmem_st16u(trow + TM_Z + s0 / 2, zv);
             tmem_st16u(trow + TM_ZL + s0 / 2, zl);
         } else if (warp >= 12) {   // S^T <- S^T Diag(dec) in place (S^T was read as fp16 in (1))
 #pragma unroll 1
-            for (int i0 = 0; i0 < 128; i0 += 32) {
-                float v[32];
-                tmem_ld32(trow + TM_S + i0, v);
+            for (int i0 = 0; i0 < 128; i0 += 64) {
+                float v[32], w[32];
+                tmem_ld32x2(trow + TM_S + i0, trow + TM_S + i0 + 32, v, w);
 #pragma unroll
                 for (int c = 0; c < 32; c += 4) {
                     const float4 d4 = *reinterpret_cast<const float4 *>(DEC + i0 + c);
-                    v[c] *= d4.x; v[c + 1] *= d4.y; v[c + 2] *= d4.z; v[c + 3] *= d4.w;
+                    const float4 e4 = *reinterpret_cast<const float4 *>(DEC + i0 + 32 + c);
+                    const float2 a2 = __fmul2_rn(make_float2(v[c], v[c + 1]), make_float2(d4.x, d4.y));
+                    const float2 b2 = __fmul2_rn(make_float2(v[c + 2], v[c + 3]), make_float2(d4.z, d4.w));
+                    const float2 c2 = __fmul2_rn(make_float2(w[c], w[c + 1]), make_float2(e4.x, e4.y));
+                    const float2 f2 = __fmul2_rn(make_float2(w[c + 2], w[c + 3]), make_float2(e4.z, e4.w));
+                    v[c] = a2.x; v[c + 1] = a2.y; v[c + 2] = b2.x; v[c + 3] = b2.y;
+                    w[c] = c2.x; w[c + 1] = c2.y; w[c + 2] = f2.x; w[c + 3] = f2.y;
                 }
                 tmem_st32(trow + TM_S + i0, v);
+                tmem_st32(trow + TM_S + i0 + 32, w);
             }
         }
         ph_p ^= 1;
@@ -663,15 +698,20 @@ kda_chunk_tc_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_consta
         fence_async_smem();
         tc_fence_before();
         if (__syncthreads_or(!got4)) { ok = false; break; }
-        // U^T = (Z^T_hi + Z^T_lo) T^T [commit: U];  V is consumed: the next chunk's V
+        // U^T = Z^T_hi T^T (U columns) + Z^T_lo T^T (the consumed P columns), issued by two
+        // threads [commit: U, two arrivals];  V is consumed: the next chunk's V
+        if (tid == 32) {
+            tc_fence_after();
+#pragma unroll
+            for (int k = 0; k < 4; ++k)
+                mma_f16_ts(tmem + TM_P, tmem + TM_ZL + 8 * k, dsm + ((OFF_T + k * 32) >> 4), IDESC_N64, k > 0);
+            mma_commit(bar_u);
+        }
         if (tid == 0) {
             tc_fence_after();
 #pragma unroll
             for (int k = 0; k < 4; ++k)
                 mma_f16_ts(tmem + TM_U, tmem + TM_Z + 8 * k, dsm + ((OFF_T + k * 32) >> 4), IDESC_N64, k > 0);
-#pragma unroll
-            for (int k = 0; k < 4; ++k)
-                mma_f16_ts(tmem + TM_U, tmem + TM_ZL + 8 * k, dsm + ((OFF_T + k * 32) >> 4), IDESC_N64, 1);
             mma_commit(bar_u);
             if (more) {
                 mbar_arrive_expect_tx(bar_v, 16384);
@@ -687,14 +727,19 @@ kda_chunk_tc_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_consta
         // ---- (5) U^T -> fp16 hi + lo pairs (TMEM); warp w: lanes 32(w%4).., columns 16(w/4)..
         {
             const int r0 = 16 * quarter;
-            float uv[16];
-            tmem_ld16(trow + TM_U + r0, uv);
+            float uv[16], u2[16];
+            tmem_ld16x2(trow + TM_U + r0, trow + TM_P + r0, uv, u2);
+#pragma unroll
+            for (int e = 0; e < 16; e += 2) {
+                const float2 a2 = __fadd2_rn(make_float2(uv[e], uv[e + 1]), make_float2(u2[e], u2[e + 1]));
+                uv[e] = a2.x; uv[e + 1] = a2.y;
+            }
             uint32_t hi[8], lo[8];
 #pragma unroll
             for (int e = 0; e < 8; ++e) {
                 hi[e] = pack_f16(uv[2 * e], uv[2 * e + 1]);
-                const float2 hf = unpack_f16(hi[e]);
-                lo[e] = pack_f16(uv[2 * e] - hf.x, uv[2 * e + 1] - hf.y);
+                const float2 lo2 = __ffma2_rn(unpack_f16(hi[e]), make_float2(-1.f, -1.f), make_float2(uv[2 * e], uv[2 * e + 1]));
+                lo[e] = pack_f16(lo2.x, lo2.y);
             }
             tmem_st8u(trow + TM_UH + r0 / 2, hi);
             tmem_st8u(trow + TM_UL + r0 / 2, lo);
