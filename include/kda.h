@@ -135,6 +135,32 @@ kda_status_t kda_recurrent_step(const void *q, const void *k, const void *v,
                                 const int32_t *state_indices, void *out,
                                 const kda_dims_t *dims, cudaStream_t stream);
 
+/* kda_recurrent_steps -- up to T decode tokens per row from the row's state, for speculative
+ * decoding.  The pages' account of it: the state is updated in place, so a rejected draft
+ * cannot be rolled back; the draft tokens' projected inputs (far smaller than the state) are
+ * kept instead and the accepted ones are rebuilt on chip ("はじめての自然言語処理 -- Kimi K3",
+ * the infrastructure paragraph on speculative decoding).  So a draft is verified with
+ * update_state = 0 (outputs only, the state untouched) and the accepted prefix is then replayed
+ * into the state with update_state = 1.
+ *
+ * Row n runs tokens 0 .. m_n - 1, m_n = num_tokens ? clamp(num_tokens[n], 0, T) : T, each as in
+ * kda_recurrent_step, starting from S = state[slot][h] (slot as in kda_recurrent_step); the
+ * state stays on chip between tokens (one read and at most one write per row and head).
+ *   q, k, g : [N, T, H, dk] dtype;  v, out : [N, T, H, dv] dtype;  beta : [N, T, H]
+ *   state   : fp32 [num_seqs, H, dk, dv]; written (the state after the row's m_n tokens) only
+ *             when update_state != 0 and m_n > 0.
+ *   state_indices: as in kda_recurrent_step (rows with a slot outside the pool are skipped).
+ *   num_tokens: int32 [N] device or NULL (every row runs all T tokens).
+ *   out     : may be NULL (no outputs); outputs of tokens m_n .. T-1 are not written.
+ * dims: batch = N rows, seqlen = T, num_seqs = pool slots.  Two rows must not name the same
+ * slot when update_state != 0.  Errors as in kda_recurrent_step; out == NULL with
+ * update_state == 0 returns KDA_OK without launching. */
+kda_status_t kda_recurrent_steps(const void *q, const void *k, const void *v,
+                                 const void *g, const void *beta, float *state,
+                                 const int32_t *state_indices, const int32_t *num_tokens,
+                                 void *out, int update_state,
+                                 const kda_dims_t *dims, cudaStream_t stream);
+
 /* A static, human-readable name for a status code (never NULL). */
 const char *kda_status_string(kda_status_t status);
 

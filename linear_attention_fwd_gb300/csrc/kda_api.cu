@@ -114,7 +114,36 @@ extern "C" kda_status_t kda_recurrent_step(const void *q, const void *k, const v
         if (!aligned(p, 16)) return KDA_ERR_ALIGN;
     if (!aligned(beta, es)) return KDA_ERR_ALIGN;
     if (state_indices && !aligned(state_indices, 4)) return KDA_ERR_ALIGN;
-    kda::DecodeArgs a{q, k, v, g, beta, state, state_indices, out, d->batch, d->num_seqs, d->heads};
+    kda::DecodeArgs a{q, k, v, g, beta, state, state_indices, out, d->batch, d->num_seqs, d->heads,
+                      1, nullptr, 1};
+    cudaError_t e = kda::launch_decode(a, d->dk, d->dv, d->dtype, stream);
+    return e == cudaSuccess ? KDA_OK : KDA_ERR_CUDA;
+}
+
+extern "C" kda_status_t kda_recurrent_steps(const void *q, const void *k, const void *v,
+                                            const void *g, const void *beta, float *state,
+                                            const int32_t *state_indices, const int32_t *num_tokens,
+                                            void *out, int update_state, const kda_dims_t *d,
+                                            cudaStream_t stream) {
+    if (d == nullptr) return KDA_ERR_NULL;
+    if (d->dtype != KDA_F32 && d->dtype != KDA_BF16) return KDA_ERR_UNSUPPORTED;
+    if (!head_size_ok(d->dk) || !head_size_ok(d->dv)) return KDA_ERR_UNSUPPORTED;
+    if (d->seqlen < 1 || d->batch < 0 || d->heads <= 0 || d->num_seqs <= 0) return KDA_ERR_SHAPE;
+    if (state_indices == nullptr && d->num_seqs < d->batch) return KDA_ERR_SHAPE;
+    if ((int64_t)d->batch * d->seqlen * d->heads > 0x7fffffffLL) return KDA_ERR_SHAPE;
+    if (d->batch == 0) return KDA_OK;
+    if (!q || !k || !v || !g || !beta || !state) return KDA_ERR_NULL;
+    if (out == nullptr && !update_state) return KDA_OK;   // nothing to write
+    const uintptr_t es = d->dtype == KDA_F32 ? 4 : 2;
+    const void *ptrs[] = {q, k, v, g, state};
+    for (const void *p : ptrs)
+        if (!aligned(p, 16)) return KDA_ERR_ALIGN;
+    if (out && !aligned(out, 16)) return KDA_ERR_ALIGN;
+    if (!aligned(beta, es)) return KDA_ERR_ALIGN;
+    if (state_indices && !aligned(state_indices, 4)) return KDA_ERR_ALIGN;
+    if (num_tokens && !aligned(num_tokens, 4)) return KDA_ERR_ALIGN;
+    kda::DecodeArgs a{q, k, v, g, beta, state, state_indices, out, d->batch, d->num_seqs, d->heads,
+                      d->seqlen, num_tokens, update_state ? 1 : 0};
     cudaError_t e = kda::launch_decode(a, d->dk, d->dv, d->dtype, stream);
     return e == cudaSuccess ? KDA_OK : KDA_ERR_CUDA;
 }

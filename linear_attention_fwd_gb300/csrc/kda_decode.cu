@@ -1,4 +1,4 @@
-// KDA recurrent decode step: one token per (row, head), fp32 state in place.
+// KDA recurrent decode: one or more tokens per (row, head), fp32 state in place.
 //
 // Per state column j (columns of S are independent, since v_j only touches
 // column j), in the order of the four-step delta rule of "はじめての自然言語処理
@@ -8,6 +8,9 @@
 //   o_j = sum_i q_i S'_ij = p_j + beta (k.q) e_j.
 // The state is streamed through registers exactly once (one HBM read and one
 // HBM write of d_k*d_v*4 bytes per (row, head)); that traffic is the roofline.
+// Several tokens of a row (speculative decoding: a draft verified without
+// touching the state, or the accepted prefix replayed into it) keep the state
+// in registers between tokens, so their state traffic is paid once.
 #include <cuda_runtime.h>
 #include <cuda_bf16.h>
 
@@ -37,8 +40,13 @@ kda_recurrent_step_kernel(DecodeArgs a) {
 
     const int t = threadIdx.x;
     const int cg = t % CG, rg = t / CG;
-    const int64_t row = (int64_t)n * a.heads + h;
     float *S = a.state + ((int64_t)slot * a.heads + h) * (DK * DV);
+    int ntok = a.ntok;
+    if (a.ntok_row) {
+        const int m = __ldg(a.ntok_row + n);
+        ntok = m < 0 ? 0 : (m < ntok ? m : ntok);
+    }
+    if (ntok == 0) return;   // uniform across the block
 
     // Issue the state loads first: they are the only traffic that matters.
     float4 s[RPT];
@@ -46,61 +54,66 @@ kda_recurrent_step_kernel(DecodeArgs a) {
     for (int m = 0; m < RPT; ++m)
         s[m] = __ldcs(reinterpret_cast<const float4 *>(S + (rg * RPT + m) * DV) + cg);
 
-    const Tin *q = static_cast<const Tin *>(a.q) + row * DK;
-    const Tin *k = static_cast<const Tin *>(a.k) + row * DK;
-    const Tin *g = static_cast<const Tin *>(a.g) + row * DK;
-    const Tin *v = static_cast<const Tin *>(a.v) + row * DV;
-    for (int i = t; i < DK; i += kDecodeThreads) {
-        sq[i] = to_f(q[i]);
-        sk[i] = to_f(k[i]);
-        sa[i] = expf(to_f(g[i]));
-    }
-    for (int j = t; j < DV; j += kDecodeThreads) sv[j] = to_f(v[j]);
-    const float beta = to_f(static_cast<const Tin *>(a.beta)[row]);
-    __syncthreads();
+#pragma unroll 1
+    for (int tok = 0; tok < ntok; ++tok) {
+        const int64_t row = ((int64_t)n * a.ntok + tok) * a.heads + h;
+        const Tin *q = static_cast<const Tin *>(a.q) + row * DK;
+        const Tin *k = static_cast<const Tin *>(a.k) + row * DK;
+        const Tin *g = static_cast<const Tin *>(a.g) + row * DK;
+        const Tin *v = static_cast<const Tin *>(a.v) + row * DV;
+        for (int i = t; i < DK; i += kDecodeThreads) {
+            sq[i] = to_f(q[i]);
+            sk[i] = to_f(k[i]);
+            sa[i] = expf(to_f(g[i]));
+        }
+        for (int j = t; j < DV; j += kDecodeThreads) sv[j] = to_f(v[j]);
+        const float beta = to_f(static_cast<const Tin *>(a.beta)[row]);
+        __syncthreads();
 
-    if (t < 32) {  // k . q
-        float d = 0.f;
-        for (int i = t; i < DK; i += 32) d += sk[i] * sq[i];
+        if (t < 32) {  // k . q
+            float d = 0.f;
+            for (int i = t; i < DK; i += 32) d += sk[i] * sq[i];
 #pragma unroll
-        for (int o = 16; o > 0; o >>= 1) d += __shfl_xor_sync(0xffffffffu, d, o);
-        if (t == 0) s_qk = d;
-    }
+            for (int o = 16; o > 0; o >>= 1) d += __shfl_xor_sync(0xffffffffu, d, o);
+            if (t == 0) s_qk = d;
+        }
 
-    float4 pv = make_float4(0.f, 0.f, 0.f, 0.f), pp = pv;
+        float4 pv = make_float4(0.f, 0.f, 0.f, 0.f), pp = pv;
 #pragma unroll
-    for (int m = 0; m < RPT; ++m) {
-        const int i = rg * RPT + m;
-        const float ak = sa[i] * sk[i], aq = sa[i] * sq[i];
-        pv.x += ak * s[m].x; pv.y += ak * s[m].y; pv.z += ak * s[m].z; pv.w += ak * s[m].w;
-        pp.x += aq * s[m].x; pp.y += aq * s[m].y; pp.z += aq * s[m].z; pp.w += aq * s[m].w;
-    }
-    *reinterpret_cast<float4 *>(&red_v[rg][4 * cg]) = pv;
-    *reinterpret_cast<float4 *>(&red_p[rg][4 * cg]) = pp;
-    __syncthreads();
+        for (int m = 0; m < RPT; ++m) {
+            const int i = rg * RPT + m;
+            const float ak = sa[i] * sk[i], aq = sa[i] * sq[i];
+            pv.x += ak * s[m].x; pv.y += ak * s[m].y; pv.z += ak * s[m].z; pv.w += ak * s[m].w;
+            pp.x += aq * s[m].x; pp.y += aq * s[m].y; pp.z += aq * s[m].z; pp.w += aq * s[m].w;
+        }
+        *reinterpret_cast<float4 *>(&red_v[rg][4 * cg]) = pv;
+        *reinterpret_cast<float4 *>(&red_p[rg][4 * cg]) = pp;
+        __syncthreads();
 
-    Tin *out = static_cast<Tin *>(a.out) + row * DV;
-    for (int j = t; j < DV; j += kDecodeThreads) {
-        float vh = 0.f, p = 0.f;
+        Tin *out = a.out ? static_cast<Tin *>(a.out) + row * DV : nullptr;
+        for (int j = t; j < DV; j += kDecodeThreads) {
+            float vh = 0.f, p = 0.f;
 #pragma unroll
-        for (int r = 0; r < RG; ++r) { vh += red_v[r][j]; p += red_p[r][j]; }
-        const float e = sv[j] - vh;
-        se[j] = e;
-        out[j] = from_f<Tin>(p + beta * s_qk * e);
-    }
-    __syncthreads();
+            for (int r = 0; r < RG; ++r) { vh += red_v[r][j]; p += red_p[r][j]; }
+            const float e = sv[j] - vh;
+            se[j] = e;
+            if (out) out[j] = from_f<Tin>(p + beta * s_qk * e);
+        }
+        __syncthreads();
 
-    const float4 e4 = *reinterpret_cast<const float4 *>(&se[4 * cg]);
+        const float4 e4 = *reinterpret_cast<const float4 *>(&se[4 * cg]);
+        const bool last = tok + 1 == ntok;
 #pragma unroll
-    for (int m = 0; m < RPT; ++m) {
-        const int i = rg * RPT + m;
-        const float al = sa[i], bk = beta * sk[i];
-        float4 o;
-        o.x = al * s[m].x + bk * e4.x;
-        o.y = al * s[m].y + bk * e4.y;
-        o.z = al * s[m].z + bk * e4.z;
-        o.w = al * s[m].w + bk * e4.w;
-        __stcs(reinterpret_cast<float4 *>(S + i * DV) + cg, o);
+        for (int m = 0; m < RPT; ++m) {
+            const int i = rg * RPT + m;
+            const float al = sa[i], bk = beta * sk[i];
+            s[m].x = al * s[m].x + bk * e4.x;
+            s[m].y = al * s[m].y + bk * e4.y;
+            s[m].z = al * s[m].z + bk * e4.z;
+            s[m].w = al * s[m].w + bk * e4.w;
+            if (last && a.update) __stcs(reinterpret_cast<float4 *>(S + i * DV) + cg, s[m]);
+        }
+        if (!last) __syncthreads();   // the shared vectors are rewritten by the next token
     }
 }
 

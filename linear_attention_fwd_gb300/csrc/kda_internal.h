@@ -29,10 +29,13 @@ struct DecodeArgs {
     const void *q, *k, *v, *g, *beta;
     float *state;
     const int32_t *idx;       // [N] or nullptr
-    void *out;
+    void *out;                // or nullptr (no outputs)
     int32_t rows;             // N
     int32_t slots;            // pool size
     int32_t heads;
+    int32_t ntok;             // tokens per row in the input layout [N, ntok, H, d]
+    const int32_t *ntok_row;  // [N] tokens to run per row (clamped to [0, ntok]) or nullptr
+    int32_t update;           // write the state back
 };
 
 // Token range [bos, eos) of sequence n, read on the device and clamped so that

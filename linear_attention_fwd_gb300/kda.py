@@ -23,7 +23,7 @@ IMPL_NAMES = {v: k for k, v in IMPLS.items()}
 
 # every symbol include/kda.h declares
 EXPORTED = ("kda_chunk_fwd", "kda_chunk_fwd_with", "kda_chunk_fwd_selected_impl",
-            "kda_recurrent_step", "kda_status_string")
+            "kda_recurrent_step", "kda_recurrent_steps", "kda_status_string")
 
 
 class KdaDims(ctypes.Structure):
@@ -58,6 +58,8 @@ def lib() -> ctypes.CDLL:
         L.kda_chunk_fwd_selected_impl.argtypes = [dp]
         L.kda_recurrent_step.restype = ctypes.c_int
         L.kda_recurrent_step.argtypes = [vp] * 8 + [dp, vp]
+        L.kda_recurrent_steps.restype = ctypes.c_int
+        L.kda_recurrent_steps.argtypes = [vp] * 9 + [ctypes.c_int, dp, vp]
         L.kda_status_string.restype = ctypes.c_char_p
         L.kda_status_string.argtypes = [ctypes.c_int]
         _lib = L
@@ -169,3 +171,37 @@ def kda_recurrent_step(q, k, v, g, beta, state, state_indices=None, *, out=None,
     if st != KDA_OK:
         raise KdaError(st, "kda_recurrent_step")
     return out
+
+
+def kda_recurrent_steps(q, k, v, g, beta, state, state_indices=None, num_tokens=None, *,
+                        out=None, want_out=True, update_state=True, stream=None):
+    """Up to T decode tokens per row through libkda (speculative decoding).
+
+    q, k, g: [N, T, H, dk]; v: [N, T, H, dv]; beta: [N, T, H]; state: fp32 [P, H, dk, dv];
+    state_indices, num_tokens: int32 [N] or None.  With update_state the state after each
+    row's tokens is written in place; without, the state is only read.  Returns out
+    [N, T, H, dv] (tokens past a row's count are left as they were), or None when
+    ``want_out`` is false.
+    """
+    dev = q.device
+    for name, t in (("q", q), ("k", k), ("v", v), ("g", g), ("beta", beta)):
+        _check_dev(name, t, dev, q.dtype)
+    _check_dev("state", state, dev, torch.float32)
+    _check_dev("state_indices", state_indices, dev, torch.int32)
+    _check_dev("num_tokens", num_tokens, dev, torch.int32)
+    N, T, H, dk = q.shape
+    dv = v.shape[-1]
+    if state.shape[1:] != (H, dk, dv):
+        raise ValueError("state must be [P, H, dk, dv]")
+    dims = KdaDims(N, T, state.shape[0], H, dk, dv, _dtype_code(q.dtype))
+    if want_out and out is None:
+        out = torch.zeros((N, T, H, dv), dtype=q.dtype, device=dev)
+    if out is not None:
+        _check_dev("out", out, dev, q.dtype)
+    st = lib().kda_recurrent_steps(_ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta), _ptr(state),
+                                   _ptr(state_indices), _ptr(num_tokens),
+                                   _ptr(out) if want_out else None, int(bool(update_state)),
+                                   ctypes.byref(dims), _stream_handle(stream))
+    if st != KDA_OK:
+        raise KdaError(st, "kda_recurrent_steps")
+    return out if want_out else None

@@ -116,6 +116,26 @@ def test_recurrent_step_validation(K):
     assert call_step(K, d1(batch=0)) == K.KDA_OK                # no rows: nothing to do
 
 
+def call_steps(K, d, q=FAKE, state=FAKE, idx=None, num=None, out=FAKE, update=1):
+    vp = ctypes.c_void_p
+    a = [vp(x) if x is not None else None for x in (q, FAKE, FAKE, FAKE, FAKE, state, idx, num, out)]
+    return K.lib().kda_recurrent_steps(*a, update, ctypes.byref(d) if d is not None else None, None)
+
+
+def test_recurrent_steps_validation(K):
+    d1 = lambda **kw: dims(**{**dict(batch=8, seqlen=4, num_seqs=8), **kw})
+    assert call_steps(K, None) == K.KDA_ERR_NULL
+    assert call_steps(K, d1(seqlen=0)) == K.KDA_ERR_SHAPE
+    assert call_steps(K, d1(num_seqs=4)) == K.KDA_ERR_SHAPE    # pool smaller than rows
+    assert call_steps(K, d1(dv=80)) == K.KDA_ERR_UNSUPPORTED
+    assert call_steps(K, d1(), state=None) == K.KDA_ERR_NULL
+    assert call_steps(K, d1(), q=FAKE + 4) == K.KDA_ERR_ALIGN
+    assert call_steps(K, d1(), num=FAKE + 2) == K.KDA_ERR_ALIGN
+    assert call_steps(K, d1(), out=FAKE + 8) == K.KDA_ERR_ALIGN
+    assert call_steps(K, d1(batch=0)) == K.KDA_OK                # no rows: nothing to do
+    assert call_steps(K, d1(), out=None, update=0) == K.KDA_OK   # nothing to write
+
+
 def test_binding_fails_loudly_without_library(monkeypatch, tmp_path):
     from linear_attention_fwd_gb300 import kda
     monkeypatch.setattr(kda, "_lib", None)
