@@ -112,6 +112,30 @@ kda_status_t kda_chunk_fwd_with(kda_impl_t impl,
                                 void *out, float *final_state,
                                 const kda_dims_t *dims, cudaStream_t stream);
 
+/* kda_chunk_fwd_checkpointed -- kda_chunk_fwd that also writes the recurrent state at every
+ * multiple of `checkpoint_interval` tokens strictly inside each sequence, for prefix caching.
+ * The pages' account: the cache hashes prompts in 512-token units and keeps recurrent-state
+ * checkpoints only at a sparse subset of those endpoints, so that a prefix hit can resume from
+ * a stored state ("はじめての自然言語処理 -- Kimi K3", the infrastructure paragraph on
+ * prefix reuse; resuming is kda_chunk_fwd with initial_state).
+ *   checkpoints       : fp32 [slots, H, dk, dv]; the state after the first (k+1)*interval
+ *                       tokens of sequence n goes to slot checkpoint_offsets[n] + k, for
+ *                       k < checkpoint_offsets[n+1] - checkpoint_offsets[n] and
+ *                       (k+1)*interval < len_n (the state at the end is final_state).
+ *                       Slots the kernel does not reach are left untouched.
+ *   checkpoint_offsets: int32 [num_seqs + 1] device, nondecreasing, offsets[num_seqs] <= slots.
+ *   checkpoint_interval: a positive multiple of 64 (the chunk), else KDA_ERR_SHAPE.
+ * Each checkpoint equals, up to rounding, the final state of the same call on the prefix
+ * (bit for bit for the same kernel, whose chunks do not depend on later tokens).
+ * Everything else as kda_chunk_fwd; NULL checkpoints or offsets give KDA_ERR_NULL. */
+kda_status_t kda_chunk_fwd_checkpointed(const void *q, const void *k, const void *v,
+                                        const void *g, const void *beta,
+                                        const float *initial_state, const int32_t *cu_seqlens,
+                                        void *out, float *final_state, float *checkpoints,
+                                        const int32_t *checkpoint_offsets,
+                                        int32_t checkpoint_interval,
+                                        const kda_dims_t *dims, cudaStream_t stream);
+
 /* The kernel kda_chunk_fwd would run for `dims` (KDA_IMPL_SIMT or
  * KDA_IMPL_TC), or -1 when the dims are invalid. */
 int kda_chunk_fwd_selected_impl(const kda_dims_t *dims);

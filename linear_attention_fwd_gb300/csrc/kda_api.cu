@@ -66,16 +66,16 @@ extern "C" int kda_chunk_fwd_selected_impl(const kda_dims_t *d) {
     return kda::chunk_tc_supported(d->dk, d->dv, d->dtype) ? KDA_IMPL_TC : KDA_IMPL_SIMT;
 }
 
-extern "C" kda_status_t kda_chunk_fwd_with(kda_impl_t impl, const void *q, const void *k,
-                                           const void *v, const void *g, const void *beta,
-                                           const float *initial_state, const int32_t *cu_seqlens,
-                                           void *out, float *final_state, const kda_dims_t *d,
-                                           cudaStream_t stream) {
+// Validated launch of one chunked forward (optionally writing state checkpoints).
+static kda_status_t chunk_run(kda_impl_t impl, const void *q, const void *k, const void *v, const void *g,
+                       const void *beta, const float *initial_state, const int32_t *cu_seqlens,
+                       void *out, float *final_state, float *ckpt, const int32_t *ckpt_off,
+                       int32_t ckpt_interval, const kda_dims_t *d, cudaStream_t stream) {
     kda_status_t st = check_chunk(impl, q, k, v, g, beta, initial_state, cu_seqlens, out,
                                   final_state, d);
     if (st != KDA_OK) return st;
     kda::ChunkArgs a{q, k, v, g, beta, initial_state, cu_seqlens, out, final_state,
-                     (int64_t)d->seqlen, d->num_seqs, d->heads};
+                     (int64_t)d->seqlen, d->num_seqs, d->heads, ckpt, ckpt_off, ckpt_interval};
     cudaError_t e;
     if ((int64_t)d->batch * d->seqlen == 0) {
         if (final_state == nullptr || final_state == initial_state) return KDA_OK;
@@ -87,6 +87,30 @@ extern "C" kda_status_t kda_chunk_fwd_with(kda_impl_t impl, const void *q, const
                                 : kda::launch_chunk_simt(a, d->dk, d->dv, d->dtype, stream);
     }
     return e == cudaSuccess ? KDA_OK : KDA_ERR_CUDA;
+}
+
+extern "C" kda_status_t kda_chunk_fwd_with(kda_impl_t impl, const void *q, const void *k,
+                                           const void *v, const void *g, const void *beta,
+                                           const float *initial_state, const int32_t *cu_seqlens,
+                                           void *out, float *final_state, const kda_dims_t *d,
+                                           cudaStream_t stream) {
+    return chunk_run(impl, q, k, v, g, beta, initial_state, cu_seqlens, out, final_state, nullptr,
+                     nullptr, 0, d, stream);
+}
+
+extern "C" kda_status_t kda_chunk_fwd_checkpointed(const void *q, const void *k, const void *v,
+                                                   const void *g, const void *beta,
+                                                   const float *initial_state,
+                                                   const int32_t *cu_seqlens, void *out,
+                                                   float *final_state, float *checkpoints,
+                                                   const int32_t *checkpoint_offsets,
+                                                   int32_t checkpoint_interval,
+                                                   const kda_dims_t *d, cudaStream_t stream) {
+    if (checkpoints == nullptr || checkpoint_offsets == nullptr) return KDA_ERR_NULL;
+    if (checkpoint_interval <= 0 || checkpoint_interval % kda::kChunk != 0) return KDA_ERR_SHAPE;
+    if (!aligned(checkpoints, 16) || !aligned(checkpoint_offsets, 4)) return KDA_ERR_ALIGN;
+    return chunk_run(KDA_IMPL_AUTO, q, k, v, g, beta, initial_state, cu_seqlens, out, final_state,
+                     checkpoints, checkpoint_offsets, checkpoint_interval, d, stream);
 }
 
 extern "C" kda_status_t kda_chunk_fwd(const void *q, const void *k, const void *v, const void *g,

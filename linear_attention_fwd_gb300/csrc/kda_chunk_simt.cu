@@ -101,6 +101,14 @@ kda_chunk_simt_kernel(ChunkArgs a) {
     for (int64_t c0 = 0; c0 < len; c0 += C) {
         const int nr = (int)(len - c0 < C ? len - c0 : C);
         __syncthreads();   // previous chunk fully consumed
+        const int64_t cs = ckpt_slot(a, n, c0);   // the state after c0 tokens, if due
+        if (cs >= 0) {
+            float *dst = a.ckpt + (cs * H + h) * DK * DV + col0;
+            for (int x = t; x < DK * kDvs; x += kThreads) {
+                const int c = x / kDvs, jj = x % kDvs;
+                dst[(int64_t)c * DV + jj] = Ss[x];
+            }
+        }
         // ---- load the chunk (rows past the sequence end are zero: k = 0, beta = 0, g = 0)
         for (int x = t; x < C * DK; x += kThreads) {
             const int r = x / DK, c = x % DK;

@@ -390,10 +390,19 @@ kda_chunk_tc_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_consta
         } else {
             if (out_pending) got = mbar_wait(bar_s, ph_s, wait_limit) && got;
             tc_fence_after();
+            const int64_t cs = ckpt_slot(a, n, (int64_t)ci * C);   // the state after ci chunks
+            float *ck = cs >= 0 ? a.ckpt + (cs * H + h) * D * D + jl : nullptr;
 #pragma unroll 1
             for (int i0 = 0; i0 < 128; i0 += 64) {
                 float v[32], w[32];
                 tmem_ld32x2(trow + TM_S + i0, trow + TM_S + i0 + 32, v, w);
+                if (ck) {   // S[i][j] = S^T[j][i]: a warp writes 128 contiguous bytes per i
+#pragma unroll
+                    for (int c = 0; c < 32; ++c) {
+                        __stcs(ck + (int64_t)(i0 + c) * D, v[c]);
+                        __stcs(ck + (int64_t)(i0 + 32 + c) * D, w[c]);
+                    }
+                }
                 uint32_t hv[16], hw[16];
 #pragma unroll
                 for (int c = 0; c < 16; ++c) {

@@ -21,7 +21,9 @@ namespace {
 
 constexpr int kDecodeThreads = 256;
 
-template <typename Tin, int DK, int DV>
+// MULTI = false: one token per row, outputs and state always written (the plain decode
+// step, compiled without the per-token loop and its branches).
+template <typename Tin, int DK, int DV, bool MULTI>
 __global__ void __launch_bounds__(kDecodeThreads)
 kda_recurrent_step_kernel(DecodeArgs a) {
     constexpr int CG = DV / 4;                 // float4 column groups
@@ -41,8 +43,8 @@ kda_recurrent_step_kernel(DecodeArgs a) {
     const int t = threadIdx.x;
     const int cg = t % CG, rg = t / CG;
     float *S = a.state + ((int64_t)slot * a.heads + h) * (DK * DV);
-    int ntok = a.ntok;
-    if (a.ntok_row) {
+    int ntok = MULTI ? a.ntok : 1;
+    if (MULTI && a.ntok_row) {
         const int m = __ldg(a.ntok_row + n);
         ntok = m < 0 ? 0 : (m < ntok ? m : ntok);
     }
@@ -90,19 +92,19 @@ kda_recurrent_step_kernel(DecodeArgs a) {
         *reinterpret_cast<float4 *>(&red_p[rg][4 * cg]) = pp;
         __syncthreads();
 
-        Tin *out = a.out ? static_cast<Tin *>(a.out) + row * DV : nullptr;
+        Tin *out = (!MULTI || a.out) ? static_cast<Tin *>(a.out) + row * DV : nullptr;
         for (int j = t; j < DV; j += kDecodeThreads) {
             float vh = 0.f, p = 0.f;
 #pragma unroll
             for (int r = 0; r < RG; ++r) { vh += red_v[r][j]; p += red_p[r][j]; }
             const float e = sv[j] - vh;
             se[j] = e;
-            if (out) out[j] = from_f<Tin>(p + beta * s_qk * e);
+            if (!MULTI || out) out[j] = from_f<Tin>(p + beta * s_qk * e);
         }
         __syncthreads();
 
         const float4 e4 = *reinterpret_cast<const float4 *>(&se[4 * cg]);
-        const bool last = tok + 1 == ntok;
+        const bool last = !MULTI || tok + 1 == ntok;
 #pragma unroll
         for (int m = 0; m < RPT; ++m) {
             const int i = rg * RPT + m;
@@ -111,7 +113,7 @@ kda_recurrent_step_kernel(DecodeArgs a) {
             s[m].y = al * s[m].y + bk * e4.y;
             s[m].z = al * s[m].z + bk * e4.z;
             s[m].w = al * s[m].w + bk * e4.w;
-            if (last && a.update) __stcs(reinterpret_cast<float4 *>(S + i * DV) + cg, s[m]);
+            if (last && (!MULTI || a.update)) __stcs(reinterpret_cast<float4 *>(S + i * DV) + cg, s[m]);
         }
         if (!last) __syncthreads();   // the shared vectors are rewritten by the next token
     }
@@ -121,7 +123,10 @@ template <typename Tin, int DK, int DV>
 cudaError_t launch_decode_t(const DecodeArgs &a, cudaStream_t st) {
     const int64_t units = (int64_t)a.rows * a.heads;
     if (units > 0x7fffffffLL) return cudaErrorInvalidValue;
-    kda_recurrent_step_kernel<Tin, DK, DV><<<(unsigned)units, kDecodeThreads, 0, st>>>(a);
+    if (a.ntok == 1 && a.ntok_row == nullptr && a.update && a.out)
+        kda_recurrent_step_kernel<Tin, DK, DV, false><<<(unsigned)units, kDecodeThreads, 0, st>>>(a);
+    else
+        kda_recurrent_step_kernel<Tin, DK, DV, true><<<(unsigned)units, kDecodeThreads, 0, st>>>(a);
     return cudaGetLastError();
 }
 

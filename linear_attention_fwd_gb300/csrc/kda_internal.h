@@ -23,7 +23,19 @@ struct ChunkArgs {
     int64_t seqlen;           // tokens per dense row, or total packed tokens
     int32_t num_seqs;         // N
     int32_t heads;            // H
+    float *ckpt;              // [slots, H, dk, dv] state checkpoints, or nullptr
+    const int32_t *ckpt_off;  // [N + 1]: sequence n's checkpoints occupy slots [off[n], off[n+1])
+    int32_t ckpt_interval;    // tokens between checkpoints (a multiple of the chunk)
 };
+
+// Checkpoint slot for the state after `pos` tokens of sequence n (pos > 0 a multiple of the
+// chunk), or -1 when none is due there.
+__device__ __forceinline__ int64_t ckpt_slot(const ChunkArgs &a, int n, int64_t pos) {
+    if (a.ckpt == nullptr || pos <= 0 || pos % a.ckpt_interval != 0) return -1;
+    const int64_t kth = pos / a.ckpt_interval - 1;
+    const int64_t b = a.ckpt_off[n], e = a.ckpt_off[n + 1];
+    return kth < e - b ? b + kth : -1;
+}
 
 struct DecodeArgs {
     const void *q, *k, *v, *g, *beta;

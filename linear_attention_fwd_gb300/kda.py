@@ -22,8 +22,9 @@ IMPLS = {"auto": 0, "simt": 1, "tc": 2}
 IMPL_NAMES = {v: k for k, v in IMPLS.items()}
 
 # every symbol include/kda.h declares
-EXPORTED = ("kda_chunk_fwd", "kda_chunk_fwd_with", "kda_chunk_fwd_selected_impl",
-            "kda_recurrent_step", "kda_recurrent_steps", "kda_status_string")
+EXPORTED = ("kda_chunk_fwd", "kda_chunk_fwd_with", "kda_chunk_fwd_checkpointed",
+            "kda_chunk_fwd_selected_impl", "kda_recurrent_step", "kda_recurrent_steps",
+            "kda_status_string")
 
 
 class KdaDims(ctypes.Structure):
@@ -54,6 +55,8 @@ def lib() -> ctypes.CDLL:
         L.kda_chunk_fwd.argtypes = [vp] * 9 + [dp, vp]
         L.kda_chunk_fwd_with.restype = ctypes.c_int
         L.kda_chunk_fwd_with.argtypes = [ctypes.c_int] + [vp] * 9 + [dp, vp]
+        L.kda_chunk_fwd_checkpointed.restype = ctypes.c_int
+        L.kda_chunk_fwd_checkpointed.argtypes = [vp] * 11 + [ctypes.c_int32, dp, vp]
         L.kda_chunk_fwd_selected_impl.restype = ctypes.c_int
         L.kda_chunk_fwd_selected_impl.argtypes = [dp]
         L.kda_recurrent_step.restype = ctypes.c_int
@@ -205,3 +208,57 @@ def kda_recurrent_steps(q, k, v, g, beta, state, state_indices=None, num_tokens=
     if st != KDA_OK:
         raise KdaError(st, "kda_recurrent_steps")
     return out if want_out else None
+
+
+def checkpoint_offsets(q, cu_seqlens, interval: int):
+    """int32 [N+1] device offsets giving each sequence one slot per multiple of ``interval``
+    strictly inside it (the layout kda_chunk_fwd_checkpointed fills)."""
+    if cu_seqlens is None:
+        B, T = q.shape[:2]
+        lens = torch.full((B,), T, dtype=torch.int64, device=q.device)
+    else:
+        lens = (cu_seqlens[1:] - cu_seqlens[:-1]).to(torch.int64)
+    counts = torch.clamp((lens - 1) // interval, min=0)
+    off = torch.zeros(counts.numel() + 1, dtype=torch.int64, device=q.device)
+    off[1:] = torch.cumsum(counts, 0)
+    return off.to(torch.int32)
+
+
+def kda_chunk_fwd_checkpointed(q, k, v, g, beta, initial_state=None, cu_seqlens=None, *,
+                               interval: int = 512, out=None, final_state=None,
+                               checkpoints=None, offsets=None, stream=None):
+    """kda_chunk_fwd that also returns the state at every multiple of ``interval`` tokens
+    strictly inside each sequence (prefix caching).
+
+    Returns (out, final_state, checkpoints fp32 [slots, H, dk, dv], offsets int32 [N+1]);
+    sequence n's k-th checkpoint (the state after (k+1)*interval tokens) is
+    checkpoints[offsets[n] + k].
+    """
+    dev = q.device
+    for name, t in (("q", q), ("k", k), ("v", v), ("g", g), ("beta", beta)):
+        _check_dev(name, t, dev, q.dtype)
+    _check_dev("initial_state", initial_state, dev, torch.float32)
+    _check_dev("cu_seqlens", cu_seqlens, dev, torch.int32)
+    B, T, H, dk = q.shape
+    dv = v.shape[-1]
+    dims = chunk_dims(q, v, cu_seqlens)
+    if offsets is None:
+        offsets = checkpoint_offsets(q, cu_seqlens, interval)
+    _check_dev("offsets", offsets, dev, torch.int32)
+    if checkpoints is None:
+        slots = int(offsets[-1].item())
+        checkpoints = torch.empty((max(slots, 1), H, dk, dv), dtype=torch.float32, device=dev)
+    _check_dev("checkpoints", checkpoints, dev, torch.float32)
+    if out is None:
+        out = torch.empty((B, T, H, dv), dtype=q.dtype, device=dev)
+    _check_dev("out", out, dev, q.dtype)
+    if final_state is None:
+        final_state = torch.empty((dims.num_seqs, H, dk, dv), dtype=torch.float32, device=dev)
+    _check_dev("final_state", final_state, dev, torch.float32)
+    st = lib().kda_chunk_fwd_checkpointed(_ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta),
+                                          _ptr(initial_state), _ptr(cu_seqlens), _ptr(out),
+                                          _ptr(final_state), _ptr(checkpoints), _ptr(offsets),
+                                          int(interval), ctypes.byref(dims), _stream_handle(stream))
+    if st != KDA_OK:
+        raise KdaError(st, "kda_chunk_fwd_checkpointed")
+    return out, final_state, checkpoints, offsets

@@ -85,6 +85,24 @@ def test_chunk_rejects_null_and_misaligned(K):
     assert call_chunk(K, dims(), impl=9) == K.KDA_ERR_UNSUPPORTED
 
 
+def call_ckpt(K, d, ck=FAKE, off=FAKE, interval=512, q=FAKE):
+    vp = ctypes.c_void_p
+    a = [vp(x) if x is not None else None
+         for x in (q, FAKE, FAKE, FAKE, FAKE, None, None, FAKE, None, ck, off)]
+    return K.lib().kda_chunk_fwd_checkpointed(*a, interval, ctypes.byref(d) if d is not None else None,
+                                              None)
+
+
+def test_checkpointed_validation(K):
+    assert call_ckpt(K, dims(), ck=None) == K.KDA_ERR_NULL
+    assert call_ckpt(K, dims(), off=None) == K.KDA_ERR_NULL
+    assert call_ckpt(K, dims(), interval=0) == K.KDA_ERR_SHAPE
+    assert call_ckpt(K, dims(), interval=100) == K.KDA_ERR_SHAPE   # not a multiple of 64
+    assert call_ckpt(K, dims(), ck=FAKE + 4) == K.KDA_ERR_ALIGN
+    assert call_ckpt(K, dims(), off=FAKE + 2) == K.KDA_ERR_ALIGN
+    assert call_ckpt(K, dims(), q=None) == K.KDA_ERR_NULL          # the usual chunk checks run
+
+
 def test_tc_kernel_refuses_shapes_it_does_not_cover(K):
     assert call_chunk(K, dims(dtype=0), impl=2) == K.KDA_ERR_UNSUPPORTED
     assert call_chunk(K, dims(dk=64, dv=64), impl=2) == K.KDA_ERR_UNSUPPORTED
