@@ -15,6 +15,10 @@ marshals arrays and splits (sequence, head) units over threads):
   final states.
 * ``decode_step``: the same single token step applied in place to a pool of
   states, row n using slot ``state_indices[n]`` (identity when None).
+* ``gated_rmsnorm``: the output gate of the same page's KDA paragraph (the
+  read-out is normalised to unit RMS over its value channels, scaled by a
+  per-channel weight, and multiplied channel-wise by a sigmoid gate in (0, 1)):
+  y = o / sqrt(mean_j o_j^2 + eps) * w * sigmoid(z), in numpy float64.
 
 Inputs may be any float dtype (the exact values the GPU sees); they are widened
 to float64.  Pinned against brute force, closed forms and invariants in
@@ -177,3 +181,19 @@ def decode_step(q, k, v, g, beta, state, state_indices=None, *,
             N, H, dk, dv, _ptr(out)]
     _run_units(lambda a, b: lib.kda_oracle_decode_step(*args, a, b), N * H, threads, units)
     return out
+
+
+def gated_rmsnorm(o, gate, weight=None, eps: float = 1e-6) -> np.ndarray:
+    """The KDA output gate: RMSNorm over the last (value-channel) axis, then the channel-wise
+    sigmoid gate ("はじめての自然言語処理 -- Kimi K3", the paragraph after the decay bound:
+    the gate multiplies each channel by a value in (0, 1) made from the token's input, and
+    the RMSNorm before it evens out the magnitude of what is read from S).
+
+    o: [..., dv] (any float dtype, e.g. ``forward``'s float64 output); gate: [..., dv] logits
+    z; weight: [dv] or None (ones).  Returns float64 o / sqrt(mean(o^2) + eps) * w * sigmoid(z).
+    """
+    o = _f64(o)
+    z = _f64(gate)
+    w = np.ones(o.shape[-1]) if weight is None else _f64(weight)
+    rstd = 1.0 / np.sqrt(np.mean(o * o, axis=-1, keepdims=True) + eps)
+    return o * rstd * w / (1.0 + np.exp(-z))
