@@ -136,6 +136,26 @@ kda_status_t kda_chunk_fwd_checkpointed(const void *q, const void *k, const void
                                         int32_t checkpoint_interval,
                                         const kda_dims_t *dims, cudaStream_t stream);
 
+/* kda_chunk_fwd_gated -- kda_chunk_fwd followed by the KDA output gate, fused into the output
+ * store.  The page's account ("はじめての自然言語処理 -- Kimi K3", the paragraph after the decay
+ * bound): the read-out o_t is put through RMSNorm over its value channels (evening out the
+ * magnitude of what is read from S) and then multiplied channel by channel by a gate in (0, 1)
+ * made from the token's input.  Here, per token and head,
+ *   out = o / sqrt(mean_j o_j^2 + norm_eps) * w * sigmoid(z),
+ * with z the gate logits (the projection that makes them from the token's input is the
+ * caller's) and w the RMSNorm weight.
+ *   gate       : [B, T, H, dv] dtype (z), required when there are tokens.
+ *   norm_weight: fp32 [dv] or NULL (ones).   norm_eps: >= 0 and finite, else KDA_ERR_SHAPE.
+ * The bf16 d = 128 kernel applies the gate while staging its output (no extra traffic beyond
+ * reading z); other shapes apply it in a second pass over the stored output.  Everything else
+ * as kda_chunk_fwd. */
+kda_status_t kda_chunk_fwd_gated(const void *q, const void *k, const void *v,
+                                 const void *g, const void *beta, const void *gate,
+                                 const float *norm_weight, float norm_eps,
+                                 const float *initial_state, const int32_t *cu_seqlens,
+                                 void *out, float *final_state,
+                                 const kda_dims_t *dims, cudaStream_t stream);
+
 /* The kernel kda_chunk_fwd would run for `dims` (KDA_IMPL_SIMT or
  * KDA_IMPL_TC), or -1 when the dims are invalid. */
 int kda_chunk_fwd_selected_impl(const kda_dims_t *dims);

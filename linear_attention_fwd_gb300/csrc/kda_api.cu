@@ -70,12 +70,14 @@ extern "C" int kda_chunk_fwd_selected_impl(const kda_dims_t *d) {
 static kda_status_t chunk_run(kda_impl_t impl, const void *q, const void *k, const void *v, const void *g,
                        const void *beta, const float *initial_state, const int32_t *cu_seqlens,
                        void *out, float *final_state, float *ckpt, const int32_t *ckpt_off,
-                       int32_t ckpt_interval, const kda_dims_t *d, cudaStream_t stream) {
+                       int32_t ckpt_interval, const void *gate, const float *norm_w, float norm_eps,
+                       const kda_dims_t *d, cudaStream_t stream) {
     kda_status_t st = check_chunk(impl, q, k, v, g, beta, initial_state, cu_seqlens, out,
                                   final_state, d);
     if (st != KDA_OK) return st;
     kda::ChunkArgs a{q, k, v, g, beta, initial_state, cu_seqlens, out, final_state,
-                     (int64_t)d->seqlen, d->num_seqs, d->heads, ckpt, ckpt_off, ckpt_interval};
+                     (int64_t)d->seqlen, d->num_seqs, d->heads, gate, norm_w, norm_eps,
+                     ckpt, ckpt_off, ckpt_interval};
     cudaError_t e;
     if ((int64_t)d->batch * d->seqlen == 0) {
         if (final_state == nullptr || final_state == initial_state) return KDA_OK;
@@ -83,8 +85,13 @@ static kda_status_t chunk_run(kda_impl_t impl, const void *q, const void *k, con
     } else {
         if (impl == KDA_IMPL_AUTO)
             impl = kda::chunk_tc_supported(d->dk, d->dv, d->dtype) ? KDA_IMPL_TC : KDA_IMPL_SIMT;
-        e = impl == KDA_IMPL_TC ? kda::launch_chunk_tc(a, d->dk, d->dv, d->dtype, stream)
-                                : kda::launch_chunk_simt(a, d->dk, d->dv, d->dtype, stream);
+        if (impl == KDA_IMPL_TC) {
+            e = kda::launch_chunk_tc(a, d->dk, d->dv, d->dtype, stream);   // gate fused
+        } else {
+            e = kda::launch_chunk_simt(a, d->dk, d->dv, d->dtype, stream);
+            if (e == cudaSuccess && gate)
+                e = kda::launch_gate_pass(a, (int64_t)d->batch * d->seqlen, d->dv, d->dtype, stream);
+        }
     }
     return e == cudaSuccess ? KDA_OK : KDA_ERR_CUDA;
 }
@@ -95,7 +102,7 @@ extern "C" kda_status_t kda_chunk_fwd_with(kda_impl_t impl, const void *q, const
                                            void *out, float *final_state, const kda_dims_t *d,
                                            cudaStream_t stream) {
     return chunk_run(impl, q, k, v, g, beta, initial_state, cu_seqlens, out, final_state, nullptr,
-                     nullptr, 0, d, stream);
+                     nullptr, 0, nullptr, nullptr, 0.f, d, stream);
 }
 
 extern "C" kda_status_t kda_chunk_fwd_checkpointed(const void *q, const void *k, const void *v,
@@ -110,7 +117,21 @@ extern "C" kda_status_t kda_chunk_fwd_checkpointed(const void *q, const void *k,
     if (checkpoint_interval <= 0 || checkpoint_interval % kda::kChunk != 0) return KDA_ERR_SHAPE;
     if (!aligned(checkpoints, 16) || !aligned(checkpoint_offsets, 4)) return KDA_ERR_ALIGN;
     return chunk_run(KDA_IMPL_AUTO, q, k, v, g, beta, initial_state, cu_seqlens, out, final_state,
-                     checkpoints, checkpoint_offsets, checkpoint_interval, d, stream);
+                     checkpoints, checkpoint_offsets, checkpoint_interval, nullptr, nullptr, 0.f, d,
+                     stream);
+}
+
+extern "C" kda_status_t kda_chunk_fwd_gated(const void *q, const void *k, const void *v,
+                                            const void *g, const void *beta, const void *gate,
+                                            const float *norm_weight, float norm_eps,
+                                            const float *initial_state, const int32_t *cu_seqlens,
+                                            void *out, float *final_state, const kda_dims_t *d,
+                                            cudaStream_t stream) {
+    if (d != nullptr && (int64_t)d->batch * d->seqlen > 0 && gate == nullptr) return KDA_ERR_NULL;
+    if (!(norm_eps >= 0.f) || norm_eps > 1e30f) return KDA_ERR_SHAPE;   // also rejects NaN
+    if ((gate && !aligned(gate, 16)) || (norm_weight && !aligned(norm_weight, 4))) return KDA_ERR_ALIGN;
+    return chunk_run(KDA_IMPL_AUTO, q, k, v, g, beta, initial_state, cu_seqlens, out, final_state,
+                     nullptr, nullptr, 0, gate, norm_weight, norm_eps, d, stream);
 }
 
 extern "C" kda_status_t kda_chunk_fwd(const void *q, const void *k, const void *v, const void *g,

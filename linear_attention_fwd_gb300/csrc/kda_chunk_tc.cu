@@ -258,6 +258,9 @@ kda_chunk_tc_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_consta
     int nr_out = 0;
     // O^T (TMEM: high-order part + low-order terms) -> bf16 staging tile [64 r][128 j] over the
     // AT and T tiles, by warps 0-7; warp w: lanes 32(w%4).., rows 32(w/4)..+31
+    // With an output gate (the paragraph after the decay bound on the same page): each row is
+    // normalised to unit RMS over its 128 value channels, scaled by the norm weight and
+    // multiplied channel-wise by sigmoid(gate logit) before it is rounded to bf16.
     auto stage_output = [&]() {
         if (warp >= 8) return;
         __nv_bfloat16 *os = reinterpret_cast<__nv_bfloat16 *>(sm + OFF_STG);
@@ -265,7 +268,39 @@ kda_chunk_tc_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_consta
         float v[32], w[32];
         tmem_ld32x2(trow + TM_O + r0, trow + TM_U + r0, v, w);
 #pragma unroll
-        for (int c = 0; c < 32; ++c) os[(r0 + c) * D + jl] = __float2bfloat16_rn(v[c] + w[c]);
+        for (int c = 0; c < 32; ++c) v[c] += w[c];
+        if (a.gate) {
+            // sums of squares of rows r0.. over this warp's 32 channels, transposed so that
+            // lane L ends with row r0 + L (5 rounds, 31 shuffles)
+#pragma unroll
+            for (int c = 0; c < 32; ++c) w[c] = v[c] * v[c];
+#pragma unroll
+            for (int sft = 16; sft > 0; sft >>= 1) {
+                const bool up = (lane & sft) != 0;
+#pragma unroll
+                for (int i = 0; i < sft; ++i) {
+                    const float send = up ? w[i] : w[i + sft];
+                    const float keep = up ? w[i + sft] : w[i];
+                    w[i] = keep + __shfl_xor_sync(0xffffffffu, send, sft);
+                }
+            }
+            float *red = reinterpret_cast<float *>(sm + OFF_EB);   // [4 channel quarters][64 rows]
+            red[(warp & 3) * 64 + r0 + lane] = w[0];
+            named_bar(5 + (warp >> 2), 128);   // the four quarters of these 32 rows
+            const float ms = ((red[r0 + lane] + red[64 + r0 + lane]) + (red[128 + r0 + lane] + red[192 + r0 + lane])) *
+                             (1.f / D);
+            const float rstd = rsqrtf(ms + a.norm_eps);
+            const float wj = a.norm_w ? a.norm_w[jl] : 1.f;
+            const __nv_bfloat16 *gz = static_cast<const __nv_bfloat16 *>(a.gate) + (t0_out * H + h) * D + jl;
+#pragma unroll
+            for (int c = 0; c < 32; ++c) {
+                const float rs = __shfl_sync(0xffffffffu, rstd, c);
+                const float z = r0 + c < nr_out ? __bfloat162float(gz[(int64_t)(r0 + c) * H * D]) : 0.f;
+                v[c] *= rs * wj * __frcp_rn(1.f + __expf(-z));
+            }
+        }
+#pragma unroll
+        for (int c = 0; c < 32; ++c) os[(r0 + c) * D + jl] = __float2bfloat16_rn(v[c]);
     };
     // staging tile -> out, 16-byte coalesced stores of the rows inside the sequence
     auto store_output = [&]() {

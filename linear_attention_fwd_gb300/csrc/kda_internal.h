@@ -23,6 +23,9 @@ struct ChunkArgs {
     int64_t seqlen;           // tokens per dense row, or total packed tokens
     int32_t num_seqs;         // N
     int32_t heads;            // H
+    const void *gate;         // [tokens, H, dv] gate logits (io dtype), or nullptr: no output gate
+    const float *norm_w;      // [dv] RMSNorm weight, or nullptr (ones)
+    float norm_eps;           // RMSNorm epsilon
     float *ckpt;              // [slots, H, dk, dv] state checkpoints, or nullptr
     const int32_t *ckpt_off;  // [N + 1]: sequence n's checkpoints occupy slots [off[n], off[n+1])
     int32_t ckpt_interval;    // tokens between checkpoints (a multiple of the chunk)
@@ -78,6 +81,9 @@ cudaError_t launch_chunk_simt(const ChunkArgs &a, int dk, int dv, kda_dtype_t dt
 cudaError_t launch_chunk_tc(const ChunkArgs &a, int dk, int dv, kda_dtype_t dt, cudaStream_t s);
 bool chunk_tc_supported(int dk, int dv, kda_dtype_t dt);
 cudaError_t launch_decode(const DecodeArgs &a, int dk, int dv, kda_dtype_t dt, cudaStream_t s);
+// out <- RMSNorm(out) * w * sigmoid(gate) over dv, in place, for every token row of a chunk call
+cudaError_t launch_gate_pass(const ChunkArgs &a, int64_t tokens, int dv, kda_dtype_t dt,
+                             cudaStream_t s);
 cudaError_t launch_state_copy(const ChunkArgs &a, int dk, int dv, cudaStream_t s);
 
 }  // namespace kda

@@ -23,8 +23,8 @@ IMPL_NAMES = {v: k for k, v in IMPLS.items()}
 
 # every symbol include/kda.h declares
 EXPORTED = ("kda_chunk_fwd", "kda_chunk_fwd_with", "kda_chunk_fwd_checkpointed",
-            "kda_chunk_fwd_selected_impl", "kda_recurrent_step", "kda_recurrent_steps",
-            "kda_status_string")
+            "kda_chunk_fwd_gated", "kda_chunk_fwd_selected_impl", "kda_recurrent_step",
+            "kda_recurrent_steps", "kda_status_string")
 
 
 class KdaDims(ctypes.Structure):
@@ -57,6 +57,8 @@ def lib() -> ctypes.CDLL:
         L.kda_chunk_fwd_with.argtypes = [ctypes.c_int] + [vp] * 9 + [dp, vp]
         L.kda_chunk_fwd_checkpointed.restype = ctypes.c_int
         L.kda_chunk_fwd_checkpointed.argtypes = [vp] * 11 + [ctypes.c_int32, dp, vp]
+        L.kda_chunk_fwd_gated.restype = ctypes.c_int
+        L.kda_chunk_fwd_gated.argtypes = [vp] * 7 + [ctypes.c_float] + [vp] * 4 + [dp, vp]
         L.kda_chunk_fwd_selected_impl.restype = ctypes.c_int
         L.kda_chunk_fwd_selected_impl.argtypes = [dp]
         L.kda_recurrent_step.restype = ctypes.c_int
@@ -262,3 +264,38 @@ def kda_chunk_fwd_checkpointed(q, k, v, g, beta, initial_state=None, cu_seqlens=
     if st != KDA_OK:
         raise KdaError(st, "kda_chunk_fwd_checkpointed")
     return out, final_state, checkpoints, offsets
+
+
+def kda_chunk_fwd_gated(q, k, v, g, beta, gate, norm_weight=None, eps: float = 1e-6,
+                        initial_state=None, cu_seqlens=None, *, out=None, final_state=None,
+                        output_final_state: bool = True, stream=None):
+    """kda_chunk_fwd with the KDA output gate fused into the output store:
+    out = RMSNorm(o) * norm_weight * sigmoid(gate) over the value channels.
+
+    gate: [B, T, H, dv] logits (q's dtype); norm_weight: fp32 [dv] or None.
+    Returns (out [B, T, H, dv], final_state or None).
+    """
+    dev = q.device
+    for name, t in (("q", q), ("k", k), ("v", v), ("g", g), ("beta", beta), ("gate", gate)):
+        _check_dev(name, t, dev, q.dtype)
+    _check_dev("norm_weight", norm_weight, dev, torch.float32)
+    _check_dev("initial_state", initial_state, dev, torch.float32)
+    _check_dev("cu_seqlens", cu_seqlens, dev, torch.int32)
+    B, T, H, dk = q.shape
+    dv = v.shape[-1]
+    if gate.shape != v.shape:
+        raise ValueError("gate must be shaped like v")
+    dims = chunk_dims(q, v, cu_seqlens)
+    if out is None:
+        out = torch.empty((B, T, H, dv), dtype=q.dtype, device=dev)
+    _check_dev("out", out, dev, q.dtype)
+    if final_state is None and output_final_state:
+        final_state = torch.empty((dims.num_seqs, H, dk, dv), dtype=torch.float32, device=dev)
+    _check_dev("final_state", final_state, dev, torch.float32)
+    st = lib().kda_chunk_fwd_gated(_ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta), _ptr(gate),
+                                   _ptr(norm_weight), ctypes.c_float(eps), _ptr(initial_state),
+                                   _ptr(cu_seqlens), _ptr(out), _ptr(final_state),
+                                   ctypes.byref(dims), _stream_handle(stream))
+    if st != KDA_OK:
+        raise KdaError(st, "kda_chunk_fwd_gated")
+    return out, final_state

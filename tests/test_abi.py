@@ -103,6 +103,23 @@ def test_checkpointed_validation(K):
     assert call_ckpt(K, dims(), q=None) == K.KDA_ERR_NULL          # the usual chunk checks run
 
 
+def call_gated(K, d, gate=FAKE, w=None, eps=1e-6, q=FAKE):
+    vp = ctypes.c_void_p
+    a = [vp(x) if x is not None else None for x in (q, FAKE, FAKE, FAKE, FAKE, gate, w)]
+    b = [vp(x) if x is not None else None for x in (None, None, FAKE, None)]
+    return K.lib().kda_chunk_fwd_gated(*a, ctypes.c_float(eps), *b,
+                                       ctypes.byref(d) if d is not None else None, None)
+
+
+def test_gated_validation(K):
+    assert call_gated(K, dims(), gate=None) == K.KDA_ERR_NULL
+    assert call_gated(K, dims(), eps=-1.0) == K.KDA_ERR_SHAPE
+    assert call_gated(K, dims(), eps=float("nan")) == K.KDA_ERR_SHAPE
+    assert call_gated(K, dims(), gate=FAKE + 2) == K.KDA_ERR_ALIGN
+    assert call_gated(K, dims(), w=FAKE + 2) == K.KDA_ERR_ALIGN
+    assert call_gated(K, dims(), q=None) == K.KDA_ERR_NULL          # the usual chunk checks run
+
+
 def test_tc_kernel_refuses_shapes_it_does_not_cover(K):
     assert call_chunk(K, dims(dtype=0), impl=2) == K.KDA_ERR_UNSUPPORTED
     assert call_chunk(K, dims(dk=64, dv=64), impl=2) == K.KDA_ERR_UNSUPPORTED
