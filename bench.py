@@ -351,6 +351,11 @@ def run_ours(args):
     if not args.no_decode:
         decode = bench_decode(args, kda, inputs, dev, stream, P, barrier, max_over_ranks, ws)
 
+    # ---- the widened rows (output gate, state checkpoints, multi-token decode), same workload
+    extras = None
+    if not args.no_extras and kernel == "tc":
+        extras = bench_extras(kda, inputs, inp, out, fs, stream, P, bytes_launch, tokens, H, dk, dv, es, N)
+
     # ---- CPU baseline: the oracle on the host cores, bounded sample (rank 0, N = 1 only)
     cpu = None
     if not args.no_cpu_baseline and ws == 1 and rank == 0:
@@ -373,11 +378,72 @@ def run_ours(args):
                        "note": w.note},
             "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e,
             "gpu_launches": args.steps, "clocks": clocks, "decode": decode,
+            "extras": extras,
         }
         print(json.dumps(line), flush=True)
     if ws > 1:
         dist.destroy_process_group()
     return 0
+
+
+def _time_ms(fn, stream, reps=5, warm=2):
+    import torch
+    for _ in range(warm):
+        fn()
+    torch.cuda.synchronize()
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    a.record(stream)
+    for _ in range(reps):
+        fn()
+    b.record(stream)
+    torch.cuda.synchronize()
+    return a.elapsed_time(b) / reps
+
+
+def bench_extras(kda, inputs, inp, out, fs, stream, P, bytes_launch, tokens, H, dk, dv, es, N):
+    """The output gate fused into the store, state checkpoints every 512 tokens, and 4 decode
+    tokens per call with the state on chip -- each against its own algorithmic bytes."""
+    import torch
+    gen = torch.Generator(device=out.device).manual_seed(5)
+    z = torch.randn(inp["v"].shape, generator=gen, device=out.device).to(inp["v"].dtype)
+    w = torch.ones(dv, device=out.device)
+    ms = _time_ms(lambda: kda.kda_chunk_fwd_gated(inp["q"], inp["k"], inp["v"], inp["g"], inp["beta"], z, w,
+                                                   1e-6, inp["initial_state"], inp["cu_seqlens"],
+                                                   out=out, final_state=fs, stream=stream), stream)
+    gb = bytes_launch + tokens * H * dv * es
+    gated = {"ms_per_step": ms, "tokens_per_s": tokens / (ms / 1e3),
+             "roofline": {"bound": "hbm", "achieved": gb / (ms / 1e3) / 1e9, "peak": P["hbm"], "unit": "GB/s",
+                          "frac": gb / (ms / 1e3) / 1e9 / P["hbm"], "algorithmic_bytes_per_launch": gb}}
+    del z
+    off = kda.checkpoint_offsets(inp["q"], inp["cu_seqlens"], 512)
+    slots = int(off[-1].item())
+    ck = torch.empty((max(slots, 1), H, dk, dv), dtype=torch.float32, device=out.device)
+    ms = _time_ms(lambda: kda.kda_chunk_fwd_checkpointed(inp["q"], inp["k"], inp["v"], inp["g"], inp["beta"],
+                                                          inp["initial_state"], inp["cu_seqlens"],
+                                                          interval=512, out=out, final_state=fs,
+                                                          checkpoints=ck, offsets=off, stream=stream), stream)
+    cb = bytes_launch + slots * H * dk * dv * 4
+    ckpt = {"interval": 512, "checkpoints": slots, "ms_per_step": ms, "tokens_per_s": tokens / (ms / 1e3),
+            "roofline": {"bound": "hbm", "achieved": cb / (ms / 1e3) / 1e9, "peak": P["hbm"], "unit": "GB/s",
+                         "frac": cb / (ms / 1e3) / 1e9 / P["hbm"], "algorithmic_bytes_per_launch": cb}}
+    del ck
+    wd = inputs.WORKLOADS["decode_n256_h64"]
+    T = 4
+    st = inputs.make_decode_state(num_slots=wd.batch, heads=wd.heads, dk=wd.dk, dv=wd.dv,
+                                  device=out.device, seed=7)
+    ins = inputs.make_decode_inputs(steps=T, rows=wd.batch, heads=wd.heads, dk=wd.dk, dv=wd.dv,
+                                    dtype=wd.dtype, device=out.device, seed=8)
+    a = {k: ins[k].transpose(0, 1).contiguous() for k in ins}
+    dout = torch.empty((wd.batch, T, wd.heads, wd.dv), dtype=wd.dtype, device=out.device)
+    ms = _time_ms(lambda: kda.kda_recurrent_steps(a["q"], a["k"], a["v"], a["g"], a["beta"], st,
+                                                   out=dout, stream=stream), stream, reps=20)
+    db = wd.batch * wd.heads * (2 * wd.dk * wd.dv * 4 + T * ((3 * wd.dk + 2 * wd.dv + 1) * 2))
+    steps4 = {"workload": "decode_n256_h64", "tokens_per_row": T, "ms_per_call": ms,
+              "row_tokens_per_s": wd.batch * T / (ms / 1e3),
+              "roofline": {"bound": "hbm", "achieved": db / (ms / 1e3) / 1e9, "peak": P["hbm"], "unit": "GB/s",
+                           "frac": db / (ms / 1e3) / 1e9 / P["hbm"], "algorithmic_bytes_per_launch": db}}
+    del st, ins, a, dout
+    return {"gated": gated, "checkpointed": ckpt, "decode_steps": steps4}
 
 
 def bench_decode(args, kda, inputs, dev, stream, P, barrier, max_over_ranks, ws):
@@ -429,6 +495,7 @@ def main():
                     help="seconds of oracle work per --impl reference step")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-decode", action="store_true")
+    ap.add_argument("--no-extras", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
     args = ap.parse_args()
     if args.warmup < 3:

@@ -86,7 +86,7 @@ constexpr uint32_t OFF_BETA = OFF_DEC + 128 * 4;        // beta             [64]
 constexpr uint32_t OFF_MRR = OFF_BETA + 64 * 4;         // q_r . k_r        [64]
 constexpr uint32_t OFF_MLO = (OFF_MRR + 64 * 4 + 1023) / 1024 * 1024;   // M - fp16(M), fp16 [64 r][64 s]
 constexpr uint32_t OFF_SCR = OFF_MLO + 8192;            // split-K partial sums [4][4][32] float4
-constexpr uint32_t OFF_BAR = OFF_SCR + 8192;            // 6 mbarriers, TMEM address
+constexpr uint32_t OFF_BAR = OFF_SCR + 8192;            // 7 mbarriers, TMEM address
 constexpr uint32_t SMEM_USED = OFF_BAR + 64;
 constexpr uint32_t SMEM_BYTES = SMEM_USED + 1024;       // + alignment slack
 static_assert(SMEM_BYTES <= 227 * 1024, "shared memory budget");
@@ -165,6 +165,7 @@ __device__ __forceinline__ void tma_tile(const CUtensorMap *map, uint32_t dst, u
 __global__ void __launch_bounds__(NT, 1)
 kda_chunk_tc_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant__ CUtensorMap tmk,
                     const __grid_constant__ CUtensorMap tmv, const __grid_constant__ CUtensorMap tmg,
+                    const __grid_constant__ CUtensorMap tmz,
                     const ChunkArgs a, const uint32_t wait_limit) {
     extern __shared__ uint8_t smem_raw[];
     uint8_t *sm = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -184,6 +185,7 @@ kda_chunk_tc_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_consta
     const uint32_t bar_tma = sb + OFF_BAR, bar_p = sb + OFF_BAR + 8, bar_v = sb + OFF_BAR + 16;
     const uint32_t bar_u = sb + OFF_BAR + 24, bar_s = sb + OFF_BAR + 32, bar_o = sb + OFF_BAR + 40;
     volatile uint32_t *tmem_holder = reinterpret_cast<volatile uint32_t *>(sm + OFF_BAR + 48);
+    const uint32_t bar_z = sb + OFF_BAR + 56;   // a chunk's gate logits landed in the staging tile
     float *AF = reinterpret_cast<float *>(sm + OFF_PART);   // A_II blocks, [4][16][LDA]
     float *PART = reinterpret_cast<float *>(sm + OFF_PART);
     float *EB = reinterpret_cast<float *>(sm + OFF_EB);
@@ -202,6 +204,7 @@ kda_chunk_tc_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_consta
         mbar_init(bar_u, 2);
         mbar_init(bar_s, 1);
         mbar_init(bar_o, 1);
+        mbar_init(bar_z, 1);
         fence_mbar_init();
         prefetch_tmap(&tmq);
         prefetch_tmap(&tmk);
@@ -252,7 +255,7 @@ kda_chunk_tc_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_consta
     __syncthreads();
     tc_fence_after();
 
-    uint32_t ph_tma = 0, ph_p = 0, ph_v = 0, ph_u = 0, ph_s = 0, ph_o = 0;
+    uint32_t ph_tma = 0, ph_p = 0, ph_v = 0, ph_u = 0, ph_s = 0, ph_o = 0, ph_z = 0;
     bool out_pending = false;   // the previous chunk's state update and O^T group are in flight
     int64_t t0_out = 0;
     int nr_out = 0;
@@ -260,7 +263,8 @@ kda_chunk_tc_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_consta
     // AT and T tiles, by warps 0-7; warp w: lanes 32(w%4).., rows 32(w/4)..+31
     // With an output gate (the paragraph after the decay bound on the same page): each row is
     // normalised to unit RMS over its 128 value channels, scaled by the norm weight and
-    // multiplied channel-wise by sigmoid(gate logit) before it is rounded to bf16.
+    // multiplied channel-wise by sigmoid(gate logit) before it is rounded to bf16; the chunk's
+    // logits were loaded by TMA into the staging tile itself (same row-major layout).
     auto stage_output = [&]() {
         if (warp >= 8) return;
         __nv_bfloat16 *os = reinterpret_cast<__nv_bfloat16 *>(sm + OFF_STG);
@@ -291,11 +295,10 @@ kda_chunk_tc_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_consta
                              (1.f / D);
             const float rstd = rsqrtf(ms + a.norm_eps);
             const float wj = a.norm_w ? a.norm_w[jl] : 1.f;
-            const __nv_bfloat16 *gz = static_cast<const __nv_bfloat16 *>(a.gate) + (t0_out * H + h) * D + jl;
 #pragma unroll
-            for (int c = 0; c < 32; ++c) {
+            for (int c = 0; c < 32; ++c) {   // the logit sits where this thread writes its output
                 const float rs = __shfl_sync(0xffffffffu, rstd, c);
-                const float z = r0 + c < nr_out ? __bfloat162float(gz[(int64_t)(r0 + c) * H * D]) : 0.f;
+                const float z = __bfloat162float(os[(r0 + c) * D + jl]);
                 v[c] *= rs * wj * __frcp_rn(1.f + __expf(-z));
             }
         }
@@ -419,6 +422,7 @@ kda_chunk_tc_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_consta
             prephase(nr);
             if (out_pending && warp < 8) {   // the previous chunk's output, once its groups landed
                 got = mbar_wait(bar_s, ph_s, wait_limit) && mbar_wait(bar_o, ph_o, wait_limit) && got;
+                if (a.gate) got = mbar_wait(bar_z, ph_z, wait_limit) && got;
                 tc_fence_after();
                 stage_output();
             }
@@ -453,7 +457,10 @@ kda_chunk_tc_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_consta
         if (__syncthreads_or(!got)) { ok = false; break; }
         tc_fence_after();
         vectors();
-        if (out_pending) ph_o ^= 1;
+        if (out_pending) {
+            ph_o ^= 1;
+            if (a.gate) ph_z ^= 1;
+        }
         __syncthreads();
         if (out_pending) {
             store_output();
@@ -767,6 +774,11 @@ kda_chunk_tc_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_consta
             ph_u ^= 1;
             if (__syncthreads_or(!got)) { ok = false; break; }
         }
+        if (a.gate && tid == 0) {   // AT and T are consumed: this chunk's gate logits -> staging tile
+            fence_async_smem();
+            mbar_arrive_expect_tx(bar_z, 64 * D * 2);
+            tma_load_3d(sb + OFF_STG, &tmz, bar_z, 0, h, (int)t0);
+        }
         tc_fence_after();
         // ---- (5) U^T -> fp16 hi + lo pairs (TMEM); warp w: lanes 32(w%4).., columns 16(w/4)..
         {
@@ -816,9 +828,11 @@ kda_chunk_tc_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_consta
     if (ok && out_pending) {   // the last chunk's state update and output
         const bool gs = mbar_wait(bar_s, ph_s, wait_limit);
         const bool go = mbar_wait(bar_o, ph_o, wait_limit);
+        const bool gg = a.gate ? mbar_wait(bar_z, ph_z, wait_limit) : true;
         ph_s ^= 1;
         ph_o ^= 1;
-        if (__syncthreads_or(!(gs && go))) {
+        if (a.gate) ph_z ^= 1;
+        if (__syncthreads_or(!(gs && go && gg))) {
             ok = false;
         } else {
             tc_fence_after();
@@ -834,6 +848,7 @@ kda_chunk_tc_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_consta
             mbar_wait(bar_o, ph_o, wait_limit);
             mbar_wait(bar_tma, ph_tma, wait_limit);
             mbar_wait(bar_v, ph_v, wait_limit);
+            if (a.gate) mbar_wait(bar_z, ph_z, wait_limit);
             atomicAdd(&g_kda_tc_timeouts, 1u);
         }
         __syncthreads();
@@ -881,6 +896,20 @@ bool make_map(CUtensorMap *m, const void *ptr, int64_t tokens, int H) {
                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// The same tensor with 128 x 1 x 64 boxes and no swizzle: a box lands as a plain row-major
+// [64 tokens][128 channels] tile (the output staging layout).
+bool make_map_rows(CUtensorMap *m, const void *ptr, int64_t tokens, int H) {
+    auto enc = encode_fn();
+    if (enc == nullptr) return false;
+    cuuint64_t dims[3] = {(cuuint64_t)D, (cuuint64_t)H, (cuuint64_t)tokens};
+    cuuint64_t strides[2] = {(cuuint64_t)D * 2, (cuuint64_t)H * D * 2};
+    cuuint32_t box[3] = {(cuuint32_t)D, 1, 64};
+    cuuint32_t es[3] = {1, 1, 1};
+    return enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void *>(ptr), dims, strides, box, es,
+               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 }  // namespace
 
 bool chunk_tc_supported(int dk, int dv, kda_dtype_t dt) {
@@ -891,16 +920,17 @@ cudaError_t launch_chunk_tc(const ChunkArgs &a, int dk, int dv, kda_dtype_t dt, 
     if (!chunk_tc_supported(dk, dv, dt)) return cudaErrorNotSupported;
     const int64_t tokens = a.cu ? a.seqlen : (int64_t)a.num_seqs * a.seqlen;
     if (tokens >= (int64_t(1) << 31)) return cudaErrorInvalidValue;
-    CUtensorMap mq, mk, mv, mg;
+    CUtensorMap mq, mk, mv, mg, mz;
     if (!make_map(&mq, a.q, tokens, a.heads) || !make_map(&mk, a.k, tokens, a.heads) ||
-        !make_map(&mv, a.v, tokens, a.heads) || !make_map(&mg, a.g, tokens, a.heads))
+        !make_map(&mv, a.v, tokens, a.heads) || !make_map(&mg, a.g, tokens, a.heads) ||
+        !make_map_rows(&mz, a.gate ? a.gate : a.v, tokens, a.heads))   // unused without a gate
         return cudaErrorInvalidValue;
     cudaError_t e = cudaFuncSetAttribute(kda_chunk_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          (int)SMEM_BYTES);
     if (e != cudaSuccess) return e;
     const int64_t units = (int64_t)a.num_seqs * a.heads;
     if (units > 0x7fffffffLL) return cudaErrorInvalidValue;
-    kda_chunk_tc_kernel<<<(unsigned)units, NT, SMEM_BYTES, st>>>(mq, mk, mv, mg, a, 1u << 20);
+    kda_chunk_tc_kernel<<<(unsigned)units, NT, SMEM_BYTES, st>>>(mq, mk, mv, mg, mz, a, 1u << 20);
     return cudaGetLastError();
 }
 
