@@ -85,8 +85,7 @@ constexpr uint32_t OFF_DEC = OFF_W6 + 6 * 128 * 2;      // e^{gl}           [128
 constexpr uint32_t OFF_BETA = OFF_DEC + 128 * 4;        // beta             [64]
 constexpr uint32_t OFF_MRR = OFF_BETA + 64 * 4;         // q_r . k_r        [64]
 constexpr uint32_t OFF_MLO = (OFF_MRR + 64 * 4 + 1023) / 1024 * 1024;   // M - fp16(M), fp16 [64 r][64 s]
-constexpr uint32_t OFF_SCR = OFF_MLO + 8192;            // split-K partial sums [4][4][32] float4
-constexpr uint32_t OFF_BAR = OFF_SCR + 8192;            // 7 mbarriers, TMEM address
+constexpr uint32_t OFF_BAR = OFF_MLO + 8192;            // 7 mbarriers, TMEM address
 constexpr uint32_t SMEM_USED = OFF_BAR + 64;
 constexpr uint32_t SMEM_BYTES = SMEM_USED + 1024;       // + alignment slack
 static_assert(SMEM_BYTES <= 227 * 1024, "shared memory budget");
@@ -543,62 +542,26 @@ kda_chunk_tc_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_consta
         }
 
         // ---- (3) A = beta K~ K^T and M = Q~ K^T on the 10 sub-tile pairs (I >= J), bf16
-        // products with fp32 accumulation.  Warps 0-7: the diagonal pair (I, I), I = warp % 4, both
-        // 8-column halves, M as the 3-term product (Q~hi + Q~lo)(K^hi + K^lo)^T less lo.lo with
-        // the exact q_r . k_r on its diagonal (the largest entries of M, where one bf16 rounding
-        // of each operand shows in the outputs); warps I and I + 4 split the 128 channels and
-        // warp I adds the other half's partial sums, then inverts (I + A_II) by forward
-        // substitution (one SM sub-partition per block).
+        // products with fp32 accumulation.  Warps 0-3: A_II, I = warp, both 8-column halves; the
+        // warp then inverts (I + A_II) by forward substitution (one SM sub-partition per block).
+        // Warps 4-7: M_II, I = warp - 4, as the 3-term product (Q~hi + Q~lo)(K^hi + K^lo)^T less
+        // lo.lo with the exact q_r . k_r on its diagonal (the largest entries of M, where one
+        // bf16 rounding of each operand shows in the outputs).
         // Warps 8-13: the 6 off-diagonal pairs, single bf16 products with the per-channel factor
         // e^{b_I - b_J} applied to the right operand.  Off-diagonal A blocks go to the fp16
         // tile AT; T_II = (I + A_II)^-1 goes to the diagonal blocks of the fp16 tile T.
-        if (warp < 8) {
-            const int I = warp & 3, kh = warp >> 2;
-            float accA[2][4], accM[3][2][4];
-#pragma unroll
-            for (int nt = 0; nt < 2; ++nt)
-#pragma unroll
-                for (int e = 0; e < 4; ++e) {
-                    accA[nt][e] = 0.f;
-                    accM[0][nt][e] = 0.f; accM[1][nt][e] = 0.f; accM[2][nt][e] = 0.f;
-                }
-#pragma unroll 2
-            for (int kk = 4 * kh; kk < 4 * kh + 4; ++kk) {
+        if (warp < 4) {
+            const int I = warp;
+            float accA[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
+#pragma unroll 4
+            for (int kk = 0; kk < 8; ++kk) {
                 const uint32_t ao = sw(16 * I + (lane & 15), 16 * kk + ((lane >> 4) << 3), 64);
                 const uint32_t bo = sw(16 * I + (lane & 7) + ((lane >> 4) << 3), 16 * kk + (((lane >> 3) & 1) << 3), 64);
-                uint32_t ka[4], qh[4], ql[4], bh[4], bl[4];
+                uint32_t ka[4], bh[4];
                 ldsm_x4(sb + OFF_SST + 16384 + ao, ka[0], ka[1], ka[2], ka[3]);
-                ldsm_x4(sb + OFF_SST + ao, qh[0], qh[1], qh[2], qh[3]);
-                ldsm_x4(sb + OFF_UST + ao, ql[0], ql[1], ql[2], ql[3]);
                 ldsm_x4(sb + OFF_KH + bo, bh[0], bh[1], bh[2], bh[3]);
-                ldsm_x4(sb + OFF_WT + bo, bl[0], bl[1], bl[2], bl[3]);
-#pragma unroll
-                for (int nt = 0; nt < 2; ++nt) {
-                    mma_16816(accA[nt], ka[0], ka[1], ka[2], ka[3], bh[2 * nt], bh[2 * nt + 1]);
-                    mma_16816(accM[0][nt], qh[0], qh[1], qh[2], qh[3], bh[2 * nt], bh[2 * nt + 1]);
-                    mma_16816(accM[1][nt], ql[0], ql[1], ql[2], ql[3], bh[2 * nt], bh[2 * nt + 1]);
-                    mma_16816(accM[2][nt], qh[0], qh[1], qh[2], qh[3], bl[2 * nt], bl[2 * nt + 1]);
-                }
-            }
-            float4 *scr = reinterpret_cast<float4 *>(sm + OFF_SCR) + I * 128 + lane;   // [I][4][32]
-#pragma unroll
-            for (int nt = 0; nt < 2; ++nt)
-#pragma unroll
-                for (int e = 0; e < 4; ++e) accM[0][nt][e] += accM[1][nt][e] + accM[2][nt][e];
-            if (kh == 1) {   // hand the partial sums of channels 64..127 to warp I
-#pragma unroll
-                for (int nt = 0; nt < 2; ++nt) {
-                    scr[(2 * nt) * 32] = make_float4(accA[nt][0], accA[nt][1], accA[nt][2], accA[nt][3]);
-                    scr[(2 * nt + 1) * 32] = make_float4(accM[0][nt][0], accM[0][nt][1], accM[0][nt][2], accM[0][nt][3]);
-                }
-                named_bar_arrive(1 + I, 64);
-            } else {
-            named_bar(1 + I, 64);
-#pragma unroll
-            for (int nt = 0; nt < 2; ++nt) {
-                const float4 pa = scr[(2 * nt) * 32], pm = scr[(2 * nt + 1) * 32];
-                accA[nt][0] += pa.x; accA[nt][1] += pa.y; accA[nt][2] += pa.z; accA[nt][3] += pa.w;
-                accM[0][nt][0] += pm.x; accM[0][nt][1] += pm.y; accM[0][nt][2] += pm.z; accM[0][nt][3] += pm.w;
+                mma_16816(accA[0], ka[0], ka[1], ka[2], ka[3], bh[0], bh[1]);
+                mma_16816(accA[1], ka[0], ka[1], ka[2], ka[3], bh[2], bh[3]);
             }
 #pragma unroll
             for (int nt = 0; nt < 2; ++nt)
@@ -609,12 +572,6 @@ kda_chunk_tc_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_consta
                     const float br = BETA[r];
                     AF[r * LDA + (s0 & 15)] = s0 < r ? br * accA[nt][2 * hh] : 0.f;
                     AF[r * LDA + (s0 & 15) + 1] = s0 + 1 < r ? br * accA[nt][2 * hh + 1] : 0.f;
-                    const float m0 = s0 < r ? accM[0][nt][2 * hh] : (s0 == r ? MRR[r] : 0.f);
-                    const float m1 = s0 + 1 < r ? accM[0][nt][2 * hh + 1] : (s0 + 1 == r ? MRR[r] : 0.f);
-                    const uint32_t mh = pack_f16(m0, m1);
-                    const float2 mhf = unpack_f16(mh);
-                    *reinterpret_cast<uint32_t *>(sm + OFF_MT + sw(r, s0, 64)) = mh;
-                    *reinterpret_cast<uint32_t *>(sm + OFF_MLO + sw(r, s0, 64)) = pack_f16(m0 - mhf.x, m1 - mhf.y);
                 }
             __syncwarp();   // the whole of A_II is in place
             if (lane < 16) {
@@ -640,7 +597,44 @@ kda_chunk_tc_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_consta
                 for (int r = 0; r < 16; ++r)
                     at[sw(16 * I + r, 16 * I + jj, 64) >> 1] = __float2half_rn(tcol[r]);
             }
+        } else if (warp < 8) {
+            const int I = warp - 4;
+            float accM[3][2][4];
+#pragma unroll
+            for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+                for (int e = 0; e < 4; ++e) { accM[0][nt][e] = 0.f; accM[1][nt][e] = 0.f; accM[2][nt][e] = 0.f; }
+#pragma unroll 2
+            for (int kk = 0; kk < 8; ++kk) {
+                const uint32_t ao = sw(16 * I + (lane & 15), 16 * kk + ((lane >> 4) << 3), 64);
+                const uint32_t bo = sw(16 * I + (lane & 7) + ((lane >> 4) << 3), 16 * kk + (((lane >> 3) & 1) << 3), 64);
+                uint32_t qh[4], ql[4], bh[4], bl[4];
+                ldsm_x4(sb + OFF_SST + ao, qh[0], qh[1], qh[2], qh[3]);
+                ldsm_x4(sb + OFF_UST + ao, ql[0], ql[1], ql[2], ql[3]);
+                ldsm_x4(sb + OFF_KH + bo, bh[0], bh[1], bh[2], bh[3]);
+                ldsm_x4(sb + OFF_WT + bo, bl[0], bl[1], bl[2], bl[3]);
+#pragma unroll
+                for (int nt = 0; nt < 2; ++nt) {
+                    mma_16816(accM[0][nt], qh[0], qh[1], qh[2], qh[3], bh[2 * nt], bh[2 * nt + 1]);
+                    mma_16816(accM[1][nt], ql[0], ql[1], ql[2], ql[3], bh[2 * nt], bh[2 * nt + 1]);
+                    mma_16816(accM[2][nt], qh[0], qh[1], qh[2], qh[3], bl[2 * nt], bl[2 * nt + 1]);
+                }
             }
+#pragma unroll
+            for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+                for (int hh = 0; hh < 2; ++hh) {
+                    const int r = 16 * I + g + 8 * hh;
+                    const int s0 = 16 * I + 8 * nt + 2 * t4;
+                    const float mv0 = accM[0][nt][2 * hh] + (accM[1][nt][2 * hh] + accM[2][nt][2 * hh]);
+                    const float mv1 = accM[0][nt][2 * hh + 1] + (accM[1][nt][2 * hh + 1] + accM[2][nt][2 * hh + 1]);
+                    const float m0 = s0 < r ? mv0 : (s0 == r ? MRR[r] : 0.f);
+                    const float m1 = s0 + 1 < r ? mv1 : (s0 + 1 == r ? MRR[r] : 0.f);
+                    const uint32_t mh = pack_f16(m0, m1);
+                    const float2 mhf = unpack_f16(mh);
+                    *reinterpret_cast<uint32_t *>(sm + OFF_MT + sw(r, s0, 64)) = mh;
+                    *reinterpret_cast<uint32_t *>(sm + OFF_MLO + sw(r, s0, 64)) = pack_f16(m0 - mhf.x, m1 - mhf.y);
+                }
         } else if (warp == 14) {   // the blocks of T above the diagonal (staging used them)
             for (int x = lane; x < 192; x += 32) {
                 const int b = x >> 5, rr = (x >> 1) & 15, hf = x & 1;   // (0,1) (0,2) (0,3) (1,2) (1,3) (2,3)
