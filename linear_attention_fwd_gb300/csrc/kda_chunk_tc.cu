@@ -12,7 +12,7 @@
 //   per 16-token sub-tile I with reference b_I = gamma before its start,
 //     x = e^{gamma - b_I} in [e^-80, 1],  Q~ = Q x,  K~ = K x,  K^ = K / x;
 //   A_rs = beta_r (K~ K^^T)_rs * (e^{b_I - b_J} per channel, J < I),  s <  r
-//   M_rs =        (Q~ K^^T)_rs * (same), s < r;   M_rr = q_r . k_r (exact)
+//   M_rs =        (Q~ K^^T)_rs * (same), s <= r
 //   T = (I + A)^-1 (16x16 diagonal inverses, then the off-diagonal blocks level by level)
 //   U = T diag(beta) (V - Kbar S),  O = Qbar S + M U,  S <- Diag(e^{gamma_last}) S + Kp^T U.
 //
@@ -69,7 +69,7 @@ constexpr uint32_t OFF_V = 32768;      // V (bf16)                 [64 r][128 j]
 constexpr uint32_t OFF_G = 49152;      // G (bf16)                 [64 r][128 i]
 constexpr uint32_t OFF_SST = 65536;    // Q~hi, K~ (bf16)          2 x [64 r][128 i]
 constexpr uint32_t OFF_UST = 98304;    // Q~lo (bf16)              [64 r][128 i]
-constexpr uint32_t OFF_WT = 114688;    // K^lo (bf16)              [64 r][128 i]
+                                       // (bytes 114688..131071 are unused)
 constexpr uint32_t OFF_KPT = 131072;   // Kp^T fp16                [128 i][64 r]
 constexpr uint32_t OFF_MT = 147456;    // M fp16                   [64 r][64 s]
 constexpr uint32_t OFF_TT = 155648;    // A_IJ (I > J) fp16        [64 r][64 s]
@@ -84,7 +84,7 @@ constexpr uint32_t OFF_W6 = OFF_EL + 4 * 128 * 4;       // e^{b_I - b_J}    [6][
 constexpr uint32_t OFF_DEC = OFF_W6 + 6 * 128 * 2;      // e^{gl}           [128]
 constexpr uint32_t OFF_BETA = OFF_DEC + 128 * 4;        // beta             [64]
 constexpr uint32_t OFF_MRR = OFF_BETA + 64 * 4;         // q_r . k_r        [64]
-constexpr uint32_t OFF_MLO = (OFF_MRR + 64 * 4 + 1023) / 1024 * 1024;   // M - fp16(M), fp16 [64 r][64 s]
+constexpr uint32_t OFF_MLO = (OFF_MRR + 64 * 4 + 1023) / 1024 * 1024;  // M - fp16(M), fp16 [64 r][64 s]
 constexpr uint32_t OFF_BAR = OFF_MLO + 8192;            // 7 mbarriers, TMEM address
 constexpr uint32_t SMEM_USED = OFF_BAR + 64;
 constexpr uint32_t SMEM_BYTES = SMEM_USED + 1024;       // + alignment slack
@@ -187,12 +187,12 @@ kda_chunk_tc_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_consta
     const uint32_t bar_z = sb + OFF_BAR + 56;   // a chunk's gate logits landed in the staging tile
     float *AF = reinterpret_cast<float *>(sm + OFF_PART);   // A_II blocks, [4][16][LDA]
     float *PART = reinterpret_cast<float *>(sm + OFF_PART);
+    float *MRR = reinterpret_cast<float *>(sm + OFF_MRR);
     float *EB = reinterpret_cast<float *>(sm + OFF_EB);
     float *EL = reinterpret_cast<float *>(sm + OFF_EL);
     __nv_bfloat16 *W6 = reinterpret_cast<__nv_bfloat16 *>(sm + OFF_W6);
     float *DEC = reinterpret_cast<float *>(sm + OFF_DEC);
     float *BETA = reinterpret_cast<float *>(sm + OFF_BETA);
-    float *MRR = reinterpret_cast<float *>(sm + OFF_MRR);
     const __nv_bfloat16 *beta = static_cast<const __nv_bfloat16 *>(a.beta);
     __nv_bfloat16 *out = static_cast<__nv_bfloat16 *>(a.out);
 
@@ -347,44 +347,45 @@ kda_chunk_tc_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_consta
     const int blk = sub >> 1, hb = sub & 1;    // sub-tile and which half of it
     const int t4 = lane & 3, g = lane >> 2;    // mma.sync fragment coordinates
 
-    // (1) of a chunk whose Q, K, G tiles have landed (nr rows inside the sequence): warps 0-7:
+    // (1) of a chunk whose G tile has landed (nr rows inside the sequence), warps 0-7:
     // log2-decay sums over the two 8-row halves of sub-tile warp/2 (cumulative sums restart at
-    // each sub-tile);  warps 8-11: q_r . k_r exactly (bf16 x bf16 products are exact in fp32)
-    // from the raw diagonal 16x16 blocks of Q K^T on mma.sync
+    // each sub-tile)
+    // Warps 0-7: the sums of log2 decays over 16-row quarters of the chunk (rows >= nr count as 0).
     auto prephase = [&](int nr) {
-        if (warp < 8) {
-            const int c = 2 * cp, q = tid >> 6;
+        const int c = 2 * cp, q = tid >> 6;
 #pragma unroll
-            for (int half = 0; half < 2; ++half) {
-                float l0 = 0.f, l1 = 0.f;
+        for (int half = 0; half < 2; ++half) {
+            float l0 = 0.f, l1 = 0.f;
 #pragma unroll
-                for (int rr = 0; rr < 8; ++rr) {
-                    const int r = 16 * q + 8 * half + rr;
-                    const float2 g2 = unpack_bf16(*reinterpret_cast<uint32_t *>(sm + OFF_G + sw(r, c, 64)));
-                    if (r < nr) { l0 = fmaf(g2.x, LOG2E, l0); l1 = fmaf(g2.y, LOG2E, l1); }
-                }
-                PART[(2 * q + half) * 128 + c] = l0;
-                PART[(2 * q + half) * 128 + c + 1] = l1;
+            for (int rr = 0; rr < 8; ++rr) {
+                const int r = 16 * q + 8 * half + rr;
+                const float2 g2 = unpack_bf16(*reinterpret_cast<uint32_t *>(sm + OFF_G + sw(r, c, 64)));
+                if (r < nr) { l0 = fmaf(g2.x, LOG2E, l0); l1 = fmaf(g2.y, LOG2E, l1); }
             }
-        } else if (warp < 12) {
-            const int I = warp - 8;
-            float acc[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
-#pragma unroll
-            for (int kk = 0; kk < 8; ++kk) {
-                uint32_t a0, a1, a2, a3, b0, b1, b2, b3;
-                ldsm_x4(sb + OFF_Q + swqk(16 * I + (lane & 15), 16 * kk + ((lane >> 4) << 3)), a0, a1, a2, a3);
-                ldsm_x4(sb + OFF_K + swqk(16 * I + (lane & 7) + ((lane >> 4) << 3), 16 * kk + (((lane >> 3) & 1) << 3)),
-                        b0, b1, b2, b3);
-                mma_16816(acc[0], a0, a1, a2, a3, b0, b1);
-                mma_16816(acc[1], a0, a1, a2, a3, b2, b3);
-            }
-            // element (row g + 8hh, col 8nt + 2t4 + e) is diagonal when nt == hh and 2t4 + e == g
-#pragma unroll
-            for (int hh = 0; hh < 2; ++hh)
-#pragma unroll
-                for (int e = 0; e < 2; ++e)
-                    if (2 * t4 + e == g) MRR[16 * I + g + 8 * hh] = acc[hh][2 * hh + e];
+            PART[(2 * q + half) * 128 + c] = l0;
+            PART[(2 * q + half) * 128 + c + 1] = l1;
         }
+    };
+    // Warps 8-11: q_r . k_r for the 16 rows of sub-tile I = warp - 8, from the raw bf16 tiles
+    // (exact products, fp32 sums): the diagonal of M, whose entries carry no decay.
+    auto diag_qk = [&]() {
+        const int I = warp - 8;
+        float acc[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
+#pragma unroll
+        for (int kk = 0; kk < 8; ++kk) {
+            uint32_t a0, a1, a2, a3, b0, b1, b2, b3;
+            ldsm_x4(sb + OFF_Q + swqk(16 * I + (lane & 15), 16 * kk + ((lane >> 4) << 3)), a0, a1, a2, a3);
+            ldsm_x4(sb + OFF_K + swqk(16 * I + (lane & 7) + ((lane >> 4) << 3), 16 * kk + (((lane >> 3) & 1) << 3)),
+                    b0, b1, b2, b3);
+            mma_16816(acc[0], a0, a1, a2, a3, b0, b1);
+            mma_16816(acc[1], a0, a1, a2, a3, b2, b3);
+        }
+        // element (row g + 8hh, col 8nt + 2t4 + e) is diagonal when nt == hh and 2t4 + e == g
+#pragma unroll
+        for (int hh = 0; hh < 2; ++hh)
+#pragma unroll
+            for (int e = 0; e < 2; ++e)
+                if (2 * t4 + e == g) MRR[16 * I + g + 8 * hh] = acc[hh][2 * hh + e];
     };
     // per-channel decay vectors of that chunk (log2 units); thread: channel c, sub-tile I
     auto vectors = [&]() {
@@ -415,23 +416,25 @@ kda_chunk_tc_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_consta
         }
         bool got = mbar_wait(bar_tma, ph_tma, wait_limit);   // checked at the next barrier
         ph_tma ^= 1;
-        // ---- (1) warps 0-11: decay sums and q_r . k_r;  warps 12-15: once the previous state
-        // update has landed, S^T -> fp16 pairs (the MMA operand of this chunk)
-        if (warp < 12) {
+        // ---- (1) warps 0-7: decay sums, then the previous chunk's output staged; warps 8-11:
+        // q_r . k_r; warps 8-15: once the previous state update has landed, S^T -> fp16 pairs
+        // (the MMA operand of this chunk), 64 key channels per warp
+        if (warp < 8) {
             prephase(nr);
-            if (out_pending && warp < 8) {   // the previous chunk's output, once its groups landed
+            if (out_pending) {   // the previous chunk's output, once its groups landed
                 got = mbar_wait(bar_s, ph_s, wait_limit) && mbar_wait(bar_o, ph_o, wait_limit) && got;
                 if (a.gate) got = mbar_wait(bar_z, ph_z, wait_limit) && got;
                 tc_fence_after();
                 stage_output();
             }
         } else {
+            if (warp < 12) diag_qk();
             if (out_pending) got = mbar_wait(bar_s, ph_s, wait_limit) && got;
             tc_fence_after();
             const int64_t cs = ckpt_slot(a, n, (int64_t)ci * C);   // the state after ci chunks
             float *ck = cs >= 0 ? a.ckpt + (cs * H + h) * D * D + jl : nullptr;
-#pragma unroll 1
-            for (int i0 = 0; i0 < 128; i0 += 64) {
+            {
+                const int i0 = 64 * ((warp - 8) >> 2);
                 float v[32], w[32];
                 tmem_ld32x2(trow + TM_S + i0, trow + TM_S + i0 + 32, v, w);
                 if (ck) {   // S[i][j] = S^T[j][i]: a warp writes 128 contiguous bytes per i
@@ -467,7 +470,7 @@ kda_chunk_tc_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_consta
         }
 
         // ---- (2) operands, each rounded from the exact inputs:
-        //   bf16 (range e^+-80): Q~ = Q x and K^ = K / x as hi + lo, K~ = K x;
+        //   bf16 (range e^+-80): Q~ = Q x as hi + lo, K~ = K x, K^ = K / x;
         //   fp16: Qbar = Q x e^{b_I} (over Q), Kbar (over K), Kp = K / x e^{gl - b_I} (transposed).
         // Rows past the end of the sequence hold finite data (the next sequence, or TMA zero
         // fill) and need no masking: their beta is 0, their decay is not accumulated, and the
@@ -494,14 +497,12 @@ kda_chunk_tc_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_consta
                     const float2 x = make_float2(ex2(l.x), ex2(l.y));
                     const float2 y = make_float2(ex2(-l.x), ex2(-l.y));
                     const float2 qt = __fmul2_rn(q2, x), kt = __fmul2_rn(k2, x), kh = __fmul2_rn(k2, y);
-                    const uint32_t qh = pack_bf16(qt.x, qt.y), khh = pack_bf16(kh.x, kh.y);
+                    const uint32_t qh = pack_bf16(qt.x, qt.y);
                     const float2 ql = __ffma2_rn(unpack_bf16(qh), minus1, qt);
-                    const float2 kl = __ffma2_rn(unpack_bf16(khh), minus1, kh);
                     *reinterpret_cast<uint32_t *>(sm + OFF_SST + off) = qh;
                     *reinterpret_cast<uint32_t *>(sm + OFF_UST + off) = pack_bf16(ql.x, ql.y);
                     *reinterpret_cast<uint32_t *>(sm + OFF_SST + 16384 + off) = pack_bf16(kt.x, kt.y);
-                    *reinterpret_cast<uint32_t *>(sm + OFF_KH + off) = khh;
-                    *reinterpret_cast<uint32_t *>(sm + OFF_WT + off) = pack_bf16(kl.x, kl.y);
+                    *reinterpret_cast<uint32_t *>(sm + OFF_KH + off) = pack_bf16(kh.x, kh.y);
                     const float2 qb = __fmul2_rn(qt, eb), kb = __fmul2_rn(kt, eb), kp2 = __fmul2_rn(kh, el);
                     *reinterpret_cast<uint32_t *>(sm + OFF_Q + oqk) = pack_f16(qb.x, qb.y);
                     *reinterpret_cast<uint32_t *>(sm + OFF_K + oqk) = pack_f16(kb.x, kb.y);
@@ -544,9 +545,9 @@ kda_chunk_tc_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_consta
         // ---- (3) A = beta K~ K^T and M = Q~ K^T on the 10 sub-tile pairs (I >= J), bf16
         // products with fp32 accumulation.  Warps 0-3: A_II, I = warp, both 8-column halves; the
         // warp then inverts (I + A_II) by forward substitution (one SM sub-partition per block).
-        // Warps 4-7: M_II, I = warp - 4, as the 3-term product (Q~hi + Q~lo)(K^hi + K^lo)^T less
-        // lo.lo with the exact q_r . k_r on its diagonal (the largest entries of M, where one
-        // bf16 rounding of each operand shows in the outputs).
+        // Warps 4-7: M_II, I = warp - 4, as (Q~hi + Q~lo) K^^T below the diagonal (the largest
+        // entries of M, where the bf16 rounding of Q~ shows in the outputs) and the exact
+        // q_r . k_r on it.
         // Warps 8-13: the 6 off-diagonal pairs, single bf16 products with the per-channel factor
         // e^{b_I - b_J} applied to the right operand.  Off-diagonal A blocks go to the fp16
         // tile AT; T_II = (I + A_II)^-1 goes to the diagonal blocks of the fp16 tile T.
@@ -599,25 +600,23 @@ kda_chunk_tc_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_consta
             }
         } else if (warp < 8) {
             const int I = warp - 4;
-            float accM[3][2][4];
+            float accM[2][2][4];
 #pragma unroll
             for (int nt = 0; nt < 2; ++nt)
 #pragma unroll
-                for (int e = 0; e < 4; ++e) { accM[0][nt][e] = 0.f; accM[1][nt][e] = 0.f; accM[2][nt][e] = 0.f; }
+                for (int e = 0; e < 4; ++e) { accM[0][nt][e] = 0.f; accM[1][nt][e] = 0.f; }
 #pragma unroll 2
             for (int kk = 0; kk < 8; ++kk) {
                 const uint32_t ao = sw(16 * I + (lane & 15), 16 * kk + ((lane >> 4) << 3), 64);
                 const uint32_t bo = sw(16 * I + (lane & 7) + ((lane >> 4) << 3), 16 * kk + (((lane >> 3) & 1) << 3), 64);
-                uint32_t qh[4], ql[4], bh[4], bl[4];
+                uint32_t qh[4], ql[4], bh[4];
                 ldsm_x4(sb + OFF_SST + ao, qh[0], qh[1], qh[2], qh[3]);
                 ldsm_x4(sb + OFF_UST + ao, ql[0], ql[1], ql[2], ql[3]);
                 ldsm_x4(sb + OFF_KH + bo, bh[0], bh[1], bh[2], bh[3]);
-                ldsm_x4(sb + OFF_WT + bo, bl[0], bl[1], bl[2], bl[3]);
 #pragma unroll
                 for (int nt = 0; nt < 2; ++nt) {
                     mma_16816(accM[0][nt], qh[0], qh[1], qh[2], qh[3], bh[2 * nt], bh[2 * nt + 1]);
                     mma_16816(accM[1][nt], ql[0], ql[1], ql[2], ql[3], bh[2 * nt], bh[2 * nt + 1]);
-                    mma_16816(accM[2][nt], qh[0], qh[1], qh[2], qh[3], bl[2 * nt], bl[2 * nt + 1]);
                 }
             }
 #pragma unroll
@@ -626,8 +625,8 @@ kda_chunk_tc_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_consta
                 for (int hh = 0; hh < 2; ++hh) {
                     const int r = 16 * I + g + 8 * hh;
                     const int s0 = 16 * I + 8 * nt + 2 * t4;
-                    const float mv0 = accM[0][nt][2 * hh] + (accM[1][nt][2 * hh] + accM[2][nt][2 * hh]);
-                    const float mv1 = accM[0][nt][2 * hh + 1] + (accM[1][nt][2 * hh + 1] + accM[2][nt][2 * hh + 1]);
+                    const float mv0 = accM[0][nt][2 * hh] + accM[1][nt][2 * hh];
+                    const float mv1 = accM[0][nt][2 * hh + 1] + accM[1][nt][2 * hh + 1];
                     const float m0 = s0 < r ? mv0 : (s0 == r ? MRR[r] : 0.f);
                     const float m1 = s0 + 1 < r ? mv1 : (s0 + 1 == r ? MRR[r] : 0.f);
                     const uint32_t mh = pack_f16(m0, m1);
