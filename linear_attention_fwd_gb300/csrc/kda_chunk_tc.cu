@@ -84,7 +84,8 @@ constexpr uint32_t OFF_W6 = OFF_EL + 4 * 128 * 4;       // e^{b_I - b_J}    [6][
 constexpr uint32_t OFF_DEC = OFF_W6 + 6 * 128 * 2;      // e^{gl}           [128]
 constexpr uint32_t OFF_BETA = OFF_DEC + 128 * 4;        // beta             [64]
 constexpr uint32_t OFF_MRR = OFF_BETA + 64 * 4;         // q_r . k_r        [64]
-constexpr uint32_t OFF_MLO = (OFF_MRR + 64 * 4 + 1023) / 1024 * 1024;  // M - fp16(M), fp16 [64 r][64 s]
+constexpr uint32_t OFF_BNEXT = OFF_MRR + 64 * 4;        // the next chunk's beta [64]
+constexpr uint32_t OFF_MLO = (OFF_BNEXT + 64 * 4 + 1023) / 1024 * 1024;  // M - fp16(M), fp16 [64 r][64 s]
 constexpr uint32_t OFF_BAR = OFF_MLO + 8192;            // 7 mbarriers, TMEM address
 constexpr uint32_t SMEM_USED = OFF_BAR + 64;
 constexpr uint32_t SMEM_BYTES = SMEM_USED + 1024;       // + alignment slack
@@ -242,6 +243,7 @@ kda_chunk_tc_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_consta
         mbar_arrive_expect_tx(bar_v, 16384);
         tma_tile(&tmv, sb + OFF_V, bar_v, h, bos);
     }
+    if (tid < C) BETA[tid] = tid < len ? __bfloat162float(beta[(bos + tid) * H + h]) : 0.f;
     // the blocks of M above the diagonal blocks stay zero for the whole sequence
     for (int x = tid; x < 64 * 32; x += NT) {
         const int r = x >> 5, s2 = 2 * (x & 31);
@@ -402,18 +404,13 @@ kda_chunk_tc_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_consta
             if (J < I) W6[pair_index(I, J) * 128 + c] = __float2bfloat16_rn(ex2(bI[I] - bI[J]));
         if (I == 0) DEC[c] = ex2(gl);
     };
-    float bnext = (tid < C && tid < len) ? __bfloat162float(beta[(bos + tid) * H + h]) : 0.f;
 #pragma unroll 1
     for (int ci = 0; ci < nchunks; ++ci) {
         const int64_t t0 = bos + (int64_t)ci * C;
         const int nr = (int)(len - (int64_t)ci * C < C ? len - (int64_t)ci * C : C);
         const bool more = ci + 1 < nchunks;
 
-        if (tid < C) {   // this chunk's beta (loaded one chunk ahead); the next chunk's
-            BETA[tid] = bnext;
-            const int64_t nn = more ? len - (int64_t)(ci + 1) * C : 0;
-            bnext = tid < nn ? __bfloat162float(beta[(t0 + C + tid) * H + h]) : 0.f;
-        }
+        if (ci > 0 && tid < C) BETA[tid] = BETA[tid + (OFF_BNEXT - OFF_BETA) / 4];   // loaded during the previous chunk
         bool got = mbar_wait(bar_tma, ph_tma, wait_limit);   // checked at the next barrier
         ph_tma ^= 1;
         // ---- (1) warps 0-7: decay sums, then the previous chunk's output staged; warps 8-11:
@@ -717,6 +714,12 @@ kda_chunk_tc_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_consta
             }
             tmem_st16u(trow + TM_Z + s0 / 2, zv);
             tmem_st16u(trow + TM_ZL + s0 / 2, zl);
+        } else if (warp == 3) {   // the next chunk's beta, the load latency hidden in this step
+            if (more) {
+                const int64_t nn = len - (int64_t)(ci + 1) * C;
+                for (int r = lane; r < C; r += 32)
+                    BETA[r + (OFF_BNEXT - OFF_BETA) / 4] = r < nn ? __bfloat162float(beta[(t0 + C + r) * H + h]) : 0.f;
+            }
         } else if (warp >= 12) {   // S^T <- S^T Diag(dec) in place (S^T was read as fp16 in (1))
 #pragma unroll 1
             for (int i0 = 0; i0 < 128; i0 += 64) {
@@ -796,14 +799,15 @@ kda_chunk_tc_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_consta
         tc_fence_before();
         __syncthreads();
         // [S^T | O^T] += U^T_hi [Kp^T; M]^T [commit: S];  low-order terms of O^T,
-        // U^T_lo M^T + U^T_hi Mlo^T, into the U^T columns (consumed) [commit: O]
+        // U^T_lo M^T + U^T_hi Mlo^T, into the U^T columns (consumed) [commit: O], issued by a
+        // warp with the least work in the next step (1)
         if (tid == 0) {
             tc_fence_after();
 #pragma unroll
             for (int ks = 0; ks < 4; ++ks)
                 mma_f16_ts(tmem + TM_S, tmem + TM_UH + 8 * ks, dsm + ((OFF_KPT + ks * 32) >> 4), IDESC_N192, 1);
             mma_commit(bar_s);
-        } else if (tid == 32) {
+        } else if (tid == 480) {
             tc_fence_after();
 #pragma unroll
             for (int ks = 0; ks < 4; ++ks)
