@@ -234,6 +234,7 @@ kda_chunk_tc_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_consta
         for (int c = 0; c < 32; ++c)
             v[c] = a.s0 ? a.s0[sbase + (int64_t)(32 * quarter + c) * D + jl] : 0.f;
         tmem_st32(trow + TM_S + 32 * quarter, v);
+        tmem_wait_st();
     }
     if (tid == 0 && nchunks > 0) {
         mbar_arrive_expect_tx(bar_tma, 3 * 16384);
@@ -449,6 +450,7 @@ kda_chunk_tc_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_consta
                 }
                 tmem_st16u(trow + TM_S16 + i0 / 2, hv);
                 tmem_st16u(trow + TM_S16 + i0 / 2 + 16, hw);
+                tmem_wait_st();
             }
         }
         if (out_pending) ph_s ^= 1;
@@ -714,6 +716,7 @@ kda_chunk_tc_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_consta
             }
             tmem_st16u(trow + TM_Z + s0 / 2, zv);
             tmem_st16u(trow + TM_ZL + s0 / 2, zl);
+            tmem_wait_st();
         } else if (warp == 3) {   // the next chunk's beta, the load latency hidden in this step
             if (more) {
                 const int64_t nn = len - (int64_t)(ci + 1) * C;
@@ -739,6 +742,7 @@ kda_chunk_tc_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_consta
                 tmem_st32(trow + TM_S + i0, v);
                 tmem_st32(trow + TM_S + i0 + 32, w);
             }
+            tmem_wait_st();
         }
         ph_p ^= 1;
         ph_v ^= 1;
@@ -795,6 +799,7 @@ kda_chunk_tc_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_consta
             }
             tmem_st8u(trow + TM_UH + r0 / 2, hi);
             tmem_st8u(trow + TM_UL + r0 / 2, lo);
+            tmem_wait_st();
         }
         tc_fence_before();
         __syncthreads();
