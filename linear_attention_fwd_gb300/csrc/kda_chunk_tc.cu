@@ -69,7 +69,8 @@ constexpr uint32_t OFF_V = 32768;      // V (bf16)                 [64 r][128 j]
 constexpr uint32_t OFF_G = 49152;      // G (bf16)                 [64 r][128 i]
 constexpr uint32_t OFF_SST = 65536;    // Q~hi, K~ (bf16)          2 x [64 r][128 i]
 constexpr uint32_t OFF_UST = 98304;    // Q~lo (bf16)              [64 r][128 i]
-                                       // (bytes 114688..131071 are unused)
+constexpr uint32_t OFF_NI = 114688;    // -I (bf16, constant)      [64 s][64 r]
+                                       // (bytes 122880..131071 are unused)
 constexpr uint32_t OFF_KPT = 131072;   // Kp^T fp16                [128 i][64 r]
 constexpr uint32_t OFF_MT = 147456;    // M fp16                   [64 r][64 s]
 constexpr uint32_t OFF_TT = 155648;    // A_IJ (I > J) fp16        [64 r][64 s]
@@ -111,6 +112,7 @@ constexpr uint32_t TM_COLS = 512;
 constexpr uint32_t IDESC_N64 = idesc_f16_f32(128, 64);
 constexpr uint32_t IDESC_N128 = idesc_f16_f32(128, 128);
 constexpr uint32_t IDESC_N192 = idesc_f16_f32(128, 192);
+constexpr uint32_t IDESC_VT = idesc_bf16_f32(128, 64) | (1u << 15);   // A (V) MN-major
 static_assert(OFF_MT == OFF_KPT + 16384 && TM_O == TM_S + 128 && TM_P == TM_O + 64, "adjacent operands");
 
 // Byte offset of element (row, col) in a 128-byte-swizzled K-major tile of
@@ -245,6 +247,11 @@ kda_chunk_tc_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_consta
         tma_tile(&tmv, sb + OFF_V, bar_v, h, bos);
     }
     if (tid < C) BETA[tid] = tid < len ? __bfloat162float(beta[(bos + tid) * H + h]) : 0.f;
+    for (int x = tid; x < 64 * 32; x += NT) {   // -I: subtracts V^T from P^T inside the MMA
+        const int r = x >> 5, s2 = 2 * (x & 31);
+        *reinterpret_cast<uint32_t *>(sm + OFF_NI + sw(r, s2, 64)) =
+            (s2 == r ? 0xBF80u : 0u) | (s2 + 1 == r ? 0xBF800000u : 0u);
+    }
     // the blocks of M above the diagonal blocks stay zero for the whole sequence
     for (int x = tid; x < 64 * 32; x += NT) {
         const int r = x >> 5, s2 = 2 * (x & 31);
@@ -519,9 +526,9 @@ kda_chunk_tc_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_consta
         fence_async_smem();
         tc_fence_before();
         __syncthreads();
-        // [O^T | P^T] = S^T [Qbar; Kbar]^T [commit: P], issued by a warp that (3) leaves idle;
-        // the same thread loads the next chunk's G (consumed) and, once the group has read Qbar
-        // and Kbar, its Q and K
+        // [O^T | P^T] = S^T [Qbar; Kbar]^T, then P^T -= V^T as V^T (-I) with V read MN-major
+        // [commit: P], issued by a warp that (3) leaves idle; the same thread loads the next
+        // chunk's G (consumed) and, once the group has read Qbar, Kbar and V, its Q, K and V
         bool gtma = true;
         if (warp == 15 && lane == 0) {
             tc_fence_after();
@@ -529,14 +536,24 @@ kda_chunk_tc_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_consta
             for (int k = 0; k < 8; ++k)
                 mma_f16_ts(tmem + TM_O, tmem + TM_S16 + 8 * k, dsm + ((OFF_Q + (k >> 2) * 16384 + (k & 3) * 32) >> 4),
                            IDESC_N128, k > 0);
+            gtma = mbar_wait(bar_v, ph_v, wait_limit);   // this chunk's V
+            if (gtma) {
+                tc_fence_after();
+                const uint64_t vdesc = sdesc_sw128_mn(sb + OFF_V, 64 * 128, 1024);
+#pragma unroll
+                for (int k = 0; k < 4; ++k)
+                    mma_f16_ss(tmem + TM_P, vdesc + ((2048 * k) >> 4), dsm + ((OFF_NI + 32 * k) >> 4), IDESC_VT, 1);
+            }
             mma_commit(bar_p);
             if (more) {
                 mbar_arrive_expect_tx(bar_tma, 3 * 16384);
                 tma_tile(&tmg, sb + OFF_G, bar_tma, h, t0 + C);
-                gtma = mbar_wait(bar_p, ph_p, wait_limit);
+                gtma = mbar_wait(bar_p, ph_p, wait_limit) && gtma;
                 if (gtma) {
                     tma_tile(&tmq, sb + OFF_Q, bar_tma, h, t0 + C, 16384);
                     tma_tile(&tmk, sb + OFF_K, bar_tma, h, t0 + C, 16384);
+                    mbar_arrive_expect_tx(bar_v, 16384);
+                    tma_tile(&tmv, sb + OFF_V, bar_v, h, t0 + C);
                 }
             }
         }
@@ -633,12 +650,18 @@ kda_chunk_tc_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_consta
                     *reinterpret_cast<uint32_t *>(sm + OFF_MT + sw(r, s0, 64)) = mh;
                     *reinterpret_cast<uint32_t *>(sm + OFF_MLO + sw(r, s0, 64)) = pack_f16(m0 - mhf.x, m1 - mhf.y);
                 }
-        } else if (warp == 14) {   // the blocks of T above the diagonal (staging used them)
+        } else if (warp == 14) {   // the blocks of T above the diagonal (staging used them), then
+                                   // the next chunk's beta
             for (int x = lane; x < 192; x += 32) {
                 const int b = x >> 5, rr = (x >> 1) & 15, hf = x & 1;   // (0,1) (0,2) (0,3) (1,2) (1,3) (2,3)
                 const int I = b < 3 ? 0 : (b < 5 ? 1 : 2);
                 const int J = b < 3 ? b + 1 : (b < 5 ? b - 1 : 3);
                 *reinterpret_cast<uint4 *>(sm + OFF_T + sw(16 * I + rr, 16 * J + 8 * hf, 64)) = make_uint4(0u, 0u, 0u, 0u);
+            }
+            if (more) {   // the next chunk's beta (the load latency is hidden in this step)
+                const int64_t nn = len - (int64_t)(ci + 1) * C;
+                for (int r = lane; r < C; r += 32)
+                    BETA[r + (OFF_BNEXT - OFF_BETA) / 4] = r < nn ? __bfloat162float(beta[(t0 + C + r) * H + h]) : 0.f;
             }
         } else if (warp >= 8 && warp < 14) {
             const int po = warp - 8;   // (1,0) (2,0) (2,1) (3,0) (3,1) (3,2)
@@ -696,20 +719,16 @@ kda_chunk_tc_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_consta
             named_bar(1, 96);
             if (warp == 0) t_block(3, 0);
         } else if (warp >= 4 && warp < 12) {
-            got4 = mbar_wait(bar_p, ph_p, wait_limit) && mbar_wait(bar_v, ph_v, wait_limit);
+            got4 = mbar_wait(bar_p, ph_p, wait_limit) && got4;
             tc_fence_after();
             const int s0 = 32 * ((warp - 4) >> 2);
             float pv[32];
-            tmem_ld32(trow + TM_P + s0, pv);
-            const __nv_bfloat16 *vt = reinterpret_cast<const __nv_bfloat16 *>(sm + OFF_V);
+            tmem_ld32(trow + TM_P + s0, pv);   // P^T - V^T
             uint32_t zv[16], zl[16];   // hi and lo: one fp16 rounding of U alone costs 2^-12
 #pragma unroll
             for (int c = 0; c < 16; ++c) {
-                const int s = s0 + 2 * c;
-                const float2 v2 = make_float2(__bfloat162float(vt[sw(s, jl, 64) >> 1]),
-                                              __bfloat162float(vt[sw(s + 1, jl, 64) >> 1]));
-                const float2 z = __fmul2_rn(__fadd2_rn(v2, make_float2(-pv[2 * c], -pv[2 * c + 1])),
-                                            *reinterpret_cast<const float2 *>(BETA + s));
+                const float2 b2 = *reinterpret_cast<const float2 *>(BETA + s0 + 2 * c);
+                const float2 z = __fmul2_rn(make_float2(pv[2 * c], pv[2 * c + 1]), make_float2(-b2.x, -b2.y));
                 zv[c] = pack_f16(z.x, z.y);
                 const float2 zlo = __ffma2_rn(unpack_f16(zv[c]), make_float2(-1.f, -1.f), z);
                 zl[c] = pack_f16(zlo.x, zlo.y);
@@ -717,12 +736,6 @@ kda_chunk_tc_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_consta
             tmem_st16u(trow + TM_Z + s0 / 2, zv);
             tmem_st16u(trow + TM_ZL + s0 / 2, zl);
             tmem_wait_st();
-        } else if (warp == 3) {   // the next chunk's beta, the load latency hidden in this step
-            if (more) {
-                const int64_t nn = len - (int64_t)(ci + 1) * C;
-                for (int r = lane; r < C; r += 32)
-                    BETA[r + (OFF_BNEXT - OFF_BETA) / 4] = r < nn ? __bfloat162float(beta[(t0 + C + r) * H + h]) : 0.f;
-            }
         } else if (warp >= 12) {   // S^T <- S^T Diag(dec) in place (S^T was read as fp16 in (1))
 #pragma unroll 1
             for (int i0 = 0; i0 < 128; i0 += 64) {
@@ -764,10 +777,6 @@ kda_chunk_tc_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_consta
             for (int k = 0; k < 4; ++k)
                 mma_f16_ts(tmem + TM_U, tmem + TM_Z + 8 * k, dsm + ((OFF_T + k * 32) >> 4), IDESC_N64, k > 0);
             mma_commit(bar_u);
-            if (more) {
-                mbar_arrive_expect_tx(bar_v, 16384);
-                tma_tile(&tmv, sb + OFF_V, bar_v, h, t0 + C);
-            }
         }
         {
             const bool got = mbar_wait(bar_u, ph_u, wait_limit);

@@ -150,6 +150,20 @@ __device__ __forceinline__ uint64_t sdesc_sw128(uint32_t saddr) {
     return d;
 }
 
+// Shared-memory matrix descriptor for an MN-major operand in the 128-byte
+// swizzle layout: 128-byte rows of 64 consecutive M (or N) elements, one row per
+// K index; 8-row groups along K `sbo` bytes apart, 64-element groups along M (N)
+// `lbo` bytes apart.  Stepping K by 16 advances the start address by 2 * sbo.
+__device__ __forceinline__ uint64_t sdesc_sw128_mn(uint32_t saddr, uint32_t lbo, uint32_t sbo) {
+    uint64_t d = 0;
+    d |= (uint64_t)((saddr >> 4) & 0x3FFFu);
+    d |= (uint64_t)((lbo >> 4) & 0x3FFFu) << 16;  // leading byte offset
+    d |= (uint64_t)((sbo >> 4) & 0x3FFFu) << 32;  // stride byte offset
+    d |= (uint64_t)1u << 46;                      // descriptor version
+    d |= (uint64_t)2u << 61;                      // 128-byte swizzle
+    return d;
+}
+
 // 32 lanes x 32 consecutive 32-bit columns, one lane per thread; the wait is
 // folded into the same statement so that no use of the values can be scheduled
 // before the data has arrived.
