@@ -26,11 +26,12 @@
 // operands, so the state path never goes through shared memory):
 //   TMA       Q, K, V, G tiles (64 x 128 bf16, 128-byte swizzle) -> smem
 //   SIMT      sub-tile cumulative decay, x and 1/x, scaled operands; S -> fp16
-//   tcgen05   P^T = S^T Kbar^T,  O^T = S^T Qbar^T           (overlapping the next two steps)
+//   tcgen05   P^T = S^T Kbar^T - V^T (V read MN-major against a constant -I),
+//             O^T = S^T Qbar^T                                (overlapping the next two steps)
 //   mma.sync  A and M as 16x16 sub-tile products (the per-pair decay factor is
 //             applied to the B fragments in registers); diagonal inverses by
 //             forward substitution; off-diagonal blocks of T
-//   SIMT      Z^T = (V^T - P^T) diag(beta) -> fp16
+//   SIMT      Z^T = -P^T diag(beta) -> fp16 hi + lo (tensor memory only)
 //   tcgen05   U^T = Z^T T^T;  then  S^T <- S^T Diag(dec) + U^T Kp,  O^T += U^T M^T
 #include <cuda.h>
 #include <cudaTypedefs.h>
@@ -100,7 +101,7 @@ static_assert(4 * 16 * LDA * 4 <= OFF_W6 - OFF_PART, "A_II fits over the sums an
 // tensor memory columns (128 lanes = value channel j)
 constexpr uint32_t TM_S = 0;      // S^T fp32                        128 columns
 constexpr uint32_t TM_O = 128;    // O^T fp32 (follows S^T: one N = 192 group updates both)   64
-constexpr uint32_t TM_P = 192;    // P^T = S^T Kbar^T fp32 (follows O^T)                     64
+constexpr uint32_t TM_P = 192;    // P^T = S^T Kbar^T - V^T fp32 (follows O^T)               64
 constexpr uint32_t TM_U = 256;    // U^T fp32, then the low-order terms of O^T                 64
 constexpr uint32_t TM_S16 = 320;  // S^T as fp16 pairs (MMA operand)  64
 constexpr uint32_t TM_Z = 384;    // Z^T fp16 pairs                   32
