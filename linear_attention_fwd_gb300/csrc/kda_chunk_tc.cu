@@ -275,6 +275,7 @@ kda_chunk_tc_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_consta
     // normalised to unit RMS over its 128 value channels, scaled by the norm weight and
     // multiplied channel-wise by sigmoid(gate logit) before it is rounded to bf16; the chunk's
     // logits were loaded by TMA into the staging tile itself (same row-major layout).
+    const float norm_wj = (a.gate && a.norm_w) ? a.norm_w[jl] : 1.f;   // this thread's channel
     auto stage_output = [&]() {
         if (warp >= 8) return;
         __nv_bfloat16 *os = reinterpret_cast<__nv_bfloat16 *>(sm + OFF_STG);
@@ -304,12 +305,11 @@ kda_chunk_tc_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_consta
             const float ms = ((red[r0 + lane] + red[64 + r0 + lane]) + (red[128 + r0 + lane] + red[192 + r0 + lane])) *
                              (1.f / D);
             const float rstd = rsqrtf(ms + a.norm_eps);
-            const float wj = a.norm_w ? a.norm_w[jl] : 1.f;
 #pragma unroll
             for (int c = 0; c < 32; ++c) {   // the logit sits where this thread writes its output
                 const float rs = __shfl_sync(0xffffffffu, rstd, c);
                 const float z = __bfloat162float(os[(r0 + c) * D + jl]);
-                v[c] *= rs * wj * __frcp_rn(1.f + __expf(-z));
+                v[c] *= rs * norm_wj * __fdividef(1.f, 1.f + __expf(-z));
             }
         }
 #pragma unroll

@@ -35,7 +35,7 @@ __global__ void __launch_bounds__(256) kda_gate_pass_kernel(T *out, const T *gat
 #pragma unroll
     for (int e = 0; e < PER; ++e) {
         const int j = lane + 32 * e;
-        const float gz = __frcp_rn(1.f + __expf(-to_f(z[j])));
+        const float gz = __fdividef(1.f, 1.f + __expf(-to_f(z[j])));
         o[j] = from_f<T>(x[e] * rstd * (w ? w[j] : 1.f) * gz);
     }
 }
