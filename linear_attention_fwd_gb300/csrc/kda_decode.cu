@@ -31,16 +31,18 @@ kda_recurrent_step_kernel(DecodeArgs a) {
     constexpr int RPT = DK / RG;               // rows per thread
     static_assert(RPT >= 1 && RG * RPT == DK, "tile split");
 
+    constexpr int TM = MULTI ? 8 : 1;          // tokens whose vectors are staged at once
+
     const int unit = blockIdx.x;
     const int n = unit / a.heads, h = unit - n * a.heads;
     const int slot = a.idx ? __ldg(a.idx + n) : n;
     if (slot < 0 || slot >= a.slots) return;   // uniform across the block
 
-    __shared__ float sq[DK], sk[DK], sa[DK], sv[DV], se[DV];
+    __shared__ float sq[TM][DK], sk[TM][DK], sa[TM][DK], sv[TM][DV], se[DV];
     __shared__ float red_v[RG][DV], red_p[RG][DV];
-    __shared__ float s_qk;
+    __shared__ float s_beta[TM], s_qk[TM];
 
-    const int t = threadIdx.x;
+    const int t = threadIdx.x, warp = t >> 5, lane = t & 31;
     const int cg = t % CG, rg = t / CG;
     float *S = a.state + ((int64_t)slot * a.heads + h) * (DK * DV);
     int ntok = MULTI ? a.ntok : 1;
@@ -57,65 +59,77 @@ kda_recurrent_step_kernel(DecodeArgs a) {
         s[m] = __ldcs(reinterpret_cast<const float4 *>(S + (rg * RPT + m) * DV) + cg);
 
 #pragma unroll 1
-    for (int tok = 0; tok < ntok; ++tok) {
-        const int64_t row = ((int64_t)n * a.ntok + tok) * a.heads + h;
-        const Tin *q = static_cast<const Tin *>(a.q) + row * DK;
-        const Tin *k = static_cast<const Tin *>(a.k) + row * DK;
-        const Tin *g = static_cast<const Tin *>(a.g) + row * DK;
-        const Tin *v = static_cast<const Tin *>(a.v) + row * DV;
-        for (int i = t; i < DK; i += kDecodeThreads) {
-            sq[i] = to_f(q[i]);
-            sk[i] = to_f(k[i]);
-            sa[i] = expf(to_f(g[i]));
+    for (int p0 = 0; p0 < ntok; p0 += TM) {
+        const int nt = ntok - p0 < TM ? ntok - p0 : TM;
+        if (p0 > 0) __syncthreads();   // the previous group's vectors are consumed
+        // this group's token vectors (alpha = e^g), loaded before any of its tokens runs
+        for (int x = t; x < nt * DK; x += kDecodeThreads) {
+            const int tk = x / DK, i = x - tk * DK;
+            const int64_t row = ((int64_t)n * a.ntok + p0 + tk) * a.heads + h;
+            sq[tk][i] = to_f(static_cast<const Tin *>(a.q)[row * DK + i]);
+            sk[tk][i] = to_f(static_cast<const Tin *>(a.k)[row * DK + i]);
+            sa[tk][i] = expf(to_f(static_cast<const Tin *>(a.g)[row * DK + i]));
         }
-        for (int j = t; j < DV; j += kDecodeThreads) sv[j] = to_f(v[j]);
-        const float beta = to_f(static_cast<const Tin *>(a.beta)[row]);
+        for (int x = t; x < nt * DV; x += kDecodeThreads) {
+            const int tk = x / DV, j = x - tk * DV;
+            const int64_t row = ((int64_t)n * a.ntok + p0 + tk) * a.heads + h;
+            sv[tk][j] = to_f(static_cast<const Tin *>(a.v)[row * DV + j]);
+        }
+        if (t < nt) {
+            const int64_t row = ((int64_t)n * a.ntok + p0 + t) * a.heads + h;
+            s_beta[t] = to_f(static_cast<const Tin *>(a.beta)[row]);
+        }
         __syncthreads();
-
-        if (t < 32) {  // k . q
+        if (warp < nt) {   // k . q of token `warp`
             float d = 0.f;
-            for (int i = t; i < DK; i += 32) d += sk[i] * sq[i];
+            for (int i = lane; i < DK; i += 32) d += sk[warp][i] * sq[warp][i];
 #pragma unroll
             for (int o = 16; o > 0; o >>= 1) d += __shfl_xor_sync(0xffffffffu, d, o);
-            if (t == 0) s_qk = d;
+            if (lane == 0) s_qk[warp] = d;
         }
 
-        float4 pv = make_float4(0.f, 0.f, 0.f, 0.f), pp = pv;
+#pragma unroll 1
+        for (int tk = 0; tk < nt; ++tk) {
+            const int64_t row = ((int64_t)n * a.ntok + p0 + tk) * a.heads + h;
+            float4 pv = make_float4(0.f, 0.f, 0.f, 0.f), pp = pv;
 #pragma unroll
-        for (int m = 0; m < RPT; ++m) {
-            const int i = rg * RPT + m;
-            const float ak = sa[i] * sk[i], aq = sa[i] * sq[i];
-            pv.x += ak * s[m].x; pv.y += ak * s[m].y; pv.z += ak * s[m].z; pv.w += ak * s[m].w;
-            pp.x += aq * s[m].x; pp.y += aq * s[m].y; pp.z += aq * s[m].z; pp.w += aq * s[m].w;
-        }
-        *reinterpret_cast<float4 *>(&red_v[rg][4 * cg]) = pv;
-        *reinterpret_cast<float4 *>(&red_p[rg][4 * cg]) = pp;
-        __syncthreads();
+            for (int m = 0; m < RPT; ++m) {
+                const int i = rg * RPT + m;
+                const float ak = sa[tk][i] * sk[tk][i], aq = sa[tk][i] * sq[tk][i];
+                pv.x += ak * s[m].x; pv.y += ak * s[m].y; pv.z += ak * s[m].z; pv.w += ak * s[m].w;
+                pp.x += aq * s[m].x; pp.y += aq * s[m].y; pp.z += aq * s[m].z; pp.w += aq * s[m].w;
+            }
+            *reinterpret_cast<float4 *>(&red_v[rg][4 * cg]) = pv;
+            *reinterpret_cast<float4 *>(&red_p[rg][4 * cg]) = pp;
+            __syncthreads();
 
-        Tin *out = (!MULTI || a.out) ? static_cast<Tin *>(a.out) + row * DV : nullptr;
-        for (int j = t; j < DV; j += kDecodeThreads) {
-            float vh = 0.f, p = 0.f;
+            const float beta = s_beta[tk];
+            Tin *out = (!MULTI || a.out) ? static_cast<Tin *>(a.out) + row * DV : nullptr;
+            for (int j = t; j < DV; j += kDecodeThreads) {
+                float vh = 0.f, p = 0.f;
 #pragma unroll
-            for (int r = 0; r < RG; ++r) { vh += red_v[r][j]; p += red_p[r][j]; }
-            const float e = sv[j] - vh;
-            se[j] = e;
-            if (!MULTI || out) out[j] = from_f<Tin>(p + beta * s_qk * e);
-        }
-        __syncthreads();
+                for (int r = 0; r < RG; ++r) { vh += red_v[r][j]; p += red_p[r][j]; }
+                const float e = sv[tk][j] - vh;
+                se[j] = e;
+                if (!MULTI || out) out[j] = from_f<Tin>(p + beta * s_qk[tk] * e);
+            }
+            __syncthreads();
 
-        const float4 e4 = *reinterpret_cast<const float4 *>(&se[4 * cg]);
-        const bool last = !MULTI || tok + 1 == ntok;
+            // the next token's partial sums are written only after its barrier, which every
+            // thread reaches after finishing this update
+            const float4 e4 = *reinterpret_cast<const float4 *>(&se[4 * cg]);
+            const bool last = !MULTI || p0 + tk + 1 == ntok;
 #pragma unroll
-        for (int m = 0; m < RPT; ++m) {
-            const int i = rg * RPT + m;
-            const float al = sa[i], bk = beta * sk[i];
-            s[m].x = al * s[m].x + bk * e4.x;
-            s[m].y = al * s[m].y + bk * e4.y;
-            s[m].z = al * s[m].z + bk * e4.z;
-            s[m].w = al * s[m].w + bk * e4.w;
-            if (last && (!MULTI || a.update)) __stcs(reinterpret_cast<float4 *>(S + i * DV) + cg, s[m]);
+            for (int m = 0; m < RPT; ++m) {
+                const int i = rg * RPT + m;
+                const float al = sa[tk][i], bk = beta * sk[tk][i];
+                s[m].x = al * s[m].x + bk * e4.x;
+                s[m].y = al * s[m].y + bk * e4.y;
+                s[m].z = al * s[m].z + bk * e4.z;
+                s[m].w = al * s[m].w + bk * e4.w;
+                if (last && (!MULTI || a.update)) __stcs(reinterpret_cast<float4 *>(S + i * DV) + cg, s[m]);
+            }
         }
-        if (!last) __syncthreads();   // the shared vectors are rewritten by the next token
     }
 }
 
