@@ -66,6 +66,24 @@ def test_steps_equal_single_steps_bit_for_bit(K, dtype, d):
         assert torch.all(o_multi[n, m[n]:] == 0)
 
 
+@pytest.mark.parametrize("T", [8, 11, 17])
+def test_steps_past_one_staging_group(K, T):
+    """More draft tokens than the kernel stages at once (8): the groups chain through the
+    on-chip state exactly like single steps, including a ragged last group."""
+    dtype, d, N, H, P = torch.bfloat16, 128, 4, 2, 5
+    a = _draft(T, N, H, d, dtype, seed=61 + T)
+    idx = torch.tensor([2, 4, 0, 1], dtype=torch.int32, device="cuda")
+    m = [T, T - 3, 9 if T > 9 else T, 1]
+    num = torch.tensor(m, dtype=torch.int32, device="cuda")
+    s_multi = inputs.make_decode_state(num_slots=P, heads=H, dk=d, dv=d, device="cuda", seed=62)
+    s_single = s_multi.clone()
+    o_multi = K.kda_recurrent_steps(a["q"], a["k"], a["v"], a["g"], a["beta"], s_multi, idx, num)
+    o_single = _single_steps(K, a, s_single, idx, m)
+    torch.cuda.synchronize()
+    torch.testing.assert_close(s_multi, s_single, rtol=0, atol=0)
+    torch.testing.assert_close(o_multi, o_single, rtol=0, atol=0)
+
+
 def test_verify_leaves_the_state_and_replay_matches_the_oracle(K):
     """Speculative decoding: verify all T draft tokens (state untouched), then replay each
     row's accepted prefix into the state (no outputs)."""
