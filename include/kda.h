@@ -112,6 +112,20 @@ kda_status_t kda_chunk_fwd_with(kda_impl_t impl,
                                 void *out, float *final_state,
                                 const kda_dims_t *dims, cudaStream_t stream);
 
+/* As kda_chunk_fwd_with, with an explicit bound on every device-side wait of the tensor-core
+ * kernel (copy and tensor-core completions): `wait_polls` polls of at most about a microsecond
+ * each (kda_chunk_fwd uses 2^20).  When a wait gives up, the CTA stops, lets its copies and
+ * tensor-core work in flight land (bounded separately, a few milliseconds), writes NaN to its
+ * (sequence, head) final state and leaves the context usable; outputs of that unit are then
+ * unspecified.  wait_polls = 0 makes every wait give up at once: a test of that path.  The SIMT
+ * kernel has no such waits and ignores the bound. */
+kda_status_t kda_chunk_fwd_bounded(kda_impl_t impl,
+                                   const void *q, const void *k, const void *v,
+                                   const void *g, const void *beta,
+                                   const float *initial_state, const int32_t *cu_seqlens,
+                                   void *out, float *final_state, uint32_t wait_polls,
+                                   const kda_dims_t *dims, cudaStream_t stream);
+
 /* kda_chunk_fwd_checkpointed -- kda_chunk_fwd that also writes the recurrent state at every
  * multiple of `checkpoint_interval` tokens strictly inside each sequence, for prefix caching.
  * The pages' account: the cache hashes prompts in 512-token units and keeps recurrent-state

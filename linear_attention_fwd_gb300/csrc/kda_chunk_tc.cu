@@ -854,13 +854,20 @@ kda_chunk_tc_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_consta
         }
     }
     if (!ok) {
-        // A bounded wait expired: let copies and MMAs in flight land (bounded
-        // again), flag the failure and mark this unit's final state invalid.
+        // A bounded wait expired: let copies and MMAs in flight land, flag the failure and mark
+        // this unit's final state invalid.  At most one phase of each barrier can be in flight
+        // (nothing is issued again on a barrier before its last phase was waited for), and it
+        // is either the phase the parity names or the one before it: wait for both, with a
+        // bound of its own (a few milliseconds) that does not depend on the expired one.
         if (tid == 0) {
-            mbar_wait(bar_o, ph_o, wait_limit);
-            mbar_wait(bar_tma, ph_tma, wait_limit);
-            mbar_wait(bar_v, ph_v, wait_limit);
-            if (a.gate) mbar_wait(bar_z, ph_z, wait_limit);
+            constexpr uint32_t drain = 1u << 12;
+            const uint32_t bars[7] = {bar_tma, bar_p, bar_v, bar_u, bar_s, bar_o, bar_z};
+            const uint32_t phs[7] = {ph_tma, ph_p, ph_v, ph_u, ph_s, ph_o, ph_z};
+#pragma unroll
+            for (int b = 0; b < 7; ++b) {
+                mbar_wait(bars[b], phs[b], drain);
+                mbar_wait(bars[b], phs[b] ^ 1u, drain);
+            }
             atomicAdd(&g_kda_tc_timeouts, 1u);
         }
         __syncthreads();
@@ -942,7 +949,7 @@ cudaError_t launch_chunk_tc(const ChunkArgs &a, int dk, int dv, kda_dtype_t dt, 
     if (e != cudaSuccess) return e;
     const int64_t units = (int64_t)a.num_seqs * a.heads;
     if (units > 0x7fffffffLL) return cudaErrorInvalidValue;
-    kda_chunk_tc_kernel<<<(unsigned)units, NT, SMEM_BYTES, st>>>(mq, mk, mv, mg, mz, a, 1u << 20);
+    kda_chunk_tc_kernel<<<(unsigned)units, NT, SMEM_BYTES, st>>>(mq, mk, mv, mg, mz, a, a.wait_polls);
     return cudaGetLastError();
 }
 

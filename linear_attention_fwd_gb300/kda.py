@@ -22,7 +22,7 @@ IMPLS = {"auto": 0, "simt": 1, "tc": 2}
 IMPL_NAMES = {v: k for k, v in IMPLS.items()}
 
 # every symbol include/kda.h declares
-EXPORTED = ("kda_chunk_fwd", "kda_chunk_fwd_with", "kda_chunk_fwd_checkpointed",
+EXPORTED = ("kda_chunk_fwd", "kda_chunk_fwd_with", "kda_chunk_fwd_bounded", "kda_chunk_fwd_checkpointed",
             "kda_chunk_fwd_gated", "kda_chunk_fwd_selected_impl", "kda_recurrent_step",
             "kda_recurrent_steps", "kda_status_string")
 
@@ -55,6 +55,8 @@ def lib() -> ctypes.CDLL:
         L.kda_chunk_fwd.argtypes = [vp] * 9 + [dp, vp]
         L.kda_chunk_fwd_with.restype = ctypes.c_int
         L.kda_chunk_fwd_with.argtypes = [ctypes.c_int] + [vp] * 9 + [dp, vp]
+        L.kda_chunk_fwd_bounded.restype = ctypes.c_int
+        L.kda_chunk_fwd_bounded.argtypes = [ctypes.c_int] + [vp] * 9 + [ctypes.c_uint32, dp, vp]
         L.kda_chunk_fwd_checkpointed.restype = ctypes.c_int
         L.kda_chunk_fwd_checkpointed.argtypes = [vp] * 11 + [ctypes.c_int32, dp, vp]
         L.kda_chunk_fwd_gated.restype = ctypes.c_int
@@ -113,13 +115,15 @@ def chunk_dims(q, v, cu_seqlens=None) -> KdaDims:
 
 def kda_chunk_fwd(q, k, v, g, beta, initial_state=None, cu_seqlens=None, *, out=None,
                   final_state=None, output_final_state: bool = True, impl: str = "auto",
-                  stream=None):
+                  stream=None, wait_polls: int | None = None):
     """Chunkwise KDA forward (prefill / prefix-cache resume) through libkda.
 
     q, k, g: [B, T, H, dk]; v: [B, T, H, dv]; beta: [B, T, H] (all fp32 or all
     bf16, CUDA, contiguous).  initial_state: fp32 [N, H, dk, dv] or None.
     cu_seqlens: int32 [N+1] (packed sequences, B == 1) or None.
     Returns (out [B, T, H, dv], final_state [N, H, dk, dv] fp32 or None).
+    wait_polls: bound on each device wait of the tensor-core kernel (kda_chunk_fwd_bounded);
+    a unit whose wait gives up gets a NaN final state.
     """
     dev = q.device
     for name, t in (("q", q), ("k", k), ("v", v), ("g", g), ("beta", beta)):
@@ -138,9 +142,13 @@ def kda_chunk_fwd(q, k, v, g, beta, initial_state=None, cu_seqlens=None, *, out=
     if final_state is None and output_final_state:
         final_state = torch.empty((dims.num_seqs, H, dk, dv), dtype=torch.float32, device=dev)
     _check_dev("final_state", final_state, dev, torch.float32)
-    st = lib().kda_chunk_fwd_with(IMPLS[impl], _ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta),
-                                  _ptr(initial_state), _ptr(cu_seqlens), _ptr(out),
-                                  _ptr(final_state), ctypes.byref(dims), _stream_handle(stream))
+    args = (_ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta), _ptr(initial_state),
+            _ptr(cu_seqlens), _ptr(out), _ptr(final_state))
+    if wait_polls is None:
+        st = lib().kda_chunk_fwd_with(IMPLS[impl], *args, ctypes.byref(dims), _stream_handle(stream))
+    else:
+        st = lib().kda_chunk_fwd_bounded(IMPLS[impl], *args, ctypes.c_uint32(int(wait_polls)),
+                                         ctypes.byref(dims), _stream_handle(stream))
     if st != KDA_OK:
         raise KdaError(st, "kda_chunk_fwd")
     return out, final_state
