@@ -17,7 +17,8 @@
 //   U = T diag(beta) (V - Kbar S),  O = Qbar S + M U,  S <- Diag(e^{gamma_last}) S + Kp^T U.
 //
 // Operand precision: the sub-tile-scaled operands of A and M span
-// [e^-80, e^80] and are bf16 (the range the decay bound was chosen for); every
+// [e^-80, e^80] and are bf16 (the range the decay bound was chosen for; Q~ as hi + lo
+// for the diagonal blocks of M, whose diagonal itself is the exact q_r . k_r); every
 // other tensor-core operand (S, Z = diag(beta)(V - Kbar S), T, U, Qbar, Kbar, Kp, M)
 // is O(1) and is rounded to fp16 for 3 more mantissa bits, Z, U and M as hi + lo
 // pairs where one rounding would show in the outputs; accumulation is fp32 throughout.
