@@ -49,6 +49,26 @@ def dist_env():
     return ws, rank, local
 
 
+def rank_ops(ws, device):
+    """The timing contract's cross-rank steps for an initialised process group (any backend):
+    a barrier, and the maximum of a per-rank value over all ranks."""
+    import torch
+    import torch.distributed as dist
+
+    def barrier():
+        if ws > 1:
+            dist.barrier()
+
+    def max_over_ranks(x):
+        if ws == 1:
+            return x
+        t = torch.tensor([x], dtype=torch.float64, device=device)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        return float(t.item())
+
+    return barrier, max_over_ranks
+
+
 def peaks():
     p = os.path.join(ROOT, "MEASURED_PEAKS.json")
     if os.path.exists(p):
@@ -240,17 +260,7 @@ def run_ours(args):
     dev = torch.device("cuda", local)
     if ws > 1:
         dist.init_process_group("nccl", device_id=dev)
-
-    def barrier():
-        if ws > 1:
-            dist.barrier()
-
-    def max_over_ranks(x):
-        if ws == 1:
-            return x
-        t = torch.tensor([x], dtype=torch.float64, device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        return float(t.item())
+    barrier, max_over_ranks = rank_ops(ws, dev)
 
     P = peaks()
     w = inputs.WORKLOADS[args.workload]
