@@ -72,7 +72,8 @@ constexpr uint32_t OFF_G = 49152;      // G (bf16)                 [64 r][128 i]
 constexpr uint32_t OFF_SST = 65536;    // Q~hi, K~ (bf16)          2 x [64 r][128 i]
 constexpr uint32_t OFF_UST = 98304;    // Q~lo (bf16)              [64 r][128 i]
 constexpr uint32_t OFF_NI = 114688;    // -I (bf16, constant)      [64 s][64 r]
-                                       // (bytes 122880..131071 are unused)
+constexpr uint32_t OFF_RED = 122880;   // gated output: row sums of squares [4][64] fp32
+                                       // (bytes 123904..131071 are unused)
 constexpr uint32_t OFF_KPT = 131072;   // Kp^T fp16                [128 i][64 r]
 constexpr uint32_t OFF_MT = 147456;    // M fp16                   [64 r][64 s]
 constexpr uint32_t OFF_TT = 155648;    // A_IJ (I > J) fp16        [64 r][64 s]
@@ -300,7 +301,7 @@ kda_chunk_tc_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_consta
                     w[i] = keep + __shfl_xor_sync(0xffffffffu, send, sft);
                 }
             }
-            float *red = reinterpret_cast<float *>(sm + OFF_EB);   // [4 channel quarters][64 rows]
+            float *red = reinterpret_cast<float *>(sm + OFF_RED);   // [4 channel quarters][64 rows]
             red[(warp & 3) * 64 + r0 + lane] = w[0];
             named_bar(5 + (warp >> 2), 128);   // the four quarters of these 32 rows
             const float ms = ((red[r0 + lane] + red[64 + r0 + lane]) + (red[128 + r0 + lane] + red[192 + r0 + lane])) *
@@ -399,20 +400,22 @@ kda_chunk_tc_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_consta
             for (int e = 0; e < 2; ++e)
                 if (2 * t4 + e == g) MRR[16 * I + g + 8 * hh] = acc[hh][2 * hh + e];
     };
-    // per-channel decay vectors of that chunk (log2 units); thread: channel c, sub-tile I
+    // per-channel decay vectors of that chunk (log2 units), by warps 12-15: thread = channel
     auto vectors = [&]() {
-        const int c = tid & 127, I = tid >> 7;
+        const int c = tid & 127;
         float t[4];
 #pragma unroll
         for (int J = 0; J < 4; ++J) t[J] = PART[(2 * J) * 128 + c] + PART[(2 * J + 1) * 128 + c];
         const float bI[4] = {0.f, t[0], t[0] + t[1], t[0] + t[1] + t[2]};
         const float gl = bI[3] + t[3];
-        EB[I * 128 + c] = ex2(bI[I]);
-        EL[I * 128 + c] = ex2(gl - bI[I]);
 #pragma unroll
-        for (int J = 0; J < 3; ++J)
-            if (J < I) W6[pair_index(I, J) * 128 + c] = __float2bfloat16_rn(ex2(bI[I] - bI[J]));
-        if (I == 0) DEC[c] = ex2(gl);
+        for (int I = 0; I < 4; ++I) {
+            EB[I * 128 + c] = ex2(bI[I]);
+            EL[I * 128 + c] = ex2(gl - bI[I]);
+#pragma unroll
+            for (int J = 0; J < I; ++J) W6[pair_index(I, J) * 128 + c] = __float2bfloat16_rn(ex2(bI[I] - bI[J]));
+        }
+        DEC[c] = ex2(gl);
     };
 #pragma unroll 1
     for (int ci = 0; ci < nchunks; ++ci) {
@@ -425,9 +428,11 @@ kda_chunk_tc_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_consta
         ph_tma ^= 1;
         // ---- (1) warps 0-7: decay sums, then the previous chunk's output staged; warps 8-11:
         // q_r . k_r; warps 8-15: once the previous state update has landed, S^T -> fp16 pairs
-        // (the MMA operand of this chunk), 64 key channels per warp
+        // (the MMA operand of this chunk), 64 key channels per warp; then warps 12-15: the
+        // decay vectors from the sums
         if (warp < 8) {
             prephase(nr);
+            named_bar_arrive(2, 384);   // the sums are in place for warps 12-15
             if (out_pending) {   // the previous chunk's output, once its groups landed
                 got = mbar_wait(bar_s, ph_s, wait_limit) && mbar_wait(bar_o, ph_o, wait_limit) && got;
                 if (a.gate) got = mbar_wait(bar_z, ph_z, wait_limit) && got;
@@ -461,18 +466,18 @@ kda_chunk_tc_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_consta
                 tmem_st16u(trow + TM_S16 + i0 / 2 + 16, hw);
                 tmem_wait_st();
             }
+            if (warp >= 12) {
+                named_bar(2, 384);
+                vectors();
+            }
         }
         if (out_pending) ph_s ^= 1;
         tc_fence_before();
         if (__syncthreads_or(!got)) { ok = false; break; }
         tc_fence_after();
-        vectors();
         if (out_pending) {
             ph_o ^= 1;
             if (a.gate) ph_z ^= 1;
-        }
-        __syncthreads();
-        if (out_pending) {
             store_output();
             out_pending = false;
         }
