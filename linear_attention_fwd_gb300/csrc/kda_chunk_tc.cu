@@ -743,26 +743,6 @@ kda_chunk_tc_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_consta
             tmem_st16u(trow + TM_Z + s0 / 2, zv);
             tmem_st16u(trow + TM_ZL + s0 / 2, zl);
             tmem_wait_st();
-        } else if (warp >= 12) {   // S^T <- S^T Diag(dec) in place (S^T was read as fp16 in (1))
-#pragma unroll 1
-            for (int i0 = 0; i0 < 128; i0 += 64) {
-                float v[32], w[32];
-                tmem_ld32x2(trow + TM_S + i0, trow + TM_S + i0 + 32, v, w);
-#pragma unroll
-                for (int c = 0; c < 32; c += 4) {
-                    const float4 d4 = *reinterpret_cast<const float4 *>(DEC + i0 + c);
-                    const float4 e4 = *reinterpret_cast<const float4 *>(DEC + i0 + 32 + c);
-                    const float2 a2 = __fmul2_rn(make_float2(v[c], v[c + 1]), make_float2(d4.x, d4.y));
-                    const float2 b2 = __fmul2_rn(make_float2(v[c + 2], v[c + 3]), make_float2(d4.z, d4.w));
-                    const float2 c2 = __fmul2_rn(make_float2(w[c], w[c + 1]), make_float2(e4.x, e4.y));
-                    const float2 f2 = __fmul2_rn(make_float2(w[c + 2], w[c + 3]), make_float2(e4.z, e4.w));
-                    v[c] = a2.x; v[c + 1] = a2.y; v[c + 2] = b2.x; v[c + 3] = b2.y;
-                    w[c] = c2.x; w[c + 1] = c2.y; w[c + 2] = f2.x; w[c + 3] = f2.y;
-                }
-                tmem_st32(trow + TM_S + i0, v);
-                tmem_st32(trow + TM_S + i0 + 32, w);
-            }
-            tmem_wait_st();
         }
         ph_p ^= 1;
         ph_v ^= 1;
@@ -784,6 +764,21 @@ kda_chunk_tc_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_consta
             for (int k = 0; k < 4; ++k)
                 mma_f16_ts(tmem + TM_U, tmem + TM_Z + 8 * k, dsm + ((OFF_T + k * 32) >> 4), IDESC_N64, k > 0);
             mma_commit(bar_u);
+        }
+        {   // while the U^T groups run: S^T <- S^T Diag(dec) in place (S^T was read as fp16 in
+            // (1)); warp w: lanes 32(w%4).., 32 columns from 32(w/4)
+            const int i0 = 32 * quarter;
+            float v[32];
+            tmem_ld32(trow + TM_S + i0, v);
+#pragma unroll
+            for (int c = 0; c < 32; c += 4) {
+                const float4 d4 = *reinterpret_cast<const float4 *>(DEC + i0 + c);
+                const float2 a2 = __fmul2_rn(make_float2(v[c], v[c + 1]), make_float2(d4.x, d4.y));
+                const float2 b2 = __fmul2_rn(make_float2(v[c + 2], v[c + 3]), make_float2(d4.z, d4.w));
+                v[c] = a2.x; v[c + 1] = a2.y; v[c + 2] = b2.x; v[c + 3] = b2.y;
+            }
+            tmem_st32(trow + TM_S + i0, v);
+            tmem_wait_st();
         }
         {
             const bool got = mbar_wait(bar_u, ph_u, wait_limit);
