@@ -126,6 +126,32 @@ kda_status_t kda_chunk_fwd_bounded(kda_impl_t impl,
                                    void *out, float *final_state, uint32_t wait_polls,
                                    const kda_dims_t *dims, cudaStream_t stream);
 
+/* kda_chunk_fwd_segmented -- kda_chunk_fwd_with and an explicit number of CTAs per
+ * (sequence, head) for the tensor-core kernel (segment parallelism within a sequence on one
+ * GPU).  The pages split a sequence over devices by giving each segment a zero-start state
+ * and a cumulative transition, composed by a prefix scan ("請求書はサービング側に回ってくる",
+ * orkas.ai, the paragraph on splitting a sequence over devices; "学習基盤", xitter.cf/solis).
+ * Here the transition is never formed: segment p of P stores the outputs of chunks
+ * [p*nc/P, (p+1)*nc/P) (nc = the sequence's 64-token chunks) and starts from a zero state at
+ * the latest chunk boundary, at most 16 chunks earlier, past which the product of the per-token
+ * bounds max_i exp(g_t,i) * max(1, |1 - beta_t |k_t|^2|) on the transitions' 2-norm is at most
+ * 2^-160 (the state it drops contributes less than 2^-160 of its own norm), or else from the
+ * start of the sequence with its initial state.  The last segment writes the final state.
+ *   segments : 0 = the library's choice (what kda_chunk_fwd does: enough segments to occupy
+ *              every SM when there are fewer (sequence, head) units than SMs, each of at least
+ *              16 chunks on average; 1 with an output gate, checkpoints or an in-place state),
+ *              1..64 = that many.
+ * Errors: KDA_ERR_SHAPE for segments outside [0, 64]; KDA_ERR_UNSUPPORTED for segments > 1
+ * with initial_state == final_state (a later segment would overwrite the state an earlier one
+ * may still read).  The SIMT kernel always runs one CTA per unit.  When a bounded wait gives up
+ * in a segment other than the last, that segment's outputs are set to NaN. */
+kda_status_t kda_chunk_fwd_segmented(kda_impl_t impl,
+                                     const void *q, const void *k, const void *v,
+                                     const void *g, const void *beta,
+                                     const float *initial_state, const int32_t *cu_seqlens,
+                                     void *out, float *final_state, int32_t segments,
+                                     const kda_dims_t *dims, cudaStream_t stream);
+
 /* kda_chunk_fwd_checkpointed -- kda_chunk_fwd that also writes the recurrent state at every
  * multiple of `checkpoint_interval` tokens strictly inside each sequence, for prefix caching.
  * The pages' account: the cache hashes prompts in 512-token units and keeps recurrent-state

@@ -71,13 +71,14 @@ static kda_status_t chunk_run(kda_impl_t impl, const void *q, const void *k, con
                        const void *beta, const float *initial_state, const int32_t *cu_seqlens,
                        void *out, float *final_state, float *ckpt, const int32_t *ckpt_off,
                        int32_t ckpt_interval, const void *gate, const float *norm_w, float norm_eps,
-                       const kda_dims_t *d, cudaStream_t stream, uint32_t wait_polls = 1u << 20) {
+                       const kda_dims_t *d, cudaStream_t stream, uint32_t wait_polls = 1u << 20,
+                       int32_t segments = 0) {
     kda_status_t st = check_chunk(impl, q, k, v, g, beta, initial_state, cu_seqlens, out,
                                   final_state, d);
     if (st != KDA_OK) return st;
     kda::ChunkArgs a{q, k, v, g, beta, initial_state, cu_seqlens, out, final_state,
                      (int64_t)d->seqlen, d->num_seqs, d->heads, gate, norm_w, norm_eps,
-                     ckpt, ckpt_off, ckpt_interval, wait_polls};
+                     ckpt, ckpt_off, ckpt_interval, wait_polls, segments};
     cudaError_t e;
     if ((int64_t)d->batch * d->seqlen == 0) {
         if (final_state == nullptr || final_state == initial_state) return KDA_OK;
@@ -141,6 +142,18 @@ extern "C" kda_status_t kda_chunk_fwd_bounded(kda_impl_t impl, const void *q, co
                                               const kda_dims_t *d, cudaStream_t stream) {
     return chunk_run(impl, q, k, v, g, beta, initial_state, cu_seqlens, out, final_state, nullptr,
                      nullptr, 0, nullptr, nullptr, 0.f, d, stream, wait_polls);
+}
+
+extern "C" kda_status_t kda_chunk_fwd_segmented(kda_impl_t impl, const void *q, const void *k,
+                                                const void *v, const void *g, const void *beta,
+                                                const float *initial_state,
+                                                const int32_t *cu_seqlens, void *out,
+                                                float *final_state, int32_t segments,
+                                                const kda_dims_t *d, cudaStream_t stream) {
+    if (segments < 0 || segments > 64) return KDA_ERR_SHAPE;
+    if (segments > 1 && initial_state && initial_state == final_state) return KDA_ERR_UNSUPPORTED;
+    return chunk_run(impl, q, k, v, g, beta, initial_state, cu_seqlens, out, final_state, nullptr,
+                     nullptr, 0, nullptr, nullptr, 0.f, d, stream, 1u << 20, segments);
 }
 
 extern "C" kda_status_t kda_chunk_fwd(const void *q, const void *k, const void *v, const void *g,

@@ -161,6 +161,65 @@ __device__ __forceinline__ void select_unit(const ChunkArgs &a, int b, int &n, i
     n = s_pick;
 }
 
+// Segments of one sequence on several CTAs.  The state a zero state reaches from chunk
+// boundary c_run differs from the true state at a later boundary c_lo by the true state at
+// c_run carried through the transitions in between, whose product has a 2-norm of at most
+// prod_t max_i e^{g_t,i} * max(1, |1 - beta_t |k_t|^2|)  (||Diag(e^g)|| = max_i e^{g_i}, and
+// I - beta k k^T has the eigenvalues 1 and 1 - beta |k|^2).  A CTA that stores the outputs of
+// chunks [c_lo, c_hi) therefore starts from a zero state at the latest boundary at most
+// kMaxWarmChunks chunks before c_lo where that bound has fallen to 2^-kHorizonLog2 (far below
+// fp32 resolution), or else at the start of the sequence with its initial state (exact).
+constexpr float kHorizonLog2 = 160.f;
+constexpr int kMaxWarmChunks = 16;
+
+// The chunk boundary c_run <= c_lo described above (block-wide; every thread returns the
+// same value).  Chunks before c_lo are whole chunks of the sequence.
+__device__ int warm_start(const ChunkArgs &a, int64_t bos, int h, int c_lo) {
+    __shared__ float s_part[NT / 32];
+    const int H = a.heads;
+    const __nv_bfloat16 *gq = static_cast<const __nv_bfloat16 *>(a.g);
+    const __nv_bfloat16 *kq = static_cast<const __nv_bfloat16 *>(a.k);
+    const __nv_bfloat16 *bq = static_cast<const __nv_bfloat16 *>(a.beta);
+    const int tid = threadIdx.x, r = tid >> 3, part = tid & 7;   // 8 threads per token row
+    const int c_min = c_lo > kMaxWarmChunks ? c_lo - kMaxWarmChunks : 0;
+    float acc = 0.f;   // log2 of the norm bound from chunk c to c_lo
+    for (int c = c_lo - 1; c >= c_min; --c) {
+        const int64_t tok = bos + (int64_t)c * C + r;
+        const uint4 *gp = reinterpret_cast<const uint4 *>(gq + (tok * H + h) * D + 16 * part);
+        const uint4 *kp = reinterpret_cast<const uint4 *>(kq + (tok * H + h) * D + 16 * part);
+        float gm = -3.0e38f, ks = 0.f;
+#pragma unroll
+        for (int u = 0; u < 2; ++u) {
+            const uint4 gv = __ldg(gp + u), kv = __ldg(kp + u);
+            const uint32_t gw[4] = {gv.x, gv.y, gv.z, gv.w}, kw[4] = {kv.x, kv.y, kv.z, kv.w};
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+                const float2 g2 = unpack_bf16(gw[e]), k2 = unpack_bf16(kw[e]);
+                gm = fmaxf(gm, fmaxf(g2.x, g2.y));
+                ks = fmaf(k2.x, k2.x, fmaf(k2.y, k2.y, ks));
+            }
+        }
+#pragma unroll
+        for (int o = 1; o < 8; o <<= 1) {
+            gm = fmaxf(gm, __shfl_xor_sync(0xffffffffu, gm, o));
+            ks += __shfl_xor_sync(0xffffffffu, ks, o);
+        }
+        const float amp = fabsf(1.f - __bfloat162float(bq[tok * H + h]) * ks);
+        float lam = gm * LOG2E + (amp > 1.f ? __log2f(amp) : 0.f);   // this token's bound, log2
+        lam += __shfl_xor_sync(0xffffffffu, lam, 8);    // the warp's 4 rows
+        lam += __shfl_xor_sync(0xffffffffu, lam, 16);
+        if ((tid & 31) == 0) s_part[tid >> 5] = lam;
+        __syncthreads();
+        float tot = 0.f;
+#pragma unroll
+        for (int w = 0; w < NT / 32; ++w) tot += s_part[w];
+        __syncthreads();
+        acc += tot;
+        if (acc <= -kHorizonLog2) return c;
+    }
+    return 0;
+}
+
 __device__ __forceinline__ void tma_tile(const CUtensorMap *map, uint32_t dst, uint32_t bar, int h,
                                          int64_t tok, uint32_t half_stride = 8192) {
     tma_load_3d(dst, map, bar, 0, h, (int)tok);
@@ -178,12 +237,23 @@ kda_chunk_tc_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_consta
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int H = a.heads;
 
+    // blockIdx.x = p * units + unit: segment p of P of one (sequence, head); this CTA stores
+    // the outputs of chunks [c_lo, c_hi), running from chunk c_run (see warm_start), and the
+    // last segment writes the final state
+    const int P = a.segments > 1 ? a.segments : 1;
+    const int64_t units = (int64_t)a.num_seqs * H;
     int n, h;
-    select_unit(a, blockIdx.x, n, h);
+    select_unit(a, (int)(blockIdx.x % units), n, h);
+    const int p = (int)(blockIdx.x / units);
     int64_t bos, eos;
     seq_range(a, n, bos, eos);
     const int64_t len = eos - bos;
     const int nchunks = (int)((len + C - 1) / C);
+    const int c_lo = (int)((int64_t)p * nchunks / P), c_hi = (int)((int64_t)(p + 1) * nchunks / P);
+    const bool last_seg = p == P - 1;
+    if (c_lo == c_hi && !last_seg) return;   // an empty segment (whole CTA, before any setup)
+    const int c_run = c_lo > 0 ? warm_start(a, bos, h, c_lo) : 0;
+    const int64_t t_run = bos + (int64_t)c_run * C;
 
     // mbarriers: Q, K, G tiles landed; [O^T | P^T] done; V tile landed; U^T done; state (and
     // O^T high-order) update done; O^T low-order terms done
@@ -237,19 +307,19 @@ kda_chunk_tc_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_consta
         float v[32];
 #pragma unroll
         for (int c = 0; c < 32; ++c)
-            v[c] = a.s0 ? a.s0[sbase + (int64_t)(32 * quarter + c) * D + jl] : 0.f;
+            v[c] = (a.s0 && c_run == 0) ? a.s0[sbase + (int64_t)(32 * quarter + c) * D + jl] : 0.f;
         tmem_st32(trow + TM_S + 32 * quarter, v);
         tmem_wait_st();
     }
-    if (tid == 0 && nchunks > 0) {
+    if (tid == 0 && c_run < c_hi) {
         mbar_arrive_expect_tx(bar_tma, 3 * 16384);
-        tma_tile(&tmq, sb + OFF_Q, bar_tma, h, bos, 16384);
-        tma_tile(&tmk, sb + OFF_K, bar_tma, h, bos, 16384);
-        tma_tile(&tmg, sb + OFF_G, bar_tma, h, bos);
+        tma_tile(&tmq, sb + OFF_Q, bar_tma, h, t_run, 16384);
+        tma_tile(&tmk, sb + OFF_K, bar_tma, h, t_run, 16384);
+        tma_tile(&tmg, sb + OFF_G, bar_tma, h, t_run);
         mbar_arrive_expect_tx(bar_v, 16384);
-        tma_tile(&tmv, sb + OFF_V, bar_v, h, bos);
+        tma_tile(&tmv, sb + OFF_V, bar_v, h, t_run);
     }
-    if (tid < C) BETA[tid] = tid < len ? __bfloat162float(beta[(bos + tid) * H + h]) : 0.f;
+    if (tid < C) BETA[tid] = tid < len - (int64_t)c_run * C ? __bfloat162float(beta[(t_run + tid) * H + h]) : 0.f;
     for (int x = tid; x < 64 * 32; x += NT) {   // -I: subtracts V^T from P^T inside the MMA
         const int r = x >> 5, s2 = 2 * (x & 31);
         *reinterpret_cast<uint32_t *>(sm + OFF_NI + sw(r, s2, 64)) =
@@ -418,12 +488,12 @@ kda_chunk_tc_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_consta
         DEC[c] = ex2(gl);
     };
 #pragma unroll 1
-    for (int ci = 0; ci < nchunks; ++ci) {
+    for (int ci = c_run; ci < c_hi; ++ci) {
         const int64_t t0 = bos + (int64_t)ci * C;
         const int nr = (int)(len - (int64_t)ci * C < C ? len - (int64_t)ci * C : C);
-        const bool more = ci + 1 < nchunks;
+        const bool more = ci + 1 < c_hi;
 
-        if (ci > 0 && tid < C) BETA[tid] = BETA[tid + (OFF_BNEXT - OFF_BETA) / 4];   // loaded during the previous chunk
+        if (ci > c_run && tid < C) BETA[tid] = BETA[tid + (OFF_BNEXT - OFF_BETA) / 4];   // loaded during the previous chunk
         bool got = mbar_wait(bar_tma, ph_tma, wait_limit);   // checked at the next barrier
         ph_tma ^= 1;
         // ---- (1) warps 0-7: decay sums, then the previous chunk's output staged; warps 8-11:
@@ -443,7 +513,7 @@ kda_chunk_tc_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_consta
             if (warp < 12) diag_qk();
             if (out_pending) got = mbar_wait(bar_s, ph_s, wait_limit) && got;
             tc_fence_after();
-            const int64_t cs = ckpt_slot(a, n, (int64_t)ci * C);   // the state after ci chunks
+            const int64_t cs = ci >= c_lo ? ckpt_slot(a, n, (int64_t)ci * C) : -1;   // the state after ci chunks
             float *ck = cs >= 0 ? a.ckpt + (cs * H + h) * D * D + jl : nullptr;
             {
                 const int i0 = 64 * ((warp - 8) >> 2);
@@ -835,7 +905,7 @@ kda_chunk_tc_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_consta
         }
         out_pending = true;
         t0_out = t0;
-        nr_out = nr;
+        nr_out = ci >= c_lo ? nr : 0;   // the warm-up chunks before c_lo store nothing
     }
 
     if (ok && out_pending) {   // the last chunk's state update and output
@@ -871,10 +941,15 @@ kda_chunk_tc_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_consta
             }
             atomicAdd(&g_kda_tc_timeouts, 1u);
         }
+        if (P > 1) {   // only the last segment writes the state: mark this segment's outputs
+            const int64_t r0 = (int64_t)c_lo * C, r1 = (int64_t)c_hi * C < len ? (int64_t)c_hi * C : len;
+            for (int64_t x = tid; x < (r1 - r0) * D; x += NT)
+                out[((bos + r0 + x / D) * H + h) * D + x % D] = __ushort_as_bfloat16((unsigned short)0x7fc0);
+        }
         __syncthreads();
     }
     tc_fence_after();
-    if (a.sT) {
+    if (a.sT && last_seg) {
         float v[32];
         tmem_ld32(trow + TM_S + 32 * quarter, v);
 #pragma unroll
@@ -932,13 +1007,34 @@ bool make_map_rows(CUtensorMap *m, const void *ptr, int64_t tokens, int H) {
 
 }  // namespace
 
+// Segments per (sequence, head) when the caller leaves the choice to the library: enough to
+// put every SM to work when there are fewer units than SMs, with segments of at least
+// kMinSegChunks chunks on average; one when the launch writes checkpoints or applies the
+// output gate, or reads and writes the state in place (the last segment would write the
+// state while another may still read it).
+static int auto_segments(const ChunkArgs &a, int64_t units, int64_t tokens) {
+    constexpr int kMaxSegments = 8, kMinSegChunks = 16;
+    if (a.gate || a.ckpt || (a.s0 && a.s0 == a.sT) || units <= 0) return 1;
+    int dev = 0, sms = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+        return 1;
+    int64_t P = sms / units;
+    if (P > kMaxSegments) P = kMaxSegments;
+    const int64_t avg_chunks = tokens / ((int64_t)a.num_seqs * C);
+    while (P > 1 && avg_chunks < (int64_t)kMinSegChunks * P) --P;
+    return P < 1 ? 1 : (int)P;
+}
+
 bool chunk_tc_supported(int dk, int dv, kda_dtype_t dt) {
     return dt == KDA_BF16 && dk == D && dv == D;
 }
 
-cudaError_t launch_chunk_tc(const ChunkArgs &a, int dk, int dv, kda_dtype_t dt, cudaStream_t st) {
+cudaError_t launch_chunk_tc(const ChunkArgs &args, int dk, int dv, kda_dtype_t dt, cudaStream_t st) {
     if (!chunk_tc_supported(dk, dv, dt)) return cudaErrorNotSupported;
+    ChunkArgs a = args;
     const int64_t tokens = a.cu ? a.seqlen : (int64_t)a.num_seqs * a.seqlen;
+    if (a.segments <= 0) a.segments = auto_segments(a, (int64_t)a.num_seqs * a.heads, tokens);
     if (tokens >= (int64_t(1) << 31)) return cudaErrorInvalidValue;
     CUtensorMap mq, mk, mv, mg, mz;
     if (!make_map(&mq, a.q, tokens, a.heads) || !make_map(&mk, a.k, tokens, a.heads) ||
@@ -949,8 +1045,9 @@ cudaError_t launch_chunk_tc(const ChunkArgs &a, int dk, int dv, kda_dtype_t dt, 
                                          (int)SMEM_BYTES);
     if (e != cudaSuccess) return e;
     const int64_t units = (int64_t)a.num_seqs * a.heads;
-    if (units > 0x7fffffffLL) return cudaErrorInvalidValue;
-    kda_chunk_tc_kernel<<<(unsigned)units, NT, SMEM_BYTES, st>>>(mq, mk, mv, mg, mz, a, a.wait_polls);
+    const int P = a.segments > 1 ? a.segments : 1;
+    if (units * P > 0x7fffffffLL) return cudaErrorInvalidValue;
+    kda_chunk_tc_kernel<<<(unsigned)(units * P), NT, SMEM_BYTES, st>>>(mq, mk, mv, mg, mz, a, a.wait_polls);
     return cudaGetLastError();
 }
 

@@ -30,6 +30,7 @@ struct ChunkArgs {
     const int32_t *ckpt_off;  // [N + 1]: sequence n's checkpoints occupy slots [off[n], off[n+1])
     int32_t ckpt_interval;    // tokens between checkpoints (a multiple of the chunk)
     uint32_t wait_polls;      // bound on each device wait of the tensor-core kernel (polls)
+    int32_t segments;         // tensor-core kernel: CTAs per (sequence, head), 0 = chosen by the launcher
 };
 
 // Checkpoint slot for the state after `pos` tokens of sequence n (pos > 0 a multiple of the

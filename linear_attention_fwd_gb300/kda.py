@@ -22,7 +22,8 @@ IMPLS = {"auto": 0, "simt": 1, "tc": 2}
 IMPL_NAMES = {v: k for k, v in IMPLS.items()}
 
 # every symbol include/kda.h declares
-EXPORTED = ("kda_chunk_fwd", "kda_chunk_fwd_with", "kda_chunk_fwd_bounded", "kda_chunk_fwd_checkpointed",
+EXPORTED = ("kda_chunk_fwd", "kda_chunk_fwd_with", "kda_chunk_fwd_bounded", "kda_chunk_fwd_segmented",
+            "kda_chunk_fwd_checkpointed",
             "kda_chunk_fwd_gated", "kda_chunk_fwd_selected_impl", "kda_recurrent_step",
             "kda_recurrent_steps", "kda_status_string")
 
@@ -57,6 +58,8 @@ def lib() -> ctypes.CDLL:
         L.kda_chunk_fwd_with.argtypes = [ctypes.c_int] + [vp] * 9 + [dp, vp]
         L.kda_chunk_fwd_bounded.restype = ctypes.c_int
         L.kda_chunk_fwd_bounded.argtypes = [ctypes.c_int] + [vp] * 9 + [ctypes.c_uint32, dp, vp]
+        L.kda_chunk_fwd_segmented.restype = ctypes.c_int
+        L.kda_chunk_fwd_segmented.argtypes = [ctypes.c_int] + [vp] * 9 + [ctypes.c_int32, dp, vp]
         L.kda_chunk_fwd_checkpointed.restype = ctypes.c_int
         L.kda_chunk_fwd_checkpointed.argtypes = [vp] * 11 + [ctypes.c_int32, dp, vp]
         L.kda_chunk_fwd_gated.restype = ctypes.c_int
@@ -115,7 +118,7 @@ def chunk_dims(q, v, cu_seqlens=None) -> KdaDims:
 
 def kda_chunk_fwd(q, k, v, g, beta, initial_state=None, cu_seqlens=None, *, out=None,
                   final_state=None, output_final_state: bool = True, impl: str = "auto",
-                  stream=None, wait_polls: int | None = None):
+                  stream=None, wait_polls: int | None = None, segments: int | None = None):
     """Chunkwise KDA forward (prefill / prefix-cache resume) through libkda.
 
     q, k, g: [B, T, H, dk]; v: [B, T, H, dv]; beta: [B, T, H] (all fp32 or all
@@ -124,6 +127,8 @@ def kda_chunk_fwd(q, k, v, g, beta, initial_state=None, cu_seqlens=None, *, out=
     Returns (out [B, T, H, dv], final_state [N, H, dk, dv] fp32 or None).
     wait_polls: bound on each device wait of the tensor-core kernel (kda_chunk_fwd_bounded);
     a unit whose wait gives up gets a NaN final state.
+    segments: CTAs per (sequence, head) on the tensor-core kernel (kda_chunk_fwd_segmented;
+    0 = the library's choice, which is also what the default call does).
     """
     dev = q.device
     for name, t in (("q", q), ("k", k), ("v", v), ("g", g), ("beta", beta)):
@@ -144,7 +149,12 @@ def kda_chunk_fwd(q, k, v, g, beta, initial_state=None, cu_seqlens=None, *, out=
     _check_dev("final_state", final_state, dev, torch.float32)
     args = (_ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta), _ptr(initial_state),
             _ptr(cu_seqlens), _ptr(out), _ptr(final_state))
-    if wait_polls is None:
+    if wait_polls is not None and segments is not None:
+        raise ValueError("wait_polls and segments select different entry points")
+    if segments is not None:
+        st = lib().kda_chunk_fwd_segmented(IMPLS[impl], *args, ctypes.c_int32(int(segments)),
+                                           ctypes.byref(dims), _stream_handle(stream))
+    elif wait_polls is None:
         st = lib().kda_chunk_fwd_with(IMPLS[impl], *args, ctypes.byref(dims), _stream_handle(stream))
     else:
         st = lib().kda_chunk_fwd_bounded(IMPLS[impl], *args, ctypes.c_uint32(int(wait_polls)),
@@ -152,6 +162,12 @@ def kda_chunk_fwd(q, k, v, g, beta, initial_state=None, cu_seqlens=None, *, out=
     if st != KDA_OK:
         raise KdaError(st, "kda_chunk_fwd")
     return out, final_state
+
+
+def kda_chunk_fwd_segmented(q, k, v, g, beta, initial_state=None, cu_seqlens=None, *,
+                            segments: int = 0, **kw):
+    """kda_chunk_fwd with an explicit number of CTAs per (sequence, head) (tensor-core kernel)."""
+    return kda_chunk_fwd(q, k, v, g, beta, initial_state, cu_seqlens, segments=segments, **kw)
 
 
 def kda_chunk_fwd_selected_impl(q, v, cu_seqlens=None) -> str:
