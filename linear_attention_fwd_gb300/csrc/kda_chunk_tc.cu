@@ -226,6 +226,9 @@ __device__ __forceinline__ void tma_tile(const CUtensorMap *map, uint32_t dst, u
     tma_load_3d(dst + half_stride, map, bar, 64, h, (int)tok);
 }
 
+// kSeg: several CTAs per (sequence, head) (a.segments > 1); without it the segment logic folds
+// away and one CTA runs each unit from its start.
+template <bool kSeg>
 __global__ void __launch_bounds__(NT, 1)
 kda_chunk_tc_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant__ CUtensorMap tmk,
                     const __grid_constant__ CUtensorMap tmv, const __grid_constant__ CUtensorMap tmg,
@@ -240,19 +243,20 @@ kda_chunk_tc_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_consta
     // blockIdx.x = p * units + unit: segment p of P of one (sequence, head); this CTA stores
     // the outputs of chunks [c_lo, c_hi), running from chunk c_run (see warm_start), and the
     // last segment writes the final state
-    const int P = a.segments > 1 ? a.segments : 1;
     const int64_t units = (int64_t)a.num_seqs * H;
+    const int P = kSeg && a.segments > 1 ? a.segments : 1;
+    const int p = kSeg ? (int)(blockIdx.x / units) : 0;
     int n, h;
-    select_unit(a, (int)(blockIdx.x % units), n, h);
-    const int p = (int)(blockIdx.x / units);
+    select_unit(a, kSeg ? (int)(blockIdx.x % units) : (int)blockIdx.x, n, h);
     int64_t bos, eos;
     seq_range(a, n, bos, eos);
     const int64_t len = eos - bos;
     const int nchunks = (int)((len + C - 1) / C);
-    const int c_lo = (int)((int64_t)p * nchunks / P), c_hi = (int)((int64_t)(p + 1) * nchunks / P);
-    const bool last_seg = p == P - 1;
-    if (c_lo == c_hi && !last_seg) return;   // an empty segment (whole CTA, before any setup)
-    const int c_run = c_lo > 0 ? warm_start(a, bos, h, c_lo) : 0;
+    const int c_lo = kSeg ? (int)((int64_t)p * nchunks / P) : 0;
+    const int c_hi = kSeg ? (int)((int64_t)(p + 1) * nchunks / P) : nchunks;
+    const bool last_seg = !kSeg || p == P - 1;
+    if (kSeg && c_lo == c_hi && !last_seg) return;   // an empty segment (whole CTA, before any setup)
+    const int c_run = kSeg && c_lo > 0 ? warm_start(a, bos, h, c_lo) : 0;
     const int64_t t_run = bos + (int64_t)c_run * C;
 
     // mbarriers: Q, K, G tiles landed; [O^T | P^T] done; V tile landed; U^T done; state (and
@@ -941,7 +945,7 @@ kda_chunk_tc_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_consta
             }
             atomicAdd(&g_kda_tc_timeouts, 1u);
         }
-        if (P > 1) {   // only the last segment writes the state: mark this segment's outputs
+        if (kSeg && P > 1) {   // only the last segment writes the state: mark this segment's outputs
             const int64_t r0 = (int64_t)c_lo * C, r1 = (int64_t)c_hi * C < len ? (int64_t)c_hi * C : len;
             for (int64_t x = tid; x < (r1 - r0) * D; x += NT)
                 out[((bos + r0 + x / D) * H + h) * D + x % D] = __ushort_as_bfloat16((unsigned short)0x7fc0);
@@ -1041,13 +1045,13 @@ cudaError_t launch_chunk_tc(const ChunkArgs &args, int dk, int dv, kda_dtype_t d
         !make_map(&mv, a.v, tokens, a.heads) || !make_map(&mg, a.g, tokens, a.heads) ||
         !make_map_rows(&mz, a.gate ? a.gate : a.v, tokens, a.heads))   // unused without a gate
         return cudaErrorInvalidValue;
-    cudaError_t e = cudaFuncSetAttribute(kda_chunk_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         (int)SMEM_BYTES);
+    const int P = a.segments > 1 ? a.segments : 1;
+    auto kernel = P > 1 ? kda_chunk_tc_kernel<true> : kda_chunk_tc_kernel<false>;
+    cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)SMEM_BYTES);
     if (e != cudaSuccess) return e;
     const int64_t units = (int64_t)a.num_seqs * a.heads;
-    const int P = a.segments > 1 ? a.segments : 1;
     if (units * P > 0x7fffffffLL) return cudaErrorInvalidValue;
-    kda_chunk_tc_kernel<<<(unsigned)(units * P), NT, SMEM_BYTES, st>>>(mq, mk, mv, mg, mz, a, a.wait_polls);
+    kernel<<<(unsigned)(units * P), NT, SMEM_BYTES, st>>>(mq, mk, mv, mg, mz, a, a.wait_polls);
     return cudaGetLastError();
 }
 
