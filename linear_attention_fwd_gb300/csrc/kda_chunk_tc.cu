@@ -1,10 +1,11 @@
 // KDA chunkwise forward on the sm_103a tensor cores (tcgen05 + TMEM + TMA).
 //
 // bf16 inputs/outputs, d_k = d_v = 128, chunk C = 64, fp32 recurrent state.
-// One CTA (16 warps) per (sequence, head); the fp32 state lives in tensor
-// memory for the whole sequence (transposed: TMEM lane j = value channel,
-// column i = key channel), so the only HBM traffic is the q/k/v/g/beta tiles,
-// the output, and the initial / final states.
+// One CTA (16 warps) per (sequence, head), or per segment of one when there are
+// fewer units than SMs (see warm_start); the fp32 state lives in tensor memory
+// for the whole run (transposed: TMEM lane j = value channel, column i = key
+// channel), so the only HBM traffic is the q/k/v/g/beta tiles, the output, and
+// the initial / final states.
 //
 // Chunk algebra ("はじめての自然言語処理 -- Kimi K3" section 3.1: chunkwise form,
 // Tril intra-chunk term, decay folded into q times Gamma and k over Gamma as in
