@@ -200,6 +200,13 @@ kda_status_t kda_chunk_fwd_gated(const void *q, const void *k, const void *v,
  * KDA_IMPL_TC), or -1 when the dims are invalid. */
 int kda_chunk_fwd_selected_impl(const kda_dims_t *dims);
 
+/* The number of CTAs per (sequence, head) kda_chunk_fwd gives the tensor-core kernel for
+ * `dims` on a GPU with `sms` SMs (host arithmetic only, no device call): floor(sms / units)
+ * with units = num_seqs * heads, at most 8, lowered until segments average at least 16
+ * chunks of 64 tokens; 1 for shapes the tensor-core kernel does not run and for invalid dims.
+ * A call with an output gate, checkpoints or initial_state == final_state always uses 1. */
+int kda_chunk_fwd_auto_segments(const kda_dims_t *dims, int sms);
+
 /* kda_recurrent_step -- one decode token per row, state updated in place.
  *
  * Operation per row n and head h, on the state S = state[slot][h] with

@@ -66,6 +66,13 @@ extern "C" int kda_chunk_fwd_selected_impl(const kda_dims_t *d) {
     return kda::chunk_tc_supported(d->dk, d->dv, d->dtype) ? KDA_IMPL_TC : KDA_IMPL_SIMT;
 }
 
+extern "C" int kda_chunk_fwd_auto_segments(const kda_dims_t *d, int sms) {
+    if (d == nullptr || d->heads <= 0 || d->num_seqs <= 0 || d->batch <= 0 || d->seqlen < 0) return 1;
+    if (!kda::chunk_tc_supported(d->dk, d->dv, d->dtype)) return 1;
+    const int64_t tokens = (int64_t)d->batch * d->seqlen;
+    return kda::segments_for((int64_t)d->num_seqs * d->heads, tokens, d->num_seqs, sms);
+}
+
 // Validated launch of one chunked forward (optionally writing state checkpoints).
 static kda_status_t chunk_run(kda_impl_t impl, const void *q, const void *k, const void *v, const void *g,
                        const void *beta, const float *initial_state, const int32_t *cu_seqlens,

@@ -1012,23 +1012,28 @@ bool make_map_rows(CUtensorMap *m, const void *ptr, int64_t tokens, int H) {
 
 }  // namespace
 
+int segments_for(int64_t units, int64_t tokens, int64_t num_seqs, int sms) {
+    constexpr int kMaxSegments = 8, kMinSegChunks = 16;
+    if (units <= 0 || num_seqs <= 0 || sms <= 0) return 1;
+    int64_t P = sms / units;
+    if (P > kMaxSegments) P = kMaxSegments;
+    const int64_t avg_chunks = tokens / (num_seqs * C);
+    while (P > 1 && avg_chunks < (int64_t)kMinSegChunks * P) --P;
+    return P < 1 ? 1 : (int)P;
+}
+
 // Segments per (sequence, head) when the caller leaves the choice to the library: enough to
 // put every SM to work when there are fewer units than SMs, with segments of at least
-// kMinSegChunks chunks on average; one when the launch writes checkpoints or applies the
-// output gate, or reads and writes the state in place (the last segment would write the
-// state while another may still read it).
+// kMinSegChunks chunks on average (segments_for); one when the launch writes checkpoints or
+// applies the output gate, or reads and writes the state in place (the last segment would
+// write the state while another may still read it).
 static int auto_segments(const ChunkArgs &a, int64_t units, int64_t tokens) {
-    constexpr int kMaxSegments = 8, kMinSegChunks = 16;
-    if (a.gate || a.ckpt || (a.s0 && a.s0 == a.sT) || units <= 0) return 1;
+    if (a.gate || a.ckpt || (a.s0 && a.s0 == a.sT)) return 1;
     int dev = 0, sms = 0;
     if (cudaGetDevice(&dev) != cudaSuccess ||
         cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
         return 1;
-    int64_t P = sms / units;
-    if (P > kMaxSegments) P = kMaxSegments;
-    const int64_t avg_chunks = tokens / ((int64_t)a.num_seqs * C);
-    while (P > 1 && avg_chunks < (int64_t)kMinSegChunks * P) --P;
-    return P < 1 ? 1 : (int)P;
+    return segments_for(units, tokens, a.num_seqs, sms);
 }
 
 bool chunk_tc_supported(int dk, int dv, kda_dtype_t dt) {

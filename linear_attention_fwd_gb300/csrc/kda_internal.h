@@ -82,6 +82,9 @@ template <> __device__ __forceinline__ __nv_bfloat16 from_f<__nv_bfloat16>(float
 cudaError_t launch_chunk_simt(const ChunkArgs &a, int dk, int dv, kda_dtype_t dt, cudaStream_t s);
 cudaError_t launch_chunk_tc(const ChunkArgs &a, int dk, int dv, kda_dtype_t dt, cudaStream_t s);
 bool chunk_tc_supported(int dk, int dv, kda_dtype_t dt);
+// Segments per (sequence, head) the tensor-core launcher picks for a plain call on a GPU with
+// `sms` SMs: floor(sms / units), at most 8, lowered until segments average >= 16 chunks.
+int segments_for(int64_t units, int64_t tokens, int64_t num_seqs, int sms);
 cudaError_t launch_decode(const DecodeArgs &a, int dk, int dv, kda_dtype_t dt, cudaStream_t s);
 // out <- RMSNorm(out) * w * sigmoid(gate) over dv, in place, for every token row of a chunk call
 cudaError_t launch_gate_pass(const ChunkArgs &a, int64_t tokens, int dv, kda_dtype_t dt,

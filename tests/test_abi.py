@@ -177,3 +177,31 @@ def test_binding_fails_loudly_without_library(monkeypatch, tmp_path):
     monkeypatch.setattr(kda, "LIB_PATH", str(tmp_path / "missing.so"))
     with pytest.raises(RuntimeError, match="missing"):
         kda.lib()
+
+
+def test_segment_count_the_library_picks(K):
+    # floor(SMs / units), at most 8, lowered until segments average >= 16 chunks of 64 tokens
+    f = K.kda_chunk_fwd_auto_segments
+    assert f(dims(batch=4, seqlen=8192, num_seqs=4, heads=32), 152) == 1       # 128 units
+    assert f(dims(batch=1, seqlen=65536, num_seqs=1, heads=64), 152) == 2      # 64 units
+    assert f(dims(batch=1, seqlen=8192, num_seqs=1, heads=4), 152) == 8        # 128 chunks >= 16 * 8
+    assert f(dims(batch=1, seqlen=8191, num_seqs=1, heads=4), 152) == 7        # 127 chunks
+    assert f(dims(batch=1, seqlen=4096, num_seqs=1, heads=1), 152) == 4        # 64 chunks
+    assert f(dims(batch=1, seqlen=1100, num_seqs=1, heads=1), 152) == 1        # 17 chunks
+    assert f(dims(batch=1, seqlen=2**20, num_seqs=16, heads=32), 152) == 1     # 512 units
+    assert f(dims(batch=1, seqlen=65536, num_seqs=1, heads=64), 76) == 1
+    # the tensor-core kernel does not run fp32 or d = 64; invalid dims and SM counts give 1
+    assert f(dims(batch=1, seqlen=65536, num_seqs=1, heads=4, dtype=0), 152) == 1
+    assert f(dims(batch=1, seqlen=65536, num_seqs=1, heads=4, dk=64, dv=64), 152) == 1
+    assert f(dims(batch=1, seqlen=65536, num_seqs=1, heads=0), 152) == 1
+    assert f(dims(batch=1, seqlen=65536, num_seqs=1, heads=4), 0) == 1
+
+
+def test_segment_count_argument_is_checked(K):
+    # segments outside [0, 64] are refused before any launch
+    vp = ctypes.c_void_p
+    d = dims()
+    for bad in (-1, 65):
+        st = K.lib().kda_chunk_fwd_segmented(2, *[vp(FAKE)] * 5, None, None, vp(FAKE), None,
+                                             ctypes.c_int32(bad), ctypes.byref(d), None)
+        assert st == 2   # KDA_ERR_SHAPE
