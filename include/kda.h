@@ -96,7 +96,12 @@ typedef struct {
  *   cu_seqlens: int32 [num_seqs + 1] device, or NULL for dense batches.
  *               Offsets are clamped to [0, seqlen] on the device.
  * Returns KDA_OK or an error listed above; seqlen = 0 is valid (only the
- * final state is written: a copy of the initial state, or zeros). */
+ * final state is written: a copy of the initial state, or zeros).
+ * On the tensor-core kernel, when there are fewer (sequence, head) units than
+ * SMs, each sequence is split over several CTAs (kda_chunk_fwd_segmented with
+ * segments = 0; kda_chunk_fwd_auto_segments reports the count); the history a
+ * segment skips contributes less than 2^-160 of the norm of the state it
+ * replaces, else the segment starts at the sequence start. */
 kda_status_t kda_chunk_fwd(const void *q, const void *k, const void *v,
                            const void *g, const void *beta,
                            const float *initial_state, const int32_t *cu_seqlens,
