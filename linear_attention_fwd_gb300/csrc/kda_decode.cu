@@ -91,16 +91,21 @@ kda_recurrent_step_kernel(DecodeArgs a) {
 #pragma unroll 1
         for (int tk = 0; tk < nt; ++tk) {
             const int64_t row = ((int64_t)n * a.ntok + p0 + tk) * a.heads + h;
-            float4 pv = make_float4(0.f, 0.f, 0.f, 0.f), pp = pv;
+            // column pairs in packed fp32x2 arithmetic (one instruction per two columns)
+            float2 pv0 = make_float2(0.f, 0.f), pv1 = pv0, pp0 = pv0, pp1 = pv0;
 #pragma unroll
             for (int m = 0; m < RPT; ++m) {
                 const int i = rg * RPT + m;
                 const float ak = sa[tk][i] * sk[tk][i], aq = sa[tk][i] * sq[tk][i];
-                pv.x += ak * s[m].x; pv.y += ak * s[m].y; pv.z += ak * s[m].z; pv.w += ak * s[m].w;
-                pp.x += aq * s[m].x; pp.y += aq * s[m].y; pp.z += aq * s[m].z; pp.w += aq * s[m].w;
+                const float2 ak2 = make_float2(ak, ak), aq2 = make_float2(aq, aq);
+                const float2 s0 = make_float2(s[m].x, s[m].y), s1 = make_float2(s[m].z, s[m].w);
+                pv0 = __ffma2_rn(ak2, s0, pv0);
+                pv1 = __ffma2_rn(ak2, s1, pv1);
+                pp0 = __ffma2_rn(aq2, s0, pp0);
+                pp1 = __ffma2_rn(aq2, s1, pp1);
             }
-            *reinterpret_cast<float4 *>(&red_v[rg][4 * cg]) = pv;
-            *reinterpret_cast<float4 *>(&red_p[rg][4 * cg]) = pp;
+            *reinterpret_cast<float4 *>(&red_v[rg][4 * cg]) = make_float4(pv0.x, pv0.y, pv1.x, pv1.y);
+            *reinterpret_cast<float4 *>(&red_p[rg][4 * cg]) = make_float4(pp0.x, pp0.y, pp1.x, pp1.y);
             __syncthreads();
 
             const float beta = s_beta[tk];
@@ -118,15 +123,16 @@ kda_recurrent_step_kernel(DecodeArgs a) {
             // the next token's partial sums are written only after its barrier, which every
             // thread reaches after finishing this update
             const float4 e4 = *reinterpret_cast<const float4 *>(&se[4 * cg]);
+            const float2 e0 = make_float2(e4.x, e4.y), e1 = make_float2(e4.z, e4.w);
             const bool last = !MULTI || p0 + tk + 1 == ntok;
 #pragma unroll
             for (int m = 0; m < RPT; ++m) {
                 const int i = rg * RPT + m;
                 const float al = sa[tk][i], bk = beta * sk[tk][i];
-                s[m].x = al * s[m].x + bk * e4.x;
-                s[m].y = al * s[m].y + bk * e4.y;
-                s[m].z = al * s[m].z + bk * e4.z;
-                s[m].w = al * s[m].w + bk * e4.w;
+                const float2 al2 = make_float2(al, al), bk2 = make_float2(bk, bk);
+                const float2 n0 = __ffma2_rn(al2, make_float2(s[m].x, s[m].y), __fmul2_rn(bk2, e0));
+                const float2 n1 = __ffma2_rn(al2, make_float2(s[m].z, s[m].w), __fmul2_rn(bk2, e1));
+                s[m] = make_float4(n0.x, n0.y, n1.x, n1.y);
                 if (last && (!MULTI || a.update)) __stcs(reinterpret_cast<float4 *>(S + i * DV) + cg, s[m]);
             }
         }
