@@ -38,8 +38,14 @@ kda_recurrent_step_kernel(DecodeArgs a) {
     const int slot = a.idx ? __ldg(a.idx + n) : n;
     if (slot < 0 || slot >= a.slots) return;   // uniform across the block
 
-    __shared__ float sq[TM][DK], sk[TM][DK], sa[TM][DK], sv[TM][DV], se[DV];
-    __shared__ float red_v[RG][DV], red_p[RG][DV];
+    // 16-byte aligned: red_v, red_p and se are accessed as float4
+    __shared__ __align__(16) float sq[TM][DK];
+    __shared__ __align__(16) float sk[TM][DK];
+    __shared__ __align__(16) float sa[TM][DK];
+    __shared__ __align__(16) float sv[TM][DV];
+    __shared__ __align__(16) float se[DV];
+    __shared__ __align__(16) float red_v[RG][DV];
+    __shared__ __align__(16) float red_p[RG][DV];
     __shared__ float s_beta[TM], s_qk[TM];
 
     const int t = threadIdx.x, warp = t >> 5, lane = t & 31;
