@@ -66,6 +66,10 @@ WORKLOADS = {
         init_state=True, seed=SEED_BASE + 3,
         note="16 packed sequences, log-uniform lengths in [1K,128K], 2^20 tokens, "
              "H=32 d=128 bf16, initial state N(0,0.02^2)"),
+    "prefill_b4_h96_t8192": Workload(
+        "prefill_b4_h96_t8192", "prefill", heads=96, dk=128, dv=128,
+        dtype=torch.bfloat16, batch=4, seqlen=8192, seed=SEED_BASE + 5,
+        note="B=4 H=96 T=8192 d=128 bf16 (96 KDA heads per layer), zero initial state"),
     "decode_n256_h64": Workload(
         "decode_n256_h64", "decode", heads=64, dk=128, dv=128,
         dtype=torch.bfloat16, batch=256, init_state=True, decode_steps=1000,
