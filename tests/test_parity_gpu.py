@@ -84,6 +84,21 @@ def test_varlen_with_short_and_empty_sequences(K, dtype, d):
         torch.testing.assert_close(sT[2], inp["initial_state"][2], rtol=0, atol=0)
 
 
+def test_more_packed_sequences_than_threads(K):
+    # 600 packed sequences (more than the 512 threads that rank them longest first, so they run
+    # in their given order), lengths 0..150 with empty and one-token members, on both kernels
+    rng = np.random.default_rng(12)
+    lengths = [int(x) for x in rng.integers(0, 151, 600)]
+    lengths[:4] = [0, 1, 64, 65]
+    for dtype, d in [(torch.bfloat16, 128), (torch.float32, 64)]:
+        for impl in impls_for(K, dtype, d):
+            inp = inputs.make_prefill(batch=1, seqlen=0, heads=2, dk=d, dv=d, dtype=dtype,
+                                      device="cuda", seed=78, init_state=True, lengths=lengths)
+            out, sT = run(K, inp, impl)
+            check(compare_prefill(inp, out, sT), dtype)
+            torch.testing.assert_close(sT[0], inp["initial_state"][0], rtol=0, atol=0)
+
+
 def test_decay_bound_extreme(K):
     """Every g = -5 (every 16-token sub-tile reaches cumulative log decay -80)."""
     for dtype, d in [(torch.float32, 64), (torch.bfloat16, 128)]:
