@@ -96,3 +96,53 @@ def test_zero_start_differs_by_at_most_the_bound(normalised, decay):
         do = np.linalg.norm(out[0, t, 0] - out_w[0, t - w, 0])
         rnd = 1e-13 * max(1.0, np.linalg.norm(out[0, t, 0]))
         assert do <= bt * np.linalg.norm(Sw[0, 0], 2) * np.linalg.norm(q[0, t, 0]) * (1 + 1e-9) + rnd
+
+
+def warm_start_rule(g, beta, k, c_lo, C=64, horizon_log2=160.0, max_chunks=16):
+    """The chunk boundary a segment whose first stored chunk is c_lo starts from: the latest
+    one at most max_chunks chunks earlier where the summed per-token log2 bounds reach
+    -horizon_log2, else 0 (the sequence start, with the initial state)."""
+    acc = 0.0
+    for c in range(c_lo - 1, max(0, c_lo - max_chunks) - 1, -1):
+        for t in range(c * C, (c + 1) * C):
+            acc += np.log2(token_bound(g[t], beta[t], k[t]))
+        if acc <= -horizon_log2:
+            return c
+    return 0
+
+
+@pytest.mark.parametrize("decay", ["bound", "sigmoid", "one_channel_still"])
+@pytest.mark.parametrize("P", [2, 3, 5])
+def test_segmented_runs_equal_the_full_run(decay, P):
+    # the segment scheme the tensor-core kernel uses, run with the oracle in fp64: segment p
+    # stores chunks [p nc / P, (p+1) nc / P) and runs from warm_start_rule's boundary
+    rng = np.random.default_rng(11)
+    C, nc, d = 64, 13, 8
+    T = nc * C - 20                      # a ragged last chunk
+    q, k, v, g, b = rand_inputs(rng, T, d, d)
+    if decay == "bound":
+        g = np.full_like(g, -5.0)
+    elif decay == "one_channel_still":
+        g[..., 2] = 0.0
+    S0 = rng.standard_normal((1, 1, d, d))
+    out, ST = oracle.forward(q, k, v, g, b, S0)
+    seg_out = np.full_like(out, np.nan)
+    for p in range(P):
+        c_lo, c_hi = p * nc // P, (p + 1) * nc // P
+        if c_lo == c_hi:
+            continue
+        c_run = warm_start_rule(g[0, :, 0], b[0, :, 0], k[0, :, 0], c_lo) if c_lo > 0 else 0
+        t0, t1 = c_run * C, min(c_hi * C, T)
+        o_p, s_p = oracle.forward(q[:, t0:t1], k[:, t0:t1], v[:, t0:t1], g[:, t0:t1], b[:, t0:t1],
+                                  S0 if c_run == 0 else None)
+        seg_out[:, c_lo * C:t1] = o_p[:, c_lo * C - t0:]
+        if p == P - 1:
+            seg_state = s_p
+        if decay == "bound" and c_lo > 0:
+            assert c_run == c_lo - 1      # one chunk of g = -5 is 461 below the log2 horizon
+        if decay == "one_channel_still" and c_lo > 0:
+            assert c_run == 0             # no horizon: from the start, with S0
+    assert not np.isnan(seg_out).any()
+    scale = np.sqrt(np.mean(out ** 2))
+    assert np.abs(seg_out - out).max() <= 1e-12 * scale
+    assert np.abs(seg_state - ST).max() <= 1e-12 * np.sqrt(np.mean(ST ** 2))
