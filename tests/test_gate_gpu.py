@@ -20,8 +20,7 @@ import torch
 
 import oracle
 from linear_attention_fwd_gb300 import inputs
-from tests.helpers import rel_max_err
-from tests.parity import TOL, excess_err, f64, oracle_prefill
+from tests.parity import TOL, f64, oracle_prefill
 
 pytestmark = pytest.mark.gpu
 

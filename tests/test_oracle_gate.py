@@ -1,7 +1,6 @@
 """Pins of oracle.gated_rmsnorm (CPU): properties the gate's definition fixes, checked
 without retyping its formula."""
 import numpy as np
-import pytest
 
 import oracle
 

@@ -15,7 +15,7 @@ import pytest
 import torch
 
 from linear_attention_fwd_gb300 import inputs
-from tests.parity import TOL, check_prefill, compare_prefill, f64
+from tests.parity import check_prefill, compare_prefill, f64
 
 pytestmark = pytest.mark.gpu
 BF = torch.bfloat16
