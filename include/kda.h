@@ -202,7 +202,7 @@ kda_status_t kda_chunk_fwd_gated(const void *q, const void *k, const void *v,
                                  const kda_dims_t *dims, cudaStream_t stream);
 
 /* The kernel kda_chunk_fwd would run for `dims` (KDA_IMPL_SIMT or
- * KDA_IMPL_TC), or -1 when the dims are invalid. */
+ * KDA_IMPL_TC), or -1 when the dims are invalid.  A library query (host only). */
 int kda_chunk_fwd_selected_impl(const kda_dims_t *dims);
 
 /* The number of CTAs per (sequence, head) kda_chunk_fwd gives the tensor-core kernel for
@@ -225,7 +225,10 @@ int kda_chunk_fwd_auto_segments(const kda_dims_t *dims, int sms);
  *               Rows whose slot is outside [0, num_seqs) are skipped: neither
  *               their state nor their output is written.  Two rows must not
  *               name the same slot.
- * dims: batch = N rows, seqlen = 1, num_seqs = pool slots. */
+ * dims: batch = N rows, seqlen = 1, num_seqs = pool slots.
+ * Returns KDA_OK, or an error found on the host before any launch (null required
+ * pointers, non-positive or inconsistent dims, unsupported head size or dtype,
+ * misalignment), in which case nothing is written. */
 kda_status_t kda_recurrent_step(const void *q, const void *k, const void *v,
                                 const void *g, const void *beta, float *state,
                                 const int32_t *state_indices, void *out,
