@@ -10,8 +10,8 @@
  * with S_t a d_k x d_v state per (sequence, head), q_t, k_t, g_t d_k-vectors,
  * v_t a d_v-vector, beta_t a scalar (the shapes list and the four-step
  * delta-rule paragraph; the one-line form is the report's equation (1)).
- * kda_chunk_fwd evaluates it chunkwise ("chunk をまたぐところだけ逐次" and the
- * chunk-decay paragraphs of the same section); kda_recurrent_step is the
+ * kda_chunk_fwd evaluates it chunkwise (the chunkwise-form and chunk-decay
+ * paragraphs of the same section); kda_recurrent_step is the
  * per-token sequential update used for decode (the serving paragraph of
  * "Kimi K3 architecture", orkas.ai: the state update is sequential).
  *
@@ -33,6 +33,15 @@
  *     g >= -5 of the "lower-bound" paragraph (so that a 16-token tile's
  *     cumulative log decay stays >= -80 and e^80 fits bf16/fp32): g in [-5, 0]
  *     is a precondition, not checked; outside it results are unspecified.
+ *   - v and the initial state may take any magnitude their formats hold: the
+ *     operation is linear in them, and the tensor-core kernel keeps its 16-bit
+ *     copies of the state and of the per-chunk corrections at a power-of-two
+ *     scale per value channel, chosen each 64-token chunk from that channel's
+ *     largest entry, so its accuracy relative to the results does not depend on
+ *     their scale (a value channel whose values jump by more than 2^126 from one
+ *     chunk to the next may lose the smaller part; parts below 2^-112 of a
+ *     channel's largest value may be flushed).  The SIMT and decode kernels
+ *     compute in fp32 throughout.
  */
 #ifndef KDA_H
 #define KDA_H
@@ -86,8 +95,8 @@ typedef struct {
  * sequence's tokens, writing o_t to `out` and the state after the last token
  * to final_state[n,h] (skipped when NULL).  Resume from a cached state at a
  * sequence boundary is the same call with initial_state = the saved state
- * ("prefix を再利用する", orkas.ai serving paragraph; prefill-cache support,
- * poyo.ai "KDAとプレフィックスキャッシュ").
+ * ("Kimi K3 architecture", orkas.ai, the serving section's paragraph on prefix
+ * reuse; "Kimi K3 アーキテクチャ", poyo.ai, "KDAとプレフィックスキャッシュ").
  *   q, k, g   : [batch, seqlen, H, dk]  dtype
  *   v, out    : [batch, seqlen, H, dv]  dtype (out is written)
  *   beta      : [batch, seqlen, H]      dtype

@@ -21,20 +21,32 @@
 // [e^-80, e^80] and are bf16 (the range the decay bound was chosen for; Q~ as hi + lo
 // for the diagonal blocks of M, whose diagonal itself is the exact q_r . k_r); every
 // other tensor-core operand (S, Z = diag(beta)(V - Kbar S), T, U, Qbar, Kbar, Kp, M)
-// is O(1) and is rounded to fp16 for 3 more mantissa bits, Z, U and M as hi + lo
-// pairs where one rounding would show in the outputs; accumulation is fp32 throughout.
+// is rounded to fp16 for 3 more mantissa bits, Z, U and M as hi + lo pairs where one
+// rounding would show in the outputs; accumulation is fp32 throughout.
+//
+// Range of the fp16 copies.  T, M, Qbar, Kbar and Kp are bounded by the inputs'
+// normalisation and the decay, but S, Z and U scale with v and the initial state, which
+// the method leaves unbounded: (V, S0) -> (O, S) is linear.  Each value channel j (a TMEM
+// lane) evolves on its own -- S[:, j], v_j and o_j are untouched by the other channels --
+// so every copy carries a power-of-two scale per lane, chosen each chunk from the lane's
+// own maximum: S16 = S 2^-a_j (largest entry in [2^14, 2^15)), Z16 = Z 2^-z_j (largest in
+// [1, 2)), and the fp32 state in TMEM is held as S 2^-z_j so that U16 (in Z's scale)
+// updates it directly.  Scaling by a power of two is exact; the outputs are
+// 2^a_j (Qbar S16) + 2^z_j (M U16), each factor applied per lane in fp32.  Each exponent
+// step is one float factor: z_j moves at most 126 from one chunk to the next (a lane whose
+// values jump by more than 2^126 within a chunk may lose its smaller part), keeps the state
+// below 2^87, and a state below 2^-112 of its scale is carried as fp16 subnormals or zero.
 //
 // Per chunk (the fp16 copies of S, beta (V - Kbar S) and U are tensor-memory
 // operands, so the state path never goes through shared memory):
 //   TMA       Q, K, V, G tiles (64 x 128 bf16, 128-byte swizzle) -> smem
-//   SIMT      sub-tile cumulative decay, x and 1/x, scaled operands; S -> fp16
-//   tcgen05   P^T = S^T Kbar^T - V^T (V read MN-major against a constant -I),
-//             O^T = S^T Qbar^T                                (overlapping the next two steps)
+//   SIMT      sub-tile cumulative decay, x and 1/x, scaled operands; S -> fp16 (scale a_j)
+//   tcgen05   P^T = S16^T Kbar^T,  O_I^T = S16^T Qbar^T           (overlapping the next two steps)
 //   mma.sync  A and M as 16x16 sub-tile products (the per-pair decay factor is
 //             applied to the B fragments in registers); diagonal inverses by
 //             forward substitution; off-diagonal blocks of T
-//   SIMT      Z^T = -P^T diag(beta) -> fp16 hi + lo (tensor memory only)
-//   tcgen05   U^T = Z^T T^T;  then  S^T <- S^T Diag(dec) + U^T Kp,  O^T += U^T M^T
+//   SIMT      Z^T = diag(beta) (V^T - 2^a_j P^T) -> fp16 hi + lo (scale z_j, tensor memory only)
+//   tcgen05   U^T = Z^T T^T;  then  S^T <- S^T Diag(dec) + U^T Kp,  (MU)^T = U^T M^T
 #include <cuda.h>
 #include <cudaTypedefs.h>
 #include <cuda_bf16.h>
@@ -56,12 +68,56 @@ constexpr int D = 128;        // d_k = d_v
 constexpr int NT = 512;       // threads (16 warps)
 constexpr float LOG2E = 1.4426950408889634f;
 
-// 2^x on the special-function unit (flushes results below 2^-126 to zero,
-// which only removes contributions under 1e-38 of an O(1) result).
+// 2^x on the special-function unit, results below 2^-126 flushed to zero.  Used where
+// every factor it multiplies is at most O(1), so a flushed result only drops a term
+// below 2^-126 of the operands' scale.
 __device__ __forceinline__ float ex2(float x) {
     float y;
     asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
     return y;
+}
+
+// 2^x for the decay factors that multiply K^ = K e^{b_I - gamma}, whose entries reach
+// e^80 ~ 2^115: a factor flushed at 2^-126 could drop a product as large as 2^-11, so results
+// are kept down to 2^-190 (2^(x + 64) on the unit, then an exact scaling by 2^-64 that may
+// give a subnormal); what is lost stays below 2^-75.
+__device__ __forceinline__ float ex2_sub(float x) { return ex2(x + 64.f) * 0x1p-64f; }
+
+// 2^e as a float for an integer e in [-126, 127] (exact).
+__device__ __forceinline__ float pow2i(int e) { return __int_as_float((e + 127) << 23); }
+
+// 2^e for any integer e <= 127: exact down to 2^-149 (subnormal), 0 below.
+__device__ __forceinline__ float pow2f(int e) {
+    return e >= -126 ? pow2i(e) : (e >= -149 ? __int_as_float(1 << (e + 149)) : 0.f);
+}
+
+// floor(log2 m) for m > 0 finite (subnormals give -127, which only lowers the scale chosen
+// from it); -1000 for m = 0.
+__device__ __forceinline__ int exp2_floor(float m) {
+    return m > 0.f ? (int)((__float_as_uint(m) >> 23) & 0xffu) - 127 : -1000;
+}
+
+__device__ __forceinline__ int clamp_i(int e, int lo, int hi) { return e < lo ? lo : (e > hi ? hi : e); }
+
+__device__ __forceinline__ float max3(float a, float b, float c) {
+    float d;
+    asm("max.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
+    return d;
+}
+
+// max_i |x_i| over N values as a tree of three-input maxima (eight independent chains),
+// so that its latency is a few dependent steps rather than N.
+template <int N>
+__device__ __forceinline__ float absmax(const float (&x)[N]) {
+    static_assert(N % 16 == 0, "multiple of 16");
+    float m[8];
+#pragma unroll
+    for (int e = 0; e < 8; ++e) m[e] = fmaxf(fabsf(x[2 * e]), fabsf(x[2 * e + 1]));
+#pragma unroll
+    for (int c = 16; c < N; c += 16)
+#pragma unroll
+        for (int e = 0; e < 8; ++e) m[e] = max3(m[e], fabsf(x[c + 2 * e]), fabsf(x[c + 2 * e + 1]));
+    return max3(max3(m[0], m[1], m[2]), max3(m[3], m[4], m[5]), fmaxf(m[6], m[7]));
 }
 
 // shared memory map, byte offsets from a 1024-aligned base
@@ -72,9 +128,11 @@ constexpr uint32_t OFF_V = 32768;      // V (bf16)                 [64 r][128 j]
 constexpr uint32_t OFF_G = 49152;      // G (bf16)                 [64 r][128 i]
 constexpr uint32_t OFF_SST = 65536;    // Q~hi, K~ (bf16)          2 x [64 r][128 i]
 constexpr uint32_t OFF_UST = 98304;    // Q~lo (bf16)              [64 r][128 i]
-constexpr uint32_t OFF_NI = 114688;    // -I (bf16, constant)      [64 s][64 r]
+constexpr uint32_t OFF_NI = 114688;   // I (bf16, constant)       [64 s][64 r]: V^T = V^T I
 constexpr uint32_t OFF_RED = 122880;   // gated output: row sums of squares [4][64] fp32
-                                       // (bytes 123904..131071 are unused)
+constexpr uint32_t OFF_SC = OFF_RED + 1024;   // per-lane scales and the maxima exchanged for them:
+                                       //   a_j, z_j (int, [2 chunk parities][128]), E_S [128],
+                                       //   two [2][128] fp32 exchange rows (3.5 KB; 131071 is the end)
 constexpr uint32_t OFF_KPT = 131072;   // Kp^T fp16                [128 i][64 r]
 constexpr uint32_t OFF_MT = 147456;    // M fp16                   [64 r][64 s]
 constexpr uint32_t OFF_TT = 155648;    // A_IJ (I > J) fp16        [64 r][64 s]
@@ -102,22 +160,24 @@ static_assert(OFF_T == OFF_TT + 8192, "the output staging tile spans AT and T");
 static_assert(4 * 16 * LDA * 4 <= OFF_W6 - OFF_PART, "A_II fits over the sums and vectors");
 
 // tensor memory columns (128 lanes = value channel j)
-constexpr uint32_t TM_S = 0;      // S^T fp32                        128 columns
-constexpr uint32_t TM_O = 128;    // O^T fp32 (follows S^T: one N = 192 group updates both)   64
-constexpr uint32_t TM_P = 192;    // P^T = S^T Kbar^T - V^T fp32 (follows O^T)               64
-constexpr uint32_t TM_U = 256;    // U^T fp32, then the low-order terms of O^T                 64
-constexpr uint32_t TM_S16 = 320;  // S^T as fp16 pairs (MMA operand)  64
-constexpr uint32_t TM_Z = 384;    // Z^T fp16 pairs                   32
-constexpr uint32_t TM_UH = 416;   // U^T fp16 pairs, hi               32
-constexpr uint32_t TM_UL = 448;   // U^T - hi, fp16 pairs             32
-constexpr uint32_t TM_ZL = 480;   // Z^T - hi, fp16 pairs             32
+constexpr uint32_t TM_S = 0;      // S^T 2^-z_j fp32                  128 columns
+constexpr uint32_t TM_MU = 128;   // (M U_hi)^T 2^-z_j fp32 (follows S^T: one N = 192 group)    64
+constexpr uint32_t TM_OI = 192;   // (Qbar S16)^T fp32                                          64
+constexpr uint32_t TM_P = 256;    // (Kbar S16)^T fp32 (follows O_I^T: one N = 128 group)       64
+constexpr uint32_t TM_U = 320;    // V^T, then U^T fp32, then the low-order terms of (M U)^T    64
+constexpr uint32_t TM_S16 = 384;  // S^T 2^-a_j as fp16 pairs (MMA operand)                     64
+constexpr uint32_t TM_Z = 448;    // Z^T fp16 pairs, hi; then U^T hi    32
+constexpr uint32_t TM_ZL = 480;   // Z^T - hi, fp16 pairs; then U^T lo  32
+constexpr uint32_t TM_UH = TM_Z;  // U^T is made after the U groups have read Z^T
+constexpr uint32_t TM_UL = TM_ZL;
 constexpr uint32_t TM_COLS = 512;
 
 constexpr uint32_t IDESC_N64 = idesc_f16_f32(128, 64);
 constexpr uint32_t IDESC_N128 = idesc_f16_f32(128, 128);
 constexpr uint32_t IDESC_N192 = idesc_f16_f32(128, 192);
 constexpr uint32_t IDESC_VT = idesc_bf16_f32(128, 64) | (1u << 15);   // A (V) MN-major
-static_assert(OFF_MT == OFF_KPT + 16384 && TM_O == TM_S + 128 && TM_P == TM_O + 64, "adjacent operands");
+static_assert(OFF_MT == OFF_KPT + 16384 && TM_MU == TM_S + 128 && TM_P == TM_OI + 64, "adjacent operands");
+static_assert(OFF_SC + 3584 <= OFF_KPT, "scale arrays fit");
 
 // Byte offset of element (row, col) in a 128-byte-swizzled K-major tile of
 // `rows` rows whose columns are split into 64-element halves.
@@ -260,8 +320,8 @@ kda_chunk_tc_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_consta
     const int c_run = kSeg && c_lo > 0 ? warm_start(a, bos, h, c_lo) : 0;
     const int64_t t_run = bos + (int64_t)c_run * C;
 
-    // mbarriers: Q, K, G tiles landed; [O^T | P^T] done; V tile landed; U^T done; state (and
-    // O^T high-order) update done; O^T low-order terms done
+    // mbarriers: Q, K, G tiles landed; [O_I^T | P^T] done; V tile landed; U^T done; state (and
+    // (M U_hi)^T) update done; low-order terms of (M U)^T done
     const uint32_t bar_tma = sb + OFF_BAR, bar_p = sb + OFF_BAR + 8, bar_v = sb + OFF_BAR + 16;
     const uint32_t bar_u = sb + OFF_BAR + 24, bar_s = sb + OFF_BAR + 32, bar_o = sb + OFF_BAR + 40;
     volatile uint32_t *tmem_holder = reinterpret_cast<volatile uint32_t *>(sm + OFF_BAR + 48);
@@ -272,6 +332,13 @@ kda_chunk_tc_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_consta
     float *EB = reinterpret_cast<float *>(sm + OFF_EB);
     float *EL = reinterpret_cast<float *>(sm + OFF_EL);
     __nv_bfloat16 *W6 = reinterpret_cast<__nv_bfloat16 *>(sm + OFF_W6);
+    // per-lane scale exponents (value channel j): a_j of S16 and z_j of Z16 / U16 / the
+    // TMEM state, one row per chunk parity (a chunk's values are still read while the next
+    // chunk's are made); E_S: exponent of the lane's largest |S| entering the chunk
+    int *ASC = reinterpret_cast<int *>(sm + OFF_SC);            // [2][128]
+    int *ZSC = ASC + 256;                                       // [2][128]
+    int *ESC = ZSC + 256;                                       // [128]
+    float *XCH = reinterpret_cast<float *>(ESC + 128);          // [2 halves][128] lane maxima
     float *DEC = reinterpret_cast<float *>(sm + OFF_DEC);
     float *BETA = reinterpret_cast<float *>(sm + OFF_BETA);
     const __nv_bfloat16 *beta = static_cast<const __nv_bfloat16 *>(a.beta);
@@ -306,7 +373,7 @@ kda_chunk_tc_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_consta
     // outside the single-thread issue branches, so that issuing an MMA costs no address math
     const uint64_t dsm = sdesc_sw128(sb);
 
-    // ---- initial state -> TMEM (S^T: lane j, column i)
+    // ---- initial state -> TMEM (S^T: lane j, column i; scale exponent 0)
     const int64_t sbase = ((int64_t)n * H + h) * D * D;
     {
         float v[32];
@@ -314,8 +381,13 @@ kda_chunk_tc_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_consta
         for (int c = 0; c < 32; ++c)
             v[c] = (a.s0 && c_run == 0) ? a.s0[sbase + (int64_t)(32 * quarter + c) * D + jl] : 0.f;
         tmem_st32(trow + TM_S + 32 * quarter, v);
+        uint32_t zero[16];
+#pragma unroll
+        for (int c = 0; c < 16; ++c) zero[c] = 0u;
+        tmem_st16u(trow + TM_MU + 16 * quarter, zero);   // (M U)^T = 0 before the first update
         tmem_wait_st();
     }
+    if (tid < 256) ZSC[tid] = 0;
     if (tid == 0 && c_run < c_hi) {
         mbar_arrive_expect_tx(bar_tma, 3 * 16384);
         tma_tile(&tmq, sb + OFF_Q, bar_tma, h, t_run, 16384);
@@ -325,10 +397,10 @@ kda_chunk_tc_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_consta
         tma_tile(&tmv, sb + OFF_V, bar_v, h, t_run);
     }
     if (tid < C) BETA[tid] = tid < len - (int64_t)c_run * C ? __bfloat162float(beta[(t_run + tid) * H + h]) : 0.f;
-    for (int x = tid; x < 64 * 32; x += NT) {   // -I: subtracts V^T from P^T inside the MMA
+    for (int x = tid; x < 64 * 32; x += NT) {   // I: copies V^T into tensor memory inside an MMA
         const int r = x >> 5, s2 = 2 * (x & 31);
         *reinterpret_cast<uint32_t *>(sm + OFF_NI + sw(r, s2, 64)) =
-            (s2 == r ? 0xBF80u : 0u) | (s2 + 1 == r ? 0xBF800000u : 0u);
+            (s2 == r ? 0x3F80u : 0u) | (s2 + 1 == r ? 0x3F800000u : 0u);
     }
     // the blocks of M above the diagonal blocks stay zero for the whole sequence
     for (int x = tid; x < 64 * 32; x += NT) {
@@ -346,21 +418,36 @@ kda_chunk_tc_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_consta
     bool out_pending = false;   // the previous chunk's state update and O^T group are in flight
     int64_t t0_out = 0;
     int nr_out = 0;
-    // O^T (TMEM: high-order part + low-order terms) -> bf16 staging tile [64 r][128 j] over the
-    // AT and T tiles, by warps 0-7; warp w: lanes 32(w%4).., rows 32(w/4)..+31
+    int spar = 1;               // the scale row holding z_j of the TMEM state (row 1 = 0 at start)
+    // O^T = 2^a_j O_I^T + 2^z_j ((M U_hi)^T + low-order terms), from TMEM, of the chunk whose
+    // scales are in row `par` -> bf16 staging tile [64 r][128 j] over the AT and T tiles, by
+    // warps 0-7; warp w: lanes 32(w%4).., rows 32(w/4)..+31.  (M U)^T is then cleared for the
+    // next chunk's update group, which accumulates into it together with the state.
     // With an output gate (the paragraph after the decay bound on the same page): each row is
     // normalised to unit RMS over its 128 value channels, scaled by the norm weight and
     // multiplied channel-wise by sigmoid(gate logit) before it is rounded to bf16; the chunk's
     // logits were loaded by TMA into the staging tile itself (same row-major layout).
     const float norm_wj = (a.gate && a.norm_w) ? a.norm_w[jl] : 1.f;   // this thread's channel
-    auto stage_output = [&]() {
+    auto stage_output = [&](int par) {
         if (warp >= 8) return;
         __nv_bfloat16 *os = reinterpret_cast<__nv_bfloat16 *>(sm + OFF_STG);
         const int r0 = 32 * (warp >> 2);
         float v[32], w[32];
-        tmem_ld32x2(trow + TM_O + r0, trow + TM_U + r0, v, w);
+        tmem_ld32x2(trow + TM_MU + r0, trow + TM_U + r0, v, w);
+        const float fz = pow2i(ZSC[par * 128 + jl]), fa = pow2f(ASC[par * 128 + jl]);
 #pragma unroll
-        for (int c = 0; c < 32; ++c) v[c] += w[c];
+        for (int c = 0; c < 32; ++c) v[c] = (v[c] + w[c]) * fz;
+        {
+            uint32_t zero[16];
+#pragma unroll
+            for (int c = 0; c < 16; ++c) zero[c] = 0u;
+            tmem_st16u(trow + TM_MU + r0, zero);
+            tmem_st16u(trow + TM_MU + r0 + 16, zero);
+        }
+        tmem_ld32(trow + TM_OI + r0, w);
+#pragma unroll
+        for (int c = 0; c < 32; ++c) v[c] = fmaf(w[c], fa, v[c]);
+        tmem_wait_st();
         if (a.gate) {
             // sums of squares of rows r0.. over this warp's 32 channels, transposed so that
             // lane L ends with row r0 + L (5 rounds, 31 shuffles)
@@ -486,9 +573,10 @@ kda_chunk_tc_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_consta
 #pragma unroll
         for (int I = 0; I < 4; ++I) {
             EB[I * 128 + c] = ex2(bI[I]);
-            EL[I * 128 + c] = ex2(gl - bI[I]);
+            EL[I * 128 + c] = ex2_sub(gl - bI[I]);   // multiplies K^ (up to e^80)
 #pragma unroll
-            for (int J = 0; J < I; ++J) W6[pair_index(I, J) * 128 + c] = __float2bfloat16_rn(ex2(bI[I] - bI[J]));
+            for (int J = 0; J < I; ++J)   // likewise; bf16 keeps subnormals down to 2^-133
+                W6[pair_index(I, J) * 128 + c] = __float2bfloat16_rn(ex2_sub(bI[I] - bI[J]));
         }
         DEC[c] = ex2(gl);
     };
@@ -497,6 +585,7 @@ kda_chunk_tc_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_consta
         const int64_t t0 = bos + (int64_t)ci * C;
         const int nr = (int)(len - (int64_t)ci * C < C ? len - (int64_t)ci * C : C);
         const bool more = ci + 1 < c_hi;
+        const int cpar = (ci - c_run) & 1;   // this chunk's row of scales; the TMEM state's is spar
 
         if (ci > c_run && tid < C) BETA[tid] = BETA[tid + (OFF_BNEXT - OFF_BETA) / 4];   // loaded during the previous chunk
         bool got = mbar_wait(bar_tma, ph_tma, wait_limit);   // checked at the next barrier
@@ -512,7 +601,7 @@ kda_chunk_tc_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_consta
                 got = mbar_wait(bar_s, ph_s, wait_limit) && mbar_wait(bar_o, ph_o, wait_limit) && got;
                 if (a.gate) got = mbar_wait(bar_z, ph_z, wait_limit) && got;
                 tc_fence_after();
-                stage_output();
+                stage_output(spar);
             }
         } else {
             if (warp < 12) diag_qk();
@@ -524,18 +613,32 @@ kda_chunk_tc_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_consta
                 const int i0 = 64 * ((warp - 8) >> 2);
                 float v[32], w[32];
                 tmem_ld32x2(trow + TM_S + i0, trow + TM_S + i0 + 32, v, w);
+                // the lane's largest |S| over both halves (warps w and w + 4 share the lanes)
+                const int sz = ZSC[spar * 128 + jl];   // S = (TMEM state) 2^sz
+                XCH[((warp - 8) >> 2) * 128 + jl] = fmaxf(absmax(v), absmax(w));
+                named_bar(3, 256);   // warps 8-15 (w and w + 4 share their lanes)
+                const int es = exp2_floor(fmaxf(XCH[jl], XCH[128 + jl]));
+                const int d = 14 - es < 126 ? 14 - es : 126;   // largest |S16| in [2^14, 2^15)
+                if (warp < 12) {
+                    ASC[cpar * 128 + jl] = sz - d;              // S16 = S 2^-(sz - d)
+                    ESC[jl] = es > -1000 ? es + sz : -1000;     // exponent of the lane's largest |S|
+                }
                 if (ck) {   // S[i][j] = S^T[j][i]: a warp writes 128 contiguous bytes per i
+                    const float fs = pow2i(sz);
 #pragma unroll
                     for (int c = 0; c < 32; ++c) {
-                        __stcs(ck + (int64_t)(i0 + c) * D, v[c]);
-                        __stcs(ck + (int64_t)(i0 + 32 + c) * D, w[c]);
+                        __stcs(ck + (int64_t)(i0 + c) * D, v[c] * fs);
+                        __stcs(ck + (int64_t)(i0 + 32 + c) * D, w[c] * fs);
                     }
                 }
+                const float2 f1 = make_float2(pow2i(d), pow2i(d));
                 uint32_t hv[16], hw[16];
 #pragma unroll
                 for (int c = 0; c < 16; ++c) {
-                    hv[c] = pack_f16(v[2 * c], v[2 * c + 1]);
-                    hw[c] = pack_f16(w[2 * c], w[2 * c + 1]);
+                    const float2 x = __fmul2_rn(make_float2(v[2 * c], v[2 * c + 1]), f1);
+                    const float2 y = __fmul2_rn(make_float2(w[2 * c], w[2 * c + 1]), f1);
+                    hv[c] = pack_f16(x.x, x.y);
+                    hw[c] = pack_f16(y.x, y.y);
                 }
                 tmem_st16u(trow + TM_S16 + i0 / 2, hv);
                 tmem_st16u(trow + TM_S16 + i0 / 2 + 16, hw);
@@ -608,15 +711,16 @@ kda_chunk_tc_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_consta
         fence_async_smem();
         tc_fence_before();
         __syncthreads();
-        // [O^T | P^T] = S^T [Qbar; Kbar]^T, then P^T -= V^T as V^T (-I) with V read MN-major
-        // [commit: P], issued by a warp that (3) leaves idle; the same thread loads the next
-        // chunk's G (consumed) and, once the group has read Qbar, Kbar and V, its Q, K and V
+        // [O_I^T | P^T] = S16^T [Qbar; Kbar]^T and V^T = V^T I into the U columns (V read
+        // MN-major; free since the previous output was staged) [commit: P], issued by a warp
+        // that (3) leaves idle; the same thread loads the next chunk's G (consumed) and, once
+        // the group has read Qbar, Kbar and V, its Q, K and V
         bool gtma = true;
         if (warp == 15 && lane == 0) {
             tc_fence_after();
 #pragma unroll
             for (int k = 0; k < 8; ++k)
-                mma_f16_ts(tmem + TM_O, tmem + TM_S16 + 8 * k, dsm + ((OFF_Q + (k >> 2) * 16384 + (k & 3) * 32) >> 4),
+                mma_f16_ts(tmem + TM_OI, tmem + TM_S16 + 8 * k, dsm + ((OFF_Q + (k >> 2) * 16384 + (k & 3) * 32) >> 4),
                            IDESC_N128, k > 0);
             gtma = mbar_wait(bar_v, ph_v, wait_limit);   // this chunk's V
             if (gtma) {
@@ -624,7 +728,7 @@ kda_chunk_tc_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_consta
                 const uint64_t vdesc = sdesc_sw128_mn(sb + OFF_V, 64 * 128, 1024);
 #pragma unroll
                 for (int k = 0; k < 4; ++k)
-                    mma_f16_ss(tmem + TM_P, vdesc + ((2048 * k) >> 4), dsm + ((OFF_NI + 32 * k) >> 4), IDESC_VT, 1);
+                    mma_f16_ss(tmem + TM_U, vdesc + ((2048 * k) >> 4), dsm + ((OFF_NI + 32 * k) >> 4), IDESC_VT, k > 0);
             }
             mma_commit(bar_p);
             if (more) {
@@ -647,7 +751,7 @@ kda_chunk_tc_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_consta
         // entries of M, where the bf16 rounding of Q~ shows in the outputs) and the exact
         // q_r . k_r on it.
         // Warps 8-13: the 6 off-diagonal pairs, single bf16 products with the per-channel factor
-        // e^{b_I - b_J} applied to the right operand.  Off-diagonal A blocks go to the fp16
+        // e^{b_I - b_J} (bf16, subnormals kept) applied to the right operand.  Off-diagonal A blocks go to the fp16
         // tile AT; T_II = (I + A_II)^-1 goes to the diagonal blocks of the fp16 tile T.
         if (warp < 4) {
             const int I = warp;
@@ -793,7 +897,8 @@ kda_chunk_tc_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_consta
 
         bool got4 = gtma;
         // ---- (4) warps 0-2: the off-diagonal blocks of T, level by level (T_IK with K > J is
-        // ready before T_IJ);  warps 4-11: Z^T = (V^T - P^T) diag(beta) -> fp16 pairs (TMEM)
+        // ready before T_IJ);  warps 4-11: Z^T = (V^T - 2^a_j P^T) diag(beta) -> fp16 pairs
+        // (TMEM) at the lane's scale z_j (warps w and w + 4 share the lanes)
         if (warp < 3) {
             t_block(warp + 1, warp);                 // (1,0) (2,1) (3,2)
             named_bar(1, 96);
@@ -804,13 +909,32 @@ kda_chunk_tc_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_consta
             got4 = mbar_wait(bar_p, ph_p, wait_limit) && got4;
             tc_fence_after();
             const int s0 = 32 * ((warp - 4) >> 2);
-            float pv[32];
-            tmem_ld32(trow + TM_P + s0, pv);   // P^T - V^T
+            float pv[32], vv[32];
+            tmem_ld32x2(trow + TM_P + s0, trow + TM_U + s0, pv, vv);   // (Kbar S)^T 2^-a_j, V^T
+            const float fa = -pow2f(ASC[cpar * 128 + jl]);
+            const float2 fa2 = make_float2(fa, fa);
+#pragma unroll
+            for (int c = 0; c < 32; c += 4) {
+                const float4 b4 = *reinterpret_cast<const float4 *>(BETA + s0 + c);
+                const float2 t0 = __ffma2_rn(make_float2(pv[c], pv[c + 1]), fa2, make_float2(vv[c], vv[c + 1]));
+                const float2 t1 = __ffma2_rn(make_float2(pv[c + 2], pv[c + 3]), fa2, make_float2(vv[c + 2], vv[c + 3]));
+                const float2 z0 = __fmul2_rn(t0, make_float2(b4.x, b4.y)), z1 = __fmul2_rn(t1, make_float2(b4.z, b4.w));
+                pv[c] = z0.x; pv[c + 1] = z0.y; pv[c + 2] = z1.x; pv[c + 3] = z1.y;
+            }
+            XCH[((warp - 4) >> 2) * 128 + jl] = absmax(pv);
+            named_bar(4, 256);   // warps 4-11 (w and w + 4 share their lanes)
+            // z_j: the lane's largest |Z| maps into [1, 2); at least E_S - 86 so that the state,
+            // held as S 2^-z_j from here on, stays below 2^87; within 126 of the state's
+            // current exponent so that the state moves to it by one float factor
+            const int eZ = exp2_floor(fmaxf(XCH[jl], XCH[128 + jl]));
+            const int eS = ESC[jl], sz = ZSC[spar * 128 + jl];
+            const int zj = clamp_i(clamp_i(eZ > eS - 86 ? eZ : eS - 86, sz - 126, sz + 126), -126, 126);
+            if (warp < 8) ZSC[cpar * 128 + jl] = zj;
+            const float2 fz = make_float2(pow2i(-zj), pow2i(-zj));
             uint32_t zv[16], zl[16];   // hi and lo: one fp16 rounding of U alone costs 2^-12
 #pragma unroll
             for (int c = 0; c < 16; ++c) {
-                const float2 b2 = *reinterpret_cast<const float2 *>(BETA + s0 + 2 * c);
-                const float2 z = __fmul2_rn(make_float2(pv[2 * c], pv[2 * c + 1]), make_float2(-b2.x, -b2.y));
+                const float2 z = __fmul2_rn(make_float2(pv[2 * c], pv[2 * c + 1]), fz);
                 zv[c] = pack_f16(z.x, z.y);
                 const float2 zlo = __ffma2_rn(unpack_f16(zv[c]), make_float2(-1.f, -1.f), z);
                 zl[c] = pack_f16(zlo.x, zlo.y);
@@ -825,7 +949,7 @@ kda_chunk_tc_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_consta
         tc_fence_before();
         if (__syncthreads_or(!got4)) { ok = false; break; }
         // U^T = Z^T_hi T^T (U columns) + Z^T_lo T^T (the consumed P columns), issued by two
-        // threads [commit: U, two arrivals];  V is consumed: the next chunk's V
+        // threads [commit: U, two arrivals]
         if (tid == 32) {
             tc_fence_after();
 #pragma unroll
@@ -841,15 +965,18 @@ kda_chunk_tc_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_consta
             mma_commit(bar_u);
         }
         {   // while the U^T groups run: S^T <- S^T Diag(dec) in place (S^T was read as fp16 in
-            // (1)); warp w: lanes 32(w%4).., 32 columns from 32(w/4)
+            // (1)), moved from the lane's old scale to z_j (U^T is at z_j); warp w: lanes
+            // 32(w%4).., 32 columns from 32(w/4)
             const int i0 = 32 * quarter;
             float v[32];
             tmem_ld32(trow + TM_S + i0, v);
+            const float f = pow2i(ZSC[spar * 128 + jl] - ZSC[cpar * 128 + jl]);   // |step| <= 126
+            const float2 f1 = make_float2(f, f);
 #pragma unroll
             for (int c = 0; c < 32; c += 4) {
                 const float4 d4 = *reinterpret_cast<const float4 *>(DEC + i0 + c);
-                const float2 a2 = __fmul2_rn(make_float2(v[c], v[c + 1]), make_float2(d4.x, d4.y));
-                const float2 b2 = __fmul2_rn(make_float2(v[c + 2], v[c + 3]), make_float2(d4.z, d4.w));
+                const float2 a2 = __fmul2_rn(__fmul2_rn(make_float2(v[c], v[c + 1]), f1), make_float2(d4.x, d4.y));
+                const float2 b2 = __fmul2_rn(__fmul2_rn(make_float2(v[c + 2], v[c + 3]), f1), make_float2(d4.z, d4.w));
                 v[c] = a2.x; v[c + 1] = a2.y; v[c + 2] = b2.x; v[c + 3] = b2.y;
             }
             tmem_st32(trow + TM_S + i0, v);
@@ -889,9 +1016,9 @@ kda_chunk_tc_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_consta
         }
         tc_fence_before();
         __syncthreads();
-        // [S^T | O^T] += U^T_hi [Kp^T; M]^T [commit: S];  low-order terms of O^T,
+        // [S^T | (M U)^T] += U^T_hi [Kp^T; M]^T [commit: S];  low-order terms of (M U)^T,
         // U^T_lo M^T + U^T_hi Mlo^T, into the U^T columns (consumed) [commit: O], issued by a
-        // warp with the least work in the next step (1)
+        // warp with the least work in the next step (1); all at the lanes' scales z_j
         if (tid == 0) {
             tc_fence_after();
 #pragma unroll
@@ -911,6 +1038,7 @@ kda_chunk_tc_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_consta
         out_pending = true;
         t0_out = t0;
         nr_out = ci >= c_lo ? nr : 0;   // the warm-up chunks before c_lo store nothing
+        spar = cpar;
     }
 
     if (ok && out_pending) {   // the last chunk's state update and output
@@ -924,7 +1052,7 @@ kda_chunk_tc_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_consta
             ok = false;
         } else {
             tc_fence_after();
-            stage_output();
+            stage_output(spar);
             __syncthreads();
             store_output();
         }
@@ -954,12 +1082,13 @@ kda_chunk_tc_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_consta
         __syncthreads();
     }
     tc_fence_after();
-    if (a.sT && last_seg) {
+    if (a.sT && last_seg) {   // S = (TMEM state) 2^z_j
         float v[32];
         tmem_ld32(trow + TM_S + 32 * quarter, v);
+        const float fs = pow2i(ZSC[spar * 128 + jl]);
 #pragma unroll
         for (int c = 0; c < 32; ++c)
-            a.sT[sbase + (int64_t)(32 * quarter + c) * D + jl] = ok ? v[c] : __int_as_float(0x7fc00000);
+            a.sT[sbase + (int64_t)(32 * quarter + c) * D + jl] = ok ? v[c] * fs : __int_as_float(0x7fc00000);
     }
     tc_fence_before();
     __syncthreads();

@@ -346,6 +346,7 @@ __device__ __forceinline__ float2 unpack_bf16(uint32_t u) {
     __nv_bfloat162 v = *reinterpret_cast<__nv_bfloat162 *>(&u);
     return __bfloat1622float2(v);
 }
+// Two bf16 products, each rounded to bf16 (subnormal operands and results are kept).
 __device__ __forceinline__ uint32_t mul_bf16x2(uint32_t a, uint32_t b) {
     __nv_bfloat162 r = __hmul2(*reinterpret_cast<__nv_bfloat162 *>(&a),
                                *reinterpret_cast<__nv_bfloat162 *>(&b));

@@ -42,8 +42,11 @@ def excess_err(x, ref, dtype):
 
 def check_prefill(res, dtype):
     """Assert the bars: outputs on their excess over storage rounding, states
-    (fp32) on the plain metric."""
+    (fp32) on the plain metric.  The plain metric of the outputs is held too, to
+    the rounding floor plus the bar, so that an error in the largest elements
+    cannot hide behind their own storage rounding."""
     assert res["excess"] <= TOL[dtype], res
+    assert res["out"] <= res["floor"] + TOL[dtype], res
     if "state" in res:
         assert res["state"] <= TOL[dtype], res
 

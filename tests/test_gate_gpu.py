@@ -12,7 +12,14 @@ the forward's bar allows on top):
     |y - y_ref| <= eps_o * rstd_row * |w sigmoid(z)| * (1 + |o_j| rstd_row)
                    (+ for bf16: the rounding of y_ref and one ulp of y),
 and, so that a systematic error cannot hide under that bound, the 99th percentile of
-|y - y_ref| stays within TOL * RMS(y_ref).
+|y - y_ref| stays within TOL * RMS(y_ref).  On the rows where the normalisation does not
+amplify (RMS(o_row) >= RMS(o): it multiplies an error in o by at most 1 / RMS(o)), the
+forward's flat bar is held as well: the error beyond y's own storage rounding (and, for bf16,
+beyond the rounding of o itself, half an ulp of |y| relative, which the separate gate pass
+after the SIMT kernel reads back) stays within TOL * RMS(y_ref).  (Rows between 0.1 RMS(o)
+and RMS(o) are amplified up to tenfold; on the bf16 tensor-core kernel their flat error
+measured 0.023, above the bar, which is why the threshold is where it is; the value at 0.1 is
+printed.)
 """
 import numpy as np
 import pytest
@@ -65,7 +72,16 @@ def _check(K, inp, heads, eps=1e-6, seed=0, with_weight=True):
         bound = bound + np.abs(stor - ry) + np.abs(ry) * 2.0 ** -8
     err = np.abs(gy - ry)
     assert np.all(err <= bound), float(np.max(err / bound))
-    assert np.quantile(err, 0.99) <= tol * np.sqrt(np.mean(ry ** 2))
+    rms_y = np.sqrt(np.mean(ry ** 2))
+    assert np.quantile(err, 0.99) <= tol * rms_y
+    row_rms = np.sqrt(np.mean(ro ** 2, axis=-1))
+    stor_y = np.abs(torch.from_numpy(np.ascontiguousarray(ry)).to(dtype).double().numpy() - ry)
+    if dtype == torch.bfloat16:
+        stor_y = stor_y + 2.0 ** -9 * np.abs(ry)
+    flat = {th: float(np.max((err - stor_y)[row_rms >= th * rms_o])) / rms_y for th in (0.1, 1.0)}
+    print(f"gate flat error beyond storage, rows with RMS(o_row) >= 0.1 / 1 RMS(o): "
+          f"{flat[0.1]:.4f} / {flat[1.0]:.4f}")
+    assert flat[1.0] <= tol, flat
 
 
 @pytest.mark.parametrize("dtype,d", [(torch.bfloat16, 128), (torch.float32, 64),

@@ -254,6 +254,27 @@ def test_decay_bound_numbers():
     assert g.min() >= -5.0 and g.max() <= 0.0
 
 
+def test_decay_across_the_bound_closed_form():
+    """One writing token after a sub-tile at the bound: with every key the same unit vector
+    and only token 15 writing (beta = 1, v = 100), o_r = 100 e^{gamma_r - gamma_15} for
+    r >= 15 and the state ends at 100 e^{gamma_63 - gamma_15} in that key's row.  Tokens
+    0-15 decay by -5 each (the sub-tile reaches -80) and later ones by -0.25, so the values
+    reach e^-12 of the write: the oracle carries them in full (they are far above fp64's
+    range limits)."""
+    T, d = 64, 4
+    q = np.zeros((1, T, 1, d)); q[..., 0] = 1.0
+    k = q.copy()
+    v = np.zeros((1, T, 1, d)); v[0, 15] = 100.0
+    g = np.full((1, T, 1, d), -0.25); g[0, :16] = -5.0
+    b = np.zeros((1, T, 1)); b[0, 15] = 1.0
+    o, s = oracle.forward(q, k, v, g, b)
+    r = np.arange(T)
+    ref = np.where(r >= 15, 100.0 * np.exp(-0.25 * np.maximum(r - 15, 0)), 0.0)
+    np.testing.assert_allclose(o[0, :, 0, 1], ref, rtol=1e-13, atol=0)
+    np.testing.assert_allclose(s[0, 0, 0, :], 100.0 * math.exp(-12.0), rtol=1e-13)
+    assert np.count_nonzero(s[0, 0, 1:, :]) == 0
+
+
 # ----------------------------------------------------------------------------- planted mistakes
 def _mutants():
     src = open(ORACLE_SRC).read()
