@@ -19,9 +19,10 @@
  *   - Pointers are DEVICE pointers unless stated; tensors are dense, row-major,
  *     contiguous, and must be 16-byte aligned (cu_seqlens / state_indices:
  *     4-byte aligned).  The caller allocates and owns all memory; the library
- *     allocates nothing and keeps no state between calls.
+ *     allocates nothing and keeps no state between calls besides one device-wide
+ *     count of expired device waits (kda_device_status reads and clears it).
  *   - Calls are asynchronous on `stream` (0 = legacy default stream) and do not
- *     synchronise the host.  Argument errors are detected on the host, before
+ *     synchronise the host (kda_device_status excepted).  Argument errors are detected on the host, before
  *     anything is launched; on error nothing is written.  Launch failures map
  *     to KDA_ERR_CUDA.  Faults of a launched kernel surface at the caller's next
  *     synchronisation, as for any CUDA call.
@@ -62,7 +63,7 @@ typedef enum {
     KDA_ERR_ALIGN = 4,       /* a pointer is not aligned as required              */
     KDA_ERR_WORKSPACE = 5,   /* reserved: workspace too small                     */
     KDA_ERR_CUDA = 6,        /* a CUDA runtime call or launch failed              */
-    KDA_ERR_TIMEOUT = 7      /* reserved: a bounded device wait gave up           */
+    KDA_ERR_TIMEOUT = 7      /* a bounded device wait gave up (kda_device_status) */
 } kda_status_t;
 
 typedef enum { KDA_F32 = 0, KDA_BF16 = 1 } kda_dtype_t;
@@ -268,6 +269,16 @@ kda_status_t kda_recurrent_steps(const void *q, const void *k, const void *v,
                                  const int32_t *state_indices, const int32_t *num_tokens,
                                  void *out, int update_state,
                                  const kda_dims_t *dims, cudaStream_t stream);
+
+/* kda_device_status -- waits for the work queued on `stream` to finish, then reads and
+ * clears the current device's count of device-side waits of the tensor-core chunk kernel that
+ * gave up (see kda_chunk_fwd_bounded).  Returns KDA_ERR_TIMEOUT when at least one wait gave up
+ * since the previous call on this device (from any stream), KDA_OK when none did, and
+ * KDA_ERR_CUDA when the stream or the copies fail.  The count is device-global: calls that
+ * run concurrently on other streams of the device report into the same count.  This is the
+ * only call of the library that synchronises the host; it does not depend on final_state
+ * being requested. */
+kda_status_t kda_device_status(cudaStream_t stream);
 
 /* A static, human-readable name for a status code (never NULL). */
 const char *kda_status_string(kda_status_t status);

@@ -1,6 +1,6 @@
-// libkda C ABI: argument validation and kernel dispatch.  No allocation, no
-// host synchronisation, no global mutable state besides per-function
-// attribute caches inside the launchers.
+// libkda C ABI: argument validation and kernel dispatch.  No allocation; no host
+// synchronisation except in kda_device_status; no global mutable state besides per-function
+// attribute caches inside the launchers and the device's count of expired bounded waits.
 #include <cstdint>
 #include <cuda_runtime.h>
 
@@ -58,6 +58,12 @@ extern "C" const char *kda_status_string(kda_status_t s) {
         case KDA_ERR_TIMEOUT: return "a bounded device wait gave up";
     }
     return "unknown status";
+}
+
+extern "C" kda_status_t kda_device_status(cudaStream_t stream) {
+    unsigned int n = 0;
+    if (kda::take_wait_expiries(stream, &n) != cudaSuccess) return KDA_ERR_CUDA;
+    return n ? KDA_ERR_TIMEOUT : KDA_OK;
 }
 
 extern "C" int kda_chunk_fwd_selected_impl(const kda_dims_t *d) {

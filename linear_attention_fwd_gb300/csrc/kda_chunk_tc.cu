@@ -57,6 +57,8 @@
 
 namespace kda {
 
+// Count of bounded device waits that gave up, on this device, since the host last read it
+// (take_wait_expiries).  Device-global status, not working memory.
 __device__ unsigned int g_kda_tc_timeouts = 0;
 
 namespace {
@@ -1163,6 +1165,17 @@ static int auto_segments(const ChunkArgs &a, int64_t units, int64_t tokens) {
         cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
         return 1;
     return segments_for(units, tokens, a.num_seqs, sms);
+}
+
+cudaError_t take_wait_expiries(cudaStream_t st, unsigned int *count) {
+    static const unsigned int zero = 0;
+    cudaError_t e = cudaMemcpyFromSymbolAsync(count, g_kda_tc_timeouts, sizeof(unsigned int), 0,
+                                              cudaMemcpyDeviceToHost, st);
+    if (e == cudaSuccess)
+        e = cudaMemcpyToSymbolAsync(g_kda_tc_timeouts, &zero, sizeof(unsigned int), 0,
+                                    cudaMemcpyHostToDevice, st);
+    if (e == cudaSuccess) e = cudaStreamSynchronize(st);
+    return e;
 }
 
 bool chunk_tc_supported(int dk, int dv, kda_dtype_t dt) {

@@ -82,6 +82,8 @@ template <> __device__ __forceinline__ __nv_bfloat16 from_f<__nv_bfloat16>(float
 cudaError_t launch_chunk_simt(const ChunkArgs &a, int dk, int dv, kda_dtype_t dt, cudaStream_t s);
 cudaError_t launch_chunk_tc(const ChunkArgs &a, int dk, int dv, kda_dtype_t dt, cudaStream_t s);
 bool chunk_tc_supported(int dk, int dv, kda_dtype_t dt);
+// Waits for `st`, then reads and clears this device's count of expired bounded waits.
+cudaError_t take_wait_expiries(cudaStream_t st, unsigned int *count);
 // Segments per (sequence, head) the tensor-core launcher picks for a plain call on a GPU with
 // `sms` SMs: floor(sms / units), at most 8, lowered until segments average >= 16 chunks.
 int segments_for(int64_t units, int64_t tokens, int64_t num_seqs, int sms);

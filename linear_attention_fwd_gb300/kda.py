@@ -25,7 +25,7 @@ IMPL_NAMES = {v: k for k, v in IMPLS.items()}
 EXPORTED = ("kda_chunk_fwd", "kda_chunk_fwd_with", "kda_chunk_fwd_bounded", "kda_chunk_fwd_segmented",
             "kda_chunk_fwd_checkpointed", "kda_chunk_fwd_auto_segments",
             "kda_chunk_fwd_gated", "kda_chunk_fwd_selected_impl", "kda_recurrent_step",
-            "kda_recurrent_steps", "kda_status_string")
+            "kda_recurrent_steps", "kda_device_status", "kda_status_string")
 
 
 class KdaDims(ctypes.Structure):
@@ -72,6 +72,8 @@ def lib() -> ctypes.CDLL:
         L.kda_recurrent_step.argtypes = [vp] * 8 + [dp, vp]
         L.kda_recurrent_steps.restype = ctypes.c_int
         L.kda_recurrent_steps.argtypes = [vp] * 9 + [ctypes.c_int, dp, vp]
+        L.kda_device_status.restype = ctypes.c_int
+        L.kda_device_status.argtypes = [vp]
         L.kda_status_string.restype = ctypes.c_char_p
         L.kda_status_string.argtypes = [ctypes.c_int]
         _lib = L
@@ -80,6 +82,14 @@ def lib() -> ctypes.CDLL:
 
 def kda_status_string(status: int) -> str:
     return lib().kda_status_string(int(status)).decode()
+
+
+def kda_device_status(stream=None) -> int:
+    """Wait for `stream` (default: the current one) and return the device's status code:
+    KDA_ERR_TIMEOUT when a bounded device wait gave up since the last call, else KDA_OK
+    (the count is cleared)."""
+    st = torch.cuda.current_stream() if stream is None else stream
+    return int(lib().kda_device_status(ctypes.c_void_p(st.cuda_stream)))
 
 
 def _dtype_code(t: torch.dtype) -> int:
