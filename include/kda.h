@@ -61,7 +61,7 @@ typedef enum {
     KDA_ERR_SHAPE = 2,       /* inconsistent or non-positive dimensions           */
     KDA_ERR_UNSUPPORTED = 3, /* valid but not implemented (head size, dtype, impl) */
     KDA_ERR_ALIGN = 4,       /* a pointer is not aligned as required              */
-    KDA_ERR_WORKSPACE = 5,   /* reserved: workspace too small                     */
+    KDA_ERR_WORKSPACE = 5,   /* the workspace is smaller than needed              */
     KDA_ERR_CUDA = 6,        /* a CUDA runtime call or launch failed              */
     KDA_ERR_TIMEOUT = 7      /* a bounded device wait gave up (kda_device_status) */
 } kda_status_t;
@@ -167,6 +167,33 @@ kda_status_t kda_chunk_fwd_segmented(kda_impl_t impl,
                                      void *out, float *final_state, int32_t segments,
                                      const kda_dims_t *dims, cudaStream_t stream);
 
+/* kda_chunk_fwd_ws -- kda_chunk_fwd in two passes over a caller-owned device workspace.
+ *
+ * For bf16 with dk = dv = 128 the chunk work splits in two: the part that does not depend on
+ * the recurrent state (the decay-scaled products A and M of each 64-token chunk and
+ * T = (I + A)^-1, "はじめての自然言語処理 -- Kimi K3", section 3.1, the chunkwise form)
+ * runs first for every chunk of every sequence at once and is written to `workspace`; the
+ * state chain then runs per (sequence, head) from it.  Results equal kda_chunk_fwd's up to
+ * rounding.  Other shapes (and seqlen = 0) run kda_chunk_fwd and ignore the workspace.
+ *   workspace       : device memory of at least kda_chunk_fwd_workspace_bytes(dims) bytes,
+ *                     16-byte aligned, owned by the caller; its contents on entry do not
+ *                     matter and are overwritten.  Calls that overlap in time on the device
+ *                     need workspaces of their own.
+ *   workspace_bytes : its size.
+ * Errors: as kda_chunk_fwd, plus KDA_ERR_NULL for a NULL workspace, KDA_ERR_WORKSPACE when it
+ * is smaller than needed, KDA_ERR_ALIGN when it is not 16-byte aligned. */
+kda_status_t kda_chunk_fwd_ws(const void *q, const void *k, const void *v,
+                              const void *g, const void *beta,
+                              const float *initial_state, const int32_t *cu_seqlens,
+                              void *out, float *final_state,
+                              void *workspace, size_t workspace_bytes,
+                              const kda_dims_t *dims, cudaStream_t stream);
+
+/* Bytes of workspace kda_chunk_fwd_ws needs for `dims`: 24 KB per (64-token chunk, head)
+ * counted as heads * (ceil(batch * seqlen / 64) + num_seqs), plus (num_seqs + 1) * 4 bytes
+ * rounded up to 1 KB; 0 when it runs the one-pass path (host arithmetic only). */
+size_t kda_chunk_fwd_workspace_bytes(const kda_dims_t *dims);
+
 /* kda_chunk_fwd_checkpointed -- kda_chunk_fwd that also writes the recurrent state at every
  * multiple of `checkpoint_interval` tokens strictly inside each sequence, for prefix caching.
  * The pages' account: the cache hashes prompts in 512-token units and keeps recurrent-state
@@ -271,13 +298,13 @@ kda_status_t kda_recurrent_steps(const void *q, const void *k, const void *v,
                                  const kda_dims_t *dims, cudaStream_t stream);
 
 /* kda_device_status -- waits for the work queued on `stream` to finish, then reads and
- * clears the current device's count of device-side waits of the tensor-core chunk kernel that
- * gave up (see kda_chunk_fwd_bounded).  Returns KDA_ERR_TIMEOUT when at least one wait gave up
- * since the previous call on this device (from any stream), KDA_OK when none did, and
- * KDA_ERR_CUDA when the stream or the copies fail.  The count is device-global: calls that
- * run concurrently on other streams of the device report into the same count.  This is the
- * only call of the library that synchronises the host; it does not depend on final_state
- * being requested. */
+ * clears the current device's count of device-side waits of the tensor-core chunk kernels
+ * that gave up (see kda_chunk_fwd_bounded; the two passes of kda_chunk_fwd_ws count theirs
+ * too).  Returns KDA_ERR_TIMEOUT when at least one wait gave up since the previous call on
+ * this device (from any stream), KDA_OK when none did, and KDA_ERR_CUDA when the stream or
+ * the copies fail.  The count is device-global: calls that run concurrently on other streams
+ * of the device report into the same count.  This is the only call of the library that
+ * synchronises the host; it does not depend on final_state being requested. */
 kda_status_t kda_device_status(cudaStream_t stream);
 
 /* A static, human-readable name for a status code (never NULL). */

@@ -61,9 +61,41 @@ extern "C" const char *kda_status_string(kda_status_t s) {
 }
 
 extern "C" kda_status_t kda_device_status(cudaStream_t stream) {
-    unsigned int n = 0;
-    if (kda::take_wait_expiries(stream, &n) != cudaSuccess) return KDA_ERR_CUDA;
-    return n ? KDA_ERR_TIMEOUT : KDA_OK;
+    unsigned int n1 = 0, n2 = 0, n3 = 0;
+    if (kda::take_wait_expiries(stream, &n1) != cudaSuccess || kda::take_prep_expiries(stream, &n2) != cudaSuccess ||
+        kda::take_state_expiries(stream, &n3) != cudaSuccess)
+        return KDA_ERR_CUDA;
+    return (n1 || n2 || n3) ? KDA_ERR_TIMEOUT : KDA_OK;
+}
+
+extern "C" size_t kda_chunk_fwd_workspace_bytes(const kda_dims_t *d) {
+    if (d == nullptr || d->heads <= 0 || d->num_seqs <= 0 || d->batch <= 0 || d->seqlen < 0) return 0;
+    if (!kda::chunk_tc_supported(d->dk, d->dv, d->dtype)) return 0;
+    const int64_t tokens = (int64_t)d->batch * d->seqlen;
+    if (tokens == 0) return 0;
+    return kda::two_pass_workspace_bytes(tokens, d->num_seqs, d->heads);
+}
+
+extern "C" kda_status_t kda_chunk_fwd_ws(const void *q, const void *k, const void *v, const void *g,
+                                         const void *beta, const float *initial_state,
+                                         const int32_t *cu_seqlens, void *out, float *final_state,
+                                         void *workspace, size_t workspace_bytes, const kda_dims_t *d,
+                                         cudaStream_t stream) {
+    kda_status_t st = check_chunk(KDA_IMPL_AUTO, q, k, v, g, beta, initial_state, cu_seqlens, out,
+                                  final_state, d);
+    if (st != KDA_OK) return st;
+    const size_t need = kda_chunk_fwd_workspace_bytes(d);
+    if (need == 0)   // no tokens, or a shape the two-pass kernels do not take: the one-pass path
+        return kda_chunk_fwd(q, k, v, g, beta, initial_state, cu_seqlens, out, final_state, d, stream);
+    if (workspace == nullptr) return KDA_ERR_NULL;
+    if (workspace_bytes < need) return KDA_ERR_WORKSPACE;
+    if (!aligned(workspace, 16)) return KDA_ERR_ALIGN;
+    kda::ChunkArgs a{q, k, v, g, beta, initial_state, cu_seqlens, out, final_state,
+                     (int64_t)d->seqlen, d->num_seqs, d->heads, nullptr, nullptr, 0.f,
+                     nullptr, nullptr, 0, 1u << 20, 1};
+    cudaError_t e = kda::launch_chunk_prep(a, workspace, stream);
+    if (e == cudaSuccess) e = kda::launch_chunk_state(a, workspace, stream);
+    return e == cudaSuccess ? KDA_OK : KDA_ERR_CUDA;
 }
 
 extern "C" int kda_chunk_fwd_selected_impl(const kda_dims_t *d) {

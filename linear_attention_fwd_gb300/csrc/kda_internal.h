@@ -78,6 +78,21 @@ template <typename T> __device__ __forceinline__ T from_f(float x);
 template <> __device__ __forceinline__ float from_f<float>(float x) { return x; }
 template <> __device__ __forceinline__ __nv_bfloat16 from_f<__nv_bfloat16>(float x) { return __float2bfloat16_rn(x); }
 
+// Two-pass form of the bf16 d = 128 chunk forward: pass 1 (kda_chunk_prep.cu) writes, per
+// (64-token chunk, head), T = (I + A)^-1, M and M - fp16(M) as three 64 x 64 fp16 tiles into
+// a caller-owned workspace; pass 2 (kda_chunk_state.cu) runs the state chain from them.  The
+// workspace starts with int32 chunk_base[N + 1] (the count of chunks before each sequence),
+// padded to 1 KB, followed by the slots; slot (chunk_base[n] + c) * H + h.
+constexpr size_t kSlotBytes = 3 * 64 * 64 * 2;
+inline size_t ws_header_bytes(int64_t num_seqs) { return ((size_t)(num_seqs + 1) * 4 + 1023) / 1024 * 1024; }
+int64_t two_pass_slots(int64_t tokens, int64_t num_seqs, int heads);
+size_t two_pass_workspace_bytes(int64_t tokens, int64_t num_seqs, int heads);
+cudaError_t launch_chunk_prep(const ChunkArgs &a, void *workspace, cudaStream_t s);
+cudaError_t launch_chunk_state(const ChunkArgs &a, const void *workspace, cudaStream_t s);
+// Wait for `st`, then read and clear the pass's count of expired bounded waits.
+cudaError_t take_prep_expiries(cudaStream_t st, unsigned int *count);
+cudaError_t take_state_expiries(cudaStream_t st, unsigned int *count);
+
 // Launchers (host).  Each returns cudaSuccess or the launch error.
 cudaError_t launch_chunk_simt(const ChunkArgs &a, int dk, int dv, kda_dtype_t dt, cudaStream_t s);
 cudaError_t launch_chunk_tc(const ChunkArgs &a, int dk, int dv, kda_dtype_t dt, cudaStream_t s);

@@ -25,7 +25,8 @@ IMPL_NAMES = {v: k for k, v in IMPLS.items()}
 EXPORTED = ("kda_chunk_fwd", "kda_chunk_fwd_with", "kda_chunk_fwd_bounded", "kda_chunk_fwd_segmented",
             "kda_chunk_fwd_checkpointed", "kda_chunk_fwd_auto_segments",
             "kda_chunk_fwd_gated", "kda_chunk_fwd_selected_impl", "kda_recurrent_step",
-            "kda_recurrent_steps", "kda_device_status", "kda_status_string")
+            "kda_recurrent_steps", "kda_device_status", "kda_chunk_fwd_ws",
+            "kda_chunk_fwd_workspace_bytes", "kda_status_string")
 
 
 class KdaDims(ctypes.Structure):
@@ -72,6 +73,10 @@ def lib() -> ctypes.CDLL:
         L.kda_recurrent_step.argtypes = [vp] * 8 + [dp, vp]
         L.kda_recurrent_steps.restype = ctypes.c_int
         L.kda_recurrent_steps.argtypes = [vp] * 9 + [ctypes.c_int, dp, vp]
+        L.kda_chunk_fwd_ws.restype = ctypes.c_int
+        L.kda_chunk_fwd_ws.argtypes = [vp] * 10 + [ctypes.c_size_t, dp, vp]
+        L.kda_chunk_fwd_workspace_bytes.restype = ctypes.c_size_t
+        L.kda_chunk_fwd_workspace_bytes.argtypes = [dp]
         L.kda_device_status.restype = ctypes.c_int
         L.kda_device_status.argtypes = [vp]
         L.kda_status_string.restype = ctypes.c_char_p
@@ -128,9 +133,16 @@ def chunk_dims(q, v, cu_seqlens=None) -> KdaDims:
     return KdaDims(B, T, n, H, dk, dv, _dtype_code(q.dtype))
 
 
+def kda_chunk_fwd_workspace_bytes(q, v, cu_seqlens=None) -> int:
+    """Bytes of device workspace the two-pass path needs for these shapes (0: one-pass)."""
+    dims = chunk_dims(q, v, cu_seqlens)
+    return int(lib().kda_chunk_fwd_workspace_bytes(ctypes.byref(dims)))
+
+
 def kda_chunk_fwd(q, k, v, g, beta, initial_state=None, cu_seqlens=None, *, out=None,
                   final_state=None, output_final_state: bool = True, impl: str = "auto",
-                  stream=None, wait_polls: int | None = None, segments: int | None = None):
+                  stream=None, wait_polls: int | None = None, segments: int | None = None,
+                  workspace=None):
     """Chunkwise KDA forward (prefill / prefix-cache resume) through libkda.
 
     q, k, g: [B, T, H, dk]; v: [B, T, H, dv]; beta: [B, T, H] (all fp32 or all
@@ -141,6 +153,9 @@ def kda_chunk_fwd(q, k, v, g, beta, initial_state=None, cu_seqlens=None, *, out=
     a unit whose wait gives up gets a NaN final state.
     segments: CTAs per (sequence, head) on the tensor-core kernel (kda_chunk_fwd_segmented;
     0 = the library's choice, which is also what the default call does).
+    impl="two_pass": kda_chunk_fwd_ws, the state-independent chunk work for all chunks first,
+    then the state chain; `workspace` is a uint8 CUDA tensor of at least
+    kda_chunk_fwd_workspace_bytes bytes (allocated here, by the caller's allocator, when None).
     """
     dev = q.device
     for name, t in (("q", q), ("k", k), ("v", v), ("g", g), ("beta", beta)):
@@ -163,6 +178,18 @@ def kda_chunk_fwd(q, k, v, g, beta, initial_state=None, cu_seqlens=None, *, out=
             _ptr(cu_seqlens), _ptr(out), _ptr(final_state))
     if wait_polls is not None and segments is not None:
         raise ValueError("wait_polls and segments select different entry points")
+    if impl == "two_pass":
+        if wait_polls is not None or segments is not None:
+            raise ValueError("the two-pass path takes neither wait_polls nor segments")
+        need = int(lib().kda_chunk_fwd_workspace_bytes(ctypes.byref(dims)))
+        if workspace is None:
+            workspace = torch.empty(max(need, 1), dtype=torch.uint8, device=dev)
+        _check_dev("workspace", workspace, dev, torch.uint8)
+        st = lib().kda_chunk_fwd_ws(*args, _ptr(workspace), ctypes.c_size_t(workspace.numel()),
+                                    ctypes.byref(dims), _stream_handle(stream))
+        if st != KDA_OK:
+            raise KdaError(st, "kda_chunk_fwd_ws")
+        return out, final_state
     if segments is not None:
         st = lib().kda_chunk_fwd_segmented(IMPLS[impl], *args, ctypes.c_int32(int(segments)),
                                            ctypes.byref(dims), _stream_handle(stream))
