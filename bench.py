@@ -35,9 +35,14 @@ SMI_FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.act
               "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
 KERNEL_SRC = {"tc": "linear_attention_fwd_gb300/csrc/kda_chunk_tc.cu",
               "simt": "linear_attention_fwd_gb300/csrc/kda_chunk_simt.cu",
-              "decode": "linear_attention_fwd_gb300/csrc/kda_decode.cu"}
+              "decode": "linear_attention_fwd_gb300/csrc/kda_decode.cu",
+              "two_pass": "linear_attention_fwd_gb300/csrc/kda_chunk_state.cu"}
 KERNEL_NAME = {"tc": "kda_chunk_tc_kernel", "simt": "kda_chunk_simt_kernel",
-               "decode": "kda_recurrent_step_kernel"}
+               "decode": "kda_recurrent_step_kernel",
+               "two_pass": "kda_chunk_prep_kernel+kda_chunk_state_kernel"}
+# kernels one prefill step launches: the two-pass path scans the chunk counts, then runs
+# its chunk-parallel pass and its state pass
+LAUNCHES_PER_STEP = {"tc": 1, "simt": 1, "two_pass": 3}
 
 
 # ----------------------------------------------------------------------------- helpers
@@ -290,11 +295,16 @@ def run_ours(args):
     out = torch.empty((B, T, H, dv), dtype=q.dtype, device=dev)
     fs = torch.empty((N, H, dk, dv), dtype=torch.float32, device=dev)
     stream = torch.cuda.current_stream()
+    # the two-pass path's workspace (per-chunk matrices), allocated once outside the timed region
+    wsp = {}
+    if kernel == "two_pass":
+        wsp["workspace"] = torch.empty(kda.kda_chunk_fwd_workspace_bytes(q, v, inp["cu_seqlens"]),
+                                       dtype=torch.uint8, device=dev)
 
     def step():
         kda.kda_chunk_fwd(inp["q"], inp["k"], inp["v"], inp["g"], inp["beta"],
                           inp["initial_state"], inp["cu_seqlens"], out=out, final_state=fs,
-                          impl=kernel, stream=stream)
+                          impl=kernel, stream=stream, **wsp)
 
     for _ in range(args.warmup):
         step()
@@ -365,7 +375,7 @@ def run_ours(args):
             with torch.cuda.stream(stream):
                 kda.kda_chunk_fwd(dbuf[sl]["q"], dbuf[sl]["k"], dbuf[sl]["v"], dbuf[sl]["g"],
                                   dbuf[sl]["beta"], s0d[sl], inp["cu_seqlens"], out=out,
-                                  final_state=fs, impl=kernel, stream=stream)
+                                  final_state=fs, impl=kernel, stream=stream, **wsp)
                 ev_free[sl].record(stream)
                 out_h.copy_(out, non_blocking=True)
                 fs_h.copy_(fs, non_blocking=True)
@@ -426,7 +436,7 @@ def run_ours(args):
             "value": value, "unit": "tokens/s", "n_gpus": ws, "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None,
-            "dtype": "bf16" if kernel == "tc" else "f32",
+            "dtype": "bf16" if kernel in ("tc", "two_pass") else "f32",
             "data": "synthetic",
             "config": {"workload": args.workload, "batch": B, "seq_len": T, "heads": H,
                        "dk": dk, "dv": dv, "num_seqs": N, "io_dtype": str(q.dtype).split(".")[-1],
@@ -438,7 +448,7 @@ def run_ours(args):
                        "l2": f"inputs larger than L2 ({bytes_launch / 1e9:.2f} GB per step)",
                        "note": w.note},
             "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e,
-            "gpu_launches": args.steps, "clocks": clocks, "decode": decode,
+            "gpu_launches": args.steps * LAUNCHES_PER_STEP[kernel], "clocks": clocks, "decode": decode,
             "extras": extras,
         }
         print(json.dumps(line), flush=True)
@@ -555,7 +565,7 @@ def main():
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--workload", default="prefill_b4_h32_t8192")
-    ap.add_argument("--kernel", default="auto", choices=["auto", "simt", "tc"])
+    ap.add_argument("--kernel", default="auto", choices=["auto", "simt", "tc", "two_pass"])
     ap.add_argument("--decode-steps", type=int, default=1000)
     ap.add_argument("--cpu-budget", type=float, default=12.0,
                     help="seconds of oracle work for the CPU baseline sample")

@@ -122,7 +122,9 @@ def test_expired_waits_under_segments(K):
                               device="cuda", seed=308, init_state=True)
     out, sT = run(K, inp, wait_polls=0)
     assert torch.isnan(sT).all() and torch.isnan(out.float()).all()
+    assert K.kda_device_status() == K.KDA_ERR_TIMEOUT   # reported to the host, and cleared
     out, sT = run(K, inp)
+    assert K.kda_device_status() == K.KDA_OK
     check_prefill(compare_prefill(inp, out, sT), BF)
 
 
