@@ -194,6 +194,30 @@ kda_status_t kda_chunk_fwd_ws(const void *q, const void *k, const void *v,
  * rounded up to 1 KB; 0 when it runs the one-pass path (host arithmetic only). */
 size_t kda_chunk_fwd_workspace_bytes(const kda_dims_t *dims);
 
+/* kda_chunk_fwd_noalloc -- kda_chunk_fwd_ws over a fixed scratch area compiled into this
+ * library, for callers that cannot supply device memory when they call (a host whose device
+ * budget is fixed at start-up, a C host with no device allocator, a loop that cannot afford the
+ * device-wide synchronisation of cudaMalloc / cudaFree).  The pages have no counterpart: this
+ * is an interface for such callers, not part of the method.  The call allocates nothing.
+ *   Scratch: one area of KDA_NOALLOC_SCRATCH_BYTES bytes per device.  Calls with
+ *            kda_chunk_fwd_workspace_bytes(dims) above that are rejected with
+ *            KDA_ERR_WORKSPACE before anything runs.  Nothing in the area has to start at
+ *            zero, and nothing is carried from one call to the next.
+ *   Set-up:  the first call with a device current looks up the area's address on that device
+ *            (and loads the library's device code there if that has not happened); make that
+ *            first call before any stream capture.  Later calls only read the kept address.
+ *   Overlap: calls that overlap in time on the same device (several streams or host threads)
+ *            share the area and race; the caller serialises them.
+ * Arguments, layouts, results and the other errors are kda_chunk_fwd_ws's (shapes the
+ * two-pass kernels do not take, and seqlen = 0, run kda_chunk_fwd); KDA_ERR_CUDA also when the
+ * address lookup fails. */
+#define KDA_NOALLOC_SCRATCH_BYTES ((size_t)64 << 20)
+kda_status_t kda_chunk_fwd_noalloc(const void *q, const void *k, const void *v,
+                                   const void *g, const void *beta,
+                                   const float *initial_state, const int32_t *cu_seqlens,
+                                   void *out, float *final_state,
+                                   const kda_dims_t *dims, cudaStream_t stream);
+
 /* kda_chunk_fwd_checkpointed -- kda_chunk_fwd that also writes the recurrent state at every
  * multiple of `checkpoint_interval` tokens strictly inside each sequence, for prefix caching.
  * The pages' account: the cache hashes prompts in 512-token units and keeps recurrent-state

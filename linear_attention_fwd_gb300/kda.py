@@ -26,7 +26,7 @@ EXPORTED = ("kda_chunk_fwd", "kda_chunk_fwd_with", "kda_chunk_fwd_bounded", "kda
             "kda_chunk_fwd_checkpointed", "kda_chunk_fwd_auto_segments",
             "kda_chunk_fwd_gated", "kda_chunk_fwd_selected_impl", "kda_recurrent_step",
             "kda_recurrent_steps", "kda_device_status", "kda_chunk_fwd_ws",
-            "kda_chunk_fwd_workspace_bytes", "kda_status_string")
+            "kda_chunk_fwd_workspace_bytes", "kda_chunk_fwd_noalloc", "kda_status_string")
 
 
 class KdaDims(ctypes.Structure):
@@ -77,6 +77,8 @@ def lib() -> ctypes.CDLL:
         L.kda_chunk_fwd_ws.argtypes = [vp] * 10 + [ctypes.c_size_t, dp, vp]
         L.kda_chunk_fwd_workspace_bytes.restype = ctypes.c_size_t
         L.kda_chunk_fwd_workspace_bytes.argtypes = [dp]
+        L.kda_chunk_fwd_noalloc.restype = ctypes.c_int
+        L.kda_chunk_fwd_noalloc.argtypes = [vp] * 9 + [dp, vp]
         L.kda_device_status.restype = ctypes.c_int
         L.kda_device_status.argtypes = [vp]
         L.kda_status_string.restype = ctypes.c_char_p
@@ -137,6 +139,35 @@ def kda_chunk_fwd_workspace_bytes(q, v, cu_seqlens=None) -> int:
     """Bytes of device workspace the two-pass path needs for these shapes (0: one-pass)."""
     dims = chunk_dims(q, v, cu_seqlens)
     return int(lib().kda_chunk_fwd_workspace_bytes(ctypes.byref(dims)))
+
+
+# KDA_NOALLOC_SCRATCH_BYTES: the fixed scratch area kda_chunk_fwd_noalloc runs in, per device
+NOALLOC_SCRATCH_BYTES = 64 << 20
+
+
+def kda_chunk_fwd_noalloc(q, k, v, g, beta, initial_state, cu_seqlens, out, final_state,
+                          stream=None):
+    """kda_chunk_fwd_noalloc: the two-pass forward in the library's own fixed scratch area.
+
+    Every tensor is the caller's (out and final_state included; final_state may be None): the
+    call allocates no device memory.  The first call with a device current sets the scratch
+    area up on it; calls that overlap in time on one device race on that area."""
+    dev = q.device
+    for name, t in (("q", q), ("k", k), ("v", v), ("g", g), ("beta", beta), ("out", out)):
+        _check_dev(name, t, dev, q.dtype)
+    _check_dev("initial_state", initial_state, dev, torch.float32)
+    _check_dev("cu_seqlens", cu_seqlens, dev, torch.int32)
+    _check_dev("final_state", final_state, dev, torch.float32)
+    if k.shape != q.shape or g.shape != q.shape or v.shape[:3] != q.shape[:3] \
+            or beta.shape != q.shape[:3] or out.shape != v.shape:
+        raise ValueError("inconsistent q/k/v/g/beta/out shapes")
+    dims = chunk_dims(q, v, cu_seqlens)
+    st = lib().kda_chunk_fwd_noalloc(_ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta),
+                                     _ptr(initial_state), _ptr(cu_seqlens), _ptr(out),
+                                     _ptr(final_state), ctypes.byref(dims), _stream_handle(stream))
+    if st != KDA_OK:
+        raise KdaError(st, "kda_chunk_fwd_noalloc")
+    return out, final_state
 
 
 def kda_chunk_fwd(q, k, v, g, beta, initial_state=None, cu_seqlens=None, *, out=None,

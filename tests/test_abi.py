@@ -205,3 +205,17 @@ def test_segment_count_argument_is_checked(K):
         st = K.lib().kda_chunk_fwd_segmented(2, *[vp(FAKE)] * 5, None, None, vp(FAKE), None,
                                              ctypes.c_int32(bad), ctypes.byref(d), None)
         assert st == 2   # KDA_ERR_SHAPE
+
+
+def test_noalloc_limit_and_rejection(K):
+    # the binding's copy of the scratch limit is the header's
+    src = open(HEADER).read()
+    m = re.search(r"#define KDA_NOALLOC_SCRATCH_BYTES \(\(size_t\)(\d+) << (\d+)\)", src)
+    assert m and int(m.group(1)) << int(m.group(2)) == K.NOALLOC_SCRATCH_BYTES
+    vp = ctypes.c_void_p
+    args = [vp(FAKE)] * 5 + [None, None, vp(FAKE), None]
+    assert K.lib().kda_chunk_fwd_noalloc(*args, None, None) == K.KDA_ERR_NULL
+    # a workspace above the limit is rejected on the host, before the device is touched
+    big = dims(batch=1, seqlen=1 << 20, num_seqs=1, heads=32)
+    assert K.lib().kda_chunk_fwd_workspace_bytes(ctypes.byref(big)) > K.NOALLOC_SCRATCH_BYTES
+    assert K.lib().kda_chunk_fwd_noalloc(*args, ctypes.byref(big), None) == K.KDA_ERR_WORKSPACE
