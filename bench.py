@@ -441,10 +441,14 @@ def run_ours(args):
             "config": {"workload": args.workload, "batch": B, "seq_len": T, "heads": H,
                        "dk": dk, "dv": dv, "num_seqs": N, "io_dtype": str(q.dtype).split(".")[-1],
                        "kernel": kernel, "parallelism": f"replicas x{ws} (independent units)",
-                       "ctas_per_unit": (kda.kda_chunk_fwd_auto_segments(
+                       "ctas": (kda.kda_chunk_fwd_auto_ctas(
                            kda.chunk_dims(q, inp["v"], inp.get("cu_seqlens")),
+                           inp.get("cu_seqlens") is not None,
                            torch.cuda.get_device_properties(dev).multi_processor_count)
-                           if kernel == "tc" else 1),
+                           if kernel == "tc" else N * H),
+                       "schedule": ("balanced: each CTA an equal share of the (sequence, head, "
+                                    "chunk) items" if kernel == "tc" and inp.get("cu_seqlens") is None
+                                    else "one CTA per (sequence, head) or uniform segments"),
                        "l2": f"inputs larger than L2 ({bytes_launch / 1e9:.2f} GB per step)",
                        "note": w.note},
             "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e,

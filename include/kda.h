@@ -107,11 +107,13 @@ typedef struct {
  *               Offsets are clamped to [0, seqlen] on the device.
  * Returns KDA_OK or an error listed above; seqlen = 0 is valid (only the
  * final state is written: a copy of the initial state, or zeros).
- * On the tensor-core kernel, when there are fewer (sequence, head) units than
- * SMs, each sequence is split over several CTAs (kda_chunk_fwd_segmented with
- * segments = 0; kda_chunk_fwd_auto_segments reports the count); the history a
- * segment skips contributes less than 2^-160 of the norm of the state it
- * replaces, else the segment starts at the sequence start. */
+ * On the tensor-core kernel (kda_chunk_fwd_segmented with segments = 0 says how,
+ * kda_chunk_fwd_auto_ctas how many CTAs) a dense batch runs the balanced schedule:
+ * one CTA per SM, each taking an equal share of all (sequence, head, chunk)
+ * items, so that a sequence may be split between two CTAs; packed sequences
+ * split each sequence over several CTAs when there are fewer units than SMs.
+ * The history a split skips contributes less than 2^-160 of the norm of the
+ * state it replaces, else the later part starts at the sequence start. */
 kda_status_t kda_chunk_fwd(const void *q, const void *k, const void *v,
                            const void *g, const void *beta,
                            const float *initial_state, const int32_t *cu_seqlens,
@@ -152,10 +154,18 @@ kda_status_t kda_chunk_fwd_bounded(kda_impl_t impl,
  * bounds max_i exp(g_t,i) * max(1, |1 - beta_t |k_t|^2|) on the transitions' 2-norm is at most
  * 2^-160 (the state it drops contributes less than 2^-160 of its own norm), or else from the
  * start of the sequence with its initial state.  The last segment writes the final state.
- *   segments : 0 = the library's choice (what kda_chunk_fwd does: enough segments to occupy
- *              every SM when there are fewer (sequence, head) units than SMs, each of at least
- *              16 chunks on average; 1 with an output gate, checkpoints or an in-place state),
- *              1..64 = that many.
+ *   segments : 0 = the library's choice (what kda_chunk_fwd does).  A dense batch runs the
+ *              balanced schedule: the W = units x chunks items in sequence-major order are
+ *              shared out, contiguously, among G = min(SMs, W, 256) CTAs; the shares are drawn
+ *              on the host to make the largest cost small (items, plus 4 for a share that
+ *              starts inside a sequence -- its warm-up -- plus 0.5 per further sequence it
+ *              touches; a share does not end fewer than 8 chunks into a sequence it entered).
+ *              Each part that starts inside a sequence warms up as a segment does, and the
+ *              part holding the last chunk writes the final state.  Packed sequences get enough uniform segments to
+ *              occupy every SM when there are fewer (sequence, head) units than SMs, each of
+ *              at least 16 chunks on average.  1 per unit with an output gate, checkpoints or
+ *              an in-place state.
+ *              1..64 = that many uniform segments.
  * Errors: KDA_ERR_SHAPE for segments outside [0, 64]; KDA_ERR_UNSUPPORTED for segments > 1
  * with initial_state == final_state (a later segment would overwrite the state an earlier one
  * may still read).  The SIMT kernel always runs one CTA per unit.  When a bounded wait gives up
@@ -266,12 +276,14 @@ kda_status_t kda_chunk_fwd_gated(const void *q, const void *k, const void *v,
  * KDA_IMPL_TC), or -1 when the dims are invalid.  A library query (host only). */
 int kda_chunk_fwd_selected_impl(const kda_dims_t *dims);
 
-/* The number of CTAs per (sequence, head) kda_chunk_fwd gives the tensor-core kernel for
- * `dims` on a GPU with `sms` SMs (host arithmetic only, no device call): floor(sms / units)
- * with units = num_seqs * heads, at most 8, lowered until segments average at least 16
- * chunks of 64 tokens; 1 for shapes the tensor-core kernel does not run and for invalid dims.
- * A call with an output gate, checkpoints or initial_state == final_state always uses 1. */
-int kda_chunk_fwd_auto_segments(const kda_dims_t *dims, int sms);
+/* The number of CTAs kda_chunk_fwd launches for the tensor-core kernel for `dims` on a GPU
+ * with `sms` SMs (host arithmetic only, no device call).  packed = 0 (dense batch): the
+ * balanced schedule's min(sms, units * ceil(seqlen / 64)), units = num_seqs * heads.
+ * packed != 0 (cu_seqlens given): units * P with P = floor(sms / units), at most 8, lowered
+ * until segments average at least 16 chunks of 64 tokens, and at least 1.  0 for shapes the
+ * tensor-core kernel does not run, seqlen = 0 and invalid dims or SM counts.  A call with an
+ * output gate, checkpoints or initial_state == final_state runs one CTA per unit instead. */
+int kda_chunk_fwd_auto_ctas(const kda_dims_t *dims, int packed, int sms);
 
 /* kda_recurrent_step -- one decode token per row, state updated in place.
  *

@@ -104,11 +104,14 @@ extern "C" int kda_chunk_fwd_selected_impl(const kda_dims_t *d) {
     return kda::chunk_tc_supported(d->dk, d->dv, d->dtype) ? KDA_IMPL_TC : KDA_IMPL_SIMT;
 }
 
-extern "C" int kda_chunk_fwd_auto_segments(const kda_dims_t *d, int sms) {
-    if (d == nullptr || d->heads <= 0 || d->num_seqs <= 0 || d->batch <= 0 || d->seqlen < 0) return 1;
-    if (!kda::chunk_tc_supported(d->dk, d->dv, d->dtype)) return 1;
-    const int64_t tokens = (int64_t)d->batch * d->seqlen;
-    return kda::segments_for((int64_t)d->num_seqs * d->heads, tokens, d->num_seqs, sms);
+extern "C" int kda_chunk_fwd_auto_ctas(const kda_dims_t *d, int packed, int sms) {
+    if (d == nullptr || d->heads <= 0 || d->num_seqs <= 0 || d->batch <= 0 || d->seqlen <= 0 || sms <= 0)
+        return 0;
+    if (!kda::chunk_tc_supported(d->dk, d->dv, d->dtype)) return 0;
+    const int64_t tokens = (int64_t)d->batch * d->seqlen, units = (int64_t)d->num_seqs * d->heads;
+    if (!packed) return kda::balanced_ctas(units, (d->seqlen + 63) / 64, sms);
+    const int64_t ctas = units * kda::segments_for(units, tokens, d->num_seqs, sms);
+    return ctas > 0x7fffffffLL ? 0x7fffffff : (int)ctas;
 }
 
 // Validated launch of one chunked forward (optionally writing state checkpoints).

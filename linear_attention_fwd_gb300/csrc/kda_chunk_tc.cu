@@ -283,44 +283,86 @@ __device__ int warm_start(const ChunkArgs &a, int64_t bos, int h, int c_lo) {
     return 0;
 }
 
+// Balanced schedule: the boundaries x_0 = 0 <= x_1 <= ... <= x_G = W of the CTAs' shares of the
+// W items (units of nc chunks each, sequence-major), drawn on the host (draw_schedule).
+constexpr int kMaxSchedCtas = 256;
+struct SchedBounds {
+    int64_t x[kMaxSchedCtas + 1];
+};
+
 __device__ __forceinline__ void tma_tile(const CUtensorMap *map, uint32_t dst, uint32_t bar, int h,
                                          int64_t tok, uint32_t half_stride = 8192) {
     tma_load_3d(dst, map, bar, 0, h, (int)tok);
     tma_load_3d(dst + half_stride, map, bar, 64, h, (int)tok);
 }
 
-// kSeg: several CTAs per (sequence, head) (a.segments > 1); without it the segment logic folds
-// away and one CTA runs each unit from its start.
-template <bool kSeg>
+// kMode: 0 = one CTA per unit (the only mode with an output gate or checkpoints), 1 = uniform
+// segments (a.segments > 1), 2 = the balanced schedule (a.sched_ctas > 0).  Each mode is its
+// own instantiation, so that the others' logic folds away.
+template <int kMode>
 __global__ void __launch_bounds__(NT, 1)
 kda_chunk_tc_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant__ CUtensorMap tmk,
                     const __grid_constant__ CUtensorMap tmv, const __grid_constant__ CUtensorMap tmg,
                     const __grid_constant__ CUtensorMap tmz,
-                    const ChunkArgs a, const uint32_t wait_limit) {
+                    const ChunkArgs a, const uint32_t wait_limit, const __grid_constant__ SchedBounds sched) {
     extern __shared__ uint8_t smem_raw[];
     uint8_t *sm = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     const uint32_t sb = smem_u32(sm);
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int H = a.heads;
 
-    // blockIdx.x = p * units + unit: segment p of P of one (sequence, head); this CTA stores
-    // the outputs of chunks [c_lo, c_hi), running from chunk c_run (see warm_start), and the
-    // last segment writes the final state
+    // The CTA's work: pieces -- (sequence n, head h) and chunks [c_lo, c_hi) -- each run from
+    // chunk c_run (see warm_start), storing the outputs of [c_lo, c_hi); the piece that holds a
+    // unit's last chunk writes its final state.
+    //  - balanced schedule (kMode 2, dense batches): the units' chunks in sequence-major order
+    //    are W = units x chunks items; CTA b takes items [sched.x[b], sched.x[b + 1]), one piece
+    //    per unit that range touches
+    //  - uniform segments (kSeg, P = a.segments > 1): blockIdx.x = p * units + unit, chunks
+    //    [p nc / P, (p + 1) nc / P) of that unit
+    //  - otherwise blockIdx.x = unit (the longest packed sequences first), the whole unit
     const int64_t units = (int64_t)a.num_seqs * H;
-    const int P = kSeg && a.segments > 1 ? a.segments : 1;
-    const int p = kSeg ? (int)(blockIdx.x / units) : 0;
-    int n, h;
-    select_unit(a, kSeg ? (int)(blockIdx.x % units) : (int)blockIdx.x, n, h);
-    int64_t bos, eos;
-    seq_range(a, n, bos, eos);
-    const int64_t len = eos - bos;
-    const int nchunks = (int)((len + C - 1) / C);
-    const int c_lo = kSeg ? (int)((int64_t)p * nchunks / P) : 0;
-    const int c_hi = kSeg ? (int)((int64_t)(p + 1) * nchunks / P) : nchunks;
-    const bool last_seg = !kSeg || p == P - 1;
-    if (kSeg && c_lo == c_hi && !last_seg) return;   // an empty segment (whole CTA, before any setup)
-    const int c_run = kSeg && c_lo > 0 ? warm_start(a, bos, h, c_lo) : 0;
-    const int64_t t_run = bos + (int64_t)c_run * C;
+    constexpr bool kSeg = kMode != 0;
+    constexpr bool balanced = kMode == 2;
+    const int P = kSeg && !balanced && a.segments > 1 ? a.segments : 1;
+    const int p = kSeg && !balanced ? (int)(blockIdx.x / units) : 0;
+    const int ncd = (int)((a.seqlen + C - 1) / C);   // chunks per unit of a dense batch
+    int n = 0, h = 0;
+    if (balanced) {
+        if (sched.x[blockIdx.x] >= sched.x[blockIdx.x + 1]) return;   // no items (whole CTA, before any setup)
+    } else {
+        select_unit(a, kSeg ? (int)(blockIdx.x % units) : (int)blockIdx.x, n, h);
+    }
+    int64_t bos = 0, len = 0;
+    int nchunks = 0, c_lo = 0, c_hi = 0, c_run = 0;
+    bool last_seg = true;
+    // Moves to the CTA's next piece; false when it has none left.  (The balanced schedule's
+    // position is recomputed from the current piece rather than kept: registers are scarce.)
+    auto next_piece = [&](bool first) -> bool {
+        if (balanced) {
+            const int64_t x = first ? sched.x[blockIdx.x] : ((int64_t)n * H + h) * ncd + c_hi;
+            const int64_t x_end = sched.x[blockIdx.x + 1];
+            if (x >= x_end) return false;
+            const int64_t u = x / ncd;
+            n = (int)(u / H);
+            h = (int)(u % H);
+            c_lo = (int)(x - u * ncd);
+            c_hi = x_end - u * ncd < ncd ? (int)(x_end - u * ncd) : ncd;
+        } else if (!first) {
+            return false;
+        }
+        int64_t eos;
+        seq_range(a, n, bos, eos);
+        len = eos - bos;
+        nchunks = (int)((len + C - 1) / C);
+        if (!balanced) {
+            c_lo = kSeg ? (int)((int64_t)p * nchunks / P) : 0;
+            c_hi = kSeg ? (int)((int64_t)(p + 1) * nchunks / P) : nchunks;
+        }
+        last_seg = balanced ? c_hi == nchunks : (!kSeg || p == P - 1);
+        return true;
+    };
+    next_piece(true);
+    if (kSeg && !balanced && c_lo == c_hi && !last_seg) return;   // an empty segment (whole CTA, before any setup)
 
     // mbarriers: Q, K, G tiles landed; [O_I^T | P^T] done; V tile landed; U^T done; state (and
     // (M U_hi)^T) update done; low-order terms of (M U)^T done
@@ -375,30 +417,6 @@ kda_chunk_tc_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_consta
     // outside the single-thread issue branches, so that issuing an MMA costs no address math
     const uint64_t dsm = sdesc_sw128(sb);
 
-    // ---- initial state -> TMEM (S^T: lane j, column i; scale exponent 0)
-    const int64_t sbase = ((int64_t)n * H + h) * D * D;
-    {
-        float v[32];
-#pragma unroll
-        for (int c = 0; c < 32; ++c)
-            v[c] = (a.s0 && c_run == 0) ? a.s0[sbase + (int64_t)(32 * quarter + c) * D + jl] : 0.f;
-        tmem_st32(trow + TM_S + 32 * quarter, v);
-        uint32_t zero[16];
-#pragma unroll
-        for (int c = 0; c < 16; ++c) zero[c] = 0u;
-        tmem_st16u(trow + TM_MU + 16 * quarter, zero);   // (M U)^T = 0 before the first update
-        tmem_wait_st();
-    }
-    if (tid < 256) ZSC[tid] = 0;
-    if (tid == 0 && c_run < c_hi) {
-        mbar_arrive_expect_tx(bar_tma, 3 * 16384);
-        tma_tile(&tmq, sb + OFF_Q, bar_tma, h, t_run, 16384);
-        tma_tile(&tmk, sb + OFF_K, bar_tma, h, t_run, 16384);
-        tma_tile(&tmg, sb + OFF_G, bar_tma, h, t_run);
-        mbar_arrive_expect_tx(bar_v, 16384);
-        tma_tile(&tmv, sb + OFF_V, bar_v, h, t_run);
-    }
-    if (tid < C) BETA[tid] = tid < len - (int64_t)c_run * C ? __bfloat162float(beta[(t_run + tid) * H + h]) : 0.f;
     for (int x = tid; x < 64 * 32; x += NT) {   // I: copies V^T into tensor memory inside an MMA
         const int r = x >> 5, s2 = 2 * (x & 31);
         *reinterpret_cast<uint32_t *>(sm + OFF_NI + sw(r, s2, 64)) =
@@ -429,7 +447,8 @@ kda_chunk_tc_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_consta
     // normalised to unit RMS over its 128 value channels, scaled by the norm weight and
     // multiplied channel-wise by sigmoid(gate logit) before it is rounded to bf16; the chunk's
     // logits were loaded by TMA into the staging tile itself (same row-major layout).
-    const float norm_wj = (a.gate && a.norm_w) ? a.norm_w[jl] : 1.f;   // this thread's channel
+    const bool gate_on = kMode == 0 && a.gate != nullptr;   // the output gate
+    const float norm_wj = (gate_on && a.norm_w) ? a.norm_w[jl] : 1.f;   // this thread's channel
     auto stage_output = [&](int par) {
         if (warp >= 8) return;
         __nv_bfloat16 *os = reinterpret_cast<__nv_bfloat16 *>(sm + OFF_STG);
@@ -450,7 +469,7 @@ kda_chunk_tc_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_consta
 #pragma unroll
         for (int c = 0; c < 32; ++c) v[c] = fmaf(w[c], fa, v[c]);
         tmem_wait_st();
-        if (a.gate) {
+        if (gate_on) {
             // sums of squares of rows r0.. over this warp's 32 channels, transposed so that
             // lane L ends with row r0 + L (5 rounds, 31 shuffles)
 #pragma unroll
@@ -582,515 +601,558 @@ kda_chunk_tc_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_consta
         }
         DEC[c] = ex2(gl);
     };
-#pragma unroll 1
-    for (int ci = c_run; ci < c_hi; ++ci) {
-        const int64_t t0 = bos + (int64_t)ci * C;
-        const int nr = (int)(len - (int64_t)ci * C < C ? len - (int64_t)ci * C : C);
-        const bool more = ci + 1 < c_hi;
-        const int cpar = (ci - c_run) & 1;   // this chunk's row of scales; the TMEM state's is spar
-
-        if (ci > c_run && tid < C) BETA[tid] = BETA[tid + (OFF_BNEXT - OFF_BETA) / 4];   // loaded during the previous chunk
-        bool got = mbar_wait(bar_tma, ph_tma, wait_limit);   // checked at the next barrier
-        ph_tma ^= 1;
-        // ---- (1) warps 0-7: decay sums, then the previous chunk's output staged; warps 8-11:
-        // q_r . k_r; warps 8-15: once the previous state update has landed, S^T -> fp16 pairs
-        // (the MMA operand of this chunk), 64 key channels per warp; then warps 12-15: the
-        // decay vectors from the sums
-        if (warp < 8) {
-            prephase(nr);
-            named_bar_arrive(2, 384);   // the sums are in place for warps 12-15
-            if (out_pending) {   // the previous chunk's output, once its groups landed
-                got = mbar_wait(bar_s, ph_s, wait_limit) && mbar_wait(bar_o, ph_o, wait_limit) && got;
-                if (a.gate) got = mbar_wait(bar_z, ph_z, wait_limit) && got;
-                tc_fence_after();
-                stage_output(spar);
-            }
-        } else {
-            if (warp < 12) diag_qk();
-            if (out_pending) got = mbar_wait(bar_s, ph_s, wait_limit) && got;
-            tc_fence_after();
-            const int64_t cs = ci >= c_lo ? ckpt_slot(a, n, (int64_t)ci * C) : -1;   // the state after ci chunks
-            float *ck = cs >= 0 ? a.ckpt + (cs * H + h) * D * D + jl : nullptr;
+    bool drained = false;   // a failed wait's in-flight copies and MMAs have been waited for
+    for (bool have = true; have; have = next_piece(false)) {
+        c_run = ok && kSeg && c_lo > 0 ? warm_start(a, bos, h, c_lo) : 0;
+        out_pending = false;
+        t0_out = 0;
+        nr_out = 0;
+        spar = 1;
+        if (ok) {
+            const int64_t t_run = bos + (int64_t)c_run * C;
+            // ---- initial state -> TMEM (S^T: lane j, column i; scale exponent 0)
             {
-                const int i0 = 64 * ((warp - 8) >> 2);
-                float v[32], w[32];
-                tmem_ld32x2(trow + TM_S + i0, trow + TM_S + i0 + 32, v, w);
-                // the lane's largest |S| over both halves (warps w and w + 4 share the lanes)
-                const int sz = ZSC[spar * 128 + jl];   // S = (TMEM state) 2^sz
-                XCH[((warp - 8) >> 2) * 128 + jl] = fmaxf(absmax(v), absmax(w));
-                named_bar(3, 256);   // warps 8-15 (w and w + 4 share their lanes)
-                const int es = exp2_floor(fmaxf(XCH[jl], XCH[128 + jl]));
-                const int d = 14 - es < 126 ? 14 - es : 126;   // largest |S16| in [2^14, 2^15)
-                if (warp < 12) {
-                    ASC[cpar * 128 + jl] = sz - d;              // S16 = S 2^-(sz - d)
-                    ESC[jl] = es > -1000 ? es + sz : -1000;     // exponent of the lane's largest |S|
-                }
-                if (ck) {   // S[i][j] = S^T[j][i]: a warp writes 128 contiguous bytes per i
-                    const float fs = pow2i(sz);
+                const int64_t sbase = ((int64_t)n * H + h) * D * D;
+                float v[32];
 #pragma unroll
-                    for (int c = 0; c < 32; ++c) {
-                        __stcs(ck + (int64_t)(i0 + c) * D, v[c] * fs);
-                        __stcs(ck + (int64_t)(i0 + 32 + c) * D, w[c] * fs);
-                    }
-                }
-                const float2 f1 = make_float2(pow2i(d), pow2i(d));
-                uint32_t hv[16], hw[16];
+                for (int c = 0; c < 32; ++c)
+                    v[c] = (a.s0 && c_run == 0) ? a.s0[sbase + (int64_t)(32 * quarter + c) * D + jl] : 0.f;
+                tmem_st32(trow + TM_S + 32 * quarter, v);
+                uint32_t zero[16];
 #pragma unroll
-                for (int c = 0; c < 16; ++c) {
-                    const float2 x = __fmul2_rn(make_float2(v[2 * c], v[2 * c + 1]), f1);
-                    const float2 y = __fmul2_rn(make_float2(w[2 * c], w[2 * c + 1]), f1);
-                    hv[c] = pack_f16(x.x, x.y);
-                    hw[c] = pack_f16(y.x, y.y);
-                }
-                tmem_st16u(trow + TM_S16 + i0 / 2, hv);
-                tmem_st16u(trow + TM_S16 + i0 / 2 + 16, hw);
+                for (int c = 0; c < 16; ++c) zero[c] = 0u;
+                tmem_st16u(trow + TM_MU + 16 * quarter, zero);   // (M U)^T = 0 before the first update
                 tmem_wait_st();
             }
-            if (warp >= 12) {
-                named_bar(2, 384);
-                vectors();
-            }
-        }
-        if (out_pending) ph_s ^= 1;
-        tc_fence_before();
-        if (__syncthreads_or(!got)) { ok = false; break; }
-        tc_fence_after();
-        if (out_pending) {
-            ph_o ^= 1;
-            if (a.gate) ph_z ^= 1;
-            store_output();
-            out_pending = false;
-        }
-
-        // ---- (2) operands, each rounded from the exact inputs:
-        //   bf16 (range e^+-80): Q~ = Q x as hi + lo, K~ = K x, K^ = K / x;
-        //   fp16: Qbar = Q x e^{b_I} (over Q), Kbar (over K), Kp = K / x e^{gl - b_I} (transposed).
-        // Rows past the end of the sequence hold finite data (the next sequence, or TMA zero
-        // fill) and need no masking: their beta is 0, their decay is not accumulated, and the
-        // entries of A and M they would feed lie above the diagonal or in rows never stored.
-        {
-            const int c = 2 * cp;
-            const float2 eb = *reinterpret_cast<const float2 *>(EB + blk * 128 + c);
-            const float2 el = *reinterpret_cast<const float2 *>(EL + blk * 128 + c);
-            float2 l = hb ? *reinterpret_cast<const float2 *>(PART + (2 * blk) * 128 + c) : make_float2(0.f, 0.f);
-            const float2 minus1 = make_float2(-1.f, -1.f);
-            uint32_t p0[4], p1[4];
-#pragma unroll
-            for (int rr = 0; rr < 8; rr += 2) {
-                float kp[2][2];
-#pragma unroll
-                for (int e = 0; e < 2; ++e) {
-                    const int r = 16 * blk + 8 * hb + rr + e;
-                    const uint32_t off = sw(r, c, 64), oqk = swqk(r, c);
-                    const float2 q2 = unpack_bf16(*reinterpret_cast<uint32_t *>(sm + OFF_Q + oqk));
-                    const float2 k2 = unpack_bf16(*reinterpret_cast<uint32_t *>(sm + OFF_K + oqk));
-                    const float2 g2 = unpack_bf16(*reinterpret_cast<uint32_t *>(sm + OFF_G + off));
-                    const float w2 = r < nr ? LOG2E : 0.f;   // decay past the sequence end is not summed
-                    l = __ffma2_rn(g2, make_float2(w2, w2), l);
-                    const float2 x = make_float2(ex2(l.x), ex2(l.y));
-                    const float2 y = make_float2(ex2(-l.x), ex2(-l.y));
-                    const float2 qt = __fmul2_rn(q2, x), kt = __fmul2_rn(k2, x), kh = __fmul2_rn(k2, y);
-                    const uint32_t qh = pack_bf16(qt.x, qt.y);
-                    const float2 ql = __ffma2_rn(unpack_bf16(qh), minus1, qt);
-                    *reinterpret_cast<uint32_t *>(sm + OFF_SST + off) = qh;
-                    *reinterpret_cast<uint32_t *>(sm + OFF_UST + off) = pack_bf16(ql.x, ql.y);
-                    *reinterpret_cast<uint32_t *>(sm + OFF_SST + 16384 + off) = pack_bf16(kt.x, kt.y);
-                    *reinterpret_cast<uint32_t *>(sm + OFF_KH + off) = pack_bf16(kh.x, kh.y);
-                    const float2 qb = __fmul2_rn(qt, eb), kb = __fmul2_rn(kt, eb), kp2 = __fmul2_rn(kh, el);
-                    *reinterpret_cast<uint32_t *>(sm + OFF_Q + oqk) = pack_f16(qb.x, qb.y);
-                    *reinterpret_cast<uint32_t *>(sm + OFF_K + oqk) = pack_f16(kb.x, kb.y);
-                    kp[e][0] = kp2.x;
-                    kp[e][1] = kp2.y;
-                }
-                p0[rr / 2] = pack_f16(kp[0][0], kp[1][0]);
-                p1[rr / 2] = pack_f16(kp[0][1], kp[1][1]);
-            }
-            const int rc = 16 * blk + 8 * hb;
-            *reinterpret_cast<uint4 *>(sm + OFF_KPT + sw(c, rc, 128)) = make_uint4(p0[0], p0[1], p0[2], p0[3]);
-            *reinterpret_cast<uint4 *>(sm + OFF_KPT + sw(c + 1, rc, 128)) = make_uint4(p1[0], p1[1], p1[2], p1[3]);
-        }
-
-        fence_async_smem();
-        tc_fence_before();
-        __syncthreads();
-        // [O_I^T | P^T] = S16^T [Qbar; Kbar]^T and V^T = V^T I into the U columns (V read
-        // MN-major; free since the previous output was staged) [commit: P], issued by a warp
-        // that (3) leaves idle; the same thread loads the next chunk's G (consumed) and, once
-        // the group has read Qbar, Kbar and V, its Q, K and V
-        bool gtma = true;
-        if (warp == 15 && lane == 0) {
-            tc_fence_after();
-#pragma unroll
-            for (int k = 0; k < 8; ++k)
-                mma_f16_ts(tmem + TM_OI, tmem + TM_S16 + 8 * k, dsm + ((OFF_Q + (k >> 2) * 16384 + (k & 3) * 32) >> 4),
-                           IDESC_N128, k > 0);
-            gtma = mbar_wait(bar_v, ph_v, wait_limit);   // this chunk's V
-            if (gtma) {
-                tc_fence_after();
-                const uint64_t vdesc = sdesc_sw128_mn(sb + OFF_V, 64 * 128, 1024);
-#pragma unroll
-                for (int k = 0; k < 4; ++k)
-                    mma_f16_ss(tmem + TM_U, vdesc + ((2048 * k) >> 4), dsm + ((OFF_NI + 32 * k) >> 4), IDESC_VT, k > 0);
-            }
-            mma_commit(bar_p);
-            if (more) {
+            if (tid < 256) ZSC[tid] = 0;
+            if (tid == 0 && c_run < c_hi) {
                 mbar_arrive_expect_tx(bar_tma, 3 * 16384);
-                tma_tile(&tmg, sb + OFF_G, bar_tma, h, t0 + C);
-                gtma = mbar_wait(bar_p, ph_p, wait_limit) && gtma;
-                if (gtma) {
-                    tma_tile(&tmq, sb + OFF_Q, bar_tma, h, t0 + C, 16384);
-                    tma_tile(&tmk, sb + OFF_K, bar_tma, h, t0 + C, 16384);
-                    mbar_arrive_expect_tx(bar_v, 16384);
-                    tma_tile(&tmv, sb + OFF_V, bar_v, h, t0 + C);
-                }
+                tma_tile(&tmq, sb + OFF_Q, bar_tma, h, t_run, 16384);
+                tma_tile(&tmk, sb + OFF_K, bar_tma, h, t_run, 16384);
+                tma_tile(&tmg, sb + OFF_G, bar_tma, h, t_run);
+                mbar_arrive_expect_tx(bar_v, 16384);
+                tma_tile(&tmv, sb + OFF_V, bar_v, h, t_run);
             }
-        }
+            if (tid < C) BETA[tid] = tid < len - (int64_t)c_run * C ? __bfloat162float(beta[(t_run + tid) * H + h]) : 0.f;
+            tc_fence_before();
+            __syncthreads();
+            tc_fence_after();
 
-        // ---- (3) A = beta K~ K^T and M = Q~ K^T on the 10 sub-tile pairs (I >= J), bf16
-        // products with fp32 accumulation.  Warps 0-3: A_II, I = warp, both 8-column halves; the
-        // warp then inverts (I + A_II) by forward substitution (one SM sub-partition per block).
-        // Warps 4-7: M_II, I = warp - 4, as (Q~hi + Q~lo) K^^T below the diagonal (the largest
-        // entries of M, where the bf16 rounding of Q~ shows in the outputs) and the exact
-        // q_r . k_r on it.
-        // Warps 8-13: the 6 off-diagonal pairs, single bf16 products with the per-channel factor
-        // e^{b_I - b_J} (bf16, subnormals kept) applied to the right operand.  Off-diagonal A blocks go to the fp16
-        // tile AT; T_II = (I + A_II)^-1 goes to the diagonal blocks of the fp16 tile T.
-        if (warp < 4) {
-            const int I = warp;
-            float accA[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
-#pragma unroll 4
-            for (int kk = 0; kk < 8; ++kk) {
-                const uint32_t ao = sw(16 * I + (lane & 15), 16 * kk + ((lane >> 4) << 3), 64);
-                const uint32_t bo = sw(16 * I + (lane & 7) + ((lane >> 4) << 3), 16 * kk + (((lane >> 3) & 1) << 3), 64);
-                uint32_t ka[4], bh[4];
-                ldsm_x4(sb + OFF_SST + 16384 + ao, ka[0], ka[1], ka[2], ka[3]);
-                ldsm_x4(sb + OFF_KH + bo, bh[0], bh[1], bh[2], bh[3]);
-                mma_16816(accA[0], ka[0], ka[1], ka[2], ka[3], bh[0], bh[1]);
-                mma_16816(accA[1], ka[0], ka[1], ka[2], ka[3], bh[2], bh[3]);
-            }
-#pragma unroll
-            for (int nt = 0; nt < 2; ++nt)
-#pragma unroll
-                for (int hh = 0; hh < 2; ++hh) {
-                    const int r = 16 * I + g + 8 * hh;
-                    const int s0 = 16 * I + 8 * nt + 2 * t4;
-                    const float br = BETA[r];
-                    AF[r * LDA + (s0 & 15)] = s0 < r ? br * accA[nt][2 * hh] : 0.f;
-                    AF[r * LDA + (s0 & 15) + 1] = s0 + 1 < r ? br * accA[nt][2 * hh + 1] : 0.f;
-                }
-            __syncwarp();   // the whole of A_II is in place
-            if (lane < 16) {
-                // column jj of T_II: t_jj = 1, t_r = -sum_{s<r} A_rs t_s (rows above jj are 0)
-                const int jj = lane;
-                const float *Ab = AF + (16 * I) * LDA;
-                float tcol[16];
-#pragma unroll
-                for (int r = 0; r < 16; ++r) {
-                    float arow[16];
-#pragma unroll
-                    for (int q4 = 0; q4 < (r + 3) / 4; ++q4) {
-                        const float4 a4 = *reinterpret_cast<const float4 *>(Ab + r * LDA + 4 * q4);
-                        arow[4 * q4] = a4.x; arow[4 * q4 + 1] = a4.y; arow[4 * q4 + 2] = a4.z; arow[4 * q4 + 3] = a4.w;
+#pragma unroll 1
+            for (int ci = c_run; ci < c_hi; ++ci) {
+                const int64_t t0 = bos + (int64_t)ci * C;
+                const int nr = (int)(len - (int64_t)ci * C < C ? len - (int64_t)ci * C : C);
+                const bool more = ci + 1 < c_hi;
+                const int cpar = (ci - c_run) & 1;   // this chunk's row of scales; the TMEM state's is spar
+
+                if (ci > c_run && tid < C) BETA[tid] = BETA[tid + (OFF_BNEXT - OFF_BETA) / 4];   // loaded during the previous chunk
+                bool got = mbar_wait(bar_tma, ph_tma, wait_limit);   // checked at the next barrier
+                ph_tma ^= 1;
+                // ---- (1) warps 0-7: decay sums, then the previous chunk's output staged; warps 8-11:
+                // q_r . k_r; warps 8-15: once the previous state update has landed, S^T -> fp16 pairs
+                // (the MMA operand of this chunk), 64 key channels per warp; then warps 12-15: the
+                // decay vectors from the sums
+                if (warp < 8) {
+                    prephase(nr);
+                    named_bar_arrive(2, 384);   // the sums are in place for warps 12-15
+                    if (out_pending) {   // the previous chunk's output, once its groups landed
+                        got = mbar_wait(bar_s, ph_s, wait_limit) && mbar_wait(bar_o, ph_o, wait_limit) && got;
+                        if (gate_on) got = mbar_wait(bar_z, ph_z, wait_limit) && got;
+                        tc_fence_after();
+                        stage_output(spar);
                     }
-                    float acc = 0.f;
+                } else {
+                    if (warp < 12) diag_qk();
+                    if (out_pending) got = mbar_wait(bar_s, ph_s, wait_limit) && got;
+                    tc_fence_after();
+                    const int64_t cs = kMode == 0 && ci >= c_lo ? ckpt_slot(a, n, (int64_t)ci * C) : -1;   // the state after ci chunks
+                    float *ck = cs >= 0 ? a.ckpt + (cs * H + h) * D * D + jl : nullptr;
+                    {
+                        const int i0 = 64 * ((warp - 8) >> 2);
+                        float v[32], w[32];
+                        tmem_ld32x2(trow + TM_S + i0, trow + TM_S + i0 + 32, v, w);
+                        // the lane's largest |S| over both halves (warps w and w + 4 share the lanes)
+                        const int sz = ZSC[spar * 128 + jl];   // S = (TMEM state) 2^sz
+                        XCH[((warp - 8) >> 2) * 128 + jl] = fmaxf(absmax(v), absmax(w));
+                        named_bar(3, 256);   // warps 8-15 (w and w + 4 share their lanes)
+                        const int es = exp2_floor(fmaxf(XCH[jl], XCH[128 + jl]));
+                        const int d = 14 - es < 126 ? 14 - es : 126;   // largest |S16| in [2^14, 2^15)
+                        if (warp < 12) {
+                            ASC[cpar * 128 + jl] = sz - d;              // S16 = S 2^-(sz - d)
+                            ESC[jl] = es > -1000 ? es + sz : -1000;     // exponent of the lane's largest |S|
+                        }
+                        if (ck) {   // S[i][j] = S^T[j][i]: a warp writes 128 contiguous bytes per i
+                            const float fs = pow2i(sz);
 #pragma unroll
-                    for (int s2 = 0; s2 < r; ++s2) acc = fmaf(arow[s2], tcol[s2], acc);
-                    tcol[r] = r == jj ? 1.f : (r < jj ? 0.f : -acc);
+                            for (int c = 0; c < 32; ++c) {
+                                __stcs(ck + (int64_t)(i0 + c) * D, v[c] * fs);
+                                __stcs(ck + (int64_t)(i0 + 32 + c) * D, w[c] * fs);
+                            }
+                        }
+                        const float2 f1 = make_float2(pow2i(d), pow2i(d));
+                        uint32_t hv[16], hw[16];
+#pragma unroll
+                        for (int c = 0; c < 16; ++c) {
+                            const float2 x = __fmul2_rn(make_float2(v[2 * c], v[2 * c + 1]), f1);
+                            const float2 y = __fmul2_rn(make_float2(w[2 * c], w[2 * c + 1]), f1);
+                            hv[c] = pack_f16(x.x, x.y);
+                            hw[c] = pack_f16(y.x, y.y);
+                        }
+                        tmem_st16u(trow + TM_S16 + i0 / 2, hv);
+                        tmem_st16u(trow + TM_S16 + i0 / 2 + 16, hw);
+                        tmem_wait_st();
+                    }
+                    if (warp >= 12) {
+                        named_bar(2, 384);
+                        vectors();
+                    }
                 }
-                __half *at = reinterpret_cast<__half *>(sm + OFF_T);
-#pragma unroll
-                for (int r = 0; r < 16; ++r)
-                    at[sw(16 * I + r, 16 * I + jj, 64) >> 1] = __float2half_rn(tcol[r]);
-            }
-        } else if (warp < 8) {
-            const int I = warp - 4;
-            float accM[2][2][4];
-#pragma unroll
-            for (int nt = 0; nt < 2; ++nt)
-#pragma unroll
-                for (int e = 0; e < 4; ++e) { accM[0][nt][e] = 0.f; accM[1][nt][e] = 0.f; }
-#pragma unroll 2
-            for (int kk = 0; kk < 8; ++kk) {
-                const uint32_t ao = sw(16 * I + (lane & 15), 16 * kk + ((lane >> 4) << 3), 64);
-                const uint32_t bo = sw(16 * I + (lane & 7) + ((lane >> 4) << 3), 16 * kk + (((lane >> 3) & 1) << 3), 64);
-                uint32_t qh[4], ql[4], bh[4];
-                ldsm_x4(sb + OFF_SST + ao, qh[0], qh[1], qh[2], qh[3]);
-                ldsm_x4(sb + OFF_UST + ao, ql[0], ql[1], ql[2], ql[3]);
-                ldsm_x4(sb + OFF_KH + bo, bh[0], bh[1], bh[2], bh[3]);
-#pragma unroll
-                for (int nt = 0; nt < 2; ++nt) {
-                    mma_16816(accM[0][nt], qh[0], qh[1], qh[2], qh[3], bh[2 * nt], bh[2 * nt + 1]);
-                    mma_16816(accM[1][nt], ql[0], ql[1], ql[2], ql[3], bh[2 * nt], bh[2 * nt + 1]);
+                if (out_pending) ph_s ^= 1;
+                tc_fence_before();
+                if (__syncthreads_or(!got)) { ok = false; break; }
+                tc_fence_after();
+                if (out_pending) {
+                    ph_o ^= 1;
+                    if (gate_on) ph_z ^= 1;
+                    store_output();
+                    out_pending = false;
                 }
-            }
-#pragma unroll
-            for (int nt = 0; nt < 2; ++nt)
-#pragma unroll
-                for (int hh = 0; hh < 2; ++hh) {
-                    const int r = 16 * I + g + 8 * hh;
-                    const int s0 = 16 * I + 8 * nt + 2 * t4;
-                    const float mv0 = accM[0][nt][2 * hh] + accM[1][nt][2 * hh];
-                    const float mv1 = accM[0][nt][2 * hh + 1] + accM[1][nt][2 * hh + 1];
-                    const float m0 = s0 < r ? mv0 : (s0 == r ? MRR[r] : 0.f);
-                    const float m1 = s0 + 1 < r ? mv1 : (s0 + 1 == r ? MRR[r] : 0.f);
-                    const uint32_t mh = pack_f16(m0, m1);
-                    const float2 mhf = unpack_f16(mh);
-                    *reinterpret_cast<uint32_t *>(sm + OFF_MT + sw(r, s0, 64)) = mh;
-                    *reinterpret_cast<uint32_t *>(sm + OFF_MLO + sw(r, s0, 64)) = pack_f16(m0 - mhf.x, m1 - mhf.y);
-                }
-        } else if (warp == 14) {   // the blocks of T above the diagonal (staging used them), then
-                                   // the next chunk's beta
-            for (int x = lane; x < 192; x += 32) {
-                const int b = x >> 5, rr = (x >> 1) & 15, hf = x & 1;   // (0,1) (0,2) (0,3) (1,2) (1,3) (2,3)
-                const int I = b < 3 ? 0 : (b < 5 ? 1 : 2);
-                const int J = b < 3 ? b + 1 : (b < 5 ? b - 1 : 3);
-                *reinterpret_cast<uint4 *>(sm + OFF_T + sw(16 * I + rr, 16 * J + 8 * hf, 64)) = make_uint4(0u, 0u, 0u, 0u);
-            }
-            if (more) {   // the next chunk's beta (the load latency is hidden in this step)
-                const int64_t nn = len - (int64_t)(ci + 1) * C;
-                for (int r = lane; r < C; r += 32)
-                    BETA[r + (OFF_BNEXT - OFF_BETA) / 4] = r < nn ? __bfloat162float(beta[(t0 + C + r) * H + h]) : 0.f;
-            }
-        } else if (warp >= 8 && warp < 14) {
-            const int po = warp - 8;   // (1,0) (2,0) (2,1) (3,0) (3,1) (3,2)
-            const int I = po < 1 ? 1 : (po < 3 ? 2 : 3);
-            const int J = po < 1 ? 0 : (po < 3 ? po - 1 : po - 3);
-            float accA[2][4], accM[2][4];
-#pragma unroll
-            for (int nt = 0; nt < 2; ++nt)
-#pragma unroll
-                for (int e = 0; e < 4; ++e) { accA[nt][e] = 0.f; accM[nt][e] = 0.f; }
-            const __nv_bfloat16 *w = W6 + pair_index(I, J) * 128 + 2 * t4;
-#pragma unroll 4
-            for (int kk = 0; kk < 8; ++kk) {
-                const uint32_t ao = sw(16 * I + (lane & 15), 16 * kk + ((lane >> 4) << 3), 64);
-                const uint32_t bo = sw(16 * J + (lane & 7) + ((lane >> 4) << 3), 16 * kk + (((lane >> 3) & 1) << 3), 64);
-                uint32_t ka[4], qh[4], bh[4];
-                ldsm_x4(sb + OFF_SST + 16384 + ao, ka[0], ka[1], ka[2], ka[3]);
-                ldsm_x4(sb + OFF_SST + ao, qh[0], qh[1], qh[2], qh[3]);
-                ldsm_x4(sb + OFF_KH + bo, bh[0], bh[1], bh[2], bh[3]);
-                const uint32_t wlo = *reinterpret_cast<const uint32_t *>(w + 16 * kk);
-                const uint32_t whi = *reinterpret_cast<const uint32_t *>(w + 16 * kk + 8);
-                bh[0] = mul_bf16x2(bh[0], wlo); bh[1] = mul_bf16x2(bh[1], whi);
-                bh[2] = mul_bf16x2(bh[2], wlo); bh[3] = mul_bf16x2(bh[3], whi);
-#pragma unroll
-                for (int nt = 0; nt < 2; ++nt) {
-                    mma_16816(accA[nt], ka[0], ka[1], ka[2], ka[3], bh[2 * nt], bh[2 * nt + 1]);
-                    mma_16816(accM[nt], qh[0], qh[1], qh[2], qh[3], bh[2 * nt], bh[2 * nt + 1]);
-                }
-            }
-#pragma unroll
-            for (int nt = 0; nt < 2; ++nt)
-#pragma unroll
-                for (int hh = 0; hh < 2; ++hh) {
-                    const int r = 16 * I + g + 8 * hh;
-                    const int s0 = 16 * J + 8 * nt + 2 * t4;
-                    const float br = BETA[r];
-                    *reinterpret_cast<uint32_t *>(sm + OFF_TT + sw(r, s0, 64)) =
-                        pack_f16(br * accA[nt][2 * hh], br * accA[nt][2 * hh + 1]);
-                    const float m0 = accM[nt][2 * hh], m1 = accM[nt][2 * hh + 1];
-                    const uint32_t mh = pack_f16(m0, m1);
-                    const float2 mhf = unpack_f16(mh);
-                    *reinterpret_cast<uint32_t *>(sm + OFF_MT + sw(r, s0, 64)) = mh;
-                    *reinterpret_cast<uint32_t *>(sm + OFF_MLO + sw(r, s0, 64)) = pack_f16(m0 - mhf.x, m1 - mhf.y);
-                }
-        }
-        __syncthreads();
 
-        bool got4 = gtma;
-        // ---- (4) warps 0-2: the off-diagonal blocks of T, level by level (T_IK with K > J is
-        // ready before T_IJ);  warps 4-11: Z^T = (V^T - 2^a_j P^T) diag(beta) -> fp16 pairs
-        // (TMEM) at the lane's scale z_j (warps w and w + 4 share the lanes)
-        if (warp < 3) {
-            t_block(warp + 1, warp);                 // (1,0) (2,1) (3,2)
-            named_bar(1, 96);
-            if (warp < 2) t_block(warp + 2, warp);   // (2,0) (3,1)
-            named_bar(1, 96);
-            if (warp == 0) t_block(3, 0);
-        } else if (warp >= 4 && warp < 12) {
-            got4 = mbar_wait(bar_p, ph_p, wait_limit) && got4;
-            tc_fence_after();
-            const int s0 = 32 * ((warp - 4) >> 2);
-            float pv[32], vv[32];
-            tmem_ld32x2(trow + TM_P + s0, trow + TM_U + s0, pv, vv);   // (Kbar S)^T 2^-a_j, V^T
-            const float fa = -pow2f(ASC[cpar * 128 + jl]);
-            const float2 fa2 = make_float2(fa, fa);
+                // ---- (2) operands, each rounded from the exact inputs:
+                //   bf16 (range e^+-80): Q~ = Q x as hi + lo, K~ = K x, K^ = K / x;
+                //   fp16: Qbar = Q x e^{b_I} (over Q), Kbar (over K), Kp = K / x e^{gl - b_I} (transposed).
+                // Rows past the end of the sequence hold finite data (the next sequence, or TMA zero
+                // fill) and need no masking: their beta is 0, their decay is not accumulated, and the
+                // entries of A and M they would feed lie above the diagonal or in rows never stored.
+                {
+                    const int c = 2 * cp;
+                    const float2 eb = *reinterpret_cast<const float2 *>(EB + blk * 128 + c);
+                    const float2 el = *reinterpret_cast<const float2 *>(EL + blk * 128 + c);
+                    float2 l = hb ? *reinterpret_cast<const float2 *>(PART + (2 * blk) * 128 + c) : make_float2(0.f, 0.f);
+                    const float2 minus1 = make_float2(-1.f, -1.f);
+                    uint32_t p0[4], p1[4];
 #pragma unroll
-            for (int c = 0; c < 32; c += 4) {
-                const float4 b4 = *reinterpret_cast<const float4 *>(BETA + s0 + c);
-                const float2 t0 = __ffma2_rn(make_float2(pv[c], pv[c + 1]), fa2, make_float2(vv[c], vv[c + 1]));
-                const float2 t1 = __ffma2_rn(make_float2(pv[c + 2], pv[c + 3]), fa2, make_float2(vv[c + 2], vv[c + 3]));
-                const float2 z0 = __fmul2_rn(t0, make_float2(b4.x, b4.y)), z1 = __fmul2_rn(t1, make_float2(b4.z, b4.w));
-                pv[c] = z0.x; pv[c + 1] = z0.y; pv[c + 2] = z1.x; pv[c + 3] = z1.y;
+                    for (int rr = 0; rr < 8; rr += 2) {
+                        float kp[2][2];
+#pragma unroll
+                        for (int e = 0; e < 2; ++e) {
+                            const int r = 16 * blk + 8 * hb + rr + e;
+                            const uint32_t off = sw(r, c, 64), oqk = swqk(r, c);
+                            const float2 q2 = unpack_bf16(*reinterpret_cast<uint32_t *>(sm + OFF_Q + oqk));
+                            const float2 k2 = unpack_bf16(*reinterpret_cast<uint32_t *>(sm + OFF_K + oqk));
+                            const float2 g2 = unpack_bf16(*reinterpret_cast<uint32_t *>(sm + OFF_G + off));
+                            const float w2 = r < nr ? LOG2E : 0.f;   // decay past the sequence end is not summed
+                            l = __ffma2_rn(g2, make_float2(w2, w2), l);
+                            const float2 x = make_float2(ex2(l.x), ex2(l.y));
+                            const float2 y = make_float2(ex2(-l.x), ex2(-l.y));
+                            const float2 qt = __fmul2_rn(q2, x), kt = __fmul2_rn(k2, x), kh = __fmul2_rn(k2, y);
+                            const uint32_t qh = pack_bf16(qt.x, qt.y);
+                            const float2 ql = __ffma2_rn(unpack_bf16(qh), minus1, qt);
+                            *reinterpret_cast<uint32_t *>(sm + OFF_SST + off) = qh;
+                            *reinterpret_cast<uint32_t *>(sm + OFF_UST + off) = pack_bf16(ql.x, ql.y);
+                            *reinterpret_cast<uint32_t *>(sm + OFF_SST + 16384 + off) = pack_bf16(kt.x, kt.y);
+                            *reinterpret_cast<uint32_t *>(sm + OFF_KH + off) = pack_bf16(kh.x, kh.y);
+                            const float2 qb = __fmul2_rn(qt, eb), kb = __fmul2_rn(kt, eb), kp2 = __fmul2_rn(kh, el);
+                            *reinterpret_cast<uint32_t *>(sm + OFF_Q + oqk) = pack_f16(qb.x, qb.y);
+                            *reinterpret_cast<uint32_t *>(sm + OFF_K + oqk) = pack_f16(kb.x, kb.y);
+                            kp[e][0] = kp2.x;
+                            kp[e][1] = kp2.y;
+                        }
+                        p0[rr / 2] = pack_f16(kp[0][0], kp[1][0]);
+                        p1[rr / 2] = pack_f16(kp[0][1], kp[1][1]);
+                    }
+                    const int rc = 16 * blk + 8 * hb;
+                    *reinterpret_cast<uint4 *>(sm + OFF_KPT + sw(c, rc, 128)) = make_uint4(p0[0], p0[1], p0[2], p0[3]);
+                    *reinterpret_cast<uint4 *>(sm + OFF_KPT + sw(c + 1, rc, 128)) = make_uint4(p1[0], p1[1], p1[2], p1[3]);
+                }
+
+                fence_async_smem();
+                tc_fence_before();
+                __syncthreads();
+                // [O_I^T | P^T] = S16^T [Qbar; Kbar]^T and V^T = V^T I into the U columns (V read
+                // MN-major; free since the previous output was staged) [commit: P], issued by a warp
+                // that (3) leaves idle; the same thread loads the next chunk's G (consumed) and, once
+                // the group has read Qbar, Kbar and V, its Q, K and V
+                bool gtma = true;
+                if (warp == 15 && lane == 0) {
+                    tc_fence_after();
+#pragma unroll
+                    for (int k = 0; k < 8; ++k)
+                        mma_f16_ts(tmem + TM_OI, tmem + TM_S16 + 8 * k, dsm + ((OFF_Q + (k >> 2) * 16384 + (k & 3) * 32) >> 4),
+                                   IDESC_N128, k > 0);
+                    gtma = mbar_wait(bar_v, ph_v, wait_limit);   // this chunk's V
+                    if (gtma) {
+                        tc_fence_after();
+                        const uint64_t vdesc = sdesc_sw128_mn(sb + OFF_V, 64 * 128, 1024);
+#pragma unroll
+                        for (int k = 0; k < 4; ++k)
+                            mma_f16_ss(tmem + TM_U, vdesc + ((2048 * k) >> 4), dsm + ((OFF_NI + 32 * k) >> 4), IDESC_VT, k > 0);
+                    }
+                    mma_commit(bar_p);
+                    if (more) {
+                        mbar_arrive_expect_tx(bar_tma, 3 * 16384);
+                        tma_tile(&tmg, sb + OFF_G, bar_tma, h, t0 + C);
+                        gtma = mbar_wait(bar_p, ph_p, wait_limit) && gtma;
+                        if (gtma) {
+                            tma_tile(&tmq, sb + OFF_Q, bar_tma, h, t0 + C, 16384);
+                            tma_tile(&tmk, sb + OFF_K, bar_tma, h, t0 + C, 16384);
+                            mbar_arrive_expect_tx(bar_v, 16384);
+                            tma_tile(&tmv, sb + OFF_V, bar_v, h, t0 + C);
+                        }
+                    }
+                }
+
+                // ---- (3) A = beta K~ K^T and M = Q~ K^T on the 10 sub-tile pairs (I >= J), bf16
+                // products with fp32 accumulation.  Warps 0-3: A_II, I = warp, both 8-column halves; the
+                // warp then inverts (I + A_II) by forward substitution (one SM sub-partition per block).
+                // Warps 4-7: M_II, I = warp - 4, as (Q~hi + Q~lo) K^^T below the diagonal (the largest
+                // entries of M, where the bf16 rounding of Q~ shows in the outputs) and the exact
+                // q_r . k_r on it.
+                // Warps 8-13: the 6 off-diagonal pairs, single bf16 products with the per-channel factor
+                // e^{b_I - b_J} (bf16, subnormals kept) applied to the right operand.  Off-diagonal A blocks go to the fp16
+                // tile AT; T_II = (I + A_II)^-1 goes to the diagonal blocks of the fp16 tile T.
+                if (warp < 4) {
+                    const int I = warp;
+                    float accA[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
+#pragma unroll 4
+                    for (int kk = 0; kk < 8; ++kk) {
+                        const uint32_t ao = sw(16 * I + (lane & 15), 16 * kk + ((lane >> 4) << 3), 64);
+                        const uint32_t bo = sw(16 * I + (lane & 7) + ((lane >> 4) << 3), 16 * kk + (((lane >> 3) & 1) << 3), 64);
+                        uint32_t ka[4], bh[4];
+                        ldsm_x4(sb + OFF_SST + 16384 + ao, ka[0], ka[1], ka[2], ka[3]);
+                        ldsm_x4(sb + OFF_KH + bo, bh[0], bh[1], bh[2], bh[3]);
+                        mma_16816(accA[0], ka[0], ka[1], ka[2], ka[3], bh[0], bh[1]);
+                        mma_16816(accA[1], ka[0], ka[1], ka[2], ka[3], bh[2], bh[3]);
+                    }
+#pragma unroll
+                    for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+                        for (int hh = 0; hh < 2; ++hh) {
+                            const int r = 16 * I + g + 8 * hh;
+                            const int s0 = 16 * I + 8 * nt + 2 * t4;
+                            const float br = BETA[r];
+                            AF[r * LDA + (s0 & 15)] = s0 < r ? br * accA[nt][2 * hh] : 0.f;
+                            AF[r * LDA + (s0 & 15) + 1] = s0 + 1 < r ? br * accA[nt][2 * hh + 1] : 0.f;
+                        }
+                    __syncwarp();   // the whole of A_II is in place
+                    if (lane < 16) {
+                        // column jj of T_II: t_jj = 1, t_r = -sum_{s<r} A_rs t_s (rows above jj are 0)
+                        const int jj = lane;
+                        const float *Ab = AF + (16 * I) * LDA;
+                        float tcol[16];
+#pragma unroll
+                        for (int r = 0; r < 16; ++r) {
+                            float arow[16];
+#pragma unroll
+                            for (int q4 = 0; q4 < (r + 3) / 4; ++q4) {
+                                const float4 a4 = *reinterpret_cast<const float4 *>(Ab + r * LDA + 4 * q4);
+                                arow[4 * q4] = a4.x; arow[4 * q4 + 1] = a4.y; arow[4 * q4 + 2] = a4.z; arow[4 * q4 + 3] = a4.w;
+                            }
+                            float acc = 0.f;
+#pragma unroll
+                            for (int s2 = 0; s2 < r; ++s2) acc = fmaf(arow[s2], tcol[s2], acc);
+                            tcol[r] = r == jj ? 1.f : (r < jj ? 0.f : -acc);
+                        }
+                        __half *at = reinterpret_cast<__half *>(sm + OFF_T);
+#pragma unroll
+                        for (int r = 0; r < 16; ++r)
+                            at[sw(16 * I + r, 16 * I + jj, 64) >> 1] = __float2half_rn(tcol[r]);
+                    }
+                } else if (warp < 8) {
+                    const int I = warp - 4;
+                    float accM[2][2][4];
+#pragma unroll
+                    for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+                        for (int e = 0; e < 4; ++e) { accM[0][nt][e] = 0.f; accM[1][nt][e] = 0.f; }
+#pragma unroll 2
+                    for (int kk = 0; kk < 8; ++kk) {
+                        const uint32_t ao = sw(16 * I + (lane & 15), 16 * kk + ((lane >> 4) << 3), 64);
+                        const uint32_t bo = sw(16 * I + (lane & 7) + ((lane >> 4) << 3), 16 * kk + (((lane >> 3) & 1) << 3), 64);
+                        uint32_t qh[4], ql[4], bh[4];
+                        ldsm_x4(sb + OFF_SST + ao, qh[0], qh[1], qh[2], qh[3]);
+                        ldsm_x4(sb + OFF_UST + ao, ql[0], ql[1], ql[2], ql[3]);
+                        ldsm_x4(sb + OFF_KH + bo, bh[0], bh[1], bh[2], bh[3]);
+#pragma unroll
+                        for (int nt = 0; nt < 2; ++nt) {
+                            mma_16816(accM[0][nt], qh[0], qh[1], qh[2], qh[3], bh[2 * nt], bh[2 * nt + 1]);
+                            mma_16816(accM[1][nt], ql[0], ql[1], ql[2], ql[3], bh[2 * nt], bh[2 * nt + 1]);
+                        }
+                    }
+#pragma unroll
+                    for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+                        for (int hh = 0; hh < 2; ++hh) {
+                            const int r = 16 * I + g + 8 * hh;
+                            const int s0 = 16 * I + 8 * nt + 2 * t4;
+                            const float mv0 = accM[0][nt][2 * hh] + accM[1][nt][2 * hh];
+                            const float mv1 = accM[0][nt][2 * hh + 1] + accM[1][nt][2 * hh + 1];
+                            const float m0 = s0 < r ? mv0 : (s0 == r ? MRR[r] : 0.f);
+                            const float m1 = s0 + 1 < r ? mv1 : (s0 + 1 == r ? MRR[r] : 0.f);
+                            const uint32_t mh = pack_f16(m0, m1);
+                            const float2 mhf = unpack_f16(mh);
+                            *reinterpret_cast<uint32_t *>(sm + OFF_MT + sw(r, s0, 64)) = mh;
+                            *reinterpret_cast<uint32_t *>(sm + OFF_MLO + sw(r, s0, 64)) = pack_f16(m0 - mhf.x, m1 - mhf.y);
+                        }
+                } else if (warp == 14) {   // the blocks of T above the diagonal (staging used them), then
+                                           // the next chunk's beta
+                    for (int x = lane; x < 192; x += 32) {
+                        const int b = x >> 5, rr = (x >> 1) & 15, hf = x & 1;   // (0,1) (0,2) (0,3) (1,2) (1,3) (2,3)
+                        const int I = b < 3 ? 0 : (b < 5 ? 1 : 2);
+                        const int J = b < 3 ? b + 1 : (b < 5 ? b - 1 : 3);
+                        *reinterpret_cast<uint4 *>(sm + OFF_T + sw(16 * I + rr, 16 * J + 8 * hf, 64)) = make_uint4(0u, 0u, 0u, 0u);
+                    }
+                    if (more) {   // the next chunk's beta (the load latency is hidden in this step)
+                        const int64_t nn = len - (int64_t)(ci + 1) * C;
+                        for (int r = lane; r < C; r += 32)
+                            BETA[r + (OFF_BNEXT - OFF_BETA) / 4] = r < nn ? __bfloat162float(beta[(t0 + C + r) * H + h]) : 0.f;
+                    }
+                } else if (warp >= 8 && warp < 14) {
+                    const int po = warp - 8;   // (1,0) (2,0) (2,1) (3,0) (3,1) (3,2)
+                    const int I = po < 1 ? 1 : (po < 3 ? 2 : 3);
+                    const int J = po < 1 ? 0 : (po < 3 ? po - 1 : po - 3);
+                    float accA[2][4], accM[2][4];
+#pragma unroll
+                    for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+                        for (int e = 0; e < 4; ++e) { accA[nt][e] = 0.f; accM[nt][e] = 0.f; }
+                    const __nv_bfloat16 *w = W6 + pair_index(I, J) * 128 + 2 * t4;
+#pragma unroll 4
+                    for (int kk = 0; kk < 8; ++kk) {
+                        const uint32_t ao = sw(16 * I + (lane & 15), 16 * kk + ((lane >> 4) << 3), 64);
+                        const uint32_t bo = sw(16 * J + (lane & 7) + ((lane >> 4) << 3), 16 * kk + (((lane >> 3) & 1) << 3), 64);
+                        uint32_t ka[4], qh[4], bh[4];
+                        ldsm_x4(sb + OFF_SST + 16384 + ao, ka[0], ka[1], ka[2], ka[3]);
+                        ldsm_x4(sb + OFF_SST + ao, qh[0], qh[1], qh[2], qh[3]);
+                        ldsm_x4(sb + OFF_KH + bo, bh[0], bh[1], bh[2], bh[3]);
+                        const uint32_t wlo = *reinterpret_cast<const uint32_t *>(w + 16 * kk);
+                        const uint32_t whi = *reinterpret_cast<const uint32_t *>(w + 16 * kk + 8);
+                        bh[0] = mul_bf16x2(bh[0], wlo); bh[1] = mul_bf16x2(bh[1], whi);
+                        bh[2] = mul_bf16x2(bh[2], wlo); bh[3] = mul_bf16x2(bh[3], whi);
+#pragma unroll
+                        for (int nt = 0; nt < 2; ++nt) {
+                            mma_16816(accA[nt], ka[0], ka[1], ka[2], ka[3], bh[2 * nt], bh[2 * nt + 1]);
+                            mma_16816(accM[nt], qh[0], qh[1], qh[2], qh[3], bh[2 * nt], bh[2 * nt + 1]);
+                        }
+                    }
+#pragma unroll
+                    for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+                        for (int hh = 0; hh < 2; ++hh) {
+                            const int r = 16 * I + g + 8 * hh;
+                            const int s0 = 16 * J + 8 * nt + 2 * t4;
+                            const float br = BETA[r];
+                            *reinterpret_cast<uint32_t *>(sm + OFF_TT + sw(r, s0, 64)) =
+                                pack_f16(br * accA[nt][2 * hh], br * accA[nt][2 * hh + 1]);
+                            const float m0 = accM[nt][2 * hh], m1 = accM[nt][2 * hh + 1];
+                            const uint32_t mh = pack_f16(m0, m1);
+                            const float2 mhf = unpack_f16(mh);
+                            *reinterpret_cast<uint32_t *>(sm + OFF_MT + sw(r, s0, 64)) = mh;
+                            *reinterpret_cast<uint32_t *>(sm + OFF_MLO + sw(r, s0, 64)) = pack_f16(m0 - mhf.x, m1 - mhf.y);
+                        }
+                }
+                __syncthreads();
+
+                bool got4 = gtma;
+                // ---- (4) warps 0-2: the off-diagonal blocks of T, level by level (T_IK with K > J is
+                // ready before T_IJ);  warps 4-11: Z^T = (V^T - 2^a_j P^T) diag(beta) -> fp16 pairs
+                // (TMEM) at the lane's scale z_j (warps w and w + 4 share the lanes)
+                if (warp < 3) {
+                    t_block(warp + 1, warp);                 // (1,0) (2,1) (3,2)
+                    named_bar(1, 96);
+                    if (warp < 2) t_block(warp + 2, warp);   // (2,0) (3,1)
+                    named_bar(1, 96);
+                    if (warp == 0) t_block(3, 0);
+                } else if (warp >= 4 && warp < 12) {
+                    got4 = mbar_wait(bar_p, ph_p, wait_limit) && got4;
+                    tc_fence_after();
+                    const int s0 = 32 * ((warp - 4) >> 2);
+                    float pv[32], vv[32];
+                    tmem_ld32x2(trow + TM_P + s0, trow + TM_U + s0, pv, vv);   // (Kbar S)^T 2^-a_j, V^T
+                    const float fa = -pow2f(ASC[cpar * 128 + jl]);
+                    const float2 fa2 = make_float2(fa, fa);
+#pragma unroll
+                    for (int c = 0; c < 32; c += 4) {
+                        const float4 b4 = *reinterpret_cast<const float4 *>(BETA + s0 + c);
+                        const float2 t0 = __ffma2_rn(make_float2(pv[c], pv[c + 1]), fa2, make_float2(vv[c], vv[c + 1]));
+                        const float2 t1 = __ffma2_rn(make_float2(pv[c + 2], pv[c + 3]), fa2, make_float2(vv[c + 2], vv[c + 3]));
+                        const float2 z0 = __fmul2_rn(t0, make_float2(b4.x, b4.y)), z1 = __fmul2_rn(t1, make_float2(b4.z, b4.w));
+                        pv[c] = z0.x; pv[c + 1] = z0.y; pv[c + 2] = z1.x; pv[c + 3] = z1.y;
+                    }
+                    XCH[((warp - 4) >> 2) * 128 + jl] = absmax(pv);
+                    named_bar(4, 256);   // warps 4-11 (w and w + 4 share their lanes)
+                    // z_j: the lane's largest |Z| maps into [1, 2); at least E_S - 86 so that the state,
+                    // held as S 2^-z_j from here on, stays below 2^87; within 126 of the state's
+                    // current exponent so that the state moves to it by one float factor
+                    const int eZ = exp2_floor(fmaxf(XCH[jl], XCH[128 + jl]));
+                    const int eS = ESC[jl], sz = ZSC[spar * 128 + jl];
+                    const int zj = clamp_i(clamp_i(eZ > eS - 86 ? eZ : eS - 86, sz - 126, sz + 126), -126, 126);
+                    if (warp < 8) ZSC[cpar * 128 + jl] = zj;
+                    const float2 fz = make_float2(pow2i(-zj), pow2i(-zj));
+                    uint32_t zv[16], zl[16];   // hi and lo: one fp16 rounding of U alone costs 2^-12
+#pragma unroll
+                    for (int c = 0; c < 16; ++c) {
+                        const float2 z = __fmul2_rn(make_float2(pv[2 * c], pv[2 * c + 1]), fz);
+                        zv[c] = pack_f16(z.x, z.y);
+                        const float2 zlo = __ffma2_rn(unpack_f16(zv[c]), make_float2(-1.f, -1.f), z);
+                        zl[c] = pack_f16(zlo.x, zlo.y);
+                    }
+                    tmem_st16u(trow + TM_Z + s0 / 2, zv);
+                    tmem_st16u(trow + TM_ZL + s0 / 2, zl);
+                    tmem_wait_st();
+                }
+                ph_p ^= 1;
+                ph_v ^= 1;
+                fence_async_smem();
+                tc_fence_before();
+                if (__syncthreads_or(!got4)) { ok = false; break; }
+                // U^T = Z^T_hi T^T (U columns) + Z^T_lo T^T (the consumed P columns), issued by two
+                // threads [commit: U, two arrivals]
+                if (tid == 32) {
+                    tc_fence_after();
+#pragma unroll
+                    for (int k = 0; k < 4; ++k)
+                        mma_f16_ts(tmem + TM_P, tmem + TM_ZL + 8 * k, dsm + ((OFF_T + k * 32) >> 4), IDESC_N64, k > 0);
+                    mma_commit(bar_u);
+                }
+                if (tid == 0) {
+                    tc_fence_after();
+#pragma unroll
+                    for (int k = 0; k < 4; ++k)
+                        mma_f16_ts(tmem + TM_U, tmem + TM_Z + 8 * k, dsm + ((OFF_T + k * 32) >> 4), IDESC_N64, k > 0);
+                    mma_commit(bar_u);
+                }
+                {   // while the U^T groups run: S^T <- S^T Diag(dec) in place (S^T was read as fp16 in
+                    // (1)), moved from the lane's old scale to z_j (U^T is at z_j); warp w: lanes
+                    // 32(w%4).., 32 columns from 32(w/4)
+                    const int i0 = 32 * quarter;
+                    float v[32];
+                    tmem_ld32(trow + TM_S + i0, v);
+                    const float f = pow2i(ZSC[spar * 128 + jl] - ZSC[cpar * 128 + jl]);   // |step| <= 126
+                    const float2 f1 = make_float2(f, f);
+#pragma unroll
+                    for (int c = 0; c < 32; c += 4) {
+                        const float4 d4 = *reinterpret_cast<const float4 *>(DEC + i0 + c);
+                        const float2 a2 = __fmul2_rn(__fmul2_rn(make_float2(v[c], v[c + 1]), f1), make_float2(d4.x, d4.y));
+                        const float2 b2 = __fmul2_rn(__fmul2_rn(make_float2(v[c + 2], v[c + 3]), f1), make_float2(d4.z, d4.w));
+                        v[c] = a2.x; v[c + 1] = a2.y; v[c + 2] = b2.x; v[c + 3] = b2.y;
+                    }
+                    tmem_st32(trow + TM_S + i0, v);
+                    tmem_wait_st();
+                }
+                {
+                    const bool got = mbar_wait(bar_u, ph_u, wait_limit);
+                    ph_u ^= 1;
+                    if (__syncthreads_or(!got)) { ok = false; break; }
+                }
+                if (gate_on && tid == 0) {   // AT and T are consumed: this chunk's gate logits -> staging tile
+                    fence_async_smem();
+                    mbar_arrive_expect_tx(bar_z, 64 * D * 2);
+                    tma_load_3d(sb + OFF_STG, &tmz, bar_z, 0, h, (int)t0);
+                }
+                tc_fence_after();
+                // ---- (5) U^T -> fp16 hi + lo pairs (TMEM); warp w: lanes 32(w%4).., columns 16(w/4)..
+                {
+                    const int r0 = 16 * quarter;
+                    float uv[16], u2[16];
+                    tmem_ld16x2(trow + TM_U + r0, trow + TM_P + r0, uv, u2);
+#pragma unroll
+                    for (int e = 0; e < 16; e += 2) {
+                        const float2 a2 = __fadd2_rn(make_float2(uv[e], uv[e + 1]), make_float2(u2[e], u2[e + 1]));
+                        uv[e] = a2.x; uv[e + 1] = a2.y;
+                    }
+                    uint32_t hi[8], lo[8];
+#pragma unroll
+                    for (int e = 0; e < 8; ++e) {
+                        hi[e] = pack_f16(uv[2 * e], uv[2 * e + 1]);
+                        const float2 lo2 = __ffma2_rn(unpack_f16(hi[e]), make_float2(-1.f, -1.f), make_float2(uv[2 * e], uv[2 * e + 1]));
+                        lo[e] = pack_f16(lo2.x, lo2.y);
+                    }
+                    tmem_st8u(trow + TM_UH + r0 / 2, hi);
+                    tmem_st8u(trow + TM_UL + r0 / 2, lo);
+                    tmem_wait_st();
+                }
+                tc_fence_before();
+                __syncthreads();
+                // [S^T | (M U)^T] += U^T_hi [Kp^T; M]^T [commit: S];  low-order terms of (M U)^T,
+                // U^T_lo M^T + U^T_hi Mlo^T, into the U^T columns (consumed) [commit: O], issued by a
+                // warp with the least work in the next step (1); all at the lanes' scales z_j
+                if (tid == 0) {
+                    tc_fence_after();
+#pragma unroll
+                    for (int ks = 0; ks < 4; ++ks)
+                        mma_f16_ts(tmem + TM_S, tmem + TM_UH + 8 * ks, dsm + ((OFF_KPT + ks * 32) >> 4), IDESC_N192, 1);
+                    mma_commit(bar_s);
+                } else if (tid == 480) {
+                    tc_fence_after();
+#pragma unroll
+                    for (int ks = 0; ks < 4; ++ks)
+                        mma_f16_ts(tmem + TM_U, tmem + TM_UL + 8 * ks, dsm + ((OFF_MT + ks * 32) >> 4), IDESC_N64, ks > 0);
+#pragma unroll
+                    for (int ks = 0; ks < 4; ++ks)
+                        mma_f16_ts(tmem + TM_U, tmem + TM_UH + 8 * ks, dsm + ((OFF_MLO + ks * 32) >> 4), IDESC_N64, 1);
+                    mma_commit(bar_o);
+                }
+                out_pending = true;
+                t0_out = t0;
+                nr_out = ci >= c_lo ? nr : 0;   // the warm-up chunks before c_lo store nothing
+                spar = cpar;
             }
-            XCH[((warp - 4) >> 2) * 128 + jl] = absmax(pv);
-            named_bar(4, 256);   // warps 4-11 (w and w + 4 share their lanes)
-            // z_j: the lane's largest |Z| maps into [1, 2); at least E_S - 86 so that the state,
-            // held as S 2^-z_j from here on, stays below 2^87; within 126 of the state's
-            // current exponent so that the state moves to it by one float factor
-            const int eZ = exp2_floor(fmaxf(XCH[jl], XCH[128 + jl]));
-            const int eS = ESC[jl], sz = ZSC[spar * 128 + jl];
-            const int zj = clamp_i(clamp_i(eZ > eS - 86 ? eZ : eS - 86, sz - 126, sz + 126), -126, 126);
-            if (warp < 8) ZSC[cpar * 128 + jl] = zj;
-            const float2 fz = make_float2(pow2i(-zj), pow2i(-zj));
-            uint32_t zv[16], zl[16];   // hi and lo: one fp16 rounding of U alone costs 2^-12
-#pragma unroll
-            for (int c = 0; c < 16; ++c) {
-                const float2 z = __fmul2_rn(make_float2(pv[2 * c], pv[2 * c + 1]), fz);
-                zv[c] = pack_f16(z.x, z.y);
-                const float2 zlo = __ffma2_rn(unpack_f16(zv[c]), make_float2(-1.f, -1.f), z);
-                zl[c] = pack_f16(zlo.x, zlo.y);
+
+            if (ok && out_pending) {   // the last chunk's state update and output
+                const bool gs = mbar_wait(bar_s, ph_s, wait_limit);
+                const bool go = mbar_wait(bar_o, ph_o, wait_limit);
+                const bool gg = gate_on ? mbar_wait(bar_z, ph_z, wait_limit) : true;
+                ph_s ^= 1;
+                ph_o ^= 1;
+                if (gate_on) ph_z ^= 1;
+                if (__syncthreads_or(!(gs && go && gg))) {
+                    ok = false;
+                } else {
+                    tc_fence_after();
+                    stage_output(spar);
+                    __syncthreads();
+                    store_output();
+                }
             }
-            tmem_st16u(trow + TM_Z + s0 / 2, zv);
-            tmem_st16u(trow + TM_ZL + s0 / 2, zl);
-            tmem_wait_st();
         }
-        ph_p ^= 1;
-        ph_v ^= 1;
-        fence_async_smem();
-        tc_fence_before();
-        if (__syncthreads_or(!got4)) { ok = false; break; }
-        // U^T = Z^T_hi T^T (U columns) + Z^T_lo T^T (the consumed P columns), issued by two
-        // threads [commit: U, two arrivals]
-        if (tid == 32) {
-            tc_fence_after();
+        if (!ok) {
+            // A bounded wait expired: let copies and MMAs in flight land, flag the failure and mark
+            // this unit's final state invalid.  At most one phase of each barrier can be in flight
+            // (nothing is issued again on a barrier before its last phase was waited for), and it
+            // is either the phase the parity names or the one before it: wait for both, with a
+            // bound of its own (a few milliseconds) that does not depend on the expired one.
+            if (tid == 0 && !drained) {
+                constexpr uint32_t drain = 1u << 12;
+                const uint32_t bars[7] = {bar_tma, bar_p, bar_v, bar_u, bar_s, bar_o, bar_z};
+                const uint32_t phs[7] = {ph_tma, ph_p, ph_v, ph_u, ph_s, ph_o, ph_z};
 #pragma unroll
-            for (int k = 0; k < 4; ++k)
-                mma_f16_ts(tmem + TM_P, tmem + TM_ZL + 8 * k, dsm + ((OFF_T + k * 32) >> 4), IDESC_N64, k > 0);
-            mma_commit(bar_u);
-        }
-        if (tid == 0) {
-            tc_fence_after();
-#pragma unroll
-            for (int k = 0; k < 4; ++k)
-                mma_f16_ts(tmem + TM_U, tmem + TM_Z + 8 * k, dsm + ((OFF_T + k * 32) >> 4), IDESC_N64, k > 0);
-            mma_commit(bar_u);
-        }
-        {   // while the U^T groups run: S^T <- S^T Diag(dec) in place (S^T was read as fp16 in
-            // (1)), moved from the lane's old scale to z_j (U^T is at z_j); warp w: lanes
-            // 32(w%4).., 32 columns from 32(w/4)
-            const int i0 = 32 * quarter;
-            float v[32];
-            tmem_ld32(trow + TM_S + i0, v);
-            const float f = pow2i(ZSC[spar * 128 + jl] - ZSC[cpar * 128 + jl]);   // |step| <= 126
-            const float2 f1 = make_float2(f, f);
-#pragma unroll
-            for (int c = 0; c < 32; c += 4) {
-                const float4 d4 = *reinterpret_cast<const float4 *>(DEC + i0 + c);
-                const float2 a2 = __fmul2_rn(__fmul2_rn(make_float2(v[c], v[c + 1]), f1), make_float2(d4.x, d4.y));
-                const float2 b2 = __fmul2_rn(__fmul2_rn(make_float2(v[c + 2], v[c + 3]), f1), make_float2(d4.z, d4.w));
-                v[c] = a2.x; v[c + 1] = a2.y; v[c + 2] = b2.x; v[c + 3] = b2.y;
+                for (int b = 0; b < 7; ++b) {
+                    mbar_wait(bars[b], phs[b], drain);
+                    mbar_wait(bars[b], phs[b] ^ 1u, drain);
+                }
+                atomicAdd(&g_kda_tc_timeouts, 1u);
             }
-            tmem_st32(trow + TM_S + i0, v);
-            tmem_wait_st();
-        }
-        {
-            const bool got = mbar_wait(bar_u, ph_u, wait_limit);
-            ph_u ^= 1;
-            if (__syncthreads_or(!got)) { ok = false; break; }
-        }
-        if (a.gate && tid == 0) {   // AT and T are consumed: this chunk's gate logits -> staging tile
-            fence_async_smem();
-            mbar_arrive_expect_tx(bar_z, 64 * D * 2);
-            tma_load_3d(sb + OFF_STG, &tmz, bar_z, 0, h, (int)t0);
+            drained = true;
+            if (kSeg && (P > 1 || balanced)) {   // only the last piece writes the state: mark this piece's outputs
+                const int64_t r0 = (int64_t)c_lo * C, r1 = (int64_t)c_hi * C < len ? (int64_t)c_hi * C : len;
+                for (int64_t x = tid; x < (r1 - r0) * D; x += NT)
+                    out[((bos + r0 + x / D) * H + h) * D + x % D] = __ushort_as_bfloat16((unsigned short)0x7fc0);
+            }
+            __syncthreads();
         }
         tc_fence_after();
-        // ---- (5) U^T -> fp16 hi + lo pairs (TMEM); warp w: lanes 32(w%4).., columns 16(w/4)..
-        {
-            const int r0 = 16 * quarter;
-            float uv[16], u2[16];
-            tmem_ld16x2(trow + TM_U + r0, trow + TM_P + r0, uv, u2);
+        if (a.sT && last_seg) {   // S = (TMEM state) 2^z_j
+            const int64_t sbase = ((int64_t)n * H + h) * D * D;
+            float v[32];
+            tmem_ld32(trow + TM_S + 32 * quarter, v);
+            const float fs = pow2i(ZSC[spar * 128 + jl]);
 #pragma unroll
-            for (int e = 0; e < 16; e += 2) {
-                const float2 a2 = __fadd2_rn(make_float2(uv[e], uv[e + 1]), make_float2(u2[e], u2[e + 1]));
-                uv[e] = a2.x; uv[e + 1] = a2.y;
-            }
-            uint32_t hi[8], lo[8];
-#pragma unroll
-            for (int e = 0; e < 8; ++e) {
-                hi[e] = pack_f16(uv[2 * e], uv[2 * e + 1]);
-                const float2 lo2 = __ffma2_rn(unpack_f16(hi[e]), make_float2(-1.f, -1.f), make_float2(uv[2 * e], uv[2 * e + 1]));
-                lo[e] = pack_f16(lo2.x, lo2.y);
-            }
-            tmem_st8u(trow + TM_UH + r0 / 2, hi);
-            tmem_st8u(trow + TM_UL + r0 / 2, lo);
-            tmem_wait_st();
+            for (int c = 0; c < 32; ++c)
+                a.sT[sbase + (int64_t)(32 * quarter + c) * D + jl] = ok ? v[c] * fs : __int_as_float(0x7fc00000);
         }
         tc_fence_before();
         __syncthreads();
-        // [S^T | (M U)^T] += U^T_hi [Kp^T; M]^T [commit: S];  low-order terms of (M U)^T,
-        // U^T_lo M^T + U^T_hi Mlo^T, into the U^T columns (consumed) [commit: O], issued by a
-        // warp with the least work in the next step (1); all at the lanes' scales z_j
-        if (tid == 0) {
-            tc_fence_after();
-#pragma unroll
-            for (int ks = 0; ks < 4; ++ks)
-                mma_f16_ts(tmem + TM_S, tmem + TM_UH + 8 * ks, dsm + ((OFF_KPT + ks * 32) >> 4), IDESC_N192, 1);
-            mma_commit(bar_s);
-        } else if (tid == 480) {
-            tc_fence_after();
-#pragma unroll
-            for (int ks = 0; ks < 4; ++ks)
-                mma_f16_ts(tmem + TM_U, tmem + TM_UL + 8 * ks, dsm + ((OFF_MT + ks * 32) >> 4), IDESC_N64, ks > 0);
-#pragma unroll
-            for (int ks = 0; ks < 4; ++ks)
-                mma_f16_ts(tmem + TM_U, tmem + TM_UH + 8 * ks, dsm + ((OFF_MLO + ks * 32) >> 4), IDESC_N64, 1);
-            mma_commit(bar_o);
-        }
-        out_pending = true;
-        t0_out = t0;
-        nr_out = ci >= c_lo ? nr : 0;   // the warm-up chunks before c_lo store nothing
-        spar = cpar;
-    }
-
-    if (ok && out_pending) {   // the last chunk's state update and output
-        const bool gs = mbar_wait(bar_s, ph_s, wait_limit);
-        const bool go = mbar_wait(bar_o, ph_o, wait_limit);
-        const bool gg = a.gate ? mbar_wait(bar_z, ph_z, wait_limit) : true;
-        ph_s ^= 1;
-        ph_o ^= 1;
-        if (a.gate) ph_z ^= 1;
-        if (__syncthreads_or(!(gs && go && gg))) {
-            ok = false;
-        } else {
-            tc_fence_after();
-            stage_output(spar);
-            __syncthreads();
-            store_output();
-        }
-    }
-    if (!ok) {
-        // A bounded wait expired: let copies and MMAs in flight land, flag the failure and mark
-        // this unit's final state invalid.  At most one phase of each barrier can be in flight
-        // (nothing is issued again on a barrier before its last phase was waited for), and it
-        // is either the phase the parity names or the one before it: wait for both, with a
-        // bound of its own (a few milliseconds) that does not depend on the expired one.
-        if (tid == 0) {
-            constexpr uint32_t drain = 1u << 12;
-            const uint32_t bars[7] = {bar_tma, bar_p, bar_v, bar_u, bar_s, bar_o, bar_z};
-            const uint32_t phs[7] = {ph_tma, ph_p, ph_v, ph_u, ph_s, ph_o, ph_z};
-#pragma unroll
-            for (int b = 0; b < 7; ++b) {
-                mbar_wait(bars[b], phs[b], drain);
-                mbar_wait(bars[b], phs[b] ^ 1u, drain);
-            }
-            atomicAdd(&g_kda_tc_timeouts, 1u);
-        }
-        if (kSeg && P > 1) {   // only the last segment writes the state: mark this segment's outputs
-            const int64_t r0 = (int64_t)c_lo * C, r1 = (int64_t)c_hi * C < len ? (int64_t)c_hi * C : len;
-            for (int64_t x = tid; x < (r1 - r0) * D; x += NT)
-                out[((bos + r0 + x / D) * H + h) * D + x % D] = __ushort_as_bfloat16((unsigned short)0x7fc0);
-        }
-        __syncthreads();
-    }
-    tc_fence_after();
-    if (a.sT && last_seg) {   // S = (TMEM state) 2^z_j
-        float v[32];
-        tmem_ld32(trow + TM_S + 32 * quarter, v);
-        const float fs = pow2i(ZSC[spar * 128 + jl]);
-#pragma unroll
-        for (int c = 0; c < 32; ++c)
-            a.sT[sbase + (int64_t)(32 * quarter + c) * D + jl] = ok ? v[c] * fs : __int_as_float(0x7fc00000);
     }
     tc_fence_before();
     __syncthreads();
@@ -1153,18 +1215,71 @@ int segments_for(int64_t units, int64_t tokens, int64_t num_seqs, int sms) {
     return P < 1 ? 1 : (int)P;
 }
 
-// Segments per (sequence, head) when the caller leaves the choice to the library: enough to
-// put every SM to work when there are fewer units than SMs, with segments of at least
-// kMinSegChunks chunks on average (segments_for); one when the launch writes checkpoints or
-// applies the output gate, or reads and writes the state in place (the last segment would
-// write the state while another may still read it).
-static int auto_segments(const ChunkArgs &a, int64_t units, int64_t tokens) {
-    if (a.gate || a.ckpt || (a.s0 && a.s0 == a.sT)) return 1;
+// CTAs of the balanced schedule for a dense batch of `units` units of `nc` chunks on `sms` SMs:
+// one per SM (at most kMaxSchedCtas), fewer when there are fewer chunks.
+int balanced_ctas(int64_t units, int64_t nc, int sms) {
+    const int64_t W = units * nc;
+    const int64_t g = sms < kMaxSchedCtas ? sms : kMaxSchedCtas;
+    return W <= 0 || g <= 0 ? 0 : (int)(W < g ? W : g);
+}
+
+// The CTAs' shares, drawn so that the largest cost is as small as bisection on it finds: a CTA
+// costs its items, plus kWarmCost when it starts inside a unit (the warm-up of its first piece,
+// which warm_start sets from the data -- one chunk at the decay bound, five with the standard
+// decay distribution; the estimate only weighs the split), plus kPieceCost for each further
+// piece (its set-up and pipeline refill).  Greedy: each CTA takes whole units while they fit its
+// budget and ends inside the next one -- unless that would leave it fewer than kMinTail chunks of
+// it, which would cost the next CTA a warm-up for little.
+constexpr double kWarmCost = 4.0, kPieceCost = 0.5;
+constexpr int64_t kMinTail = 8;
+static int64_t fill(int64_t W, int64_t nc, int G, double T, SchedBounds *out) {
+    int64_t x = 0;
+    for (int b = 0; b < G; ++b) {
+        if (out) out->x[b] = x;
+        double cost = x % nc ? kWarmCost : 0.0;
+        const int64_t start = x;
+        while (x < W) {
+            const int64_t r = nc - x % nc;
+            const double extra = x != start ? kPieceCost : 0.0;
+            if (cost + extra + (double)r <= T) {
+                x += r;
+                cost += extra + (double)r;
+                continue;
+            }
+            const int64_t take = (int64_t)(T - cost - extra);
+            if (take > 0 && (x == start || take >= kMinTail)) x += take;
+            break;
+        }
+    }
+    if (out) out->x[G] = W;
+    return x;
+}
+static void draw_schedule(int64_t units, int64_t nc, int G, SchedBounds *sb) {
+    const int64_t W = units * nc;
+    double lo = (double)W / G, hi = lo + (double)nc + kWarmCost + kPieceCost + 1.0;   // hi covers W
+    for (int it = 0; it < 30; ++it) {
+        const double mid = 0.5 * (lo + hi);
+        if (fill(W, nc, G, mid, nullptr) >= W) hi = mid;
+        else lo = mid;
+    }
+    fill(W, nc, G, hi, sb);   // the last CTA ends at W (fill covers W at hi)
+}
+
+// The library's choice when the caller leaves it open (a.segments == 0): a dense batch runs the
+// balanced schedule over one CTA per SM; packed sequences run segments_for's count of segments
+// per unit (the order in which their units are dispatched already puts the longest first); one
+// CTA per unit when the launch writes checkpoints or applies the output gate, or reads and
+// writes the state in place (a later piece of a unit would write the state while an earlier one
+// may still read it).
+static void library_schedule(ChunkArgs &a, int64_t units, int64_t tokens) {
+    a.segments = 1;
+    if (a.gate || a.ckpt || (a.s0 && a.s0 == a.sT)) return;
     int dev = 0, sms = 0;
     if (cudaGetDevice(&dev) != cudaSuccess ||
         cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
-        return 1;
-    return segments_for(units, tokens, a.num_seqs, sms);
+        return;
+    if (a.cu == nullptr) a.sched_ctas = balanced_ctas(units, (a.seqlen + C - 1) / C, sms);
+    else a.segments = segments_for(units, tokens, a.num_seqs, sms);
 }
 
 cudaError_t take_wait_expiries(cudaStream_t st, unsigned int *count) {
@@ -1186,7 +1301,9 @@ cudaError_t launch_chunk_tc(const ChunkArgs &args, int dk, int dv, kda_dtype_t d
     if (!chunk_tc_supported(dk, dv, dt)) return cudaErrorNotSupported;
     ChunkArgs a = args;
     const int64_t tokens = a.cu ? a.seqlen : (int64_t)a.num_seqs * a.seqlen;
-    if (a.segments <= 0) a.segments = auto_segments(a, (int64_t)a.num_seqs * a.heads, tokens);
+    const int64_t units = (int64_t)a.num_seqs * a.heads;
+    a.sched_ctas = 0;
+    if (a.segments <= 0) library_schedule(a, units, tokens);
     if (tokens >= (int64_t(1) << 31)) return cudaErrorInvalidValue;
     CUtensorMap mq, mk, mv, mg, mz;
     if (!make_map(&mq, a.q, tokens, a.heads) || !make_map(&mk, a.k, tokens, a.heads) ||
@@ -1194,12 +1311,25 @@ cudaError_t launch_chunk_tc(const ChunkArgs &args, int dk, int dv, kda_dtype_t d
         !make_map_rows(&mz, a.gate ? a.gate : a.v, tokens, a.heads))   // unused without a gate
         return cudaErrorInvalidValue;
     const int P = a.segments > 1 ? a.segments : 1;
-    auto kernel = P > 1 ? kda_chunk_tc_kernel<true> : kda_chunk_tc_kernel<false>;
+    auto kernel = a.sched_ctas > 0 ? kda_chunk_tc_kernel<2> : (P > 1 ? kda_chunk_tc_kernel<1> : kda_chunk_tc_kernel<0>);
     cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)SMEM_BYTES);
     if (e != cudaSuccess) return e;
-    const int64_t units = (int64_t)a.num_seqs * a.heads;
-    if (units * P > 0x7fffffffLL) return cudaErrorInvalidValue;
-    kernel<<<(unsigned)(units * P), NT, SMEM_BYTES, st>>>(mq, mk, mv, mg, mz, a, a.wait_polls);
+    const int64_t grid = a.sched_ctas > 0 ? a.sched_ctas : units * P;
+    if (grid > 0x7fffffffLL) return cudaErrorInvalidValue;
+    // the schedule is a kernel parameter (copied at the launch); the last one drawn on this host
+    // thread is kept, so that repeated launches of one shape do not redraw it
+    static thread_local SchedBounds sb{};
+    static thread_local int64_t drawn[3] = {-1, -1, -1};
+    if (a.sched_ctas > 0) {
+        const int64_t nc = (a.seqlen + C - 1) / C;
+        if (drawn[0] != units || drawn[1] != nc || drawn[2] != a.sched_ctas) {
+            draw_schedule(units, nc, a.sched_ctas, &sb);
+            drawn[0] = units;
+            drawn[1] = nc;
+            drawn[2] = a.sched_ctas;
+        }
+    }
+    kernel<<<(unsigned)grid, NT, SMEM_BYTES, st>>>(mq, mk, mv, mg, mz, a, a.wait_polls, sb);
     return cudaGetLastError();
 }
 

@@ -31,6 +31,7 @@ struct ChunkArgs {
     int32_t ckpt_interval;    // tokens between checkpoints (a multiple of the chunk)
     uint32_t wait_polls;      // bound on each device wait of the tensor-core kernel (polls)
     int32_t segments;         // tensor-core kernel: CTAs per (sequence, head), 0 = chosen by the launcher
+    int32_t sched_ctas = 0;   // tensor-core kernel: CTAs of the balanced schedule (set by the launcher), or 0
 };
 
 // Checkpoint slot for the state after `pos` tokens of sequence n (pos > 0 a multiple of the
@@ -102,6 +103,7 @@ cudaError_t take_wait_expiries(cudaStream_t st, unsigned int *count);
 // Segments per (sequence, head) the tensor-core launcher picks for a plain call on a GPU with
 // `sms` SMs: floor(sms / units), at most 8, lowered until segments average >= 16 chunks.
 int segments_for(int64_t units, int64_t tokens, int64_t num_seqs, int sms);
+int balanced_ctas(int64_t units, int64_t nc, int sms);
 cudaError_t launch_decode(const DecodeArgs &a, int dk, int dv, kda_dtype_t dt, cudaStream_t s);
 // out <- RMSNorm(out) * w * sigmoid(gate) over dv, in place, for every token row of a chunk call
 cudaError_t launch_gate_pass(const ChunkArgs &a, int64_t tokens, int dv, kda_dtype_t dt,

@@ -23,7 +23,7 @@ IMPL_NAMES = {v: k for k, v in IMPLS.items()}
 
 # every symbol include/kda.h declares
 EXPORTED = ("kda_chunk_fwd", "kda_chunk_fwd_with", "kda_chunk_fwd_bounded", "kda_chunk_fwd_segmented",
-            "kda_chunk_fwd_checkpointed", "kda_chunk_fwd_auto_segments",
+            "kda_chunk_fwd_checkpointed", "kda_chunk_fwd_auto_ctas",
             "kda_chunk_fwd_gated", "kda_chunk_fwd_selected_impl", "kda_recurrent_step",
             "kda_recurrent_steps", "kda_device_status", "kda_chunk_fwd_ws",
             "kda_chunk_fwd_workspace_bytes", "kda_chunk_fwd_noalloc", "kda_status_string")
@@ -65,8 +65,8 @@ def lib() -> ctypes.CDLL:
         L.kda_chunk_fwd_checkpointed.argtypes = [vp] * 11 + [ctypes.c_int32, dp, vp]
         L.kda_chunk_fwd_gated.restype = ctypes.c_int
         L.kda_chunk_fwd_gated.argtypes = [vp] * 7 + [ctypes.c_float] + [vp] * 4 + [dp, vp]
-        L.kda_chunk_fwd_auto_segments.restype = ctypes.c_int
-        L.kda_chunk_fwd_auto_segments.argtypes = [dp, ctypes.c_int]
+        L.kda_chunk_fwd_auto_ctas.restype = ctypes.c_int
+        L.kda_chunk_fwd_auto_ctas.argtypes = [dp, ctypes.c_int, ctypes.c_int]
         L.kda_chunk_fwd_selected_impl.restype = ctypes.c_int
         L.kda_chunk_fwd_selected_impl.argtypes = [dp]
         L.kda_recurrent_step.restype = ctypes.c_int
@@ -240,9 +240,9 @@ def kda_chunk_fwd_segmented(q, k, v, g, beta, initial_state=None, cu_seqlens=Non
     return kda_chunk_fwd(q, k, v, g, beta, initial_state, cu_seqlens, segments=segments, **kw)
 
 
-def kda_chunk_fwd_auto_segments(dims: KdaDims, sms: int) -> int:
-    """CTAs per (sequence, head) kda_chunk_fwd gives the tensor-core kernel on `sms` SMs."""
-    return int(lib().kda_chunk_fwd_auto_segments(ctypes.byref(dims), int(sms)))
+def kda_chunk_fwd_auto_ctas(dims: KdaDims, packed: bool, sms: int) -> int:
+    """CTAs kda_chunk_fwd launches for the tensor-core kernel on `sms` SMs (0: not that kernel)."""
+    return int(lib().kda_chunk_fwd_auto_ctas(ctypes.byref(dims), int(bool(packed)), int(sms)))
 
 
 def kda_chunk_fwd_selected_impl(q, v, cu_seqlens=None) -> str:
