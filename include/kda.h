@@ -19,8 +19,10 @@
  *   - Pointers are DEVICE pointers unless stated; tensors are dense, row-major,
  *     contiguous, and must be 16-byte aligned (cu_seqlens / state_indices:
  *     4-byte aligned).  The caller allocates and owns all memory; the library
- *     allocates nothing and keeps no state between calls besides one device-wide
- *     count of expired device waits (kda_device_status reads and clears it).
+ *     allocates nothing and keeps no state between calls besides device-wide
+ *     counts of expired device waits and of failed debug-build input checks
+ *     (kda_device_status reads and clears them) and kda_chunk_fwd_noalloc's
+ *     fixed scratch area.
  *   - Calls are asynchronous on `stream` (0 = legacy default stream) and do not
  *     synchronise the host (kda_device_status excepted).  Argument errors are detected on the host, before
  *     anything is launched; on error nothing is written.  Launch failures map
@@ -33,7 +35,10 @@
  *     caller's).  g is the log decay; the kernels rely on the lower bound
  *     g >= -5 of the "lower-bound" paragraph (so that a 16-token tile's
  *     cumulative log decay stays >= -80 and e^80 fits bf16/fp32): g in [-5, 0]
- *     is a precondition, not checked; outside it results are unspecified.
+ *     is a precondition; outside it results are unspecified.  The release library
+ *     does not check it; a library built with debug checks (kda_debug_checks) checks
+ *     it, and the packed offsets, on the device before each call and reports a
+ *     failure through kda_device_status (KDA_ERR_INPUT).
  *   - v and the initial state may take any magnitude their formats hold: the
  *     operation is linear in them, and the tensor-core kernel keeps its 16-bit
  *     copies of the state and of the per-chunk corrections at a power-of-two
@@ -63,7 +68,8 @@ typedef enum {
     KDA_ERR_ALIGN = 4,       /* a pointer is not aligned as required              */
     KDA_ERR_WORKSPACE = 5,   /* the workspace is smaller than needed              */
     KDA_ERR_CUDA = 6,        /* a CUDA runtime call or launch failed              */
-    KDA_ERR_TIMEOUT = 7      /* a bounded device wait gave up (kda_device_status) */
+    KDA_ERR_TIMEOUT = 7,     /* a bounded device wait gave up (kda_device_status) */
+    KDA_ERR_INPUT = 8        /* an input failed a debug-build check (kda_device_status) */
 } kda_status_t;
 
 typedef enum { KDA_F32 = 0, KDA_BF16 = 1 } kda_dtype_t;
@@ -336,12 +342,22 @@ kda_status_t kda_recurrent_steps(const void *q, const void *k, const void *v,
 /* kda_device_status -- waits for the work queued on `stream` to finish, then reads and
  * clears the current device's count of device-side waits of the tensor-core chunk kernels
  * that gave up (see kda_chunk_fwd_bounded; the two passes of kda_chunk_fwd_ws count theirs
- * too).  Returns KDA_ERR_TIMEOUT when at least one wait gave up since the previous call on
- * this device (from any stream), KDA_OK when none did, and KDA_ERR_CUDA when the stream or
- * the copies fail.  The count is device-global: calls that run concurrently on other streams
- * of the device report into the same count.  This is the only call of the library that
- * synchronises the host; it does not depend on final_state being requested. */
+ * too) and its word of failed debug-build input checks.  Returns KDA_ERR_INPUT when a check
+ * failed since the previous call on this device (only a library built with debug checks
+ * makes any), else KDA_ERR_TIMEOUT when at least one wait gave up, KDA_OK when neither
+ * happened, and KDA_ERR_CUDA when the stream or the copies fail.  Both are device-global:
+ * calls that run concurrently on other streams of the device report into the same word and
+ * count.  This is the only call of the library that synchronises the host; it does not
+ * depend on final_state being requested. */
 kda_status_t kda_device_status(cudaStream_t stream);
+
+/* kda_debug_checks -- which device-side input checks this build of the library runs before
+ * each chunk forward and decode call: a bit mask, 1 = g in [-5, 0] (NaN fails), 2 = packed
+ * offsets 0 = cu[0] <= ... <= cu[N] = seqlen; 0 for the release build, which runs none (the
+ * precondition is "はじめての自然言語処理 -- Kimi K3", section 3.1: g = -5 sigmoid(x)).  A failed
+ * check launches nothing extra and traps nothing: the call still runs, its results are
+ * unspecified, and kda_device_status returns KDA_ERR_INPUT.  A host query. */
+int kda_debug_checks(void);
 
 /* A static, human-readable name for a status code (never NULL). */
 const char *kda_status_string(kda_status_t status);

@@ -19,6 +19,7 @@ CSRC = os.path.join(HERE, "csrc")
 INCLUDE = os.path.join(os.path.dirname(HERE), "include")
 BUILD = os.path.join(HERE, "_build")
 LIB = os.path.join(HERE, "libkda.so")
+LIB_DEBUG = os.path.join(HERE, "libkda_debug.so")
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 NVCC_FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "--expt-relaxed-constexpr",
               "-Xptxas", "-v"]
@@ -50,22 +51,29 @@ def _digest(paths, extra=""):
     return h.hexdigest()
 
 
-def build(verbose: bool = False, force: bool = False) -> str:
-    """Compile csrc/*.cu for sm_103a and link libkda.so; returns its path."""
-    os.makedirs(BUILD, exist_ok=True)
+def build(verbose: bool = False, force: bool = False, debug: bool = False) -> str:
+    """Compile csrc/*.cu for sm_103a and link libkda.so; returns its path.
+
+    debug=True builds libkda_debug.so instead (objects in _build_debug/): the same kernels with
+    KDA_DEBUG_CHECKS defined, so that every chunk forward and decode call first checks g and the
+    packed offsets on the device (kda_debug_checks, kda_device_status)."""
+    build_dir = BUILD + "_debug" if debug else BUILD
+    lib_path = LIB_DEBUG if debug else LIB
+    flags = NVCC_FLAGS + (["-DKDA_DEBUG_CHECKS=1"] if debug else [])
+    os.makedirs(build_dir, exist_ok=True)
     nvcc = _nvcc()
     srcs = _sources()
-    hdr_digest = _digest(_headers(), " ".join(ARCH + NVCC_FLAGS))
-    stamp = os.path.join(BUILD, "stamp")
+    hdr_digest = _digest(_headers(), " ".join(ARCH + flags))
+    stamp = os.path.join(build_dir, "stamp")
     want = _digest(srcs, hdr_digest)
-    if not force and os.path.exists(LIB) and os.path.exists(stamp):
+    if not force and os.path.exists(lib_path) and os.path.exists(stamp):
         with open(stamp) as f:
             if f.read() == want:
-                return LIB
+                return lib_path
 
     def compile_one(src):
-        obj = os.path.join(BUILD, os.path.basename(src)[:-3] + ".o")
-        cmd = [nvcc, *ARCH, *NVCC_FLAGS, "-I", INCLUDE, "-c", src, "-o", obj]
+        obj = os.path.join(build_dir, os.path.basename(src)[:-3] + ".o")
+        cmd = [nvcc, *ARCH, *flags, "-I", INCLUDE, "-c", src, "-o", obj]
         r = subprocess.run(cmd, capture_output=True, text=True)
         if r.returncode != 0:
             raise RuntimeError(f"nvcc failed for {src}:\n{r.stdout}\n{r.stderr}")
@@ -75,20 +83,20 @@ def build(verbose: bool = False, force: bool = False) -> str:
 
     with ThreadPoolExecutor(max_workers=min(8, len(srcs))) as ex:
         objs = list(ex.map(compile_one, srcs))
-    tmp = LIB + f".tmp{os.getpid()}"
+    tmp = lib_path + f".tmp{os.getpid()}"
     cmd = [nvcc, *ARCH, "-shared", "-o", tmp, *objs, "-cudart", "static"]
     r = subprocess.run(cmd, capture_output=True, text=True)
     if r.returncode != 0:
         raise RuntimeError(f"link failed:\n{r.stdout}\n{r.stderr}")
-    os.replace(tmp, LIB)
+    os.replace(tmp, lib_path)
     with open(stamp, "w") as f:
         f.write(want)
     if verbose:
         for o in objs:
             with open(o + ".log") as f:
                 sys.stdout.write(f.read())
-    return LIB
+    return lib_path
 
 
 if __name__ == "__main__":
-    print(build(verbose="-v" in sys.argv, force="-f" in sys.argv))
+    print(build(verbose="-v" in sys.argv, force="-f" in sys.argv, debug="--debug" in sys.argv))

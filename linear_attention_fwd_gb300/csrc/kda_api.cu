@@ -56,17 +56,21 @@ extern "C" const char *kda_status_string(kda_status_t s) {
         case KDA_ERR_WORKSPACE: return "workspace too small";
         case KDA_ERR_CUDA: return "CUDA launch or runtime error";
         case KDA_ERR_TIMEOUT: return "a bounded device wait gave up";
+        case KDA_ERR_INPUT: return "an input failed a debug-build precondition check";
     }
     return "unknown status";
 }
 
 extern "C" kda_status_t kda_device_status(cudaStream_t stream) {
-    unsigned int n1 = 0, n2 = 0, n3 = 0;
+    unsigned int n1 = 0, n2 = 0, n3 = 0, bad = 0;
     if (kda::take_wait_expiries(stream, &n1) != cudaSuccess || kda::take_prep_expiries(stream, &n2) != cudaSuccess ||
-        kda::take_state_expiries(stream, &n3) != cudaSuccess)
+        kda::take_state_expiries(stream, &n3) != cudaSuccess || kda::take_input_errors(stream, &bad) != cudaSuccess)
         return KDA_ERR_CUDA;
+    if (bad) return KDA_ERR_INPUT;
     return (n1 || n2 || n3) ? KDA_ERR_TIMEOUT : KDA_OK;
 }
+
+extern "C" int kda_debug_checks(void) { return kda::debug_checks_built(); }
 
 extern "C" size_t kda_chunk_fwd_workspace_bytes(const kda_dims_t *d) {
     if (d == nullptr || d->heads <= 0 || d->num_seqs <= 0 || d->batch <= 0 || d->seqlen < 0) return 0;
@@ -93,7 +97,9 @@ extern "C" kda_status_t kda_chunk_fwd_ws(const void *q, const void *k, const voi
     kda::ChunkArgs a{q, k, v, g, beta, initial_state, cu_seqlens, out, final_state,
                      (int64_t)d->seqlen, d->num_seqs, d->heads, nullptr, nullptr, 0.f,
                      nullptr, nullptr, 0, 1u << 20, 1};
-    cudaError_t e = kda::launch_chunk_prep(a, workspace, stream);
+    cudaError_t e = kda::debug_check_inputs(g, (int64_t)d->batch * d->seqlen * d->heads * d->dk, d->dtype,
+                                            cu_seqlens, d->num_seqs, d->seqlen, stream);
+    if (e == cudaSuccess) e = kda::launch_chunk_prep(a, workspace, stream);
     if (e == cudaSuccess) e = kda::launch_chunk_state(a, workspace, stream);
     return e == cudaSuccess ? KDA_OK : KDA_ERR_CUDA;
 }
@@ -127,7 +133,9 @@ static kda_status_t chunk_run(kda_impl_t impl, const void *q, const void *k, con
     kda::ChunkArgs a{q, k, v, g, beta, initial_state, cu_seqlens, out, final_state,
                      (int64_t)d->seqlen, d->num_seqs, d->heads, gate, norm_w, norm_eps,
                      ckpt, ckpt_off, ckpt_interval, wait_polls, segments};
-    cudaError_t e;
+    cudaError_t e = kda::debug_check_inputs(g, (int64_t)d->batch * d->seqlen * d->heads * d->dk, d->dtype,
+                                            cu_seqlens, d->num_seqs, d->seqlen, stream);
+    if (e != cudaSuccess) return KDA_ERR_CUDA;
     if ((int64_t)d->batch * d->seqlen == 0) {
         if (final_state == nullptr || final_state == initial_state) return KDA_OK;
         e = kda::launch_state_copy(a, d->dk, d->dv, stream);
@@ -231,7 +239,8 @@ extern "C" kda_status_t kda_recurrent_step(const void *q, const void *k, const v
     if (state_indices && !aligned(state_indices, 4)) return KDA_ERR_ALIGN;
     kda::DecodeArgs a{q, k, v, g, beta, state, state_indices, out, d->batch, d->num_seqs, d->heads,
                       1, nullptr, 1};
-    cudaError_t e = kda::launch_decode(a, d->dk, d->dv, d->dtype, stream);
+    cudaError_t e = kda::debug_check_inputs(g, (int64_t)d->batch * d->heads * d->dk, d->dtype, nullptr, 0, 0, stream);
+    if (e == cudaSuccess) e = kda::launch_decode(a, d->dk, d->dv, d->dtype, stream);
     return e == cudaSuccess ? KDA_OK : KDA_ERR_CUDA;
 }
 
@@ -259,6 +268,8 @@ extern "C" kda_status_t kda_recurrent_steps(const void *q, const void *k, const 
     if (num_tokens && !aligned(num_tokens, 4)) return KDA_ERR_ALIGN;
     kda::DecodeArgs a{q, k, v, g, beta, state, state_indices, out, d->batch, d->num_seqs, d->heads,
                       d->seqlen, num_tokens, update_state ? 1 : 0};
-    cudaError_t e = kda::launch_decode(a, d->dk, d->dv, d->dtype, stream);
+    cudaError_t e = kda::debug_check_inputs(g, (int64_t)d->batch * d->seqlen * d->heads * d->dk, d->dtype,
+                                            nullptr, 0, 0, stream);
+    if (e == cudaSuccess) e = kda::launch_decode(a, d->dk, d->dv, d->dtype, stream);
     return e == cudaSuccess ? KDA_OK : KDA_ERR_CUDA;
 }

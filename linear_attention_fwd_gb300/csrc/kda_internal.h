@@ -104,6 +104,13 @@ cudaError_t take_wait_expiries(cudaStream_t st, unsigned int *count);
 // `sms` SMs: floor(sms / units), at most 8, lowered until segments average >= 16 chunks.
 int segments_for(int64_t units, int64_t tokens, int64_t num_seqs, int sms);
 int balanced_ctas(int64_t units, int64_t nc, int sms);
+// Debug-build checks of the device-resident preconditions (g in [-5, 0], packed offsets): launched
+// on `st` before a call's kernels when the library is built with KDA_DEBUG_CHECKS, no-ops
+// otherwise; failures set bits of a device error word that take_input_errors reads and clears.
+cudaError_t debug_check_inputs(const void *g, int64_t g_elems, kda_dtype_t dt, const int32_t *cu,
+                               int num_seqs, int64_t seqlen, cudaStream_t st);
+int debug_checks_built();
+cudaError_t take_input_errors(cudaStream_t st, unsigned int *bits);
 cudaError_t launch_decode(const DecodeArgs &a, int dk, int dv, kda_dtype_t dt, cudaStream_t s);
 // out <- RMSNorm(out) * w * sigmoid(gate) over dv, in place, for every token row of a chunk call
 cudaError_t launch_gate_pass(const ChunkArgs &a, int64_t tokens, int dv, kda_dtype_t dt,

@@ -14,9 +14,10 @@ import torch
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(_HERE, "libkda.so")
+DEBUG_LIB_PATH = os.path.join(_HERE, "libkda_debug.so")   # build.build(debug=True): device input checks
 
 KDA_OK, KDA_ERR_NULL, KDA_ERR_SHAPE, KDA_ERR_UNSUPPORTED = 0, 1, 2, 3
-KDA_ERR_ALIGN, KDA_ERR_WORKSPACE, KDA_ERR_CUDA, KDA_ERR_TIMEOUT = 4, 5, 6, 7
+KDA_ERR_ALIGN, KDA_ERR_WORKSPACE, KDA_ERR_CUDA, KDA_ERR_TIMEOUT, KDA_ERR_INPUT = 4, 5, 6, 7, 8
 KDA_F32, KDA_BF16 = 0, 1
 IMPLS = {"auto": 0, "simt": 1, "tc": 2}
 IMPL_NAMES = {v: k for k, v in IMPLS.items()}
@@ -26,7 +27,8 @@ EXPORTED = ("kda_chunk_fwd", "kda_chunk_fwd_with", "kda_chunk_fwd_bounded", "kda
             "kda_chunk_fwd_checkpointed", "kda_chunk_fwd_auto_ctas",
             "kda_chunk_fwd_gated", "kda_chunk_fwd_selected_impl", "kda_recurrent_step",
             "kda_recurrent_steps", "kda_device_status", "kda_chunk_fwd_ws",
-            "kda_chunk_fwd_workspace_bytes", "kda_chunk_fwd_noalloc", "kda_status_string")
+            "kda_chunk_fwd_workspace_bytes", "kda_chunk_fwd_noalloc", "kda_debug_checks",
+            "kda_status_string")
 
 
 class KdaDims(ctypes.Structure):
@@ -81,6 +83,8 @@ def lib() -> ctypes.CDLL:
         L.kda_chunk_fwd_noalloc.argtypes = [vp] * 9 + [dp, vp]
         L.kda_device_status.restype = ctypes.c_int
         L.kda_device_status.argtypes = [vp]
+        L.kda_debug_checks.restype = ctypes.c_int
+        L.kda_debug_checks.argtypes = []
         L.kda_status_string.restype = ctypes.c_char_p
         L.kda_status_string.argtypes = [ctypes.c_int]
         _lib = L
@@ -89,6 +93,20 @@ def lib() -> ctypes.CDLL:
 
 def kda_status_string(status: int) -> str:
     return lib().kda_status_string(int(status)).decode()
+
+
+def use_library(path: str) -> None:
+    """Load libkda from `path` for the calls that follow (LIB_PATH, or DEBUG_LIB_PATH for the
+    build with device-side input checks)."""
+    global _lib, LIB_PATH
+    LIB_PATH = path
+    _lib = None
+    lib()
+
+
+def kda_debug_checks() -> int:
+    """Bit mask of the device-side input checks the loaded library runs (0: release build)."""
+    return int(lib().kda_debug_checks())
 
 
 def kda_device_status(stream=None) -> int:

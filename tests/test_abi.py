@@ -38,7 +38,7 @@ def test_every_declared_symbol_is_exported(K):
 
 
 def test_status_strings(K):
-    for code in range(8):
+    for code in range(9):
         s = K.kda_status_string(code)
         assert s and s != "unknown status"
     assert K.kda_status_string(99) == "unknown status"
@@ -224,3 +224,18 @@ def test_noalloc_limit_and_rejection(K):
     big = dims(batch=1, seqlen=1 << 20, num_seqs=1, heads=32)
     assert K.lib().kda_chunk_fwd_workspace_bytes(ctypes.byref(big)) > K.NOALLOC_SCRATCH_BYTES
     assert K.lib().kda_chunk_fwd_noalloc(*args, ctypes.byref(big), None) == K.KDA_ERR_WORKSPACE
+
+
+def test_debug_build_reports_its_checks(K):
+    # the release library runs no device-side input check; the debug build (separate objects,
+    # libkda_debug.so) runs both, and exports the same symbols
+    assert K.kda_debug_checks() == 0
+    path = kbuild.build(debug=True)
+    assert path.endswith("libkda_debug.so")
+    dbg = ctypes.CDLL(path)
+    dbg.kda_debug_checks.restype = ctypes.c_int
+    assert dbg.kda_debug_checks() == 3
+    for n in declared_functions():
+        assert hasattr(dbg, n), n
+    dbg.kda_status_string.restype = ctypes.c_char_p
+    assert b"debug-build" in dbg.kda_status_string(K.KDA_ERR_INPUT)
