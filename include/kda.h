@@ -75,7 +75,9 @@ typedef enum {
 typedef enum { KDA_F32 = 0, KDA_BF16 = 1 } kda_dtype_t;
 
 /* Which chunk-forward kernel to run.  AUTO picks the tensor-core kernel where
- * it applies (bf16, dk = dv = 128) and the SIMT fp32 kernel otherwise. */
+ * it applies (bf16; a head size of 64 runs there at 128 with the missing channels
+ * read as zeros, except with the output gate or checkpoints, which need
+ * dk = dv = 128) and the SIMT fp32 kernel otherwise. */
 typedef enum { KDA_IMPL_AUTO = 0, KDA_IMPL_SIMT = 1, KDA_IMPL_TC = 2 } kda_impl_t;
 
 /* Problem dimensions.

@@ -74,7 +74,7 @@ extern "C" int kda_debug_checks(void) { return kda::debug_checks_built(); }
 
 extern "C" size_t kda_chunk_fwd_workspace_bytes(const kda_dims_t *d) {
     if (d == nullptr || d->heads <= 0 || d->num_seqs <= 0 || d->batch <= 0 || d->seqlen < 0) return 0;
-    if (!kda::chunk_tc_supported(d->dk, d->dv, d->dtype)) return 0;
+    if (!kda::chunk_tc_full(d->dk, d->dv, d->dtype)) return 0;
     const int64_t tokens = (int64_t)d->batch * d->seqlen;
     if (tokens == 0) return 0;
     return kda::two_pass_workspace_bytes(tokens, d->num_seqs, d->heads);
@@ -140,8 +140,11 @@ static kda_status_t chunk_run(kda_impl_t impl, const void *q, const void *k, con
         if (final_state == nullptr || final_state == initial_state) return KDA_OK;
         e = kda::launch_state_copy(a, d->dk, d->dv, stream);
     } else {
-        if (impl == KDA_IMPL_AUTO)
-            impl = kda::chunk_tc_supported(d->dk, d->dv, d->dtype) ? KDA_IMPL_TC : KDA_IMPL_SIMT;
+        // the output gate and checkpoints run on the tensor-core kernel at dk = dv = 128 only
+        const bool tc_ok = kda::chunk_tc_supported(d->dk, d->dv, d->dtype) &&
+                           (kda::chunk_tc_full(d->dk, d->dv, d->dtype) || (!gate && !ckpt));
+        if (impl == KDA_IMPL_AUTO) impl = tc_ok ? KDA_IMPL_TC : KDA_IMPL_SIMT;
+        else if (impl == KDA_IMPL_TC && !tc_ok) return KDA_ERR_UNSUPPORTED;
         if (impl == KDA_IMPL_TC) {
             e = kda::launch_chunk_tc(a, d->dk, d->dv, d->dtype, stream);   // gate fused
         } else {

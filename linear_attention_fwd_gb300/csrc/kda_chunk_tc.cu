@@ -66,7 +66,7 @@ namespace {
 using namespace ptx;
 
 constexpr int C = 64;         // chunk
-constexpr int D = 128;        // d_k = d_v
+constexpr int D = 128;        // the head size the kernel computes at (d_k = d_v; 64-wide heads are padded)
 constexpr int NT = 512;       // threads (16 warps)
 constexpr float LOG2E = 1.4426950408889634f;
 
@@ -248,11 +248,12 @@ __device__ int warm_start(const ChunkArgs &a, int64_t bos, int h, int c_lo) {
     float acc = 0.f;   // log2 of the norm bound from chunk c to c_lo
     for (int c = c_lo - 1; c >= c_min; --c) {
         const int64_t tok = bos + (int64_t)c * C + r;
-        const uint4 *gp = reinterpret_cast<const uint4 *>(gq + (tok * H + h) * D + 16 * part);
-        const uint4 *kp = reinterpret_cast<const uint4 *>(kq + (tok * H + h) * D + 16 * part);
+        const uint4 *gp = reinterpret_cast<const uint4 *>(gq + (tok * H + h) * a.dk + 16 * part);
+        const uint4 *kp = reinterpret_cast<const uint4 *>(kq + (tok * H + h) * a.dk + 16 * part);
         float gm = -3.0e38f, ks = 0.f;
 #pragma unroll
         for (int u = 0; u < 2; ++u) {
+            if (16 * part >= a.dk) break;   // a 64-wide head: parts 4-7 hold nothing
             const uint4 gv = __ldg(gp + u), kv = __ldg(kp + u);
             const uint32_t gw[4] = {gv.x, gv.y, gv.z, gv.w}, kw[4] = {kv.x, kv.y, kv.z, kv.w};
 #pragma unroll
@@ -505,10 +506,10 @@ kda_chunk_tc_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_consta
         const uint4 *os = reinterpret_cast<const uint4 *>(sm + OFF_STG);
 #pragma unroll
         for (int e = 0; e < 1024 / NT; ++e) {
-            const int idx = tid + NT * e;          // 64 rows x 16 uint4
+            const int idx = tid + NT * e;          // 64 rows x 16 uint4 (the first dv / 8 of a row stored)
             const int r = idx >> 4, c16 = idx & 15;
-            if (r < nr_out)
-                reinterpret_cast<uint4 *>(out + ((t0_out + r) * H + h) * D)[c16] = os[idx];
+            if (r < nr_out && c16 < (a.dv >> 3))
+                reinterpret_cast<uint4 *>(out + ((t0_out + r) * H + h) * a.dv)[c16] = os[idx];
         }
     };
     // T_IJ = -(sum_{K=J+1..I} T_IK A_KJ) T_JJ for one 16x16 block below the diagonal (one warp)
@@ -612,11 +613,12 @@ kda_chunk_tc_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_consta
             const int64_t t_run = bos + (int64_t)c_run * C;
             // ---- initial state -> TMEM (S^T: lane j, column i; scale exponent 0)
             {
-                const int64_t sbase = ((int64_t)n * H + h) * D * D;
+                const int64_t sbase = ((int64_t)n * H + h) * a.dk * a.dv;
                 float v[32];
 #pragma unroll
-                for (int c = 0; c < 32; ++c)
-                    v[c] = (a.s0 && c_run == 0) ? a.s0[sbase + (int64_t)(32 * quarter + c) * D + jl] : 0.f;
+                for (int c = 0; c < 32; ++c)   // S[i][j], zero outside a 64-wide head's channels
+                    v[c] = (a.s0 && c_run == 0 && 32 * quarter + c < a.dk && jl < a.dv)
+                               ? a.s0[sbase + (int64_t)(32 * quarter + c) * a.dv + jl] : 0.f;
                 tmem_st32(trow + TM_S + 32 * quarter, v);
                 uint32_t zero[16];
 #pragma unroll
@@ -1136,20 +1138,21 @@ kda_chunk_tc_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_consta
             drained = true;
             if (kSeg && (P > 1 || balanced)) {   // only the last piece writes the state: mark this piece's outputs
                 const int64_t r0 = (int64_t)c_lo * C, r1 = (int64_t)c_hi * C < len ? (int64_t)c_hi * C : len;
-                for (int64_t x = tid; x < (r1 - r0) * D; x += NT)
-                    out[((bos + r0 + x / D) * H + h) * D + x % D] = __ushort_as_bfloat16((unsigned short)0x7fc0);
+                for (int64_t x = tid; x < (r1 - r0) * a.dv; x += NT)
+                    out[((bos + r0 + x / a.dv) * H + h) * a.dv + x % a.dv] = __ushort_as_bfloat16((unsigned short)0x7fc0);
             }
             __syncthreads();
         }
         tc_fence_after();
         if (a.sT && last_seg) {   // S = (TMEM state) 2^z_j
-            const int64_t sbase = ((int64_t)n * H + h) * D * D;
+            const int64_t sbase = ((int64_t)n * H + h) * a.dk * a.dv;
             float v[32];
             tmem_ld32(trow + TM_S + 32 * quarter, v);
             const float fs = pow2i(ZSC[spar * 128 + jl]);
 #pragma unroll
             for (int c = 0; c < 32; ++c)
-                a.sT[sbase + (int64_t)(32 * quarter + c) * D + jl] = ok ? v[c] * fs : __int_as_float(0x7fc00000);
+                if (32 * quarter + c < a.dk && jl < a.dv)
+                    a.sT[sbase + (int64_t)(32 * quarter + c) * a.dv + jl] = ok ? v[c] * fs : __int_as_float(0x7fc00000);
         }
         tc_fence_before();
         __syncthreads();
@@ -1175,13 +1178,14 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
     return fn;
 }
 
-// [tokens][H][128] bf16 as a 3-D tensor (128, H, tokens); 64 x 1 x 64 boxes,
-// 128-byte swizzle (the layout the MMA operand descriptors expect).
-bool make_map(CUtensorMap *m, const void *ptr, int64_t tokens, int H) {
+// [tokens][H][d] bf16 as a 3-D tensor (d, H, tokens); 64 x 1 x 64 boxes, 128-byte swizzle (the
+// layout the MMA operand descriptors expect).  With d = 64 the kernel's second 64-channel box lies
+// wholly past the tensor's first dimension and lands as zeros.
+bool make_map(CUtensorMap *m, const void *ptr, int64_t tokens, int H, int d) {
     auto enc = encode_fn();
     if (enc == nullptr) return false;
-    cuuint64_t dims[3] = {(cuuint64_t)D, (cuuint64_t)H, (cuuint64_t)tokens};
-    cuuint64_t strides[2] = {(cuuint64_t)D * 2, (cuuint64_t)H * D * 2};
+    cuuint64_t dims[3] = {(cuuint64_t)d, (cuuint64_t)H, (cuuint64_t)tokens};
+    cuuint64_t strides[2] = {(cuuint64_t)d * 2, (cuuint64_t)H * d * 2};
     cuuint32_t box[3] = {64, 1, 64};
     cuuint32_t es[3] = {1, 1, 1};
     return enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void *>(ptr), dims, strides, box, es,
@@ -1294,8 +1298,10 @@ cudaError_t take_wait_expiries(cudaStream_t st, unsigned int *count) {
 }
 
 bool chunk_tc_supported(int dk, int dv, kda_dtype_t dt) {
-    return dt == KDA_BF16 && dk == D && dv == D;
+    return dt == KDA_BF16 && (dk == 64 || dk == D) && (dv == 64 || dv == D);
 }
+
+bool chunk_tc_full(int dk, int dv, kda_dtype_t dt) { return dt == KDA_BF16 && dk == D && dv == D; }
 
 cudaError_t launch_chunk_tc(const ChunkArgs &args, int dk, int dv, kda_dtype_t dt, cudaStream_t st) {
     if (!chunk_tc_supported(dk, dv, dt)) return cudaErrorNotSupported;
@@ -1306,8 +1312,11 @@ cudaError_t launch_chunk_tc(const ChunkArgs &args, int dk, int dv, kda_dtype_t d
     if (a.segments <= 0) library_schedule(a, units, tokens);
     if (tokens >= (int64_t(1) << 31)) return cudaErrorInvalidValue;
     CUtensorMap mq, mk, mv, mg, mz;
-    if (!make_map(&mq, a.q, tokens, a.heads) || !make_map(&mk, a.k, tokens, a.heads) ||
-        !make_map(&mv, a.v, tokens, a.heads) || !make_map(&mg, a.g, tokens, a.heads) ||
+    a.dk = dk;
+    a.dv = dv;
+    if ((a.gate || a.ckpt) && !chunk_tc_full(dk, dv, dt)) return cudaErrorNotSupported;
+    if (!make_map(&mq, a.q, tokens, a.heads, dk) || !make_map(&mk, a.k, tokens, a.heads, dk) ||
+        !make_map(&mv, a.v, tokens, a.heads, dv) || !make_map(&mg, a.g, tokens, a.heads, dk) ||
         !make_map_rows(&mz, a.gate ? a.gate : a.v, tokens, a.heads))   // unused without a gate
         return cudaErrorInvalidValue;
     const int P = a.segments > 1 ? a.segments : 1;

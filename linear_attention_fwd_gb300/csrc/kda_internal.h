@@ -32,6 +32,8 @@ struct ChunkArgs {
     uint32_t wait_polls;      // bound on each device wait of the tensor-core kernel (polls)
     int32_t segments;         // tensor-core kernel: CTAs per (sequence, head), 0 = chosen by the launcher
     int32_t sched_ctas = 0;   // tensor-core kernel: CTAs of the balanced schedule (set by the launcher), or 0
+    int32_t dk = 128, dv = 128;   // head sizes in memory (the tensor-core kernel computes at 128 and
+                                  // reads the missing channels of a 64-wide head as zeros)
 };
 
 // Checkpoint slot for the state after `pos` tokens of sequence n (pos > 0 a multiple of the
@@ -97,7 +99,8 @@ cudaError_t take_state_expiries(cudaStream_t st, unsigned int *count);
 // Launchers (host).  Each returns cudaSuccess or the launch error.
 cudaError_t launch_chunk_simt(const ChunkArgs &a, int dk, int dv, kda_dtype_t dt, cudaStream_t s);
 cudaError_t launch_chunk_tc(const ChunkArgs &a, int dk, int dv, kda_dtype_t dt, cudaStream_t s);
-bool chunk_tc_supported(int dk, int dv, kda_dtype_t dt);
+bool chunk_tc_supported(int dk, int dv, kda_dtype_t dt);   // any of the head sizes, bf16
+bool chunk_tc_full(int dk, int dv, kda_dtype_t dt);        // dk = dv = 128 (gate, checkpoints, two-pass)
 // Waits for `st`, then reads and clears this device's count of expired bounded waits.
 cudaError_t take_wait_expiries(cudaStream_t st, unsigned int *count);
 // Segments per (sequence, head) the tensor-core launcher picks for a plain call on a GPU with

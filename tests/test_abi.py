@@ -121,14 +121,16 @@ def test_gated_validation(K):
 
 
 def test_tc_kernel_refuses_shapes_it_does_not_cover(K):
-    assert call_chunk(K, dims(dtype=0), impl=2) == K.KDA_ERR_UNSUPPORTED
-    assert call_chunk(K, dims(dk=64, dv=64), impl=2) == K.KDA_ERR_UNSUPPORTED
+    assert call_chunk(K, dims(dtype=0), impl=2) == K.KDA_ERR_UNSUPPORTED   # fp32
+    assert call_chunk(K, dims(dk=96), impl=2) == K.KDA_ERR_UNSUPPORTED     # not a supported head size
 
 
 def test_selected_impl(K):
     sel = K.lib().kda_chunk_fwd_selected_impl
     assert sel(ctypes.byref(dims(dtype=0))) == 1           # fp32 -> SIMT kernel
-    assert sel(ctypes.byref(dims(dk=64, dv=64))) == 1
+    assert sel(ctypes.byref(dims(dtype=0, dk=64, dv=64))) == 1
+    assert sel(ctypes.byref(dims(dk=64, dv=64))) == 2      # bf16 64-wide heads -> tensor cores, padded
+    assert sel(ctypes.byref(dims(dk=64, dv=128))) == 2
     assert sel(ctypes.byref(dims(dk=96))) == -1
     assert sel(ctypes.byref(dims())) in (1, 2)
 
@@ -194,9 +196,10 @@ def test_cta_count_the_library_picks(K):
     assert f(dims(batch=1, seqlen=1100, num_seqs=1, heads=1), True, 152) == 1         # 17 chunks
     assert f(dims(batch=1, seqlen=2**20, num_seqs=16, heads=32), True, 152) == 512    # 512 units
     assert f(dims(batch=1, seqlen=65536, num_seqs=1, heads=64), True, 76) == 64
-    # the tensor-core kernel does not run fp32 or d = 64; empty, invalid dims and SM counts give 0
+    # 64-wide bf16 heads run on the tensor-core kernel too; it does not run fp32; empty, invalid
+    # dims and SM counts give 0
+    assert f(dims(batch=1, seqlen=65536, num_seqs=1, heads=4, dk=64, dv=64), False, 152) == 152
     assert f(dims(batch=1, seqlen=65536, num_seqs=1, heads=4, dtype=0), False, 152) == 0
-    assert f(dims(batch=1, seqlen=65536, num_seqs=1, heads=4, dk=64, dv=64), False, 152) == 0
     assert f(dims(batch=1, seqlen=65536, num_seqs=1, heads=0), False, 152) == 0
     assert f(dims(batch=1, seqlen=0, num_seqs=1, heads=4), False, 152) == 0
     assert f(dims(batch=1, seqlen=65536, num_seqs=1, heads=4), False, 0) == 0

@@ -1,6 +1,6 @@
 """GPU tests of kda_chunk_fwd_checkpointed (recurrent-state checkpoints inside each sequence,
 for prefix caching) through the C ABI, on both chunk kernels (fp32 and bf16 d=64: the SIMT
-kernel; bf16 d=128: the tensor-core kernel).
+kernel, which the library keeps for checkpoints at d=64; bf16 d=128: the tensor-core kernel).
 
 Pins: a checkpoint is the final state of the same computation on the prefix, which the oracle
 computes independently (its token recurrence over the first (k+1)*interval tokens); and, for
@@ -51,8 +51,10 @@ def test_checkpoints_match_prefix_states(K, dtype, d, varlen):
                                                     inp["beta"], inp["initial_state"], cu,
                                                     interval=interval)
     torch.cuda.synchronize()
+    # the plain calls compared bit for bit run the kernel the checkpointed call runs
+    impl = "tc" if (dtype == torch.bfloat16 and d == 128) else "simt"
     ref_out, ref_fs = K.kda_chunk_fwd(inp["q"], inp["k"], inp["v"], inp["g"], inp["beta"],
-                                      inp["initial_state"], cu)
+                                      inp["initial_state"], cu, impl=impl)
     torch.testing.assert_close(out, ref_out, rtol=0, atol=0)   # checkpoints change nothing else
     torch.testing.assert_close(fs, ref_fs, rtol=0, atol=0)
     offs = off.cpu().numpy()
@@ -65,7 +67,7 @@ def test_checkpoints_match_prefix_states(K, dtype, d, varlen):
             P = (kth + 1) * interval
             pre = _prefix(inp, n, cuh, P)
             s0 = inp["initial_state"][n:n + 1].contiguous()
-            _, gpu_fs = K.kda_chunk_fwd(pre["q"], pre["k"], pre["v"], pre["g"], pre["beta"], s0)
+            _, gpu_fs = K.kda_chunk_fwd(pre["q"], pre["k"], pre["v"], pre["g"], pre["beta"], s0, impl=impl)
             torch.cuda.synchronize()
             torch.testing.assert_close(ck[offs[n] + kth], gpu_fs[0], rtol=0, atol=0)
             _, rs = oracle.forward(pre["q"], pre["k"], pre["v"], pre["g"], pre["beta"], s0)

@@ -72,6 +72,25 @@ def test_rectangular_heads(K, dk, dv):
     check(compare_prefill(inp, out, sT), torch.float32)
 
 
+@pytest.mark.parametrize("dk,dv", [(64, 64), (64, 128), (128, 64)])
+def test_narrow_heads_on_the_tensor_cores(K, dk, dv):
+    # a 64-wide head runs on the tensor-core kernel at 128 channels, the missing ones read as
+    # zeros by the TMA; outputs and states of the real channels only, against the oracle; dense
+    # (balanced schedule, sequences split between CTAs) and packed, with initial states
+    assert K.kda_chunk_fwd_selected_impl(torch.empty((1, 1, 1, dk), dtype=torch.bfloat16, device="cuda"),
+                                         torch.empty((1, 1, 1, dv), dtype=torch.bfloat16, device="cuda")) == "tc"
+    inp = inputs.make_prefill(batch=2, seqlen=2000, heads=3, dk=dk, dv=dv, dtype=torch.bfloat16,
+                              device="cuda", seed=6, init_state=True)
+    out, sT = run(K, inp, "tc")
+    assert out.shape[-1] == dv and sT.shape[-2:] == (dk, dv)
+    check(compare_prefill(inp, out, sT), torch.bfloat16)
+    inp = inputs.make_prefill(batch=1, seqlen=0, heads=2, dk=dk, dv=dv, dtype=torch.bfloat16,
+                              device="cuda", seed=7, init_state=True, lengths=[1, 64, 0, 130, 17, 65])
+    out, sT = run(K, inp, "tc")
+    check(compare_prefill(inp, out, sT), torch.bfloat16)
+    torch.testing.assert_close(sT[2], inp["initial_state"][2], rtol=0, atol=0)
+
+
 @pytest.mark.parametrize("dtype,d", [(torch.float32, 64), (torch.bfloat16, 128)])
 def test_varlen_with_short_and_empty_sequences(K, dtype, d):
     lengths = [1, 64, 0, 130, 17, 1, 65]
