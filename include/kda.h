@@ -171,8 +171,9 @@ kda_status_t kda_chunk_fwd_bounded(kda_impl_t impl,
  *              Each part that starts inside a sequence warms up as a segment does, and the
  *              part holding the last chunk writes the final state.  Packed sequences get enough uniform segments to
  *              occupy every SM when there are fewer (sequence, head) units than SMs, each of
- *              at least 16 chunks on average.  1 per unit with an output gate, checkpoints or
- *              an in-place state.
+ *              at least 16 chunks on average.  1 per unit with checkpoints (each then equals
+ *              the final state of a call on its prefix bit for bit), with an in-place state,
+ *              and for packed sequences with the output gate.
  *              1..64 = that many uniform segments.
  * Errors: KDA_ERR_SHAPE for segments outside [0, 64]; KDA_ERR_UNSUPPORTED for segments > 1
  * with initial_state == final_state (a later segment would overwrite the state an earlier one
@@ -289,8 +290,9 @@ int kda_chunk_fwd_selected_impl(const kda_dims_t *dims);
  * balanced schedule's min(sms, units * ceil(seqlen / 64)), units = num_seqs * heads.
  * packed != 0 (cu_seqlens given): units * P with P = floor(sms / units), at most 8, lowered
  * until segments average at least 16 chunks of 64 tokens, and at least 1.  0 for shapes the
- * tensor-core kernel does not run, seqlen = 0 and invalid dims or SM counts.  A call with an
- * output gate, checkpoints or initial_state == final_state runs one CTA per unit instead. */
+ * tensor-core kernel does not run, seqlen = 0 and invalid dims or SM counts.  A call with
+ * checkpoints or initial_state == final_state, or a packed one with the output gate, runs one CTA
+ * per unit instead. */
 int kda_chunk_fwd_auto_ctas(const kda_dims_t *dims, int packed, int sms);
 
 /* kda_recurrent_step -- one decode token per row, state updated in place.

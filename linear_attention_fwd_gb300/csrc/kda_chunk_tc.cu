@@ -297,9 +297,10 @@ __device__ __forceinline__ void tma_tile(const CUtensorMap *map, uint32_t dst, u
     tma_load_3d(dst + half_stride, map, bar, 64, h, (int)tok);
 }
 
-// kMode: 0 = one CTA per unit (the only mode with an output gate or checkpoints), 1 = uniform
-// segments (a.segments > 1), 2 = the balanced schedule (a.sched_ctas > 0).  Each mode is its
-// own instantiation, so that the others' logic folds away.
+// kMode: 0 = one CTA per unit, 1 = uniform segments (a.segments > 1), 2 = the balanced schedule
+// (a.sched_ctas > 0), 3 = the balanced schedule with the output gate (which modes 1 and 2 never
+// carry; checkpoints run in mode 0 only).  Each mode is its own instantiation, so that the
+// others' logic folds away.
 template <int kMode>
 __global__ void __launch_bounds__(NT, 1)
 kda_chunk_tc_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant__ CUtensorMap tmk,
@@ -323,7 +324,9 @@ kda_chunk_tc_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_consta
     //  - otherwise blockIdx.x = unit (the longest packed sequences first), the whole unit
     const int64_t units = (int64_t)a.num_seqs * H;
     constexpr bool kSeg = kMode != 0;
-    constexpr bool balanced = kMode == 2;
+    constexpr bool balanced = kMode >= 2;
+    constexpr bool kGate = kMode == 0 || kMode == 3;   // the output gate
+    constexpr bool kCkpt = kMode == 0;                 // checkpoints
     const int P = kSeg && !balanced && a.segments > 1 ? a.segments : 1;
     const int p = kSeg && !balanced ? (int)(blockIdx.x / units) : 0;
     const int ncd = (int)((a.seqlen + C - 1) / C);   // chunks per unit of a dense batch
@@ -448,7 +451,7 @@ kda_chunk_tc_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_consta
     // normalised to unit RMS over its 128 value channels, scaled by the norm weight and
     // multiplied channel-wise by sigmoid(gate logit) before it is rounded to bf16; the chunk's
     // logits were loaded by TMA into the staging tile itself (same row-major layout).
-    const bool gate_on = kMode == 0 && a.gate != nullptr;   // the output gate
+    const bool gate_on = kGate && a.gate != nullptr;
     const float norm_wj = (gate_on && a.norm_w) ? a.norm_w[jl] : 1.f;   // this thread's channel
     auto stage_output = [&](int par) {
         if (warp >= 8) return;
@@ -667,7 +670,7 @@ kda_chunk_tc_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_consta
                     if (warp < 12) diag_qk();
                     if (out_pending) got = mbar_wait(bar_s, ph_s, wait_limit) && got;
                     tc_fence_after();
-                    const int64_t cs = kMode == 0 && ci >= c_lo ? ckpt_slot(a, n, (int64_t)ci * C) : -1;   // the state after ci chunks
+                    const int64_t cs = kCkpt && ci >= c_lo ? ckpt_slot(a, n, (int64_t)ci * C) : -1;   // the state after ci chunks
                     float *ck = cs >= 0 ? a.ckpt + (cs * H + h) * D * D + jl : nullptr;
                     {
                         const int i0 = 64 * ((warp - 8) >> 2);
@@ -1270,14 +1273,17 @@ static void draw_schedule(int64_t units, int64_t nc, int G, SchedBounds *sb) {
 }
 
 // The library's choice when the caller leaves it open (a.segments == 0): a dense batch runs the
-// balanced schedule over one CTA per SM; packed sequences run segments_for's count of segments
-// per unit (the order in which their units are dispatched already puts the longest first); one
-// CTA per unit when the launch writes checkpoints or applies the output gate, or reads and
-// writes the state in place (a later piece of a unit would write the state while an earlier one
-// may still read it).
+// balanced schedule over one CTA per SM (with the output gate too); packed sequences run
+// segments_for's count of segments per unit (the order in which their units are dispatched
+// already puts the longest first), or one CTA per unit with the gate.  One CTA per unit for every
+// launch that writes checkpoints (each checkpoint then equals, bit for bit, the final state of a
+// call on its prefix: a part of a sequence that warms up from a zero state reaches the same
+// state only to within 2^-160 of its norm) or that reads and writes the state in place (a later
+// piece of a unit would write the state while an earlier one may still read it).
 static void library_schedule(ChunkArgs &a, int64_t units, int64_t tokens) {
     a.segments = 1;
-    if (a.gate || a.ckpt || (a.s0 && a.s0 == a.sT)) return;
+    if (a.ckpt || (a.s0 && a.s0 == a.sT)) return;
+    if (a.cu != nullptr && a.gate) return;
     int dev = 0, sms = 0;
     if (cudaGetDevice(&dev) != cudaSuccess ||
         cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
@@ -1320,7 +1326,8 @@ cudaError_t launch_chunk_tc(const ChunkArgs &args, int dk, int dv, kda_dtype_t d
         !make_map_rows(&mz, a.gate ? a.gate : a.v, tokens, a.heads))   // unused without a gate
         return cudaErrorInvalidValue;
     const int P = a.segments > 1 ? a.segments : 1;
-    auto kernel = a.sched_ctas > 0 ? kda_chunk_tc_kernel<2> : (P > 1 ? kda_chunk_tc_kernel<1> : kda_chunk_tc_kernel<0>);
+    auto kernel = a.sched_ctas > 0 ? (a.gate ? kda_chunk_tc_kernel<3> : kda_chunk_tc_kernel<2>)
+                                   : (P > 1 ? kda_chunk_tc_kernel<1> : kda_chunk_tc_kernel<0>);
     cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)SMEM_BYTES);
     if (e != cudaSuccess) return e;
     const int64_t grid = a.sched_ctas > 0 ? a.sched_ctas : units * P;
