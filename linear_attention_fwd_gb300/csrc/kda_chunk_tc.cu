@@ -1,11 +1,14 @@
 // KDA chunkwise forward on the sm_103a tensor cores (tcgen05 + TMEM + TMA).
 //
-// bf16 inputs/outputs, d_k = d_v = 128, chunk C = 64, fp32 recurrent state.
-// One CTA (16 warps) per (sequence, head), or per segment of one when there are
-// fewer units than SMs (see warm_start); the fp32 state lives in tensor memory
-// for the whole run (transposed: TMEM lane j = value channel, column i = key
-// channel), so the only HBM traffic is the q/k/v/g/beta tiles, the output, and
-// the initial / final states.
+// bf16 inputs/outputs, computed at d_k = d_v = 128 (a 64-wide head reads its missing channels
+// as zeros), chunk C = 64, fp32 recurrent state.  CTAs of 16 warps run pieces of (sequence,
+// head) units: for a dense batch the balanced schedule (one CTA per SM, each an equal-cost
+// share of all chunks, so that a unit may be split between two CTAs), otherwise one CTA per
+// unit or uniform segments of one; a piece that starts inside a sequence warms up from a zero
+// state (see warm_start).  The fp32 state lives in tensor memory for the whole piece
+// (transposed: TMEM lane j = value channel, column i = key channel), so the only HBM traffic is
+// the q/k/v/g/beta tiles, the output, and the initial / final states (plus the warm-up chunks'
+// tiles).
 //
 // Chunk algebra ("はじめての自然言語処理 -- Kimi K3" section 3.1: chunkwise form,
 // Tril intra-chunk term, decay folded into q times Gamma and k over Gamma as in
