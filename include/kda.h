@@ -119,7 +119,7 @@ typedef struct {
  * kda_chunk_fwd_auto_ctas how many CTAs) a dense batch runs the balanced schedule:
  * one CTA per SM, each taking an equal share of all (sequence, head, chunk)
  * items, so that a sequence may be split between two CTAs; packed sequences
- * split each sequence over several CTAs when there are fewer units than SMs.
+ * do the same when there are fewer units than twice the SMs.
  * The history a split skips contributes less than 2^-160 of the norm of the
  * state it replaces, else the later part starts at the sequence start. */
 kda_status_t kda_chunk_fwd(const void *q, const void *k, const void *v,
@@ -169,11 +169,13 @@ kda_status_t kda_chunk_fwd_bounded(kda_impl_t impl,
  *              starts inside a sequence -- its warm-up -- plus 0.5 per further sequence it
  *              touches; a share does not end fewer than 8 chunks into a sequence it entered).
  *              Each part that starts inside a sequence warms up as a segment does, and the
- *              part holding the last chunk writes the final state.  Packed sequences get enough uniform segments to
- *              occupy every SM when there are fewer (sequence, head) units than SMs, each of
- *              at least 16 chunks on average.  1 per unit with checkpoints (each then equals
- *              the final state of a call on its prefix bit for bit), with an in-place state,
- *              and for packed sequences with the output gate.
+ *              part holding the last chunk writes the final state.  Packed sequences with
+ *              fewer units than twice the SMs run the same schedule with shares found on the
+ *              device (uniform in items, one item per chunk and at least one per unit; a
+ *              boundary within 4 chunks of a unit's start or end moved there); with more
+ *              units, one CTA per unit, longest first.  1 per unit with checkpoints (each
+ *              then equals the final state of a call on its prefix bit for bit) and with an
+ *              in-place state.
  *              1..64 = that many uniform segments.
  * Errors: KDA_ERR_SHAPE for segments outside [0, 64]; KDA_ERR_UNSUPPORTED for segments > 1
  * with initial_state == final_state (a later segment would overwrite the state an earlier one
@@ -288,11 +290,11 @@ int kda_chunk_fwd_selected_impl(const kda_dims_t *dims);
 /* The number of CTAs kda_chunk_fwd launches for the tensor-core kernel for `dims` on a GPU
  * with `sms` SMs (host arithmetic only, no device call).  packed = 0 (dense batch): the
  * balanced schedule's min(sms, units * ceil(seqlen / 64)), units = num_seqs * heads.
- * packed != 0 (cu_seqlens given): units * P with P = floor(sms / units), at most 8, lowered
- * until segments average at least 16 chunks of 64 tokens, and at least 1.  0 for shapes the
- * tensor-core kernel does not run, seqlen = 0 and invalid dims or SM counts.  A call with
- * checkpoints or initial_state == final_state, or a packed one with the output gate, runs one CTA
- * per unit instead. */
+ * packed != 0 (cu_seqlens given): with units < 2 * sms, the balanced schedule's
+ * min(sms, 256, heads * (ceil(seqlen / 64) + num_seqs)) (a bound on its items; CTAs past the
+ * last item exit at once), else one per unit.  0 for shapes the tensor-core kernel does not run,
+ * seqlen = 0 and invalid dims or SM counts.  A call with checkpoints or initial_state ==
+ * final_state runs one CTA per unit instead. */
 int kda_chunk_fwd_auto_ctas(const kda_dims_t *dims, int packed, int sms);
 
 /* kda_recurrent_step -- one decode token per row, state updated in place.

@@ -116,8 +116,8 @@ extern "C" int kda_chunk_fwd_auto_ctas(const kda_dims_t *d, int packed, int sms)
     if (!kda::chunk_tc_supported(d->dk, d->dv, d->dtype)) return 0;
     const int64_t tokens = (int64_t)d->batch * d->seqlen, units = (int64_t)d->num_seqs * d->heads;
     if (!packed) return kda::balanced_ctas(units, (d->seqlen + 63) / 64, sms);
-    const int64_t ctas = units * kda::segments_for(units, tokens, d->num_seqs, sms);
-    return ctas > 0x7fffffffLL ? 0x7fffffff : (int)ctas;
+    return units < 2 * (int64_t)sms ? kda::packed_ctas(units, tokens, d->num_seqs, sms)
+                                    : (int)(units > 0x7fffffffLL ? 0x7fffffff : units);
 }
 
 // Validated launch of one chunked forward (optionally writing state checkpoints).

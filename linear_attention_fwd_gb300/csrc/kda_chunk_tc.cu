@@ -287,6 +287,81 @@ __device__ int warm_start(const ChunkArgs &a, int64_t bos, int h, int c_lo) {
     return 0;
 }
 
+// Balanced schedule, packed sequences: the host does not see the lengths, so each CTA finds its
+// share on the device.  Items: max(chunks, 1) per (sequence, head) unit, sequence-major (an empty
+// sequence's item writes its final state).  CTA b of G takes [snap(b W / G), snap((b+1) W / G)),
+// where snap moves a boundary to its unit's start or end when either is at most kSnapChunks
+// items away -- a pure function of the boundary, so neighbouring CTAs agree on it.
+constexpr int kSnapChunks = 4;
+__device__ __forceinline__ int64_t seq_items(const ChunkArgs &a, int n) {
+    int64_t b, e;
+    seq_range(a, n, b, e);
+    const int64_t nc = (e - b + C - 1) / C;
+    return nc > 0 ? nc : 1;
+}
+// Block-wide: W, the raw end (b + 1) W / G, and where the share starts: sequence n, head h,
+// chunk c within that unit and the unit's first item us (c is the snapped start; it may equal the
+// unit's item count, i.e. the start is the next unit's first item).
+__device__ void packed_share(const ChunkArgs &a, int G, int b, int &n, int &h, int &c, int64_t &us,
+                             int64_t &raw1) {
+    __shared__ long long s_part[NT / 32];
+    __shared__ long long s_w, s_start;
+    __shared__ int s_seq;
+    const int t = threadIdx.x, lane = t & 31, warp = t >> 5;
+    const int H = a.heads, N = a.num_seqs;
+    long long mine = 0;
+    for (int s = t; s < N; s += NT) mine += seq_items(a, s);
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) mine += __shfl_xor_sync(0xffffffffu, mine, o);
+    if (lane == 0) s_part[warp] = mine;
+    __syncthreads();
+    if (t == 0) {
+        long long w = 0;
+        for (int i = 0; i < NT / 32; ++i) w += s_part[i];
+        s_w = w * H;
+        s_seq = 0;
+        s_start = 0;
+    }
+    __syncthreads();
+    const long long W = s_w;
+    const long long raw0 = (long long)b * W / G;
+    raw1 = (long long)(b + 1) * W / G;
+    long long run = 0;   // items before this pass's first sequence (the same in every thread)
+    for (int base = 0; base < N; base += NT) {
+        __syncthreads();   // s_part is reused
+        const int s = base + t;
+        const long long w = s < N ? (long long)H * seq_items(a, s) : 0;
+        long long v = w;   // inclusive scan within the warp
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const long long y = __shfl_up_sync(0xffffffffu, v, o);
+            if (lane >= o) v += y;
+        }
+        if (lane == 31) s_part[warp] = v;
+        __syncthreads();
+        long long off = 0, tot = 0;
+        for (int i = 0; i < NT / 32; ++i) {
+            const long long u = s_part[i];
+            off += i < warp ? u : 0;
+            tot += u;
+        }
+        const long long excl = run + off + v - w;
+        if (s < N && excl <= raw0 && raw0 < excl + w) {
+            s_seq = s;
+            s_start = excl;
+        }
+        run += tot;
+    }
+    __syncthreads();
+    n = s_seq;
+    const long long items = seq_items(a, n);
+    h = (int)((raw0 - s_start) / items);
+    us = s_start + (long long)h * items;
+    const long long cc = raw0 - us;
+    c = (int)(cc <= kSnapChunks ? 0 : (items - cc <= kSnapChunks ? items : cc));
+    __syncthreads();   // the shared words are read before any later reuse
+}
+
 // Balanced schedule: the boundaries x_0 = 0 <= x_1 <= ... <= x_G = W of the CTAs' shares of the
 // W items (units of nc chunks each, sequence-major), drawn on the host (draw_schedule).
 constexpr int kMaxSchedCtas = 256;
@@ -333,9 +408,25 @@ kda_chunk_tc_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_consta
     const int P = kSeg && !balanced && a.segments > 1 ? a.segments : 1;
     const int p = kSeg && !balanced ? (int)(blockIdx.x / units) : 0;
     const int ncd = (int)((a.seqlen + C - 1) / C);   // chunks per unit of a dense batch
-    int n = 0, h = 0;
+    const bool packed = balanced && a.cu != nullptr;   // the share is found on the device
+    int n = 0, h = 0, c_start = 0;
+    // packed: the current unit's first item, the share's raw end, whether the share ends inside
+    // the current unit -- in shared memory (read at piece boundaries only, written by thread 0
+    // between barriers), not in registers that the chunk loop needs
+    __shared__ long long s_pk[3];
     if (balanced) {
-        if (sched.x[blockIdx.x] >= sched.x[blockIdx.x + 1]) return;   // no items (whole CTA, before any setup)
+        if (packed) {
+            int64_t us0, raw1;
+            packed_share(a, a.sched_ctas, (int)blockIdx.x, n, h, c_start, us0, raw1);
+            if (threadIdx.x == 0) {
+                s_pk[0] = us0;
+                s_pk[1] = raw1;
+                s_pk[2] = 0;
+            }
+            __syncthreads();
+        } else if (sched.x[blockIdx.x] >= sched.x[blockIdx.x + 1]) {
+            return;   // no items (whole CTA, before any setup)
+        }
     } else {
         select_unit(a, kSeg ? (int)(blockIdx.x % units) : (int)blockIdx.x, n, h);
     }
@@ -345,6 +436,50 @@ kda_chunk_tc_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_consta
     // Moves to the CTA's next piece; false when it has none left.  (The balanced schedule's
     // position is recomputed from the current piece rather than kept: registers are scarce.)
     auto next_piece = [&](bool first) -> bool {
+        if (packed) {
+            int64_t us = s_pk[0], items = seq_items(a, n);
+            const int64_t raw1 = s_pk[1];
+            bool found = true, ends = false;
+            if (first) {
+                c_lo = c_start;
+            } else if (s_pk[2]) {
+                found = false;   // the share ended with the previous piece
+            } else {
+                c_lo = (int)items;   // the previous piece ended with its unit
+            }
+            if (found && c_lo >= items) {   // the next unit
+                us += items;
+                if (++h == H) {
+                    h = 0;
+                    ++n;
+                }
+                c_lo = 0;
+                found = n < a.num_seqs;
+                if (found) items = seq_items(a, n);
+            }
+            int64_t e = items;   // the piece's end item within the unit
+            if (found) {
+                ends = raw1 < us + items;
+                if (ends) {
+                    const int64_t ce = raw1 - us;
+                    e = ce <= kSnapChunks ? 0 : (items - ce <= kSnapChunks ? items : ce);
+                }
+                found = c_lo < e;
+            }
+            __syncthreads();   // every thread has read s_pk
+            if (threadIdx.x == 0) {
+                s_pk[0] = us;
+                s_pk[2] = ends;
+            }
+            if (!found) return false;
+            int64_t eos;
+            seq_range(a, n, bos, eos);
+            len = eos - bos;
+            nchunks = (int)((len + C - 1) / C);
+            c_hi = e < nchunks ? (int)e : nchunks;
+            last_seg = e == items;
+            return true;
+        }
         if (balanced) {
             const int64_t x = first ? sched.x[blockIdx.x] : ((int64_t)n * H + h) * ncd + c_hi;
             const int64_t x_end = sched.x[blockIdx.x + 1];
@@ -368,7 +503,7 @@ kda_chunk_tc_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_consta
         last_seg = balanced ? c_hi == nchunks : (!kSeg || p == P - 1);
         return true;
     };
-    next_piece(true);
+    if (!next_piece(true)) return;   // an empty packed share (whole CTA, before any setup)
     if (kSeg && !balanced && c_lo == c_hi && !last_seg) return;   // an empty segment (whole CTA, before any setup)
 
     // mbarriers: Q, K, G tiles landed; [O_I^T | P^T] done; V tile landed; U^T done; state (and
@@ -1275,24 +1410,34 @@ static void draw_schedule(int64_t units, int64_t nc, int G, SchedBounds *sb) {
     fill(W, nc, G, hi, sb);   // the last CTA ends at W (fill covers W at hi)
 }
 
-// The library's choice when the caller leaves it open (a.segments == 0): a dense batch runs the
-// balanced schedule over one CTA per SM (with the output gate too); packed sequences run
-// segments_for's count of segments per unit (the order in which their units are dispatched
-// already puts the longest first), or one CTA per unit with the gate.  One CTA per unit for every
-// launch that writes checkpoints (each checkpoint then equals, bit for bit, the final state of a
-// call on its prefix: a part of a sequence that warms up from a zero state reaches the same
-// state only to within 2^-160 of its norm) or that reads and writes the state in place (a later
-// piece of a unit would write the state while an earlier one may still read it).
+// CTAs of the balanced schedule for packed sequences: one per SM, fewer when there are fewer
+// items than that (W >= units; W <= heads * (ceil(tokens / 64) + sequences) bounds it).
+int packed_ctas(int64_t units, int64_t tokens, int64_t num_seqs, int sms) {
+    const int64_t w_max = units / (num_seqs > 0 ? num_seqs : 1) * ((tokens + C - 1) / C + num_seqs);
+    const int64_t g = sms < kMaxSchedCtas ? sms : kMaxSchedCtas;
+    return w_max <= 0 || g <= 0 ? 0 : (int)(w_max < g ? w_max : g);
+}
+
+// The library's choice when the caller leaves it open (a.segments == 0): the balanced schedule
+// over one CTA per SM, with the output gate too -- shares drawn on the host for a dense batch,
+// found on the device for packed sequences.  Packed sequences with at least twice as many units
+// as SMs run one CTA per unit instead, longest first: the hardware hands each unit to the first
+// SM that frees up, which evens out the spread in per-chunk speed between units that a static
+// share cannot see (measured on 16 sequences x 32 heads: 23.95 ms against 24.35 ms balanced).
+// One CTA per unit for every launch that writes
+// checkpoints (each checkpoint then equals, bit for bit, the final state of a call on its
+// prefix: a part of a sequence that warms up from a zero state reaches the same state only to
+// within 2^-160 of its norm) or that reads and writes the state in place (a later piece of a
+// unit would write the state while an earlier one may still read it).
 static void library_schedule(ChunkArgs &a, int64_t units, int64_t tokens) {
     a.segments = 1;
     if (a.ckpt || (a.s0 && a.s0 == a.sT)) return;
-    if (a.cu != nullptr && a.gate) return;
     int dev = 0, sms = 0;
     if (cudaGetDevice(&dev) != cudaSuccess ||
         cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
         return;
     if (a.cu == nullptr) a.sched_ctas = balanced_ctas(units, (a.seqlen + C - 1) / C, sms);
-    else a.segments = segments_for(units, tokens, a.num_seqs, sms);
+    else if (units < 2 * (int64_t)sms) a.sched_ctas = packed_ctas(units, tokens, a.num_seqs, sms);
 }
 
 cudaError_t take_wait_expiries(cudaStream_t st, unsigned int *count) {
@@ -1339,7 +1484,7 @@ cudaError_t launch_chunk_tc(const ChunkArgs &args, int dk, int dv, kda_dtype_t d
     // thread is kept, so that repeated launches of one shape do not redraw it
     static thread_local SchedBounds sb{};
     static thread_local int64_t drawn[3] = {-1, -1, -1};
-    if (a.sched_ctas > 0) {
+    if (a.sched_ctas > 0 && a.cu == nullptr) {
         const int64_t nc = (a.seqlen + C - 1) / C;
         if (drawn[0] != units || drawn[1] != nc || drawn[2] != a.sched_ctas) {
             draw_schedule(units, nc, a.sched_ctas, &sb);

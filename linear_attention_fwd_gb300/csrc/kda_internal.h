@@ -107,6 +107,7 @@ cudaError_t take_wait_expiries(cudaStream_t st, unsigned int *count);
 // `sms` SMs: floor(sms / units), at most 8, lowered until segments average >= 16 chunks.
 int segments_for(int64_t units, int64_t tokens, int64_t num_seqs, int sms);
 int balanced_ctas(int64_t units, int64_t nc, int sms);
+int packed_ctas(int64_t units, int64_t tokens, int64_t num_seqs, int sms);
 // Debug-build checks of the device-resident preconditions (g in [-5, 0], packed offsets): launched
 // on `st` before a call's kernels when the library is built with KDA_DEBUG_CHECKS, no-ops
 // otherwise; failures set bits of a device error word that take_input_errors reads and clears.

@@ -182,20 +182,19 @@ def test_binding_fails_loudly_without_library(monkeypatch, tmp_path):
 
 
 def test_cta_count_the_library_picks(K):
-    # dense: the balanced schedule over min(SMs, units x chunks) CTAs; packed: units x P with
-    # P = floor(SMs / units), at most 8, lowered until segments average >= 16 chunks
+    # dense: the balanced schedule over min(SMs, units x chunks) CTAs; packed with fewer units than
+    # twice the SMs: the same over min(SMs, heads x (ceil(tokens / 64) + sequences)), a bound on
+    # the items the device counts; packed with more: one CTA per unit
     f = K.kda_chunk_fwd_auto_ctas
     assert f(dims(batch=4, seqlen=8192, num_seqs=4, heads=32), False, 152) == 152     # 128 units
     assert f(dims(batch=1, seqlen=65536, num_seqs=1, heads=64), False, 152) == 152
     assert f(dims(batch=1, seqlen=1100, num_seqs=1, heads=1), False, 152) == 18       # 18 chunks
     assert f(dims(batch=2, seqlen=64, num_seqs=2, heads=3), False, 152) == 6
-    assert f(dims(batch=1, seqlen=65536, num_seqs=1, heads=64), True, 152) == 128     # 64 units x 2
-    assert f(dims(batch=1, seqlen=8192, num_seqs=1, heads=4), True, 152) == 32        # 128 chunks >= 16 * 8
-    assert f(dims(batch=1, seqlen=8191, num_seqs=1, heads=4), True, 152) == 28        # 127 chunks
-    assert f(dims(batch=1, seqlen=4096, num_seqs=1, heads=1), True, 152) == 4         # 64 chunks
-    assert f(dims(batch=1, seqlen=1100, num_seqs=1, heads=1), True, 152) == 1         # 17 chunks
-    assert f(dims(batch=1, seqlen=2**20, num_seqs=16, heads=32), True, 152) == 512    # 512 units
-    assert f(dims(batch=1, seqlen=65536, num_seqs=1, heads=64), True, 76) == 64
+    assert f(dims(batch=1, seqlen=65536, num_seqs=1, heads=64), True, 152) == 152
+    assert f(dims(batch=1, seqlen=1100, num_seqs=1, heads=1), True, 152) == 19        # 18 chunks + 1
+    assert f(dims(batch=1, seqlen=100, num_seqs=3, heads=2), True, 152) == 2 * (2 + 3)
+    assert f(dims(batch=1, seqlen=2**20, num_seqs=16, heads=32), True, 152) == 512    # 512 units >= 2 x 152
+    assert f(dims(batch=1, seqlen=2**20, num_seqs=16, heads=32), True, 400) == 256    # at most 256
     # 64-wide bf16 heads run on the tensor-core kernel too; it does not run fp32; empty, invalid
     # dims and SM counts give 0
     assert f(dims(batch=1, seqlen=65536, num_seqs=1, heads=4, dk=64, dv=64), False, 152) == 152

@@ -138,3 +138,63 @@ def test_expired_waits_under_the_balanced_schedule(K):
     out, sT = run(K, inp)
     assert K.kda_device_status() == K.KDA_OK
     check_prefill(compare_prefill(inp, out, sT), BF)
+
+
+# ---------------------------------------------------------------- packed sequences
+def packed_splits(K, lengths, H):
+    """Host restatement of the device-side packed shares: how many start inside a unit."""
+    items = [max((L + 63) // 64, 1) for L in lengths]
+    units = [(n, h) for n in range(len(lengths)) for h in range(H)]
+    starts, acc = [], 0
+    for n, _ in units:
+        starts.append(acc)
+        acc += items[n]
+    W = acc
+    G = K.kda_chunk_fwd_auto_ctas(K.KdaDims(batch=1, seqlen=sum(lengths), num_seqs=len(lengths), heads=H,
+                                            dk=128, dv=128, dtype=1), True, sms())
+
+    def snap(x):
+        if x >= W:
+            return W
+        u = max(i for i, s0 in enumerate(starts) if s0 <= x)
+        c, it = x - starts[u], items[units[u][0]]
+        return starts[u] if c <= 4 else (starts[u] + it if it - c <= 4 else x)
+    xs = [snap(b * W // G) for b in range(G + 1)]
+    assert all(a <= b for a, b in zip(xs, xs[1:])) and xs[-1] == W
+    return sum(1 for b in range(1, G) if xs[b] < xs[b + 1] and xs[b] not in starts)
+
+
+def test_packed_pieces_inside_sequences(K):
+    # long, short, one-token and empty members: shares start inside the long ones
+    lengths = [3000, 1, 0, 130, 2000, 65, 64, 700]
+    inp = inputs.make_prefill(batch=1, seqlen=0, heads=3, dk=128, dv=128, dtype=BF, device="cuda",
+                              seed=405, init_state=True, lengths=lengths)
+    assert packed_splits(K, lengths, 3) > 20
+    out, sT = run(K, inp)
+    check_prefill(compare_prefill(inp, out, sT), BF)
+    torch.testing.assert_close(sT[2], inp["initial_state"][2], rtol=0, atol=0)   # the empty one
+    out1, sT1 = run(K, inp, segments=1)
+    assert rel_diff(sT, sT1) <= 1e-3
+
+
+def test_packed_no_horizon_equals_one_cta_per_unit(K):
+    lengths = [2600, 5, 1400, 0, 900]
+    inp = inputs.make_prefill(batch=1, seqlen=0, heads=4, dk=128, dv=128, dtype=BF, device="cuda",
+                              seed=406, g_mode="near_bound", init_state=True, lengths=lengths)
+    inp["g"][..., 11] = 0
+    assert packed_splits(K, lengths, 4) > 0
+    out1, sT1 = run(K, inp, segments=1)
+    out, sT = run(K, inp)
+    assert torch.equal(out, out1) and torch.equal(sT, sT1)
+
+
+def test_packed_more_sequences_than_threads(K):
+    # 600 sequences: the device's scans over them run in more than one pass of 512
+    rng = np.random.default_rng(407)
+    lengths = [int(x) for x in rng.integers(0, 150, size=600)]
+    inp = inputs.make_prefill(batch=1, seqlen=0, heads=2, dk=128, dv=128, dtype=BF, device="cuda",
+                              seed=408, init_state=True, lengths=lengths)
+    out, sT = run(K, inp)
+    check_prefill(compare_prefill(inp, out, sT, heads=[1]), BF)
+    out1, sT1 = run(K, inp, segments=1)
+    assert rel_diff(sT, sT1) <= 1e-3

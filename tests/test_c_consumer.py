@@ -23,7 +23,7 @@ int main(void) {
     d.batch = 1; d.seqlen = 65536; d.num_seqs = 1; d.heads = 64; d.dk = 128; d.dv = 128;
     d.dtype = KDA_BF16;
     if (kda_chunk_fwd_selected_impl(&d) != KDA_IMPL_TC) bad |= 4;
-    if (kda_chunk_fwd_auto_ctas(&d, 0, 152) != 152 || kda_chunk_fwd_auto_ctas(&d, 1, 152) != 128) bad |= 8;
+    if (kda_chunk_fwd_auto_ctas(&d, 0, 152) != 152 || kda_chunk_fwd_auto_ctas(&d, 1, 152) != 152) bad |= 8;
     d.dtype = KDA_F32; d.dk = 64; d.dv = 64;
     if (kda_chunk_fwd_selected_impl(&d) != KDA_IMPL_SIMT) bad |= 16;
     d.heads = 0;   /* non-positive dimensions are refused on the host */
