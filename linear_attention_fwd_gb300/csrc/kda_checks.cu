@@ -20,9 +20,8 @@ __device__ unsigned int g_kda_input_errors = 0;
 namespace kda {
 namespace {
 
-constexpr unsigned int kErrDecay = 1u, kErrOffsets = 2u;
-
 #ifdef KDA_DEBUG_CHECKS
+constexpr unsigned int kErrDecay = 1u, kErrOffsets = 2u;   // bits of the error word
 constexpr int kCheckThreads = 256;
 
 // Flags any g outside [-5, 0] (NaN included) among n elements.
