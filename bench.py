@@ -530,7 +530,21 @@ def bench_extras(kda, inputs, inp, out, fs, stream, P, bytes_launch, tokens, H, 
         other[name] = {"kernel": KERNEL_NAME[impl], "ms_per_step": ms,
                        "tokens_per_s": 4 * 8192 / (ms / 1e3), "roofline": hbm_roofline(nb, ms, P)}
         del x, o2, f2
-    return {"gated": gated, "checkpointed": ckpt, "decode_steps": steps4, "other_shapes": other}
+    # q and k L2-normalised inside the call (kda_chunk_fwd_qknorm) on raw N(0, 1) q and k of the
+    # same shape: the same bytes as the plain call
+    B_, T_ = inp["q"].shape[:2]
+    x = inputs.make_prefill(batch=B_, seqlen=T_, heads=H, dk=dk, dv=dv, dtype=inp["q"].dtype,
+                            device=out.device, seed=10, raw_qk=True,
+                            init_state=inp["initial_state"] is not None) if inp["cu_seqlens"] is None else None
+    qkn = None
+    if x is not None:
+        ms = _time_ms(lambda: kda.kda_chunk_fwd(x["q"], x["k"], x["v"], x["g"], x["beta"], x["initial_state"], None,
+                                                 out=out, final_state=fs, qk_eps=1e-6, stream=stream), stream)
+        qkn = {"ms_per_step": ms, "tokens_per_s": tokens / (ms / 1e3),
+               "roofline": hbm_roofline(bytes_launch, ms, P)}
+        del x
+    return {"gated": gated, "checkpointed": ckpt, "decode_steps": steps4, "other_shapes": other,
+            "qk_l2norm": qkn}
 
 
 def bench_decode(args, kda, inputs, dev, stream, P, barrier, max_over_ranks, ws):

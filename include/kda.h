@@ -128,6 +128,25 @@ kda_status_t kda_chunk_fwd(const void *q, const void *k, const void *v,
                            void *out, float *final_state,
                            const kda_dims_t *dims, cudaStream_t stream);
 
+/* kda_chunk_fwd_qknorm -- kda_chunk_fwd with the L2 normalisation of q and k fused in.
+ *
+ * The method reads q and k after L2 normalisation, so that q . k is a cosine
+ * ("はじめての自然言語処理 -- Kimi K3", section 3.1, the associative-memory read-out
+ * paragraph); kda_chunk_fwd leaves that to the caller.  Here every token row of q and of k
+ * (per head, over dk) is first replaced by x / sqrt(|x|^2 + qk_eps), computed and kept in
+ * fp32 (not rounded back to the io dtype, so the products the kernels form from it are as
+ * accurate as from the raw inputs); a row with |x|^2 + qk_eps = 0 stays zero.  The inputs in
+ * memory are not modified.  The rest is kda_chunk_fwd, on the kernel kda_chunk_fwd would
+ * choose.  The tensor-core kernel computes the row norms on the tensor cores while four of
+ * its warps would otherwise wait, and scales the rows as it forms its operands.
+ *   qk_eps : >= 0 and finite (1e-6 is usual), else KDA_ERR_SHAPE.
+ * Other arguments, errors and schedules as kda_chunk_fwd. */
+kda_status_t kda_chunk_fwd_qknorm(const void *q, const void *k, const void *v,
+                                  const void *g, const void *beta, float qk_eps,
+                                  const float *initial_state, const int32_t *cu_seqlens,
+                                  void *out, float *final_state,
+                                  const kda_dims_t *dims, cudaStream_t stream);
+
 /* As kda_chunk_fwd, with an explicit kernel choice (tests and benchmarks).
  * Returns KDA_ERR_UNSUPPORTED when the chosen kernel cannot run the shape. */
 kda_status_t kda_chunk_fwd_with(kda_impl_t impl,
@@ -318,6 +337,15 @@ kda_status_t kda_recurrent_step(const void *q, const void *k, const void *v,
                                 const void *g, const void *beta, float *state,
                                 const int32_t *state_indices, void *out,
                                 const kda_dims_t *dims, cudaStream_t stream);
+
+/* kda_recurrent_step_qknorm -- kda_recurrent_step with q and k L2-normalised first, as in
+ * kda_chunk_fwd_qknorm (x / sqrt(|x|^2 + qk_eps) per row, in fp32; a zero row stays
+ * zero).  qk_eps >= 0 and finite, else KDA_ERR_SHAPE; the rest as
+ * kda_recurrent_step. */
+kda_status_t kda_recurrent_step_qknorm(const void *q, const void *k, const void *v,
+                                       const void *g, const void *beta, float qk_eps,
+                                       float *state, const int32_t *state_indices, void *out,
+                                       const kda_dims_t *dims, cudaStream_t stream);
 
 /* kda_recurrent_steps -- up to T decode tokens per row from the row's state, for speculative
  * decoding.  The pages' account of it: the state is updated in place, so a rejected draft

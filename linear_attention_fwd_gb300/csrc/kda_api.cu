@@ -126,13 +126,14 @@ static kda_status_t chunk_run(kda_impl_t impl, const void *q, const void *k, con
                        void *out, float *final_state, float *ckpt, const int32_t *ckpt_off,
                        int32_t ckpt_interval, const void *gate, const float *norm_w, float norm_eps,
                        const kda_dims_t *d, cudaStream_t stream, uint32_t wait_polls = 1u << 20,
-                       int32_t segments = 0) {
+                       int32_t segments = 0, float qk_eps = -1.f) {
     kda_status_t st = check_chunk(impl, q, k, v, g, beta, initial_state, cu_seqlens, out,
                                   final_state, d);
     if (st != KDA_OK) return st;
     kda::ChunkArgs a{q, k, v, g, beta, initial_state, cu_seqlens, out, final_state,
                      (int64_t)d->seqlen, d->num_seqs, d->heads, gate, norm_w, norm_eps,
                      ckpt, ckpt_off, ckpt_interval, wait_polls, segments};
+    a.qk_eps = qk_eps;
     cudaError_t e = kda::debug_check_inputs(g, (int64_t)d->batch * d->seqlen * d->heads * d->dk, d->dtype,
                                             cu_seqlens, d->num_seqs, d->seqlen, stream);
     if (e != cudaSuccess) return KDA_ERR_CUDA;
@@ -223,10 +224,19 @@ extern "C" kda_status_t kda_chunk_fwd(const void *q, const void *k, const void *
                               final_state, dims, stream);
 }
 
-extern "C" kda_status_t kda_recurrent_step(const void *q, const void *k, const void *v,
-                                           const void *g, const void *beta, float *state,
-                                           const int32_t *state_indices, void *out,
-                                           const kda_dims_t *d, cudaStream_t stream) {
+extern "C" kda_status_t kda_chunk_fwd_qknorm(const void *q, const void *k, const void *v, const void *g,
+                                             const void *beta, float qk_eps, const float *initial_state,
+                                             const int32_t *cu_seqlens, void *out, float *final_state,
+                                             const kda_dims_t *dims, cudaStream_t stream) {
+    if (!(qk_eps >= 0.f) || qk_eps > 1e30f) return KDA_ERR_SHAPE;   // also rejects NaN
+    return chunk_run(KDA_IMPL_AUTO, q, k, v, g, beta, initial_state, cu_seqlens, out, final_state,
+                     nullptr, nullptr, 0, nullptr, nullptr, 0.f, dims, stream, 1u << 20, 0, qk_eps);
+}
+
+// Validated launch of one or more decode tokens per row.
+static kda_status_t decode_run(const void *q, const void *k, const void *v, const void *g,
+                               const void *beta, float *state, const int32_t *state_indices,
+                               void *out, const kda_dims_t *d, float qk_eps, cudaStream_t stream) {
     if (d == nullptr) return KDA_ERR_NULL;
     if (d->dtype != KDA_F32 && d->dtype != KDA_BF16) return KDA_ERR_UNSUPPORTED;
     if (!head_size_ok(d->dk) || !head_size_ok(d->dv)) return KDA_ERR_UNSUPPORTED;
@@ -242,9 +252,25 @@ extern "C" kda_status_t kda_recurrent_step(const void *q, const void *k, const v
     if (state_indices && !aligned(state_indices, 4)) return KDA_ERR_ALIGN;
     kda::DecodeArgs a{q, k, v, g, beta, state, state_indices, out, d->batch, d->num_seqs, d->heads,
                       1, nullptr, 1};
+    a.qk_eps = qk_eps;
     cudaError_t e = kda::debug_check_inputs(g, (int64_t)d->batch * d->heads * d->dk, d->dtype, nullptr, 0, 0, stream);
     if (e == cudaSuccess) e = kda::launch_decode(a, d->dk, d->dv, d->dtype, stream);
     return e == cudaSuccess ? KDA_OK : KDA_ERR_CUDA;
+}
+
+extern "C" kda_status_t kda_recurrent_step(const void *q, const void *k, const void *v,
+                                           const void *g, const void *beta, float *state,
+                                           const int32_t *state_indices, void *out,
+                                           const kda_dims_t *d, cudaStream_t stream) {
+    return decode_run(q, k, v, g, beta, state, state_indices, out, d, -1.f, stream);
+}
+
+extern "C" kda_status_t kda_recurrent_step_qknorm(const void *q, const void *k, const void *v,
+                                                  const void *g, const void *beta, float qk_eps,
+                                                  float *state, const int32_t *state_indices,
+                                                  void *out, const kda_dims_t *d, cudaStream_t stream) {
+    if (!(qk_eps >= 0.f) || qk_eps > 1e30f) return KDA_ERR_SHAPE;   // also rejects NaN
+    return decode_run(q, k, v, g, beta, state, state_indices, out, d, qk_eps, stream);
 }
 
 extern "C" kda_status_t kda_recurrent_steps(const void *q, const void *k, const void *v,

@@ -125,6 +125,23 @@ kda_chunk_simt_kernel(ChunkArgs a) {
         }
         if (t < C) Bs[t] = t < nr ? to_f(beta[(bos + c0 + t) * H + h]) : 0.f;
         __syncthreads();
+        if (a.qk_eps >= 0.f) {
+            // q and k rows L2-normalised ("はじめての自然言語処理 -- Kimi K3", section 3.1, the
+            // read-out paragraph): x / sqrt(|x|^2 + eps) in fp32; a row with |x|^2 + eps = 0
+            // stays zero.  One warp per row; rows past the sequence end are zero and stay so.
+            const int warp = t >> 5, lane = t & 31;
+            for (int row = warp; row < 2 * C; row += kThreads / 32) {
+                float *x = row < C ? Qs + row * L::LDQ : Ks + (row - C) * L::LDK;
+                float ss = 0.f;
+                for (int c = lane; c < DK; c += 32) ss = fmaf(x[c], x[c], ss);
+#pragma unroll
+                for (int o = 16; o > 0; o >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, o);
+                const float den = ss + a.qk_eps;
+                const float sc = den > 0.f ? rsqrtf(den) : 0.f;
+                for (int c = lane; c < DK; c += 32) x[c] *= sc;
+            }
+            __syncthreads();
+        }
 
         // ---- cumulative log decay per channel and the per-sub-tile reference vectors
         if (t < DK) {

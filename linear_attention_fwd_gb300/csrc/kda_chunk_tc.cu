@@ -53,6 +53,7 @@
 #include <cuda.h>
 #include <cudaTypedefs.h>
 #include <cuda_bf16.h>
+#include <type_traits>
 #include <cuda_runtime.h>
 
 #include "kda_internal.h"
@@ -155,7 +156,8 @@ constexpr uint32_t OFF_MRR = OFF_BETA + 64 * 4;         // q_r . k_r        [64]
 constexpr uint32_t OFF_BNEXT = OFF_MRR + 64 * 4;        // the next chunk's beta [64]
 constexpr uint32_t OFF_MLO = (OFF_BNEXT + 64 * 4 + 1023) / 1024 * 1024;  // M - fp16(M), fp16 [64 r][64 s]
 constexpr uint32_t OFF_BAR = OFF_MLO + 8192;            // 7 mbarriers, TMEM address
-constexpr uint32_t SMEM_USED = OFF_BAR + 64;
+constexpr uint32_t OFF_NQK = OFF_BAR + 64;              // q and k row factors 1/|x| (L2 option) [2][64]
+constexpr uint32_t SMEM_USED = OFF_NQK + 2 * 64 * 4;
 constexpr uint32_t SMEM_BYTES = SMEM_USED + 1024;       // + alignment slack
 static_assert(SMEM_BYTES <= 227 * 1024, "shared memory budget");
 static_assert(OFF_KH % 1024 == 0 && OFF_PART % 16 == 0 && OFF_T % 1024 == 0 && OFF_MLO % 1024 == 0 &&
@@ -271,7 +273,10 @@ __device__ int warm_start(const ChunkArgs &a, int64_t bos, int h, int c_lo) {
             gm = fmaxf(gm, __shfl_xor_sync(0xffffffffu, gm, o));
             ks += __shfl_xor_sync(0xffffffffu, ks, o);
         }
-        const float amp = fabsf(1.f - __bfloat162float(bq[tok * H + h]) * ks);
+        // with q and k normalised first, |k|^2 <= |k|^2 / (|k|^2 + eps) times 1 + 2^-7 (the bf16
+        // rounding of the normalised entries)
+        const float kn = a.qk_eps < 0.f ? ks : (ks + a.qk_eps > 0.f ? ks / (ks + a.qk_eps) * 1.0078125f : 0.f);
+        const float amp = fabsf(1.f - __bfloat162float(bq[tok * H + h]) * kn);
         float lam = gm * LOG2E + (amp > 1.f ? __log2f(amp) : 0.f);   // this token's bound, log2
         lam += __shfl_xor_sync(0xffffffffu, lam, 8);    // the warp's 4 rows
         lam += __shfl_xor_sync(0xffffffffu, lam, 16);
@@ -378,8 +383,9 @@ __device__ __forceinline__ void tma_tile(const CUtensorMap *map, uint32_t dst, u
 // kMode: 0 = one CTA per unit, 1 = uniform segments (a.segments > 1), 2 = the balanced schedule
 // (a.sched_ctas > 0), 3 = the balanced schedule with the output gate (which modes 1 and 2 never
 // carry; checkpoints run in mode 0 only).  Each mode is its own instantiation, so that the
-// others' logic folds away.
-template <int kMode>
+// others' logic folds away.  kQk: q and k L2-normalised first (modes 0-2, without the gate or
+// checkpoints).
+template <int kMode, bool kQk = false>
 __global__ void __launch_bounds__(NT, 1)
 kda_chunk_tc_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant__ CUtensorMap tmk,
                     const __grid_constant__ CUtensorMap tmv, const __grid_constant__ CUtensorMap tmg,
@@ -684,6 +690,11 @@ kda_chunk_tc_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_consta
     const int cp = tid & 63, sub = tid >> 6;   // elementwise ownership: channel pair, 8-row group
     const int blk = sub >> 1, hb = sub & 1;    // sub-tile and which half of it
     const int t4 = lane & 3, g = lane >> 2;    // mma.sync fragment coordinates
+    // q and k L2-normalised first ("はじめての自然言語処理 -- Kimi K3", section 3.1, the read-out
+    // paragraph: q and k enter after L2 normalisation, so q . k is a cosine): each row's factor
+    // 1 / sqrt(|x|^2 + eps) comes from a pass of warps 0-7 in step (1) and multiplies the row
+    // in fp32 before any operand is rounded from it
+    constexpr bool qkn = kQk;
 
     // (1) of a chunk whose G tile has landed (nr rows inside the sequence), warps 0-7:
     // log2-decay sums over the two 8-row halves of sub-tile warp/2 (cumulative sums restart at
@@ -724,6 +735,34 @@ kda_chunk_tc_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_consta
 #pragma unroll
             for (int e = 0; e < 2; ++e)
                 if (2 * t4 + e == g) MRR[16 * I + g + 8 * hh] = acc[hh][2 * hh + e];
+    };
+    // With the L2 option, warps 0-7 after the decay sums (while the previous chunk's groups
+    // land): |x_r|^2 for the 16 rows of sub-tile I = warp % 4 of Q (warps 0-3) or K (warps 4-7),
+    // the diagonal of X_I X_I^T (exact products, fp32 sums), and from it the row factor
+    // 1 / sqrt(|x_r|^2 + eps), 0 where that is 0.  The operands of step (2) take the factors on,
+    // and the diagonal of M in step (3).
+    auto row_norms = [&]() {
+        const int I = warp & 3, which = warp >> 2;
+        const uint32_t tile = which ? OFF_K : OFF_Q;
+        float acc[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
+#pragma unroll
+        for (int kk = 0; kk < 8; ++kk) {
+            uint32_t a0, a1, a2, a3, b0, b1, b2, b3;
+            ldsm_x4(sb + tile + swqk(16 * I + (lane & 15), 16 * kk + ((lane >> 4) << 3)), a0, a1, a2, a3);
+            ldsm_x4(sb + tile + swqk(16 * I + (lane & 7) + ((lane >> 4) << 3), 16 * kk + (((lane >> 3) & 1) << 3)),
+                    b0, b1, b2, b3);
+            mma_16816(acc[0], a0, a1, a2, a3, b0, b1);
+            mma_16816(acc[1], a0, a1, a2, a3, b2, b3);
+        }
+        float *nqk = reinterpret_cast<float *>(sm + OFF_NQK) + 64 * which;
+#pragma unroll
+        for (int hh = 0; hh < 2; ++hh)
+#pragma unroll
+            for (int e = 0; e < 2; ++e)
+                if (2 * t4 + e == g) {   // element (row g + 8hh, col 8hh + 2t4 + e) is diagonal
+                    const float d = acc[hh][2 * hh + e] + a.qk_eps;
+                    nqk[16 * I + g + 8 * hh] = d > 0.f ? rsqrtf(d) : 0.f;
+                }
     };
     // per-channel decay vectors of that chunk (log2 units), by warps 12-15: thread = channel
     auto vectors = [&]() {
@@ -798,6 +837,7 @@ kda_chunk_tc_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_consta
                 if (warp < 8) {
                     prephase(nr);
                     named_bar_arrive(2, 384);   // the sums are in place for warps 12-15
+                    if constexpr (qkn) row_norms();
                     if (out_pending) {   // the previous chunk's output, once its groups landed
                         got = mbar_wait(bar_s, ph_s, wait_limit) && mbar_wait(bar_o, ph_o, wait_limit) && got;
                         if (gate_on) got = mbar_wait(bar_z, ph_z, wait_limit) && got;
@@ -867,7 +907,9 @@ kda_chunk_tc_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_consta
                 // Rows past the end of the sequence hold finite data (the next sequence, or TMA zero
                 // fill) and need no masking: their beta is 0, their decay is not accumulated, and the
                 // entries of A and M they would feed lie above the diagonal or in rows never stored.
-                {
+                // With the L2 option each q and k row is first multiplied by its factor in fp32.
+                auto operands = [&](auto qkn_c) {
+                    constexpr bool kQkn = decltype(qkn_c)::value;
                     const int c = 2 * cp;
                     const float2 eb = *reinterpret_cast<const float2 *>(EB + blk * 128 + c);
                     const float2 el = *reinterpret_cast<const float2 *>(EL + blk * 128 + c);
@@ -881,8 +923,14 @@ kda_chunk_tc_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_consta
                         for (int e = 0; e < 2; ++e) {
                             const int r = 16 * blk + 8 * hb + rr + e;
                             const uint32_t off = sw(r, c, 64), oqk = swqk(r, c);
-                            const float2 q2 = unpack_bf16(*reinterpret_cast<uint32_t *>(sm + OFF_Q + oqk));
-                            const float2 k2 = unpack_bf16(*reinterpret_cast<uint32_t *>(sm + OFF_K + oqk));
+                            float2 q2 = unpack_bf16(*reinterpret_cast<uint32_t *>(sm + OFF_Q + oqk));
+                            float2 k2 = unpack_bf16(*reinterpret_cast<uint32_t *>(sm + OFF_K + oqk));
+                            if constexpr (kQkn) {
+                                const float *nqk = reinterpret_cast<const float *>(sm + OFF_NQK);
+                                const float nq = nqk[r], nk = nqk[64 + r];
+                                q2 = __fmul2_rn(q2, make_float2(nq, nq));
+                                k2 = __fmul2_rn(k2, make_float2(nk, nk));
+                            }
                             const float2 g2 = unpack_bf16(*reinterpret_cast<uint32_t *>(sm + OFF_G + off));
                             const float w2 = r < nr ? LOG2E : 0.f;   // decay past the sequence end is not summed
                             l = __ffma2_rn(g2, make_float2(w2, w2), l);
@@ -907,7 +955,8 @@ kda_chunk_tc_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_consta
                     const int rc = 16 * blk + 8 * hb;
                     *reinterpret_cast<uint4 *>(sm + OFF_KPT + sw(c, rc, 128)) = make_uint4(p0[0], p0[1], p0[2], p0[3]);
                     *reinterpret_cast<uint4 *>(sm + OFF_KPT + sw(c + 1, rc, 128)) = make_uint4(p1[0], p1[1], p1[2], p1[3]);
-                }
+                };
+                operands(std::integral_constant<bool, qkn>());
 
                 fence_async_smem();
                 tc_fence_before();
@@ -1030,8 +1079,13 @@ kda_chunk_tc_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_consta
                             const int s0 = 16 * I + 8 * nt + 2 * t4;
                             const float mv0 = accM[0][nt][2 * hh] + accM[1][nt][2 * hh];
                             const float mv1 = accM[0][nt][2 * hh + 1] + accM[1][nt][2 * hh + 1];
-                            const float m0 = s0 < r ? mv0 : (s0 == r ? MRR[r] : 0.f);
-                            const float m1 = s0 + 1 < r ? mv1 : (s0 + 1 == r ? MRR[r] : 0.f);
+                            float mrr = MRR[r];
+                            if constexpr (qkn) {   // q_r . k_r of the normalised rows
+                                const float *nqk = reinterpret_cast<const float *>(sm + OFF_NQK);
+                                mrr *= nqk[r] * nqk[64 + r];
+                            }
+                            const float m0 = s0 < r ? mv0 : (s0 == r ? mrr : 0.f);
+                            const float m1 = s0 + 1 < r ? mv1 : (s0 + 1 == r ? mrr : 0.f);
                             const uint32_t mh = pack_f16(m0, m1);
                             const float2 mhf = unpack_f16(mh);
                             *reinterpret_cast<uint32_t *>(sm + OFF_MT + sw(r, s0, 64)) = mh;
@@ -1469,13 +1523,16 @@ cudaError_t launch_chunk_tc(const ChunkArgs &args, int dk, int dv, kda_dtype_t d
     a.dk = dk;
     a.dv = dv;
     if ((a.gate || a.ckpt) && !chunk_tc_full(dk, dv, dt)) return cudaErrorNotSupported;
+    const bool qk = a.qk_eps >= 0.f;
+    if (qk && (a.gate || a.ckpt)) return cudaErrorNotSupported;
     if (!make_map(&mq, a.q, tokens, a.heads, dk) || !make_map(&mk, a.k, tokens, a.heads, dk) ||
         !make_map(&mv, a.v, tokens, a.heads, dv) || !make_map(&mg, a.g, tokens, a.heads, dk) ||
         !make_map_rows(&mz, a.gate ? a.gate : a.v, tokens, a.heads))   // unused without a gate
         return cudaErrorInvalidValue;
     const int P = a.segments > 1 ? a.segments : 1;
-    auto kernel = a.sched_ctas > 0 ? (a.gate ? kda_chunk_tc_kernel<3> : kda_chunk_tc_kernel<2>)
-                                   : (P > 1 ? kda_chunk_tc_kernel<1> : kda_chunk_tc_kernel<0>);
+    auto kernel = a.sched_ctas > 0 ? (a.gate ? kda_chunk_tc_kernel<3> : qk ? kda_chunk_tc_kernel<2, true> : kda_chunk_tc_kernel<2>)
+                                   : P > 1 ? (qk ? kda_chunk_tc_kernel<1, true> : kda_chunk_tc_kernel<1>)
+                                           : (qk ? kda_chunk_tc_kernel<0, true> : kda_chunk_tc_kernel<0>);
     cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)SMEM_BYTES);
     if (e != cudaSuccess) return e;
     const int64_t grid = a.sched_ctas > 0 ? a.sched_ctas : units * P;

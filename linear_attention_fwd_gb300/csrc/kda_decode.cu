@@ -86,6 +86,25 @@ kda_recurrent_step_kernel(DecodeArgs a) {
             s_beta[t] = to_f(static_cast<const Tin *>(a.beta)[row]);
         }
         __syncthreads();
+        if (a.qk_eps >= 0.f) {   // uniform across the block
+            // q and k L2-normalised ("はじめての自然言語処理 -- Kimi K3", section 3.1, the
+            // read-out paragraph): x / sqrt(|x|^2 + eps) in fp32; a row with |x|^2 + eps = 0
+            // stays zero.  Item u (warps in turn) is token u's q, or for u >= TM
+            // token (u - TM)'s k.
+            for (int u = warp; u < 2 * TM; u += kDecodeThreads / 32) {
+                const int tk = u % TM;
+                if (tk >= nt) continue;
+                float *x = u < TM ? sq[tk] : sk[tk];
+                float ss = 0.f;
+                for (int i = lane; i < DK; i += 32) ss = fmaf(x[i], x[i], ss);
+#pragma unroll
+                for (int o = 16; o > 0; o >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, o);
+                const float den = ss + a.qk_eps;
+                const float sc = den > 0.f ? rsqrtf(den) : 0.f;
+                for (int i = lane; i < DK; i += 32) x[i] *= sc;
+            }
+            __syncthreads();
+        }
         if (warp < nt) {   // k . q of token `warp`
             float d = 0.f;
             for (int i = lane; i < DK; i += 32) d += sk[warp][i] * sq[warp][i];

@@ -34,6 +34,8 @@ struct ChunkArgs {
     int32_t sched_ctas = 0;   // tensor-core kernel: CTAs of the balanced schedule (set by the launcher), or 0
     int32_t dk = 128, dv = 128;   // head sizes in memory (the tensor-core kernel computes at 128 and
                                   // reads the missing channels of a 64-wide head as zeros)
+    float qk_eps = -1.f;          // >= 0: q and k rows are L2-normalised first, x / sqrt(|x|^2 + eps)
+                                  // in fp32 (a row with |x|^2 + eps = 0 stays zero)
 };
 
 // Checkpoint slot for the state after `pos` tokens of sequence n (pos > 0 a multiple of the
@@ -56,6 +58,7 @@ struct DecodeArgs {
     int32_t ntok;             // tokens per row in the input layout [N, ntok, H, d]
     const int32_t *ntok_row;  // [N] tokens to run per row (clamped to [0, ntok]) or nullptr
     int32_t update;           // write the state back
+    float qk_eps = -1.f;      // >= 0: q and k L2-normalised first, as in ChunkArgs
 };
 
 // Token range [bos, eos) of sequence n, read on the device and clamped so that

@@ -126,12 +126,13 @@ def _draw_g(gen, shape, mode, device):
 def make_prefill(*, batch: int, seqlen: int, heads: int, dk: int, dv: int,
                  dtype: torch.dtype, device="cpu", seed: int = SEED_BASE,
                  g_mode: str = "sigmoid", init_state: bool = False,
-                 lengths: list[int] | None = None) -> dict:
+                 lengths: list[int] | None = None, raw_qk: bool = False) -> dict:
     """Inputs for one prefill / resume call.
 
     Dense when ``lengths`` is None ([batch, seqlen, heads, d]); otherwise packed
     ([1, sum(lengths), heads, d]) with int32 ``cu_seqlens``.  The initial state,
-    when requested, is fp32 [N, heads, dk, dv] ~ N(0, 0.02^2).
+    when requested, is fp32 [N, heads, dk, dv] ~ N(0, 0.02^2).  ``raw_qk``: q and k
+    are left as drawn, N(0, 1) entries (for calls that normalise them themselves).
     """
     device = torch.device(device)
     gen = torch.Generator(device=device)
@@ -142,8 +143,9 @@ def make_prefill(*, batch: int, seqlen: int, heads: int, dk: int, dv: int,
         n_seq = batch
     shp_k = (batch, seqlen, heads, dk)
     shp_v = (batch, seqlen, heads, dv)
-    q = _l2n(torch.randn(shp_k, generator=gen, device=device)).to(dtype)
-    k = _l2n(torch.randn(shp_k, generator=gen, device=device)).to(dtype)
+    nrm = (lambda x: x) if raw_qk else _l2n
+    q = nrm(torch.randn(shp_k, generator=gen, device=device)).to(dtype)
+    k = nrm(torch.randn(shp_k, generator=gen, device=device)).to(dtype)
     v = torch.randn(shp_v, generator=gen, device=device).to(dtype)
     g = _draw_g(gen, shp_k, g_mode, device).to(dtype)
     beta = torch.sigmoid(torch.randn((batch, seqlen, heads), generator=gen,
@@ -167,13 +169,15 @@ def make_decode_state(*, num_slots: int, heads: int, dk: int, dv: int, device="c
 
 def make_decode_inputs(*, steps: int, rows: int, heads: int, dk: int, dv: int,
                        dtype: torch.dtype, device="cpu", seed: int = SEED_BASE + 1,
-                       g_mode: str = "sigmoid") -> dict:
-    """Per-step decode inputs [steps, rows, heads, d] (beta: [steps, rows, heads])."""
+                       g_mode: str = "sigmoid", raw_qk: bool = False) -> dict:
+    """Per-step decode inputs [steps, rows, heads, d] (beta: [steps, rows, heads]); ``raw_qk``
+    as in ``make_prefill``."""
     device = torch.device(device)
     gen = torch.Generator(device=device)
     gen.manual_seed(seed)
-    q = _l2n(torch.randn((steps, rows, heads, dk), generator=gen, device=device)).to(dtype)
-    k = _l2n(torch.randn((steps, rows, heads, dk), generator=gen, device=device)).to(dtype)
+    nrm = (lambda x: x) if raw_qk else _l2n
+    q = nrm(torch.randn((steps, rows, heads, dk), generator=gen, device=device)).to(dtype)
+    k = nrm(torch.randn((steps, rows, heads, dk), generator=gen, device=device)).to(dtype)
     v = torch.randn((steps, rows, heads, dv), generator=gen, device=device).to(dtype)
     g = _draw_g(gen, (steps, rows, heads, dk), g_mode, device).to(dtype)
     beta = torch.sigmoid(torch.randn((steps, rows, heads), generator=gen,

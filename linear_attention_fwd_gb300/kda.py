@@ -28,7 +28,7 @@ EXPORTED = ("kda_chunk_fwd", "kda_chunk_fwd_with", "kda_chunk_fwd_bounded", "kda
             "kda_chunk_fwd_gated", "kda_chunk_fwd_selected_impl", "kda_recurrent_step",
             "kda_recurrent_steps", "kda_device_status", "kda_chunk_fwd_ws",
             "kda_chunk_fwd_workspace_bytes", "kda_chunk_fwd_noalloc", "kda_debug_checks",
-            "kda_status_string")
+            "kda_chunk_fwd_qknorm", "kda_recurrent_step_qknorm", "kda_status_string")
 
 
 class KdaDims(ctypes.Structure):
@@ -73,6 +73,10 @@ def lib() -> ctypes.CDLL:
         L.kda_chunk_fwd_selected_impl.argtypes = [dp]
         L.kda_recurrent_step.restype = ctypes.c_int
         L.kda_recurrent_step.argtypes = [vp] * 8 + [dp, vp]
+        L.kda_chunk_fwd_qknorm.restype = ctypes.c_int
+        L.kda_chunk_fwd_qknorm.argtypes = [vp] * 5 + [ctypes.c_float] + [vp] * 4 + [dp, vp]
+        L.kda_recurrent_step_qknorm.restype = ctypes.c_int
+        L.kda_recurrent_step_qknorm.argtypes = [vp] * 5 + [ctypes.c_float] + [vp] * 3 + [dp, vp]
         L.kda_recurrent_steps.restype = ctypes.c_int
         L.kda_recurrent_steps.argtypes = [vp] * 9 + [ctypes.c_int, dp, vp]
         L.kda_chunk_fwd_ws.restype = ctypes.c_int
@@ -191,7 +195,7 @@ def kda_chunk_fwd_noalloc(q, k, v, g, beta, initial_state, cu_seqlens, out, fina
 def kda_chunk_fwd(q, k, v, g, beta, initial_state=None, cu_seqlens=None, *, out=None,
                   final_state=None, output_final_state: bool = True, impl: str = "auto",
                   stream=None, wait_polls: int | None = None, segments: int | None = None,
-                  workspace=None):
+                  workspace=None, qk_eps: float | None = None):
     """Chunkwise KDA forward (prefill / prefix-cache resume) through libkda.
 
     q, k, g: [B, T, H, dk]; v: [B, T, H, dv]; beta: [B, T, H] (all fp32 or all
@@ -205,6 +209,8 @@ def kda_chunk_fwd(q, k, v, g, beta, initial_state=None, cu_seqlens=None, *, out=
     impl="two_pass": kda_chunk_fwd_ws, the state-independent chunk work for all chunks first,
     then the state chain; `workspace` is a uint8 CUDA tensor of at least
     kda_chunk_fwd_workspace_bytes bytes (allocated here, by the caller's allocator, when None).
+    qk_eps: when given, kda_chunk_fwd_qknorm: q and k rows are L2-normalised first,
+    x / sqrt(|x|^2 + qk_eps) in fp32 (impl="auto" only).
     """
     dev = q.device
     for name, t in (("q", q), ("k", k), ("v", v), ("g", g), ("beta", beta)):
@@ -227,6 +233,16 @@ def kda_chunk_fwd(q, k, v, g, beta, initial_state=None, cu_seqlens=None, *, out=
             _ptr(cu_seqlens), _ptr(out), _ptr(final_state))
     if wait_polls is not None and segments is not None:
         raise ValueError("wait_polls and segments select different entry points")
+    if qk_eps is not None:
+        if impl != "auto" or wait_polls is not None or segments is not None:
+            raise ValueError("qk_eps selects kda_chunk_fwd_qknorm, which takes impl='auto' only")
+        st = lib().kda_chunk_fwd_qknorm(_ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta),
+                                        ctypes.c_float(qk_eps), _ptr(initial_state),
+                                        _ptr(cu_seqlens), _ptr(out), _ptr(final_state),
+                                        ctypes.byref(dims), _stream_handle(stream))
+        if st != KDA_OK:
+            raise KdaError(st, "kda_chunk_fwd_qknorm")
+        return out, final_state
     if impl == "two_pass":
         if wait_polls is not None or segments is not None:
             raise ValueError("the two-pass path takes neither wait_polls nor segments")
@@ -268,11 +284,13 @@ def kda_chunk_fwd_selected_impl(q, v, cu_seqlens=None) -> str:
     return IMPL_NAMES.get(code, "invalid")
 
 
-def kda_recurrent_step(q, k, v, g, beta, state, state_indices=None, *, out=None, stream=None):
+def kda_recurrent_step(q, k, v, g, beta, state, state_indices=None, *, out=None, stream=None,
+                       qk_eps: float | None = None):
     """One decode token per row through libkda; ``state`` is updated in place.
 
     q, k, g: [N, H, dk]; v: [N, H, dv]; beta: [N, H]; state: fp32 [P, H, dk, dv];
     state_indices: int32 [N] or None.  Returns out [N, H, dv].
+    qk_eps: when given, kda_recurrent_step_qknorm (q and k L2-normalised first).
     """
     dev = q.device
     for name, t in (("q", q), ("k", k), ("v", v), ("g", g), ("beta", beta)):
@@ -287,11 +305,17 @@ def kda_recurrent_step(q, k, v, g, beta, state, state_indices=None, *, out=None,
     if out is None:
         out = torch.empty((N, H, dv), dtype=q.dtype, device=dev)
     _check_dev("out", out, dev, q.dtype)
-    st = lib().kda_recurrent_step(_ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta), _ptr(state),
-                                  _ptr(state_indices), _ptr(out), ctypes.byref(dims),
-                                  _stream_handle(stream))
+    if qk_eps is None:
+        st = lib().kda_recurrent_step(_ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta), _ptr(state),
+                                      _ptr(state_indices), _ptr(out), ctypes.byref(dims),
+                                      _stream_handle(stream))
+    else:
+        st = lib().kda_recurrent_step_qknorm(_ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta),
+                                             ctypes.c_float(qk_eps), _ptr(state),
+                                             _ptr(state_indices), _ptr(out), ctypes.byref(dims),
+                                             _stream_handle(stream))
     if st != KDA_OK:
-        raise KdaError(st, "kda_recurrent_step")
+        raise KdaError(st, "kda_recurrent_step" if qk_eps is None else "kda_recurrent_step_qknorm")
     return out
 
 

@@ -15,6 +15,11 @@ marshals arrays and splits (sequence, head) units over threads):
   final states.
 * ``decode_step``: the same single token step applied in place to a pool of
   states, row n using slot ``state_indices[n]`` (identity when None).
+* ``l2norm_rows``: the L2 normalisation q and k go through before the recurrence
+  reads them (same section, the associative-memory read-out paragraph: with
+  normalised q and k, q . k is a cosine), x / sqrt(|x|^2 + eps) per row in
+  float64, optionally rounded to an io dtype (``round_bf16`` for bf16); a row
+  with |x|^2 + eps = 0 stays zero.
 * ``gated_rmsnorm``: the output gate of the same page's KDA paragraph (the
   read-out is normalised to unit RMS over its value channels, scaled by a
   per-channel weight, and multiplied channel-wise by a sigmoid gate in (0, 1)):
@@ -197,3 +202,37 @@ def gated_rmsnorm(o, gate, weight=None, eps: float = 1e-6) -> np.ndarray:
     w = np.ones(o.shape[-1]) if weight is None else _f64(weight)
     rstd = 1.0 / np.sqrt(np.mean(o * o, axis=-1, keepdims=True) + eps)
     return o * rstd * w / (1.0 + np.exp(-z))
+
+
+def round_bf16(x) -> np.ndarray:
+    """float64 values rounded to the nearest bfloat16 (ties to even), returned as float64.
+
+    bfloat16 keeps 8 significant bits and float32's exponent range: a normal value
+    m 2^e (0.5 <= |m| < 1) becomes rint(m 2^8) 2^(e-8), with numpy's rint rounding
+    halfway cases to even; below 2^-126 the spacing is the subnormal step 2^-133.
+    Finite inputs of magnitude below bfloat16's largest finite value only.
+    """
+    x = _f64(x)
+    m, e = np.frexp(x)
+    normal = np.ldexp(np.rint(np.ldexp(m, 8)), e - 8)
+    sub = np.rint(np.ldexp(x, 133)) * 2.0 ** -133
+    return np.where(np.abs(x) < 2.0 ** -126, sub, normal)
+
+
+def l2norm_rows(x, eps: float, io_dtype: str = "f64") -> np.ndarray:
+    """x / sqrt(sum(x^2) + eps) over the last axis, in float64 ("はじめての自然言語処理 --
+    Kimi K3", section 3.1, the read-out paragraph: q and k are used after L2
+    normalisation).  A row with sum(x^2) + eps = 0 stays zero.  io_dtype "bf16" or "f32"
+    rounds the result to that type (what a caller storing its normalised q and k passes
+    on); "f64" leaves it unrounded.
+    """
+    x = _f64(x)
+    den = np.sum(x * x, axis=-1, keepdims=True) + eps
+    y = np.where(den > 0.0, x / np.sqrt(np.where(den > 0.0, den, 1.0)), 0.0)
+    if io_dtype == "bf16":
+        return round_bf16(y)
+    if io_dtype == "f32":
+        return y.astype(np.float32).astype(np.float64)
+    if io_dtype != "f64":
+        raise ValueError(f"io_dtype {io_dtype!r}")
+    return y
