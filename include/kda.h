@@ -121,12 +121,10 @@ typedef struct {
  * items, so that a sequence may be split between two CTAs; packed sequences
  * do the same when there are fewer units than twice the SMs.
  * The history a split skips contributes less than 2^-160 of the norm of the
- * state it replaces.  Where no such start lies within 16 chunks (a key channel
- * that barely decays), a dense batch's CTA that ends its piece at that boundary
- * runs on through the next piece instead (the CTAs exchange that answer through
- * a small device-side table tagged with the launch's grid id, never waiting for
- * one another beyond a short bound); a packed batch's later part starts at the
- * sequence start. */
+ * state it replaces, else the later part starts at the sequence start (a key
+ * channel that barely decays makes every later part do so, up to about one
+ * sequence more per CTA; kda_chunk_fwd_segmented with segments = 1 runs one CTA
+ * per sequence and head instead). */
 kda_status_t kda_chunk_fwd(const void *q, const void *k, const void *v,
                            const void *g, const void *beta,
                            const float *initial_state, const int32_t *cu_seqlens,

@@ -5,8 +5,7 @@
 // head) units: for a dense batch the balanced schedule (one CTA per SM, each an equal-cost
 // share of all chunks, so that a unit may be split between two CTAs), otherwise one CTA per
 // unit or uniform segments of one; a piece that starts inside a sequence warms up from a zero
-// state (see warm_start), or, in a dense batch where no warm-up start exists, is run on by the
-// CTA before it (g_kda_bal_decision).  The fp32 state lives in tensor memory for the whole piece
+// state (see warm_start).  The fp32 state lives in tensor memory for the whole piece
 // (transposed: TMEM lane j = value channel, column i = key channel), so the only HBM traffic is
 // the q/k/v/g/beta tiles, the output, and the initial / final states (plus the warm-up chunks'
 // tiles).
@@ -241,16 +240,9 @@ __device__ __forceinline__ void select_unit(const ChunkArgs &a, int b, int &n, i
 constexpr float kHorizonLog2 = 160.f;
 constexpr int kMaxWarmChunks = 16;
 
-__device__ __forceinline__ unsigned long long grid_id() {
-    unsigned long long v;
-    asm volatile("mov.u64 %0, %%gridid;" : "=l"(v));
-    return v;
-}
-
 // The chunk boundary c_run <= c_lo described above (block-wide; every thread returns the
-// same value, and two CTAs asking about the same boundary get the same answer: the arithmetic
-// and its order depend only on the data).  Chunks before c_lo are whole chunks of the sequence.
-__device__ __noinline__ int warm_start(const ChunkArgs &a, int64_t bos, int h, int c_lo) {
+// same value).  Chunks before c_lo are whole chunks of the sequence.
+__device__ int warm_start(const ChunkArgs &a, int64_t bos, int h, int c_lo) {
     __shared__ float s_part[NT / 32];
     const int H = a.heads;
     const __nv_bfloat16 *gq = static_cast<const __nv_bfloat16 *>(a.g);
@@ -281,8 +273,8 @@ __device__ __noinline__ int warm_start(const ChunkArgs &a, int64_t bos, int h, i
             gm = fmaxf(gm, __shfl_xor_sync(0xffffffffu, gm, o));
             ks += __shfl_xor_sync(0xffffffffu, ks, o);
         }
-        // with q and k normalised first, |k|^2 <= |k|^2 / (|k|^2 + eps), times 1 + 2^-7 for the
-        // rounding in the row norms
+        // with q and k normalised first, |k|^2 <= |k|^2 / (|k|^2 + eps) times 1 + 2^-7 (the bf16
+        // rounding of the normalised entries)
         const float kn = a.qk_eps < 0.f ? ks : (ks + a.qk_eps > 0.f ? ks / (ks + a.qk_eps) * 1.0078125f : 0.f);
         const float amp = fabsf(1.f - __bfloat162float(bq[tok * H + h]) * kn);
         float lam = gm * LOG2E + (amp > 1.f ? __log2f(amp) : 0.f);   // this token's bound, log2
@@ -382,16 +374,6 @@ struct SchedBounds {
     int64_t x[kMaxSchedCtas + 1];
 };
 
-// Balanced schedule, dense batches: a share that starts inside a unit more than kMaxWarmChunks
-// chunks in publishes, in its slot, whether that boundary has a warm-up start (bit 0 clear) or
-// not (set), tagged with the launch's grid id (%gridid: a per-context launch number, so a slot
-// written by another launch, earlier or concurrent, never matches).  The CTA whose piece ends at
-// that boundary reads the slot; where it does not match (the other CTA has not decided yet) it
-// runs the same test itself.  Either way both act on the same answer.
-__device__ unsigned long long g_kda_bal_decision[kMaxSchedCtas + 1];
-constexpr uint32_t kDecisionPolls = 512;   // ~50 us at most (the test itself takes ~5 us)
-
-
 __device__ __forceinline__ void tma_tile(const CUtensorMap *map, uint32_t dst, uint32_t bar, int h,
                                          int64_t tok, uint32_t half_stride = 8192) {
     tma_load_3d(dst, map, bar, 0, h, (int)tok);
@@ -438,7 +420,6 @@ kda_chunk_tc_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_consta
     // the current unit -- in shared memory (read at piece boundaries only, written by thread 0
     // between barriers), not in registers that the chunk loop needs
     __shared__ long long s_pk[3];
-    __shared__ int s_dec;   // balanced, dense: the answer read from the next share's slot
     if (balanced) {
         if (packed) {
             int64_t us0, raw1;
@@ -460,37 +441,6 @@ kda_chunk_tc_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_consta
     bool last_seg = true;
     // Moves to the CTA's next piece; false when it has none left.  (The balanced schedule's
     // position is recomputed from the current piece rather than kept: registers are scarce.)
-    // the CTA whose non-empty share starts at item xb (a share boundary inside the item range)
-    auto share_at = [&](int64_t xb) -> int {
-        int b = blockIdx.x + 1;
-        while (!(sched.x[b] == xb && sched.x[b + 1] > xb)) ++b;
-        return b;
-    };
-    // Dense balanced schedule: extend [c_lo, c_hi) through the following shares' pieces of this
-    // unit that have no warm-up start (block-wide).
-    auto extend_piece = [&]() {
-        while (c_hi < nchunks && c_hi > kMaxWarmChunks) {
-            const int64_t u0 = ((int64_t)n * a.heads + h) * nchunks, xb = u0 + c_hi;
-            const int b2 = share_at(xb);
-            if (tid == 0) {
-                int dec = 2;
-                for (uint32_t i = 0; i < kDecisionPolls && dec == 2; ++i) {
-                    const unsigned long long v = atomicAdd(&g_kda_bal_decision[b2], 0ull);
-                    if ((v >> 1) == grid_id()) dec = (int)(v & 1ull);
-                    else __nanosleep(64);
-                }
-                s_dec = dec;
-            }
-            __syncthreads();
-            int dec = s_dec;
-            __syncthreads();   // before s_dec is written again
-            if (dec == 2) dec = warm_start(a, bos, h, c_hi) == 0;   // not published: the same test
-            if (dec == 0) break;
-            const int64_t e2 = sched.x[b2 + 1] - u0;
-            c_hi = e2 < nchunks ? (int)e2 : nchunks;
-        }
-        last_seg = c_hi == nchunks;
-    };
     auto next_piece = [&](bool first) -> bool {
         if (packed) {
             int64_t us = s_pk[0], items = seq_items(a, n);
@@ -834,22 +784,7 @@ kda_chunk_tc_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_consta
     };
     bool drained = false;   // a failed wait's in-flight copies and MMAs have been waited for
     for (bool have = true; have; have = next_piece(false)) {
-        if (!balanced || packed) {
-            c_run = ok && kSeg && c_lo > 0 ? warm_start(a, bos, h, c_lo) : 0;
-        } else {
-            // Dense balanced schedule.  A piece more than kMaxWarmChunks chunks into its unit with
-            // no warm-up start there (a key channel that barely decays) is left to the CTA whose
-            // piece ends at that boundary; this CTA publishes the answer for it.  A piece that
-            // ends inside its unit takes the next share's answer (or, when that is not published
-            // within a bound, runs the same test) and runs on through each piece so left to it.
-            c_run = c_lo > 0 ? warm_start(a, bos, h, c_lo) : 0;
-            if (c_lo > kMaxWarmChunks) {
-                if (tid == 0)
-                    atomicExch(&g_kda_bal_decision[blockIdx.x], (grid_id() << 1) | (c_run == 0 ? 1ull : 0ull));
-                if (c_run == 0) continue;
-            }
-            extend_piece();
-        }
+        c_run = ok && kSeg && c_lo > 0 ? warm_start(a, bos, h, c_lo) : 0;
         out_pending = false;
         t0_out = 0;
         nr_out = 0;

@@ -9,11 +9,10 @@ share touches, a piece that starts inside a sequence warms up as a segment does 
 the 2^-160 transition bound, else from the sequence start), and the piece holding a unit's last
 chunk writes its final state.  Checked here: pieces that start and end inside sequences (several
 per CTA) with the standard decay and an initial state, short sequences (whole sequences per
-CTA), a decay-free channel (no horizon: a piece more than 16 chunks into its sequence is run on
-by the CTA before it, one nearer the start runs from the sequence start, and the result equals
-one CTA per unit bit for bit), a channel that stops decaying for part of each sequence (some
-boundaries warm up, the others are run through), agreement with one CTA per unit at full size,
-and the bounded-wait expiry path (every output and final state NaN, the status reported).
+CTA), a decay-free channel (no horizon: every piece runs from the sequence start and the result
+equals one CTA per unit bit for bit), a channel that stops decaying for part of each sequence
+(some pieces warm up, the others run from the start), agreement with one CTA per unit at full
+size, and the bounded-wait expiry path (every output and final state NaN, the status reported).
 """
 import numpy as np
 import pytest
@@ -108,9 +107,8 @@ def test_short_sequences_snap_to_sequence_boundaries(K):
 
 
 def test_no_horizon_runs_every_piece_from_the_sequence_start(K):
-    # one channel never decays: no piece that starts inside a sequence has a warm-up start, so
-    # each is run on by the CTA before it (or, within 16 chunks of the start, recomputed from
-    # the start with the initial state): exactly what one CTA per unit computes
+    # one channel never decays: pieces that start inside a sequence recompute it from its start
+    # with the initial state, which is exactly what one CTA per unit computes
     inp = inputs.make_prefill(batch=1, seqlen=2600, heads=6, dk=128, dv=128, dtype=BF,
                               device="cuda", seed=403, g_mode="near_bound", init_state=True)
     inp["g"][..., 7] = 0
@@ -123,8 +121,8 @@ def test_no_horizon_runs_every_piece_from_the_sequence_start(K):
 
 def test_decay_free_stretch_inside_each_sequence(K):
     # 4 units of 128 chunks over the SMs (shares of ~3-4 chunks); channel 7 does not decay in
-    # chunks 40-89 of every sequence.  Boundaries whose 16-chunk look-back lies in that stretch
-    # have no warm-up start and are run through by the CTA before them; the rest warm up.
+    # chunks 40-89 of every sequence.  Pieces whose 16-chunk look-back lies in that stretch have
+    # no warm-up start and run from the sequence start; the rest warm up.
     inp = inputs.make_prefill(batch=2, seqlen=128 * 64, heads=2, dk=128, dv=128, dtype=BF,
                               device="cuda", seed=405, init_state=True)
     inp["g"][:, 40 * 64:90 * 64, :, 7] = 0

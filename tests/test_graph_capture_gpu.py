@@ -56,3 +56,45 @@ def test_prefill_and_decode_replayed_from_a_graph(K):
     assert torch.equal(graph_bufs[2], eager[2])
     for a, b in zip(graph_bufs[3], eager[3]):
         assert torch.equal(a, b)
+
+
+def test_balanced_schedule_replayed_with_changing_decay(K):
+    # The balanced schedule decides on the device, from the data, where each piece starts (a
+    # warm-up start, or the sequence start when a key channel does not decay).  One graph
+    # replayed while the decay changes under it (a channel without decay, then the standard
+    # decay, in the same buffers) must give what the eager calls give, replay after replay:
+    # nothing carried from one replay to the next may decide anything.
+    inp = inputs.make_prefill(batch=1, seqlen=64 * 64, heads=4, dk=128, dv=128,
+                              dtype=torch.bfloat16, device="cuda", seed=503)
+    g_dec = inp["g"].clone()
+    g_flat = g_dec.clone()
+    g_flat[..., 5] = 0
+    out = torch.empty_like(inp["v"])
+    fs = torch.empty((1, 4, 128, 128), dtype=torch.float32, device="cuda")
+
+    def run():
+        K.kda_chunk_fwd(inp["q"], inp["k"], inp["v"], inp["g"], inp["beta"], out=out, final_state=fs)
+
+    eager = {}
+    for name, gv in (("decaying", g_dec), ("flat", g_flat)):
+        inp["g"].copy_(gv)
+        run()
+        torch.cuda.synchronize()
+        eager[name] = (out.clone(), fs.clone())
+    assert not torch.equal(eager["decaying"][1], eager["flat"][1])
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(s):
+        run()
+    torch.cuda.current_stream().wait_stream(s)
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        run()
+    for name in ("flat", "decaying", "flat", "flat", "decaying", "decaying", "flat"):
+        inp["g"].copy_(g_dec if name == "decaying" else g_flat)
+        out.zero_()
+        fs.zero_()
+        g.replay()
+        torch.cuda.synchronize()
+        assert torch.equal(out, eager[name][0]) and torch.equal(fs, eager[name][1]), name
