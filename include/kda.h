@@ -376,6 +376,15 @@ kda_status_t kda_recurrent_steps(const void *q, const void *k, const void *v,
                                  void *out, int update_state,
                                  const kda_dims_t *dims, cudaStream_t stream);
 
+/* kda_recurrent_steps_qknorm -- kda_recurrent_steps with q and k L2-normalised first, as in
+ * kda_chunk_fwd_qknorm (x / sqrt(|x|^2 + qk_eps) per token row, in fp32; a zero row stays
+ * zero).  qk_eps >= 0 and finite, else KDA_ERR_SHAPE; the rest as kda_recurrent_steps. */
+kda_status_t kda_recurrent_steps_qknorm(const void *q, const void *k, const void *v,
+                                        const void *g, const void *beta, float qk_eps,
+                                        float *state, const int32_t *state_indices,
+                                        const int32_t *num_tokens, void *out, int update_state,
+                                        const kda_dims_t *dims, cudaStream_t stream);
+
 /* kda_device_status -- waits for the work queued on `stream` to finish, then reads and
  * clears the current device's count of device-side waits of the tensor-core chunk kernels
  * that gave up (see kda_chunk_fwd_bounded; the two passes of kda_chunk_fwd_ws count theirs

@@ -273,11 +273,11 @@ extern "C" kda_status_t kda_recurrent_step_qknorm(const void *q, const void *k, 
     return decode_run(q, k, v, g, beta, state, state_indices, out, d, qk_eps, stream);
 }
 
-extern "C" kda_status_t kda_recurrent_steps(const void *q, const void *k, const void *v,
-                                            const void *g, const void *beta, float *state,
-                                            const int32_t *state_indices, const int32_t *num_tokens,
-                                            void *out, int update_state, const kda_dims_t *d,
-                                            cudaStream_t stream) {
+// Validated launch of several decode tokens per row.
+static kda_status_t steps_run(const void *q, const void *k, const void *v, const void *g,
+                              const void *beta, float *state, const int32_t *state_indices,
+                              const int32_t *num_tokens, void *out, int update_state,
+                              const kda_dims_t *d, float qk_eps, cudaStream_t stream) {
     if (d == nullptr) return KDA_ERR_NULL;
     if (d->dtype != KDA_F32 && d->dtype != KDA_BF16) return KDA_ERR_UNSUPPORTED;
     if (!head_size_ok(d->dk) || !head_size_ok(d->dv)) return KDA_ERR_UNSUPPORTED;
@@ -297,8 +297,29 @@ extern "C" kda_status_t kda_recurrent_steps(const void *q, const void *k, const 
     if (num_tokens && !aligned(num_tokens, 4)) return KDA_ERR_ALIGN;
     kda::DecodeArgs a{q, k, v, g, beta, state, state_indices, out, d->batch, d->num_seqs, d->heads,
                       d->seqlen, num_tokens, update_state ? 1 : 0};
+    a.qk_eps = qk_eps;
     cudaError_t e = kda::debug_check_inputs(g, (int64_t)d->batch * d->seqlen * d->heads * d->dk, d->dtype,
                                             nullptr, 0, 0, stream);
     if (e == cudaSuccess) e = kda::launch_decode(a, d->dk, d->dv, d->dtype, stream);
     return e == cudaSuccess ? KDA_OK : KDA_ERR_CUDA;
+}
+
+extern "C" kda_status_t kda_recurrent_steps(const void *q, const void *k, const void *v,
+                                            const void *g, const void *beta, float *state,
+                                            const int32_t *state_indices, const int32_t *num_tokens,
+                                            void *out, int update_state, const kda_dims_t *d,
+                                            cudaStream_t stream) {
+    return steps_run(q, k, v, g, beta, state, state_indices, num_tokens, out, update_state, d, -1.f,
+                     stream);
+}
+
+extern "C" kda_status_t kda_recurrent_steps_qknorm(const void *q, const void *k, const void *v,
+                                                   const void *g, const void *beta, float qk_eps,
+                                                   float *state, const int32_t *state_indices,
+                                                   const int32_t *num_tokens, void *out,
+                                                   int update_state, const kda_dims_t *d,
+                                                   cudaStream_t stream) {
+    if (!(qk_eps >= 0.f) || qk_eps > 1e30f) return KDA_ERR_SHAPE;   // also rejects NaN
+    return steps_run(q, k, v, g, beta, state, state_indices, num_tokens, out, update_state, d, qk_eps,
+                     stream);
 }

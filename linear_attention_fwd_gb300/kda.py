@@ -28,7 +28,8 @@ EXPORTED = ("kda_chunk_fwd", "kda_chunk_fwd_with", "kda_chunk_fwd_bounded", "kda
             "kda_chunk_fwd_gated", "kda_chunk_fwd_selected_impl", "kda_recurrent_step",
             "kda_recurrent_steps", "kda_device_status", "kda_chunk_fwd_ws",
             "kda_chunk_fwd_workspace_bytes", "kda_chunk_fwd_noalloc", "kda_debug_checks",
-            "kda_chunk_fwd_qknorm", "kda_recurrent_step_qknorm", "kda_status_string")
+            "kda_chunk_fwd_qknorm", "kda_recurrent_step_qknorm", "kda_recurrent_steps_qknorm",
+            "kda_status_string")
 
 
 class KdaDims(ctypes.Structure):
@@ -77,6 +78,8 @@ def lib() -> ctypes.CDLL:
         L.kda_chunk_fwd_qknorm.argtypes = [vp] * 5 + [ctypes.c_float] + [vp] * 4 + [dp, vp]
         L.kda_recurrent_step_qknorm.restype = ctypes.c_int
         L.kda_recurrent_step_qknorm.argtypes = [vp] * 5 + [ctypes.c_float] + [vp] * 3 + [dp, vp]
+        L.kda_recurrent_steps_qknorm.restype = ctypes.c_int
+        L.kda_recurrent_steps_qknorm.argtypes = [vp] * 5 + [ctypes.c_float] + [vp] * 4 + [ctypes.c_int, dp, vp]
         L.kda_recurrent_steps.restype = ctypes.c_int
         L.kda_recurrent_steps.argtypes = [vp] * 9 + [ctypes.c_int, dp, vp]
         L.kda_chunk_fwd_ws.restype = ctypes.c_int
@@ -320,14 +323,16 @@ def kda_recurrent_step(q, k, v, g, beta, state, state_indices=None, *, out=None,
 
 
 def kda_recurrent_steps(q, k, v, g, beta, state, state_indices=None, num_tokens=None, *,
-                        out=None, want_out=True, update_state=True, stream=None):
+                        out=None, want_out=True, update_state=True, stream=None,
+                        qk_eps: float | None = None):
     """Up to T decode tokens per row through libkda (speculative decoding).
 
     q, k, g: [N, T, H, dk]; v: [N, T, H, dv]; beta: [N, T, H]; state: fp32 [P, H, dk, dv];
     state_indices, num_tokens: int32 [N] or None.  With update_state the state after each
     row's tokens is written in place; without, the state is only read.  Returns out
     [N, T, H, dv] (tokens past a row's count are left as they were), or None when
-    ``want_out`` is false.
+    ``want_out`` is false.  qk_eps: when given, kda_recurrent_steps_qknorm (q and k
+    L2-normalised first).
     """
     dev = q.device
     for name, t in (("q", q), ("k", k), ("v", v), ("g", g), ("beta", beta)):
@@ -344,12 +349,20 @@ def kda_recurrent_steps(q, k, v, g, beta, state, state_indices=None, num_tokens=
         out = torch.zeros((N, T, H, dv), dtype=q.dtype, device=dev)
     if out is not None:
         _check_dev("out", out, dev, q.dtype)
-    st = lib().kda_recurrent_steps(_ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta), _ptr(state),
-                                   _ptr(state_indices), _ptr(num_tokens),
-                                   _ptr(out) if want_out else None, int(bool(update_state)),
-                                   ctypes.byref(dims), _stream_handle(stream))
+    if qk_eps is None:
+        st = lib().kda_recurrent_steps(_ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta), _ptr(state),
+                                       _ptr(state_indices), _ptr(num_tokens),
+                                       _ptr(out) if want_out else None, int(bool(update_state)),
+                                       ctypes.byref(dims), _stream_handle(stream))
+    else:
+        st = lib().kda_recurrent_steps_qknorm(_ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta),
+                                              ctypes.c_float(qk_eps), _ptr(state),
+                                              _ptr(state_indices), _ptr(num_tokens),
+                                              _ptr(out) if want_out else None,
+                                              int(bool(update_state)), ctypes.byref(dims),
+                                              _stream_handle(stream))
     if st != KDA_OK:
-        raise KdaError(st, "kda_recurrent_steps")
+        raise KdaError(st, "kda_recurrent_steps" if qk_eps is None else "kda_recurrent_steps_qknorm")
     return out if want_out else None
 
 

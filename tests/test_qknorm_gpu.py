@@ -140,3 +140,41 @@ def test_recurrent_step_equals_one_token_prefill(K):
                               inp["beta"][:, 0].contiguous(), st, qk_eps=EPS)
     torch.testing.assert_close(o2, o1[:, 0], rtol=1e-5, atol=1e-5)
     torch.testing.assert_close(st, s1, rtol=1e-5, atol=1e-5)
+
+
+@pytest.mark.parametrize("dtype,d", [(torch.bfloat16, 128), (torch.float32, 64)])
+def test_recurrent_steps_verify_and_replay(K, dtype, d):
+    # several tokens per row with the normalisation: equal bit for bit to the same tokens run
+    # one kda_recurrent_step_qknorm call at a time, and within the bars of the oracle; a verify
+    # call (update_state off) leaves the state untouched
+    N, T, H, P = 4, 5, 2, 6
+    ins = inputs.make_decode_inputs(steps=T, rows=N, heads=H, dk=d, dv=d, dtype=dtype,
+                                    device="cuda", seed=43, raw_qk=True)
+    a = {kk: ins[kk].transpose(0, 1).contiguous() for kk in ins}
+    idx = torch.tensor([5, 0, 3, 1], dtype=torch.int32, device="cuda")
+    m = [5, 3, 0, 2]
+    num = torch.tensor(m, dtype=torch.int32, device="cuda")
+    s0 = inputs.make_decode_state(num_slots=P, heads=H, dk=d, dv=d, device="cuda", seed=44)
+    s_ver = s0.clone()
+    K.kda_recurrent_steps(a["q"], a["k"], a["v"], a["g"], a["beta"], s_ver, idx, num,
+                          update_state=False, qk_eps=EPS)
+    torch.cuda.synchronize()
+    assert torch.equal(s_ver, s0)
+    s_multi = s0.clone()
+    o_multi = K.kda_recurrent_steps(a["q"], a["k"], a["v"], a["g"], a["beta"], s_multi, idx, num,
+                                    qk_eps=EPS)
+    s_single = s0.clone()
+    pool = f64(s0).copy()
+    for t in range(T):
+        rows = [n for n in range(N) if m[n] > t]
+        sel = torch.tensor(rows, device="cuda")
+        sl = {kk: a[kk][sel, t].contiguous() for kk in a}
+        o = K.kda_recurrent_step(sl["q"], sl["k"], sl["v"], sl["g"], sl["beta"], s_single,
+                                 idx[sel].contiguous(), qk_eps=EPS)
+        assert torch.equal(o, o_multi[sel, t])
+        ro = oracle.decode_step(oracle.l2norm_rows(sl["q"], EPS), oracle.l2norm_rows(sl["k"], EPS),
+                                sl["v"], sl["g"], sl["beta"], pool, idx[sel].cpu())
+        assert excess_err(f64(o), ro, dtype) <= TOL[dtype]
+    torch.cuda.synchronize()
+    assert torch.equal(s_multi, s_single)
+    assert rel_max_err(f64(s_multi), pool) <= TOL[dtype]
