@@ -140,8 +140,9 @@ kda_status_t kda_chunk_fwd(const void *q, const void *k, const void *v,
  * fp32 (not rounded back to the io dtype, so the products the kernels form from it are as
  * accurate as from the raw inputs); a row with |x|^2 + qk_eps = 0 stays zero.  The inputs in
  * memory are not modified.  The rest is kda_chunk_fwd, on the kernel kda_chunk_fwd would
- * choose.  The tensor-core kernel computes the row norms on the tensor cores while four of
- * its warps would otherwise wait, and scales the rows as it forms its operands.
+ * choose.  The tensor-core kernel computes the row norms (mma.sync) on eight warps while they
+ * wait for the previous chunk's tensor-core groups, and scales the rows as it forms its
+ * operands.
  *   qk_eps : >= 0 and finite (1e-6 is usual), else KDA_ERR_SHAPE.
  * Other arguments, errors and schedules as kda_chunk_fwd. */
 kda_status_t kda_chunk_fwd_qknorm(const void *q, const void *k, const void *v,
