@@ -21,7 +21,7 @@
 // paragraph), so the diagonal sub-tiles are ordinary dot products with no
 // per-position-pair exponentials.
 //
-// One CTA of 256 threads per (sequence, head, 64-column slice of d_v).
+// One CTA of 512 threads per (sequence, head, 64-column slice of d_v).
 #include <cuda_runtime.h>
 #include <cuda_bf16.h>
 
@@ -30,7 +30,9 @@
 namespace kda {
 namespace {
 
-constexpr int kThreads = 256;
+constexpr int kThreads = 512;
+constexpr int kRows = kThreads / 64;   // row phases: a thread takes rows rq, rq + kRows, ...
+constexpr int kRpt = kChunk / kRows;   // rows per thread in the 64-row loops
 constexpr int kDvs = 64;               // d_v columns per CTA
 constexpr int kNb = kChunk / kSub;     // sub-tiles per chunk (4)
 constexpr int kLdu = kDvs + 8;         // row stride of the V/Y/U tile (conflict-free solve)
@@ -96,7 +98,7 @@ kda_chunk_simt_kernel(ChunkArgs a) {
     }
 
     const int j = t & (kDvs - 1);   // column owned in the GEMM-like phases
-    const int rq = t >> 6;          // row phase (0..3)
+    const int rq = t >> 6;          // row phase (0..kRows-1)
 
     for (int64_t c0 = 0; c0 < len; c0 += C) {
         const int nr = (int)(len - c0 < C ? len - c0 : C);
@@ -178,9 +180,9 @@ kda_chunk_simt_kernel(ChunkArgs a) {
         {
             const int s = t & (C - 1);
             const int Js = s / kSub;
-            float accA[16], accM[16];
+            float accA[kRpt], accM[kRpt];
 #pragma unroll
-            for (int m = 0; m < 16; ++m) { accA[m] = 0.f; accM[m] = 0.f; }
+            for (int m = 0; m < kRpt; ++m) { accA[m] = 0.f; accM[m] = 0.f; }
             for (int c = 0; c < DK; ++c) {
                 const float kh = Hs[s * L::LDH + c];
                 float khI[kNb];
@@ -188,15 +190,15 @@ kda_chunk_simt_kernel(ChunkArgs a) {
                 for (int I = 0; I < kNb; ++I)
                     khI[I] = I > Js ? kh * Wv[pair_index(I, Js) * DK + c] : kh;
 #pragma unroll
-                for (int m = 0; m < 16; ++m) {
-                    const int r = rq + 4 * m;
-                    accA[m] += Ks[r * L::LDK + c] * khI[m >> 2];
-                    accM[m] += Qs[r * L::LDQ + c] * khI[m >> 2];
+                for (int m = 0; m < kRpt; ++m) {
+                    const int r = rq + kRows * m;   // in sub-tile (kRows m) / kSub: rq < kRows
+                    accA[m] += Ks[r * L::LDK + c] * khI[kRows * m / kSub];
+                    accM[m] += Qs[r * L::LDQ + c] * khI[kRows * m / kSub];
                 }
             }
 #pragma unroll
-            for (int m = 0; m < 16; ++m) {
-                const int r = rq + 4 * m;
+            for (int m = 0; m < kRpt; ++m) {
+                const int r = rq + kRows * m;
                 As[r * C + s] = s < r ? Bs[r] * accA[m] : 0.f;
                 Ms[r * C + s] = s <= r ? accM[m] : 0.f;
             }
@@ -213,69 +215,72 @@ kda_chunk_simt_kernel(ChunkArgs a) {
 
         // ---- Y = diag(beta) (V - Kbar S), in place over V
         {
-            float acc[16];
+            float acc[kRpt];
 #pragma unroll
-            for (int m = 0; m < 16; ++m) acc[m] = 0.f;
+            for (int m = 0; m < kRpt; ++m) acc[m] = 0.f;
             for (int c = 0; c < DK; ++c) {
                 const float sv = Ss[c * kDvs + j];
 #pragma unroll
-                for (int m = 0; m < 16; ++m) acc[m] += Ks[(rq + 4 * m) * L::LDK + c] * sv;
+                for (int m = 0; m < kRpt; ++m) acc[m] += Ks[(rq + kRows * m) * L::LDK + c] * sv;
             }
 #pragma unroll
-            for (int m = 0; m < 16; ++m) {
-                const int r = rq + 4 * m;
+            for (int m = 0; m < kRpt; ++m) {
+                const int r = rq + kRows * m;
                 Us[r * kLdu + j] = Bs[r] * (Us[r * kLdu + j] - acc[m]);
             }
         }
         __syncthreads();
-        // ---- (I + A) U = Y by forward substitution (row r uses rows s < r)
+        // ---- (I + A) U = Y by forward substitution (row r uses rows s < r).  Columns are
+        // independent: column jj belongs to eight lanes of one warp, which sync among themselves.
         {
-            const int jj = t >> 2, part = t & 3;
+            const int jj = t >> 3, part = t & 7;
             for (int r = 1; r < C; ++r) {
                 float acc = 0.f;
-                for (int s = part; s < r; s += 4) acc += As[r * C + s] * Us[s * kLdu + jj];
+                for (int s = part; s < r; s += 8) acc += As[r * C + s] * Us[s * kLdu + jj];
                 acc += __shfl_xor_sync(0xffffffffu, acc, 1);
                 acc += __shfl_xor_sync(0xffffffffu, acc, 2);
+                acc += __shfl_xor_sync(0xffffffffu, acc, 4);
                 if (part == 0) Us[r * kLdu + jj] -= acc;
-                __syncthreads();
+                __syncwarp();
             }
         }
+        __syncthreads();
         // ---- O = Qbar S + M U
         {
-            float acc[16];
+            float acc[kRpt];
 #pragma unroll
-            for (int m = 0; m < 16; ++m) acc[m] = 0.f;
+            for (int m = 0; m < kRpt; ++m) acc[m] = 0.f;
             for (int c = 0; c < DK; ++c) {
                 const float sv = Ss[c * kDvs + j];
 #pragma unroll
-                for (int m = 0; m < 16; ++m) acc[m] += Qs[(rq + 4 * m) * L::LDQ + c] * sv;
+                for (int m = 0; m < kRpt; ++m) acc[m] += Qs[(rq + kRows * m) * L::LDQ + c] * sv;
             }
             for (int s = 0; s < C; ++s) {
                 const float u = Us[s * kLdu + j];
 #pragma unroll
-                for (int m = 0; m < 16; ++m) acc[m] += Ms[(rq + 4 * m) * C + s] * u;
+                for (int m = 0; m < kRpt; ++m) acc[m] += Ms[(rq + kRows * m) * C + s] * u;
             }
 #pragma unroll
-            for (int m = 0; m < 16; ++m) {
-                const int r = rq + 4 * m;
+            for (int m = 0; m < kRpt; ++m) {
+                const int r = rq + kRows * m;
                 if (r < nr) out[((bos + c0 + r) * H + h) * DV + col0 + j] = from_f<Tin>(acc[m]);
             }
         }
         __syncthreads();
         // ---- S <- Diag(e^{gl}) S + Kp^T U
         {
-            constexpr int MR = DK / 4;
+            constexpr int MR = DK / kRows;
             float acc[MR];
 #pragma unroll
             for (int m = 0; m < MR; ++m) acc[m] = 0.f;
             for (int r = 0; r < C; ++r) {
                 const float u = Us[r * kLdu + j];
 #pragma unroll
-                for (int m = 0; m < MR; ++m) acc[m] += Hs[r * L::LDH + rq + 4 * m] * u;
+                for (int m = 0; m < MR; ++m) acc[m] += Hs[r * L::LDH + rq + kRows * m] * u;
             }
 #pragma unroll
             for (int m = 0; m < MR; ++m) {
-                const int c = rq + 4 * m;
+                const int c = rq + kRows * m;
                 Ss[c * kDvs + j] = Dec[c] * Ss[c * kDvs + j] + acc[m];
             }
         }
