@@ -57,6 +57,8 @@ struct SimtSmem {
     static constexpr int kDec = kW + 6 * DK;        // e^{gl}         [DK]
     static constexpr int kFloats = kDec + DK;
     static constexpr size_t kBytes = sizeof(float) * kFloats;
+    static_assert(kK % 4 == 0 && kQ % 4 == 0 && kM % 4 == 0 && kW % 4 == 0 && LDQ % 4 == 0 && LDK % 4 == 0,
+                  "16-byte row loads");
 };
 
 __device__ __forceinline__ int pair_index(int I, int J) { return I * (I - 1) / 2 + J; }
@@ -183,17 +185,27 @@ kda_chunk_simt_kernel(ChunkArgs a) {
             float accA[kRpt], accM[kRpt];
 #pragma unroll
             for (int m = 0; m < kRpt; ++m) { accA[m] = 0.f; accM[m] = 0.f; }
-            for (int c = 0; c < DK; ++c) {
-                const float kh = Hs[s * L::LDH + c];
-                float khI[kNb];
+            for (int c = 0; c < DK; c += 4) {   // four channels a step: 16-byte row loads
+                const float4 kh = make_float4(Hs[s * L::LDH + c], Hs[s * L::LDH + c + 1],
+                                              Hs[s * L::LDH + c + 2], Hs[s * L::LDH + c + 3]);
+                float4 khI[kNb];
 #pragma unroll
-                for (int I = 0; I < kNb; ++I)
-                    khI[I] = I > Js ? kh * Wv[pair_index(I, Js) * DK + c] : kh;
+                for (int I = 0; I < kNb; ++I) {
+                    if (I > Js) {
+                        const float4 w = *reinterpret_cast<const float4 *>(Wv + pair_index(I, Js) * DK + c);
+                        khI[I] = make_float4(kh.x * w.x, kh.y * w.y, kh.z * w.z, kh.w * w.w);
+                    } else {
+                        khI[I] = kh;
+                    }
+                }
 #pragma unroll
                 for (int m = 0; m < kRpt; ++m) {
                     const int r = rq + kRows * m;   // in sub-tile (kRows m) / kSub: rq < kRows
-                    accA[m] += Ks[r * L::LDK + c] * khI[kRows * m / kSub];
-                    accM[m] += Qs[r * L::LDQ + c] * khI[kRows * m / kSub];
+                    const float4 f = khI[kRows * m / kSub];
+                    const float4 k4 = *reinterpret_cast<const float4 *>(Ks + r * L::LDK + c);
+                    const float4 q4 = *reinterpret_cast<const float4 *>(Qs + r * L::LDQ + c);
+                    accA[m] = fmaf(k4.w, f.w, fmaf(k4.z, f.z, fmaf(k4.y, f.y, fmaf(k4.x, f.x, accA[m]))));
+                    accM[m] = fmaf(q4.w, f.w, fmaf(q4.z, f.z, fmaf(q4.y, f.y, fmaf(q4.x, f.x, accM[m]))));
                 }
             }
 #pragma unroll
@@ -218,10 +230,14 @@ kda_chunk_simt_kernel(ChunkArgs a) {
             float acc[kRpt];
 #pragma unroll
             for (int m = 0; m < kRpt; ++m) acc[m] = 0.f;
-            for (int c = 0; c < DK; ++c) {
-                const float sv = Ss[c * kDvs + j];
+            for (int c = 0; c < DK; c += 4) {
+                const float s0 = Ss[c * kDvs + j], s1 = Ss[(c + 1) * kDvs + j];
+                const float s2 = Ss[(c + 2) * kDvs + j], s3 = Ss[(c + 3) * kDvs + j];
 #pragma unroll
-                for (int m = 0; m < kRpt; ++m) acc[m] += Ks[(rq + kRows * m) * L::LDK + c] * sv;
+                for (int m = 0; m < kRpt; ++m) {
+                    const float4 k4 = *reinterpret_cast<const float4 *>(Ks + (rq + kRows * m) * L::LDK + c);
+                    acc[m] = fmaf(k4.w, s3, fmaf(k4.z, s2, fmaf(k4.y, s1, fmaf(k4.x, s0, acc[m]))));
+                }
             }
 #pragma unroll
             for (int m = 0; m < kRpt; ++m) {
@@ -250,15 +266,23 @@ kda_chunk_simt_kernel(ChunkArgs a) {
             float acc[kRpt];
 #pragma unroll
             for (int m = 0; m < kRpt; ++m) acc[m] = 0.f;
-            for (int c = 0; c < DK; ++c) {
-                const float sv = Ss[c * kDvs + j];
+            for (int c = 0; c < DK; c += 4) {
+                const float s0 = Ss[c * kDvs + j], s1 = Ss[(c + 1) * kDvs + j];
+                const float s2 = Ss[(c + 2) * kDvs + j], s3 = Ss[(c + 3) * kDvs + j];
 #pragma unroll
-                for (int m = 0; m < kRpt; ++m) acc[m] += Qs[(rq + kRows * m) * L::LDQ + c] * sv;
+                for (int m = 0; m < kRpt; ++m) {
+                    const float4 q4 = *reinterpret_cast<const float4 *>(Qs + (rq + kRows * m) * L::LDQ + c);
+                    acc[m] = fmaf(q4.w, s3, fmaf(q4.z, s2, fmaf(q4.y, s1, fmaf(q4.x, s0, acc[m]))));
+                }
             }
-            for (int s = 0; s < C; ++s) {
-                const float u = Us[s * kLdu + j];
+            for (int s = 0; s < C; s += 4) {
+                const float u0 = Us[s * kLdu + j], u1 = Us[(s + 1) * kLdu + j];
+                const float u2 = Us[(s + 2) * kLdu + j], u3 = Us[(s + 3) * kLdu + j];
 #pragma unroll
-                for (int m = 0; m < kRpt; ++m) acc[m] += Ms[(rq + kRows * m) * C + s] * u;
+                for (int m = 0; m < kRpt; ++m) {
+                    const float4 m4 = *reinterpret_cast<const float4 *>(Ms + (rq + kRows * m) * C + s);
+                    acc[m] = fmaf(m4.w, u3, fmaf(m4.z, u2, fmaf(m4.y, u1, fmaf(m4.x, u0, acc[m]))));
+                }
             }
 #pragma unroll
             for (int m = 0; m < kRpt; ++m) {
