@@ -241,3 +241,34 @@ def test_debug_build_reports_its_checks(K):
         assert hasattr(dbg, n), n
     dbg.kda_status_string.restype = ctypes.c_char_p
     assert b"debug-build" in dbg.kda_status_string(K.KDA_ERR_INPUT)
+
+
+def test_qknorm_validation(K):
+    # the fused normalisation's epsilon is checked before anything else; the rest of each
+    # call's checks are those of the call it extends
+    vp, L = ctypes.c_void_p, K.lib()
+
+    def chunk(eps, q=FAKE, d=None):
+        d = dims() if d is None else d
+        a = [vp(x) if x is not None else None for x in (q, FAKE, FAKE, FAKE, FAKE)]
+        return L.kda_chunk_fwd_qknorm(*a, ctypes.c_float(eps), None, None, vp(FAKE), None,
+                                      ctypes.byref(d), None)
+
+    def step(eps, q=FAKE):
+        d = dims(batch=8, seqlen=1, num_seqs=8)
+        a = [vp(x) if x is not None else None for x in (q, FAKE, FAKE, FAKE, FAKE)]
+        return L.kda_recurrent_step_qknorm(*a, ctypes.c_float(eps), vp(FAKE), None, vp(FAKE),
+                                           ctypes.byref(d), None)
+
+    def steps(eps, q=FAKE):
+        d = dims(batch=8, seqlen=4, num_seqs=8)
+        a = [vp(x) if x is not None else None for x in (q, FAKE, FAKE, FAKE, FAKE)]
+        return L.kda_recurrent_steps_qknorm(*a, ctypes.c_float(eps), vp(FAKE), None, None,
+                                            vp(FAKE), 1, ctypes.byref(d), None)
+
+    for f in (chunk, step, steps):
+        for bad in (-1.0, float("nan"), float("inf")):
+            assert f(bad) == K.KDA_ERR_SHAPE, (f.__name__, bad)
+        assert f(1e-6, q=None) == K.KDA_ERR_NULL, f.__name__
+        assert f(1e-6, q=FAKE + 2) == K.KDA_ERR_ALIGN, f.__name__
+    assert chunk(1e-6, d=dims(dk=96)) == K.KDA_ERR_UNSUPPORTED
