@@ -178,3 +178,24 @@ def test_recurrent_steps_verify_and_replay(K, dtype, d):
     torch.cuda.synchronize()
     assert torch.equal(s_multi, s_single)
     assert rel_max_err(f64(s_multi), pool) <= TOL[dtype]
+
+
+def test_in_place_resume_and_many_packed_units(K):
+    # the one-CTA-per-unit instantiation of the tensor-core kernel with the normalisation: an
+    # in-place resume (the initial state buffer is also the final one), and more packed units
+    # than twice the SMs (one CTA each, longest first)
+    inp = inputs.make_prefill(batch=2, seqlen=300, heads=3, dk=128, dv=128, dtype=torch.bfloat16,
+                              device="cuda", seed=4707, init_state=True, raw_qk=True)
+    ref = normalised(inp, EPS)
+    ref["initial_state"] = inp["initial_state"].clone()
+    st = inp["initial_state"]
+    out, sT = K.kda_chunk_fwd(inp["q"], inp["k"], inp["v"], inp["g"], inp["beta"], st, None,
+                              final_state=st, qk_eps=EPS)
+    check_prefill(compare_prefill(ref, out, sT), torch.bfloat16)
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    nseq = sms + 8   # x 2 heads: more than twice the SMs
+    lengths = [1 + (37 * i) % 150 for i in range(nseq)]
+    inp = inputs.make_prefill(batch=1, seqlen=0, heads=2, dk=128, dv=128, dtype=torch.bfloat16,
+                              device="cuda", seed=4708, init_state=True, raw_qk=True, lengths=lengths)
+    out, sT = run(K, inp)
+    check_prefill(compare_prefill(normalised(inp, EPS), out, sT), torch.bfloat16)
