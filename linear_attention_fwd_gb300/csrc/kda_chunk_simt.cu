@@ -57,7 +57,8 @@ struct SimtSmem {
     static constexpr int kDec = kW + 6 * DK;        // e^{gl}         [DK]
     static constexpr int kFloats = kDec + DK;
     static constexpr size_t kBytes = sizeof(float) * kFloats;
-    static_assert(kK % 4 == 0 && kQ % 4 == 0 && kM % 4 == 0 && kW % 4 == 0 && LDQ % 4 == 0 && LDK % 4 == 0,
+    static_assert(kK % 4 == 0 && kQ % 4 == 0 && kM % 4 == 0 && kW % 4 == 0 && kU % 4 == 0 && kS % 4 == 0 &&
+                      LDQ % 4 == 0 && LDK % 4 == 0 && kLdu % 4 == 0 && kDvs % 4 == 0,
                   "16-byte row loads");
 };
 
@@ -291,21 +292,37 @@ kda_chunk_simt_kernel(ChunkArgs a) {
             }
         }
         __syncthreads();
-        // ---- S <- Diag(e^{gl}) S + Kp^T U
+        // ---- S <- Diag(e^{gl}) S + Kp^T U: a 4 x 4 tile of (key channel, value column) per
+        // thread, so each step over r reads four Kp values and one 16-byte row of U
         {
-            constexpr int MR = DK / kRows;
-            float acc[MR];
+            constexpr int JB = kDvs / 4, CB = DK / 4;
+            static_assert(CB * JB <= kThreads, "one tile per thread");
+            if (t < CB * JB) {
+                const int jb = t % JB, cb = t / JB;
+                float4 acc[4];
 #pragma unroll
-            for (int m = 0; m < MR; ++m) acc[m] = 0.f;
-            for (int r = 0; r < C; ++r) {
-                const float u = Us[r * kLdu + j];
+                for (int e = 0; e < 4; ++e) acc[e] = make_float4(0.f, 0.f, 0.f, 0.f);
+                for (int r = 0; r < C; ++r) {
+                    const float4 u = *reinterpret_cast<const float4 *>(Us + r * kLdu + 4 * jb);
+                    const float *hr = Hs + r * L::LDH + 4 * cb;
 #pragma unroll
-                for (int m = 0; m < MR; ++m) acc[m] += Hs[r * L::LDH + rq + kRows * m] * u;
-            }
+                    for (int e = 0; e < 4; ++e) {
+                        const float hv = hr[e];
+                        acc[e].x = fmaf(hv, u.x, acc[e].x);
+                        acc[e].y = fmaf(hv, u.y, acc[e].y);
+                        acc[e].z = fmaf(hv, u.z, acc[e].z);
+                        acc[e].w = fmaf(hv, u.w, acc[e].w);
+                    }
+                }
 #pragma unroll
-            for (int m = 0; m < MR; ++m) {
-                const int c = rq + kRows * m;
-                Ss[c * kDvs + j] = Dec[c] * Ss[c * kDvs + j] + acc[m];
+                for (int e = 0; e < 4; ++e) {
+                    const int c = 4 * cb + e;
+                    float4 *sp = reinterpret_cast<float4 *>(Ss + c * kDvs + 4 * jb);
+                    const float4 o = *sp;
+                    const float d = Dec[c];
+                    *sp = make_float4(fmaf(d, o.x, acc[e].x), fmaf(d, o.y, acc[e].y), fmaf(d, o.z, acc[e].z),
+                                      fmaf(d, o.w, acc[e].w));
+                }
             }
         }
     }
