@@ -8,7 +8,8 @@
 // state (see warm_start).  The fp32 state lives in tensor memory for the whole piece
 // (transposed: TMEM lane j = value channel, column i = key channel), so the only HBM traffic is
 // the q/k/v/g/beta tiles, the output, and the initial / final states (plus the warm-up chunks'
-// tiles).
+// tiles).  With the L2 option (kQk) each q and k row is first scaled by 1 / sqrt(|x|^2 + eps),
+// the norms taken on mma.sync in step (1).
 //
 // Chunk algebra ("はじめての自然言語処理 -- Kimi K3" section 3.1: chunkwise form,
 // Tril intra-chunk term, decay folded into q times Gamma and k over Gamma as in
